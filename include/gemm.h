@@ -1,0 +1,144 @@
+/*
+ * gemm.h -- C ABI of the any-layout half-precision GEMM for GB300 (sm_103a).
+ *
+ *   C = A . B,  A logically M x K, B logically K x N, C row-major M x N,
+ *   products accumulated in fp32, C written once (round to nearest even).
+ *
+ * Operand layouts.  The two storage orders of each operand are the cases the
+ * Triton inThreadTranspose page ("[AMD] inThreadTranspose ...", "Feature
+ * description" and "PR description") distinguishes: a dot operand that is
+ * contiguous along K, and a "non-KContig" one that is contiguous along M
+ * (for A) or N (for B).
+ *   A, GEMM_K_CONTIG : row-major M x K, element (m,k) at A[m*lda + k]
+ *   A, GEMM_MN_CONTIG: column-major M x K, element (m,k) at A[k*lda + m]
+ *   B, GEMM_K_CONTIG : stored N x K row-major, element (k,n) at B[n*ldb + k]
+ *   B, GEMM_MN_CONTIG: stored K x N row-major, element (k,n) at B[k*ldb + n]
+ *   C                : element (m,n) at C[m*ldc + n]
+ * Leading dimensions are in elements; 0 means dense (K, M, K, N, N).
+ *
+ * Split-K.  split_k = 0 selects the SM-waste rule of the BitBLAS TileLang
+ * page ("SplitK Infer for dequantize cases"), evaluated on the 128 x 128 x 64
+ * tile and a 0.05 threshold; split z covers k in [z*Ks, min(K,(z+1)*Ks)) with
+ * Ks = ceil(K / (split_k*64)) * 64, following the page's per-split K offset
+ * in its T.Parallel / T.copy example.  Partial sums are reduced across CTAs
+ * in fp32 (the reduction-across-workers pattern of the IREE page,
+ * "[LLVMGPUVectorDistribute] Add support for inter-subgroup multi_reduction").
+ *
+ * int4 weights (b_dtype = GEMM_INT4).  B is N rows of K/2 bytes, code q(n,k)
+ * in the low nibble of byte k/2 for even k and the high nibble for odd k;
+ * w(k,n) = (q(n,k) - z(n,k/g)) * s(n,k/g) with g = group_size and fp16
+ * scales / zeros stored [N, K/g] row-major (zeros NULL means z = 8).  The
+ * weight is dequantised inside the GEMM mainloop (BitBLAS TileLang page,
+ * "Relevant Issues": dequantize layout transformations).  A must be fp16.
+ *
+ * Errors: every entry point returns a status code; nothing aborts or prints.
+ * All pointers passed to gemm_run are device pointers owned by the caller.
+ */
+#ifndef LGT_GEMM_H
+#define LGT_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = 1, /* bad shape, enum, leading dimension or NULL pointer */
+  GEMM_ERR_UNSUPPORTED = 2, /* valid request this library does not implement */
+  GEMM_ERR_ALIGNMENT = 3,   /* an operand pointer is not aligned to its element size */
+  GEMM_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than gemm_workspace_size */
+  GEMM_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed, or no device */
+  GEMM_ERR_TIMEOUT = 6      /* a kernel gave up waiting (bounded waits); output invalid */
+} gemm_status_t;
+
+typedef enum { GEMM_K_CONTIG = 0, GEMM_MN_CONTIG = 1 } gemm_layout_t;
+
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_INT4 = 2, GEMM_F32 = 3 } gemm_dtype_t;
+
+/* Problem description.  Enum-valued fields are int32_t so the struct has the
+ * same layout from every language. */
+typedef struct {
+  int64_t M, N, K;
+  int32_t a_layout, b_layout; /* gemm_layout_t; int4 B must be GEMM_K_CONTIG */
+  int64_t lda, ldb, ldc;      /* elements (bytes for int4 B: ldb = K/2 or 0); 0 = dense */
+  int32_t a_dtype, b_dtype, c_dtype; /* F16 / BF16 (A and B alike), or B = INT4 with A = F16; C = F16 / BF16 */
+  int32_t split_k;            /* 0 = SM-waste rule; >= 1 explicit factor */
+  int32_t group_size;         /* int4 quantisation group along K (0 = 128); must divide K and the split length */
+  int32_t num_sms;            /* SM count the split-K rule uses: 0 = the current device's */
+  int32_t flags;              /* reserved, must be 0 */
+} gemm_desc_t;
+
+/* What a plan decided. */
+typedef struct {
+  int32_t split_k;     /* factor in use */
+  int32_t tile_m, tile_n, tile_k; /* output tile of one work unit (M x N x K) */
+  int32_t swap_ab;     /* 1: the MMA runs C^T = B^T A^T (skinny M) */
+  int32_t num_units;   /* (tile, split) work units */
+  int32_t k_per_split; /* Ks in elements */
+  int32_t repack_a, repack_b; /* operand copied into the workspace first (stride TMA cannot express) */
+  int32_t kernel;      /* 0 = tensor-core any-layout, 1 = int4 dequant */
+} gemm_info_t;
+
+typedef struct gemm_plan gemm_plan_t;
+
+/* Validate `desc`, choose tiles and the split factor, and return a plan.
+ * Needs a CUDA device only when desc->num_sms == 0 (to count its SMs); the
+ * plan's kernels run on the device current at gemm_create.  The plan is
+ * immutable and may be used from several streams, each with its own
+ * workspace.  *out is NULL on error. */
+gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out);
+
+/* Bytes of device workspace gemm_run needs (0 if none).  The workspace holds
+ * the fp32 split-K partial sums and per-tile arrival counters, and repacked
+ * operand copies.  It must be zero-filled before its first use; every
+ * successful gemm_run leaves it zero-filled again (a run that returns or
+ * records GEMM_ERR_TIMEOUT does not). */
+gemm_status_t gemm_workspace_size(const gemm_plan_t* plan, size_t* bytes);
+
+gemm_status_t gemm_query(const gemm_plan_t* plan, gemm_info_t* info);
+
+/* Enqueue C = A.B on `stream` (a cudaStream_t; NULL = legacy default stream).
+ * A, B, C: device pointers in the plan's layouts; A and B are read only, C is
+ * written only.  scales / zeros: int4 only (zeros may be NULL).  The call is
+ * asynchronous; errors found on the host are returned at once, a device-side
+ * timeout is reported by gemm_sync_status.  Concurrent runs of one plan must
+ * use distinct workspaces. */
+gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C, const void* scales,
+                       const void* zeros, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Wait for `stream`, then read and clear the plan's device status word:
+ * GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel of this plan gave up a wait. */
+gemm_status_t gemm_sync_status(gemm_plan_t* plan, void* stream);
+
+gemm_status_t gemm_destroy(gemm_plan_t* plan);
+
+/* The split-K rule on its own (host computation, no device needed). */
+int32_t gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int32_t block_m, int32_t block_n, int32_t block_k,
+                         int32_t num_sms, double threshold);
+
+/* Perpendicular-dimension stride permutation of the hipBLASLt DTL page ("Add
+ * support for permuting perpDim"), over `count` indices in blocks of `block`
+ * with stride `stride` (must divide `block`; a trailing partial block and an
+ * invalid stride map indices to themselves).  Host computation. */
+uint32_t gemm_perm_fwd(uint32_t index, uint32_t count, uint32_t block, uint32_t stride);
+uint32_t gemm_perm_inv(uint32_t index, uint32_t count, uint32_t block, uint32_t stride);
+
+/* Magic-number division by a divisor fixed in advance (hipBLASLt DTL page,
+ * "Add support for generalized NLC=1": static divisors use a magic multiply).
+ * gemm_magic_divmod_host runs the kernels' own quotient routine on the host
+ * over `count` dividends (< 2^31); gemm_magic_divmod_device runs it on the
+ * device over device arrays on `stream`.  divisor must be >= 1. */
+gemm_status_t gemm_magic_divmod_host(const uint32_t* n, size_t count, uint32_t divisor, uint32_t* q, uint32_t* r);
+gemm_status_t gemm_magic_divmod_device(const uint32_t* n, size_t count, uint32_t divisor, uint32_t* q, uint32_t* r,
+                                       void* stream);
+
+const char* gemm_status_string(gemm_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LGT_GEMM_H */

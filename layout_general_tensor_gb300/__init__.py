@@ -1,0 +1,223 @@
+"""Python binding of the any-layout GEMM C ABI (``include/gemm.h``).
+
+Argument marshalling only: every function forwards to the entry point of the
+same name in ``_lib/libgemm.so``; all arithmetic runs in the library's CUDA
+kernels.  Importing this package fails loudly when the library has not been
+built -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libgemm.so")
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_UNSUPPORTED = 2
+GEMM_ERR_ALIGNMENT = 3
+GEMM_ERR_WORKSPACE = 4
+GEMM_ERR_CUDA = 5
+GEMM_ERR_TIMEOUT = 6
+
+GEMM_K_CONTIG = 0
+GEMM_MN_CONTIG = 1
+
+GEMM_F16 = 0
+GEMM_BF16 = 1
+GEMM_INT4 = 2
+GEMM_F32 = 3
+
+# Every entry point include/gemm.h declares.
+EXPORTS = (
+    "gemm_create", "gemm_workspace_size", "gemm_query", "gemm_run", "gemm_sync_status", "gemm_destroy",
+    "gemm_splitk_auto", "gemm_perm_fwd", "gemm_perm_inv", "gemm_magic_divmod_host",
+    "gemm_magic_divmod_device", "gemm_status_string",
+)
+
+
+class gemm_desc_t(ctypes.Structure):
+    _fields_ = [
+        ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+        ("a_layout", ctypes.c_int32), ("b_layout", ctypes.c_int32),
+        ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
+        ("a_dtype", ctypes.c_int32), ("b_dtype", ctypes.c_int32), ("c_dtype", ctypes.c_int32),
+        ("split_k", ctypes.c_int32), ("group_size", ctypes.c_int32), ("num_sms", ctypes.c_int32),
+        ("flags", ctypes.c_int32),
+    ]
+
+
+class gemm_info_t(ctypes.Structure):
+    _fields_ = [
+        ("split_k", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+        ("tile_k", ctypes.c_int32), ("swap_ab", ctypes.c_int32), ("num_units", ctypes.c_int32),
+        ("k_per_split", ctypes.c_int32), ("repack_a", ctypes.c_int32), ("repack_b", ctypes.c_int32),
+        ("kernel", ctypes.c_int32),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m layout_general_tensor_gb300.build` "
+                          "(there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.c_void_p
+    sig = {
+        "gemm_create": (ctypes.c_int, [ctypes.POINTER(gemm_desc_t), ctypes.POINTER(P)]),
+        "gemm_workspace_size": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_size_t)]),
+        "gemm_query": (ctypes.c_int, [P, ctypes.POINTER(gemm_info_t)]),
+        "gemm_run": (ctypes.c_int, [P, P, P, P, P, P, P, ctypes.c_size_t, P]),
+        "gemm_sync_status": (ctypes.c_int, [P, P]),
+        "gemm_destroy": (ctypes.c_int, [P]),
+        "gemm_splitk_auto": (ctypes.c_int32, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_double]),
+        "gemm_perm_fwd": (ctypes.c_uint32, [ctypes.c_uint32] * 4),
+        "gemm_perm_inv": (ctypes.c_uint32, [ctypes.c_uint32] * 4),
+        "gemm_magic_divmod_host": (ctypes.c_int, [P, ctypes.c_size_t, ctypes.c_uint32, P, P]),
+        "gemm_magic_divmod_device": (ctypes.c_int, [P, ctypes.c_size_t, ctypes.c_uint32, P, P, P]),
+        "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__(f"{what}: {gemm_status_string(status)} ({status})")
+
+
+def _check(status, what):
+    if status != GEMM_OK:
+        raise GemmError(status, what)
+
+
+# ------------------------------------------------------------- thin wrappers
+
+def gemm_status_string(status: int) -> str:
+    return _lib.gemm_status_string(int(status)).decode()
+
+
+def gemm_create(desc: gemm_desc_t) -> int:
+    h = ctypes.c_void_p()
+    _check(_lib.gemm_create(ctypes.byref(desc), ctypes.byref(h)), "gemm_create")
+    return h.value
+
+
+def gemm_create_status(desc: gemm_desc_t):
+    """gemm_create returning (status, handle or None) without raising."""
+    h = ctypes.c_void_p()
+    st = _lib.gemm_create(ctypes.byref(desc), ctypes.byref(h))
+    return st, h.value
+
+
+def gemm_workspace_size(plan: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.gemm_workspace_size(plan, ctypes.byref(n)), "gemm_workspace_size")
+    return n.value
+
+
+def gemm_query(plan: int) -> gemm_info_t:
+    info = gemm_info_t()
+    _check(_lib.gemm_query(plan, ctypes.byref(info)), "gemm_query")
+    return info
+
+
+def gemm_run(plan: int, A: int, B: int, C: int, scales: int = 0, zeros: int = 0, workspace: int = 0,
+             workspace_bytes: int = 0, stream: int = 0) -> int:
+    """Raw entry point: integer device addresses; returns the status code."""
+    return _lib.gemm_run(plan, A or None, B or None, C or None, scales or None, zeros or None, workspace or None,
+                         workspace_bytes, stream or None)
+
+
+def gemm_sync_status(plan: int, stream: int = 0) -> int:
+    return _lib.gemm_sync_status(plan, stream or None)
+
+
+def gemm_destroy(plan: int) -> None:
+    _check(_lib.gemm_destroy(plan), "gemm_destroy")
+
+
+def gemm_splitk_auto(M, N, K, block_m=128, block_n=128, block_k=64, num_sms=148, threshold=0.05) -> int:
+    return _lib.gemm_splitk_auto(M, N, K, block_m, block_n, block_k, num_sms, threshold)
+
+
+def gemm_perm_fwd(index, count, block, stride) -> int:
+    return _lib.gemm_perm_fwd(index, count, block, stride)
+
+
+def gemm_perm_inv(index, count, block, stride) -> int:
+    return _lib.gemm_perm_inv(index, count, block, stride)
+
+
+def gemm_magic_divmod_host(n_array, divisor):
+    """n_array: numpy uint32 array (C-contiguous).  Returns (q, r) arrays."""
+    import numpy as np
+    n = np.ascontiguousarray(n_array, dtype=np.uint32)
+    q = np.empty_like(n)
+    r = np.empty_like(n)
+    _check(_lib.gemm_magic_divmod_host(n.ctypes.data, n.size, divisor, q.ctypes.data, r.ctypes.data),
+           "gemm_magic_divmod_host")
+    return q, r
+
+
+def gemm_magic_divmod_device(n_ptr, count, divisor, q_ptr, r_ptr, stream=0) -> int:
+    return _lib.gemm_magic_divmod_device(n_ptr, count, divisor, q_ptr, r_ptr, stream or None)
+
+
+def make_desc(M, N, K, a_layout=GEMM_K_CONTIG, b_layout=GEMM_K_CONTIG, a_dtype=GEMM_BF16, b_dtype=None,
+              c_dtype=None, lda=0, ldb=0, ldc=0, split_k=1, group_size=0, num_sms=0, flags=0) -> gemm_desc_t:
+    b_dtype = a_dtype if b_dtype is None else b_dtype
+    c_dtype = a_dtype if c_dtype is None else c_dtype
+    return gemm_desc_t(M, N, K, a_layout, b_layout, lda, ldb, ldc, a_dtype, b_dtype, c_dtype, split_k,
+                       group_size, num_sms, flags)
+
+
+class Gemm:
+    """A plan plus its (zero-filled) device workspace, run on torch tensors.
+
+    Marshalling only: passes the tensors' device addresses and the current
+    torch stream to gemm_run."""
+
+    def __init__(self, desc: gemm_desc_t, device=None):
+        import torch
+        self.desc = desc
+        self.plan = gemm_create(desc)
+        self.info = gemm_query(self.plan)
+        self.ws_bytes = gemm_workspace_size(self.plan)
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.workspace = torch.zeros(max(self.ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+    def run(self, A, B, C, scales=None, zeros=None, stream=None, workspace=None, workspace_bytes=None):
+        import torch
+        s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+        ws = self.workspace if workspace is None else workspace
+        wsb = self.ws_bytes if workspace_bytes is None else workspace_bytes
+        st = gemm_run(self.plan, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                      scales.data_ptr() if scales is not None else 0,
+                      zeros.data_ptr() if zeros is not None else 0,
+                      ws.data_ptr() if wsb else 0, wsb, s)
+        _check(st, "gemm_run")
+
+    def sync_status(self, stream=None) -> int:
+        import torch
+        s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+        return gemm_sync_status(self.plan, s)
+
+    def close(self):
+        if self.plan:
+            gemm_destroy(self.plan)
+            self.plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

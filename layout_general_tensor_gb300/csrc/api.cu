@@ -1,0 +1,429 @@
+// C ABI: planning (tile, swap, split-K factor, workspace), validation, TMA
+// descriptor encoding and kernel launch.  See include/gemm.h for the contract.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/gemm.h"
+#include "kernels.h"
+
+using lgt::MagicDiv;
+
+struct gemm_plan {
+  gemm_desc_t d;
+  int device;        // device current at create time, -1 if none was queried
+  int sms_rule;      // SM count fed to the split-K rule
+  int sms_grid;      // persistent grid size (device SMs), 0 without a device
+  int kernel;        // 0: tensor-core any-layout
+  int swap;
+  int bn;
+  int split, kb_per_split, kb_total;
+  int tiles_p, tiles_q, num_units;
+  int64_t lda, ldb, ldc;
+  int a_mn, b_mn;
+  // operand repacking (leading dimension not a multiple of 16 bytes)
+  int repack_a, repack_b;
+  int64_t a_rows, a_row_elems, b_rows, b_row_elems;  // storage rows of each operand
+  int64_t a_pack_ld, b_pack_ld;
+  size_t off_partial, off_counters, off_pack_a, off_pack_b, ws_bytes;
+  size_t ws_bytes_misaligned;
+  lgt::DeviceStatus* d_status;
+  uint64_t wait_limit_ns;
+};
+
+namespace {
+
+constexpr int kBlockK = 64;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int next_pow2_at_least16(int64_t v) {
+  int p = 16;
+  while (p < v && p < 256) p <<= 1;
+  return p;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D tensor map over a 16-bit operand.  K-major: dims {K, rows}, box
+// {64, box_rows}.  MN-major: dims {mn, K}, box {64, 64}.  128-byte swizzle,
+// zero fill outside the tensor (ragged M / N / K tails).
+bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major, int64_t rows_or_mn, int64_t K,
+                    int64_t ld, int box_rows) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  const CUtensorMapDataType dt =
+      dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[2];
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2];
+  cuuint32_t estr[2] = {1, 1};
+  if (!mn_major) {
+    dims[0] = static_cast<cuuint64_t>(K);
+    dims[1] = static_cast<cuuint64_t>(rows_or_mn);
+    box[0] = kBlockK;
+    box[1] = static_cast<cuuint32_t>(box_rows);
+  } else {
+    dims[0] = static_cast<cuuint64_t>(rows_or_mn);
+    dims[1] = static_cast<cuuint64_t>(K);
+    box[0] = 64;
+    box[1] = kBlockK;
+  }
+  CUresult r = enc(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool is_half(int t) { return t == GEMM_F16 || t == GEMM_BF16; }
+
+gemm_status_t validate(const gemm_desc_t& d) {
+  const int64_t lim = (1ll << 31) - 1;
+  if (d.M < 0 || d.N < 0 || d.K < 0 || d.M > lim || d.N > lim || d.K > lim) return GEMM_ERR_INVALID_ARG;
+  if ((d.a_layout != GEMM_K_CONTIG && d.a_layout != GEMM_MN_CONTIG) ||
+      (d.b_layout != GEMM_K_CONTIG && d.b_layout != GEMM_MN_CONTIG))
+    return GEMM_ERR_INVALID_ARG;
+  if (!is_half(d.c_dtype)) return GEMM_ERR_INVALID_ARG;
+  if (d.b_dtype == GEMM_INT4) {
+    if (d.a_dtype != GEMM_F16 || d.b_layout != GEMM_K_CONTIG) return GEMM_ERR_INVALID_ARG;
+  } else if (!is_half(d.a_dtype) || d.a_dtype != d.b_dtype) {
+    return GEMM_ERR_INVALID_ARG;
+  }
+  if (d.split_k < 0 || d.split_k > 65536 || d.num_sms < 0 || d.group_size < 0 || d.flags != 0)
+    return GEMM_ERR_INVALID_ARG;
+  if (d.lda < 0 || d.ldb < 0 || d.ldc < 0) return GEMM_ERR_INVALID_ARG;
+  const int64_t a_min = d.a_layout == GEMM_K_CONTIG ? d.K : d.M;
+  const int64_t c_min = d.N;
+  if (d.lda && d.lda < a_min) return GEMM_ERR_INVALID_ARG;
+  if (d.ldc && d.ldc < c_min) return GEMM_ERR_INVALID_ARG;
+  if (d.b_dtype != GEMM_INT4) {
+    const int64_t b_min = d.b_layout == GEMM_K_CONTIG ? d.K : d.N;
+    if (d.ldb && d.ldb < b_min) return GEMM_ERR_INVALID_ARG;
+  }
+  return GEMM_OK;
+}
+
+uint64_t wait_limit_from_env() {
+  const char* s = std::getenv("LGT_GEMM_WAIT_LIMIT_MS");
+  if (s && *s) {
+    const double ms = std::atof(s);
+    if (ms > 0) return static_cast<uint64_t>(ms * 1e6);
+  }
+  return 2000ull * 1000ull * 1000ull;  // 2 s
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gemm_status_string(gemm_status_t s) {
+  switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
+    case GEMM_ERR_ALIGNMENT: return "GEMM_ERR_ALIGNMENT";
+    case GEMM_ERR_WORKSPACE: return "GEMM_ERR_WORKSPACE";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    default: return "GEMM_ERR_UNKNOWN";
+  }
+}
+
+int32_t gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int32_t bm, int32_t bn, int32_t bk, int32_t num_sms,
+                         double threshold) {
+  return lgt::splitk_auto(M, N, K, bm, bn, bk, num_sms, threshold);
+}
+
+uint32_t gemm_perm_fwd(uint32_t i, uint32_t count, uint32_t block, uint32_t stride) {
+  return lgt::perm_fwd(i, count, block, stride);
+}
+
+uint32_t gemm_perm_inv(uint32_t i, uint32_t count, uint32_t block, uint32_t stride) {
+  return lgt::perm_inv(i, count, block, stride);
+}
+
+gemm_status_t gemm_magic_divmod_host(const uint32_t* n, size_t count, uint32_t divisor, uint32_t* q, uint32_t* r) {
+  if (divisor == 0 || (count && (!n || !q || !r))) return GEMM_ERR_INVALID_ARG;
+  const MagicDiv m = lgt::magic_encode(divisor);
+  for (size_t i = 0; i < count; ++i) {
+    if (n[i] >= (1u << 31)) return GEMM_ERR_INVALID_ARG;
+    lgt::magic_divmod(n[i], m, q[i], r[i]);
+  }
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_magic_divmod_device(const uint32_t* n, size_t count, uint32_t divisor, uint32_t* q, uint32_t* r,
+                                       void* stream) {
+  if (divisor == 0 || (count && (!n || !q || !r))) return GEMM_ERR_INVALID_ARG;
+  const MagicDiv m = lgt::magic_encode(divisor);
+  return lgt::launch_magic_divmod(n, count, m, q, r, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GEMM_OK
+             : GEMM_ERR_CUDA;
+}
+
+gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
+  if (!out) return GEMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!desc) return GEMM_ERR_INVALID_ARG;
+  const gemm_status_t v = validate(*desc);
+  if (v != GEMM_OK) return v;
+  if (desc->b_dtype == GEMM_INT4) return GEMM_ERR_UNSUPPORTED;
+
+  gemm_plan p;
+  std::memset(&p, 0, sizeof(p));
+  p.d = *desc;
+  const gemm_desc_t& d = p.d;
+  p.device = -1;
+  p.wait_limit_ns = wait_limit_from_env();
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
+    ndev = 0;
+    cudaGetLastError();
+  }
+  if (ndev > 0) {
+    if (cudaGetDevice(&p.device) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&p.sms_grid, cudaDevAttrMultiProcessorCount, p.device) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+  }
+  p.sms_rule = d.num_sms > 0 ? d.num_sms : p.sms_grid;
+  if (p.sms_rule <= 0) return GEMM_ERR_CUDA;  // rule needs an SM count and there is no device
+
+  p.lda = d.lda ? d.lda : (d.a_layout == GEMM_K_CONTIG ? d.K : d.M);
+  p.ldb = d.ldb ? d.ldb : (d.b_layout == GEMM_K_CONTIG ? d.K : d.N);
+  p.ldc = d.ldc ? d.ldc : d.N;
+  if (p.lda == 0) p.lda = 1;
+  if (p.ldb == 0) p.ldb = 1;
+  if (p.ldc == 0) p.ldc = 1;
+  p.a_mn = d.a_layout == GEMM_MN_CONTIG;
+  p.b_mn = d.b_layout == GEMM_MN_CONTIG;
+
+  // Tile shape.  Skinny M runs swapped: the 128-row MMA side walks N and the
+  // MMA's N extent covers all of M.
+  p.swap = (d.M <= 64 && d.N > d.M) ? 1 : 0;
+  const bool q_mn = p.swap ? p.a_mn : p.b_mn;
+  const int64_t q_extent = p.swap ? d.M : d.N;
+  int bn = q_extent >= 128 ? 128 : next_pow2_at_least16(q_extent);
+  if (q_mn && bn < 64) bn = 64;  // MN-major tiles come in 64-element swizzle atoms
+  p.bn = bn;
+  p.tiles_p = static_cast<int>(ceil_div(p.swap ? d.N : d.M, lgt::TILE_P));
+  p.tiles_q = static_cast<int>(ceil_div(q_extent, bn));
+
+  // Split-K factor: the SM-waste rule on the logical M x N with 128 x 128 x 64
+  // tiles, or the caller's factor.
+  p.kb_total = static_cast<int>(ceil_div(d.K, kBlockK));
+  if (d.K == 0) {
+    p.split = 1;
+  } else if (d.split_k == 0) {
+    p.split = lgt::splitk_auto(d.M, d.N, d.K, 128, 128, kBlockK, p.sms_rule, 0.05);
+  } else {
+    p.split = d.split_k;
+  }
+  p.kb_per_split = p.kb_total > 0 ? static_cast<int>(ceil_div(p.kb_total, p.split)) : 0;
+  const int64_t units = static_cast<int64_t>(p.tiles_p) * p.tiles_q * p.split;
+  if (units >= (1ll << 31)) return GEMM_ERR_UNSUPPORTED;
+  p.num_units = static_cast<int>(units);
+
+  // Storage rows of each operand and whether TMA can address them in place.
+  p.a_rows = p.a_mn ? d.K : d.M;
+  p.a_row_elems = p.a_mn ? d.M : d.K;
+  p.b_rows = p.b_mn ? d.K : d.N;
+  p.b_row_elems = p.b_mn ? d.N : d.K;
+  p.repack_a = (p.lda * 2) % 16 != 0;
+  p.repack_b = (p.ldb * 2) % 16 != 0;
+  p.a_pack_ld = align_up(static_cast<size_t>(p.a_row_elems), 8);
+  p.b_pack_ld = align_up(static_cast<size_t>(p.b_row_elems), 8);
+
+  size_t off = 0;
+  if (p.split > 1) {
+    p.off_partial = off;
+    off = align_up(off + static_cast<size_t>(d.M) * d.N * sizeof(float), 256);
+    p.off_counters = off;
+    off = align_up(off + static_cast<size_t>(p.tiles_p) * p.tiles_q * sizeof(int32_t), 256);
+  }
+  const size_t pack_a_bytes = align_up(static_cast<size_t>(p.a_rows) * p.a_pack_ld * 2, 256);
+  const size_t pack_b_bytes = align_up(static_cast<size_t>(p.b_rows) * p.b_pack_ld * 2, 256);
+  size_t off_aligned = off;
+  p.off_pack_a = off;
+  if (p.repack_a) off_aligned += pack_a_bytes;
+  p.off_pack_b = off_aligned;
+  if (p.repack_b) off_aligned += pack_b_bytes;
+  p.ws_bytes = off_aligned;
+  // When a base pointer is not 16-byte aligned the operand is repacked too.
+  p.ws_bytes_misaligned = off + pack_a_bytes + pack_b_bytes;
+
+  if (p.device >= 0) {
+    if (cudaMalloc(&p.d_status, sizeof(lgt::DeviceStatus)) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (cudaMemset(p.d_status, 0, sizeof(lgt::DeviceStatus)) != cudaSuccess) {
+      cudaFree(p.d_status);
+      return GEMM_ERR_CUDA;
+    }
+  }
+  gemm_plan* h = new (std::nothrow) gemm_plan(p);
+  if (!h) {
+    if (p.d_status) cudaFree(p.d_status);
+    return GEMM_ERR_INVALID_ARG;
+  }
+  *out = h;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_workspace_size(const gemm_plan_t* plan, size_t* bytes) {
+  if (!plan || !bytes) return GEMM_ERR_INVALID_ARG;
+  *bytes = plan->ws_bytes;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_query(const gemm_plan_t* plan, gemm_info_t* info) {
+  if (!plan || !info) return GEMM_ERR_INVALID_ARG;
+  std::memset(info, 0, sizeof(*info));
+  info->split_k = plan->split;
+  info->tile_m = plan->swap ? plan->bn : lgt::TILE_P;
+  info->tile_n = plan->swap ? lgt::TILE_P : plan->bn;
+  info->tile_k = kBlockK;
+  info->swap_ab = plan->swap;
+  info->num_units = plan->num_units;
+  info->k_per_split = plan->kb_per_split * kBlockK;
+  info->repack_a = plan->repack_a;
+  info->repack_b = plan->repack_b;
+  info->kernel = plan->kernel;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C, const void* scales,
+                       const void* zeros, void* workspace, size_t workspace_bytes, void* stream_ptr) {
+  (void)scales;
+  (void)zeros;
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  const gemm_desc_t& d = plan->d;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (d.M == 0 || d.N == 0) return GEMM_OK;
+  if (!C) return GEMM_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(C) % 2) return GEMM_ERR_ALIGNMENT;
+  if (plan->device < 0) return GEMM_ERR_CUDA;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device) return GEMM_ERR_INVALID_ARG;
+  if (d.K == 0) {
+    return cudaMemset2DAsync(C, plan->ldc * 2, 0, d.N * 2, d.M, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
+  if (!A || !B) return GEMM_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(A) % 2 || reinterpret_cast<uintptr_t>(B) % 2) return GEMM_ERR_ALIGNMENT;
+
+  const bool a_mis = reinterpret_cast<uintptr_t>(A) % 16 != 0;
+  const bool b_mis = reinterpret_cast<uintptr_t>(B) % 16 != 0;
+  const bool pack_a = plan->repack_a || a_mis;
+  const bool pack_b = plan->repack_b || b_mis;
+  const size_t need = (a_mis || b_mis) ? plan->ws_bytes_misaligned : plan->ws_bytes;
+  if (need > 0 && (!workspace || workspace_bytes < need)) return GEMM_ERR_WORKSPACE;
+  if (need > 0 && reinterpret_cast<uintptr_t>(workspace) % 256) return GEMM_ERR_ALIGNMENT;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  // Operand addresses and leading dimensions the kernel sees.
+  const void* a_eff = A;
+  const void* b_eff = B;
+  int64_t lda = plan->lda, ldb = plan->ldb;
+  size_t next_pack = plan->off_pack_a;  // repacked copies follow the split-K region
+  if (pack_a) {
+    void* dst = ws + next_pack;
+    if (lgt::launch_repack_rows(A, plan->lda * 2, dst, plan->a_pack_ld * 2, plan->a_rows, plan->a_row_elems * 2,
+                                stream) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    a_eff = dst;
+    lda = plan->a_pack_ld;
+    next_pack += align_up(static_cast<size_t>(plan->a_rows) * plan->a_pack_ld * 2, 256);
+  }
+  if (pack_b) {
+    void* dst = ws + next_pack;
+    if (lgt::launch_repack_rows(B, plan->ldb * 2, dst, plan->b_pack_ld * 2, plan->b_rows, plan->b_row_elems * 2,
+                                stream) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    b_eff = dst;
+    ldb = plan->b_pack_ld;
+  }
+
+  lgt::TcArgs args;
+  std::memset(&args, 0, sizeof(args));
+  const bool a_is_p = !plan->swap;
+  // P operand: 128-row tiles.  Q operand: bn-row tiles.
+  const void* p_ptr = a_is_p ? a_eff : b_eff;
+  const void* q_ptr = a_is_p ? b_eff : a_eff;
+  const int p_mn = a_is_p ? plan->a_mn : plan->b_mn;
+  const int q_mn = a_is_p ? plan->b_mn : plan->a_mn;
+  const int64_t p_ext = a_is_p ? d.M : d.N;
+  const int64_t q_ext = a_is_p ? d.N : d.M;
+  const int64_t p_ld = a_is_p ? lda : ldb;
+  const int64_t q_ld = a_is_p ? ldb : lda;
+  if (!encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, lgt::TILE_P)) return GEMM_ERR_CUDA;
+  if (!encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, plan->bn)) return GEMM_ERR_CUDA;
+
+  args.c = C;
+  args.ldc = plan->ldc;
+  if (plan->split > 1) {
+    args.ws = reinterpret_cast<float*>(ws + plan->off_partial);
+    args.counters = reinterpret_cast<int32_t*>(ws + plan->off_counters);
+  }
+  args.status = plan->d_status;
+  args.wait_limit_ns = plan->wait_limit_ns;
+  args.M = static_cast<int32_t>(d.M);
+  args.N = static_cast<int32_t>(d.N);
+  args.K = static_cast<int32_t>(d.K);
+  args.tiles_p = plan->tiles_p;
+  args.tiles_q = plan->tiles_q;
+  args.split = plan->split;
+  args.kb_per_split = plan->kb_per_split;
+  args.kb_total = plan->kb_total;
+  args.num_units = plan->num_units;
+  args.div_split = lgt::magic_encode(static_cast<uint32_t>(plan->split));
+  args.div_tiles_p = lgt::magic_encode(static_cast<uint32_t>(plan->tiles_p));
+  args.p_mn = p_mn;
+  args.q_mn = q_mn;
+  args.swap = plan->swap;
+  args.c_bf16 = d.c_dtype == GEMM_BF16;
+  args.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (plan->ldc % 8 == 0);
+  args.ws_vec = (d.N % 4 == 0);
+  args.idesc = lgt::idesc_f16(d.a_dtype == GEMM_BF16 ? 1u : 0u, static_cast<uint32_t>(p_mn),
+                              static_cast<uint32_t>(q_mn), lgt::TILE_P, static_cast<uint32_t>(plan->bn));
+  const int grid = plan->num_units < plan->sms_grid ? plan->num_units : plan->sms_grid;
+  return lgt::launch_tc_gemm(args, plan->bn, grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t gemm_sync_status(gemm_plan_t* plan, void* stream) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  if (plan->device < 0 || !plan->d_status) return GEMM_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GEMM_ERR_CUDA;
+  lgt::DeviceStatus st;
+  if (cudaMemcpy(&st, plan->d_status, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (st.code != 0) {
+    if (cudaMemset(plan->d_status, 0, sizeof(st)) != cudaSuccess) return GEMM_ERR_CUDA;
+    return static_cast<gemm_status_t>(st.code);
+  }
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_destroy(gemm_plan_t* plan) {
+  if (!plan) return GEMM_OK;
+  if (plan->d_status) cudaFree(plan->d_status);
+  delete plan;
+  return GEMM_OK;
+}
+
+}  // extern "C"

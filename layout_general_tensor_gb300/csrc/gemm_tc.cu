@@ -1,0 +1,479 @@
+// Any-layout fp16 / bf16 GEMM on the sm_103a tensor cores.
+//
+// One persistent CTA per SM walks (tile, split) work units.  Warp roles:
+//   warp 0      TMA producer: one elected lane loads the P and Q tiles of each
+//               64-deep K block into a ring of shared-memory stages.
+//   warp 1      MMA issuer: allocates TMEM, one lane issues tcgen05.mma into a
+//               double-buffered fp32 accumulator and commits each stage back.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator, then either convert and
+//               store C, or add the fp32 partial into the workspace and let the
+//               last-arriving CTA of the tile convert and store.
+//
+// Operand layouts.  The Triton inThreadTranspose page ("Feature description")
+// fixes the problem: a dot operand that is not contiguous along K must still
+// reach the matrix unit as K-ordered fragments with conflict-free shared
+// memory reads; it transposes in registers.  Here the TMA box is laid along
+// the contiguous dimension and written with the 128-byte swizzle, and the
+// tcgen05 shared-memory descriptor is marked K-major or MN-major to match
+// (the SharedEncodingAttr order swap of the same page, "PR description",
+// item 1), so no operand is transposed by threads at all.
+//
+// Split-K: unit u covers tile u / split and K blocks
+// [(u % split) * kb_per_split, ...) -- the per-split K offset of the BitBLAS
+// TileLang page's T.Parallel / T.copy example.  With split > 1 each CTA takes
+// a contiguous run of units, so consecutive splits of one tile accumulate in
+// TMEM and only the run's total leaves the SM; the partial runs of a tile are
+// reduced in fp32 through L2 (red.global.add) and an arrival counter -- the
+// partials -> shared storage -> second reduction pattern of the IREE page
+// ("Add support for inter-subgroup multi_reduction"), lifted from subgroups
+// to CTAs.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace lgt {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kEpiWarp0 = 2;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kP_BYTES = TILE_P * TILE_K * 2;   // 16 KiB
+constexpr uint32_t kMnChunkBytes = 64 * TILE_K * 2;  // one 64-wide MN box, 64 K rows: 8 KiB
+constexpr int kTimeoutCode = 6;                      // GEMM_ERR_TIMEOUT
+
+template <int BN>
+struct Cfg {
+  static constexpr uint32_t Q_BYTES = BN * TILE_K * 2;
+  static constexpr uint32_t STAGE_BYTES = kP_BYTES + Q_BYTES;
+  static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+  static constexpr uint32_t TMEM_COLS = (2 * BN) < 32 ? 32 : 2 * BN;
+  static constexpr int CH = BN < 32 ? BN : 32;          // accumulator columns per tcgen05.ld
+  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], teardown
+  static constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr uint32_t SMEM_USED = MISC_OFF + 64;
+  static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
+  static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM allocation");
+};
+
+struct Group {
+  int32_t tile;
+  int32_t s0, s1;    // splits [s0, s1) of the tile
+  int32_t kb0, nkb;  // K blocks
+};
+
+// Work assignment.  split == 1: units are tiles, taken round-robin.
+// split > 1: CTA b takes the contiguous unit range
+// [b*U/G, (b+1)*U/G) and a group is a maximal run of one tile's splits.
+struct Sched {
+  int32_t u, u_end, step;
+  __device__ Sched(const TcArgs& a) {
+    const int32_t G = gridDim.x, b = blockIdx.x;
+    if (a.split == 1) {
+      u = b;
+      u_end = a.num_units;
+      step = G;
+    } else {
+      u = static_cast<int32_t>((static_cast<int64_t>(b) * a.num_units) / G);
+      u_end = static_cast<int32_t>((static_cast<int64_t>(b + 1) * a.num_units) / G);
+      step = 0;
+    }
+  }
+  __device__ bool next(const TcArgs& a, Group& g) {
+    if (u >= u_end) return false;
+    if (step) {
+      g.tile = u;
+      g.s0 = 0;
+      g.s1 = 1;
+      u += step;
+    } else {
+      uint32_t tile, s;
+      magic_divmod(static_cast<uint32_t>(u), a.div_split, tile, s);
+      const int32_t avail = u_end - u;
+      const int32_t s1 = min(a.split, static_cast<int32_t>(s) + avail);
+      g.tile = static_cast<int32_t>(tile);
+      g.s0 = static_cast<int32_t>(s);
+      g.s1 = s1;
+      u += s1 - static_cast<int32_t>(s);
+    }
+    g.kb0 = g.s0 * a.kb_per_split;
+    const int32_t kb1 = min(a.kb_total, g.s1 * a.kb_per_split);
+    g.nkb = kb1 > g.kb0 ? kb1 - g.kb0 : 0;
+    return true;
+  }
+};
+
+__device__ __forceinline__ void record_timeout(const TcArgs& a, volatile int* abort_flag, int where) {
+  *abort_flag = 1;
+  if (atomicCAS(&a.status->code, 0, kTimeoutCode) == 0) a.status->where = where;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
+  if (bf16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint16_t cvt1(float v, int bf16) {
+  if (bf16) {
+    __nv_bfloat16 h = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t*>(&h);
+  }
+  __half h = __float2half_rn(v);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// (m, n) ranges of a tile in C coordinates.
+__device__ __forceinline__ void tile_ranges(const TcArgs& a, int32_t tile, int bn, int32_t& tp, int32_t& tq,
+                                            int32_t& m0, int32_t& m1, int32_t& n0, int32_t& n1) {
+  uint32_t q, r;
+  magic_divmod(static_cast<uint32_t>(tile), a.div_tiles_p, q, r);
+  tp = static_cast<int32_t>(r);
+  tq = static_cast<int32_t>(q);
+  if (!a.swap) {
+    m0 = tp * TILE_P;
+    n0 = tq * bn;
+    m1 = min(a.M, m0 + TILE_P);
+    n1 = min(a.N, n0 + bn);
+  } else {
+    n0 = tp * TILE_P;
+    m0 = tq * bn;
+    n1 = min(a.N, n0 + TILE_P);
+    m1 = min(a.M, m0 + bn);
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcArgs a) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_base);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar0 = base + C::BAR_OFF;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 + b); };
+  const uint32_t teardown_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  volatile int* consumed_slot = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 12);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), kEpiThreads / 32);
+    }
+    mbar_init(teardown_bar, 1);
+    *abort_flag = 0;
+    *consumed_slot = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&a.tm_p);
+    tma_prefetch_desc(&a.tm_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int issued = 0;  // producer lane: K blocks whose loads were issued
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      Sched sched(a);
+      Group g;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      while (ok && sched.next(a, g)) {
+        int32_t tp, tq, m0, m1, n0, n1;
+        tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
+        const int32_t prow = tp * TILE_P, qrow = tq * BN;
+        for (int kb = 0; kb < g.nkb; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, a.wait_limit_ns, abort_flag)) {
+            if (!*abort_flag) record_timeout(a, abort_flag, 0 * 16 + 1);
+            ok = false;
+            break;
+          }
+          const uint32_t sp = base + stage * C::STAGE_BYTES;
+          const uint32_t sq = sp + kP_BYTES;
+          const int32_t k0 = (g.kb0 + kb) * TILE_K;
+          mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
+          if (!a.p_mn) {
+            tma_load_2d(sp, &a.tm_p, full_bar(stage), k0, prow);
+          } else {
+            tma_load_2d(sp, &a.tm_p, full_bar(stage), prow, k0);
+            tma_load_2d(sp + kMnChunkBytes, &a.tm_p, full_bar(stage), prow + 64, k0);
+          }
+          if (!a.q_mn) {
+            tma_load_2d(sq, &a.tm_q, full_bar(stage), k0, qrow);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sq + j * kMnChunkBytes, &a.tm_q, full_bar(stage), qrow + 64 * j, k0);
+          }
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      Sched sched(a);
+      Group g;
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc_iter = 0;
+      int consumed = 0;
+      bool ok = true;
+      // Per-MMA (K = 16) start-address advance inside a stage, and the
+      // descriptor offsets: K-major rows are 128 bytes along K (advance 32 B
+      // per 16 elements, LBO unused); MN-major tiles hold 128-byte rows along
+      // M/N, one per k (advance 16 rows = 2 KiB), 64-wide chunks 8 KiB apart.
+      const uint32_t p_step = a.p_mn ? 2048u : 32u;
+      const uint32_t q_step = a.q_mn ? 2048u : 32u;
+      const uint32_t p_lbo = a.p_mn ? kMnChunkBytes : 16u;
+      const uint32_t q_lbo = a.q_mn ? kMnChunkBytes : 16u;
+      while (ok && sched.next(a, g)) {
+        if (g.nkb == 0) continue;
+        const int buf = acc_iter & 1;
+        const uint32_t acc_phase = (acc_iter >> 1) & 1;
+        if (!mbar_wait_bounded(acce_bar(buf), acc_phase ^ 1u, a.wait_limit_ns, abort_flag)) {
+          if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 3);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < g.nkb; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, a.wait_limit_ns, abort_flag)) {
+            if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 0);
+            ok = false;
+            break;
+          }
+          ++consumed;
+          tc_fence_after();
+          const uint32_t sp = base + stage * C::STAGE_BYTES;
+          const uint32_t sq = sp + kP_BYTES;
+#pragma unroll
+          for (int k = 0; k < TILE_K / 16; ++k) {
+            const uint64_t pd = sw128_desc(sp + k * p_step, p_lbo, 1024u);
+            const uint64_t qd = sw128_desc(sq + k * q_step, q_lbo, 1024u);
+            tc_mma_f16_ss(d_tmem, pd, qd, a.idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(accf_bar(buf));
+        ++acc_iter;
+      }
+      *consumed_slot = consumed;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int row = q4 * 32 + lane;           // accumulator row (TMEM lane)
+    const int et = threadIdx.x - kEpiWarp0 * 32;
+    Sched sched(a);
+    Group g;
+    int acc_iter = 0;
+    bool ok = true;
+    while (ok && sched.next(a, g)) {
+      int32_t tp, tq, m0, m1, n0, n1;
+      tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
+      const bool full_tile = (g.s0 == 0 && g.s1 == a.split);
+      if (g.nkb > 0) {
+        const int buf = acc_iter & 1;
+        const uint32_t acc_phase = (acc_iter >> 1) & 1;
+        const bool got = mbar_wait_bounded(accf_bar(buf), acc_phase, a.wait_limit_ns, abort_flag);
+        if (!got && !*abort_flag) record_timeout(a, abort_flag, 2 * 16 + 2);
+        // all epilogue threads leave together if any of them gave up
+        if (named_bar_or(1, kEpiThreads, !got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(buf * BN);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += C::CH) {
+          uint32_t v[C::CH];
+          if constexpr (C::CH == 32) {
+            tc_ld_32x32b_x32(t_row + c0, v);
+          } else {
+            tc_ld_32x32b_x16(t_row + c0, v);
+          }
+          tc_wait_ld();
+          if (!a.swap) {
+            const int m = m0 + row;
+            const int nb = n0 + c0;
+            if (m < m1) {
+              if (full_tile) {
+                uint16_t* crow = reinterpret_cast<uint16_t*>(a.c) + static_cast<int64_t>(m) * a.ldc;
+                if (a.c_vec && nb + C::CH <= n1) {
+#pragma unroll
+                  for (int j = 0; j < C::CH; j += 8) {
+                    st_global_v4(crow + nb + j, pack2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), a.c_bf16),
+                                 pack2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), a.c_bf16),
+                                 pack2(__uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]), a.c_bf16),
+                                 pack2(__uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]), a.c_bf16));
+                  }
+                } else {
+#pragma unroll
+                  for (int j = 0; j < C::CH; ++j)
+                    if (nb + j < n1) crow[nb + j] = cvt1(__uint_as_float(v[j]), a.c_bf16);
+                }
+              } else {
+                float* wrow = a.ws + static_cast<int64_t>(m) * a.N;
+                if (a.ws_vec && nb + C::CH <= n1) {
+#pragma unroll
+                  for (int j = 0; j < C::CH; j += 4)
+                    red_add_v4_f32(wrow + nb + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                   __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                } else {
+#pragma unroll
+                  for (int j = 0; j < C::CH; ++j)
+                    if (nb + j < n1) red_add_f32(wrow + nb + j, __uint_as_float(v[j]));
+                }
+              }
+            }
+          } else {
+            const int n = n0 + row;
+            if (n < n1) {
+              if (full_tile) {
+                uint16_t* cc = reinterpret_cast<uint16_t*>(a.c) + n;
+#pragma unroll
+                for (int j = 0; j < C::CH; ++j) {
+                  const int m = m0 + c0 + j;
+                  if (m < m1) cc[static_cast<int64_t>(m) * a.ldc] = cvt1(__uint_as_float(v[j]), a.c_bf16);
+                }
+              } else {
+                float* wc = a.ws + n;
+#pragma unroll
+                for (int j = 0; j < C::CH; ++j) {
+                  const int m = m0 + c0 + j;
+                  if (m < m1) red_add_f32(wc + static_cast<int64_t>(m) * a.N, __uint_as_float(v[j]));
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(buf));
+        ++acc_iter;
+      }
+      if (!full_tile) {
+        // Publish this run's partial, count its splits, and let the CTA that
+        // completes the count convert the tile.
+        __threadfence();
+        named_bar_sync(1, kEpiThreads);
+        bool mine_last = false;
+        if (et == 0) {
+          const int old = atomicAdd(&a.counters[g.tile], g.s1 - g.s0);
+          mine_last = (old + (g.s1 - g.s0) == a.split);
+        }
+        if (named_bar_or(1, kEpiThreads, mine_last)) {
+          __threadfence();
+          const int rows = m1 - m0, cols = n1 - n0;
+          const int total = rows * cols;
+          for (int i = et; i < total; i += kEpiThreads) {
+            const int r = i / cols, cidx = i - r * cols;
+            float* w = a.ws + static_cast<int64_t>(m0 + r) * a.N + (n0 + cidx);
+            const float s = __ldcg(w);
+            __stcg(w, 0.0f);
+            reinterpret_cast<uint16_t*>(a.c)[static_cast<int64_t>(m0 + r) * a.ldc + (n0 + cidx)] = cvt1(s, a.c_bf16);
+          }
+          named_bar_sync(1, kEpiThreads);
+          if (et == 0) a.counters[g.tile] = 0;
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  if (*abort_flag) {
+    if (warp == 0 && lane == 0) {
+      // Let every TMA load still in flight land before the CTA exits.
+      volatile int no_abort = 0;
+      const int consumed = *consumed_slot;
+      for (int it = consumed; it < issued; ++it)
+        mbar_wait_bounded(full_bar(it % C::STAGES), (it / C::STAGES) & 1, a.wait_limit_ns, &no_abort);
+    }
+  }
+  if (warp == 1 && lane == 0) {
+    // Wait until every MMA this CTA issued has completed.
+    volatile int no_abort = 0;
+    tc_commit(teardown_bar);
+    mbar_wait_bounded(teardown_bar, 0, a.wait_limit_ns, &no_abort);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+template <int BN>
+cudaError_t launch_bn(const TcArgs& args, int grid, cudaStream_t stream) {
+  using C = Cfg<BN>;
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::SMEM_ALLOC));
+  if (e != cudaSuccess) return e;
+  tc_gemm_kernel<BN><<<grid, kThreads, C::SMEM_ALLOC, stream>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t tc_gemm_smem_bytes(int bn) {
+  switch (bn) {
+    case 16: return Cfg<16>::SMEM_ALLOC;
+    case 32: return Cfg<32>::SMEM_ALLOC;
+    case 64: return Cfg<64>::SMEM_ALLOC;
+    case 128: return Cfg<128>::SMEM_ALLOC;
+    case 256: return Cfg<256>::SMEM_ALLOC;
+    default: return 0;
+  }
+}
+
+cudaError_t launch_tc_gemm(const TcArgs& args, int bn, int grid, cudaStream_t stream) {
+  switch (bn) {
+    case 16: return launch_bn<16>(args, grid, stream);
+    case 32: return launch_bn<32>(args, grid, stream);
+    case 64: return launch_bn<64>(args, grid, stream);
+    case 128: return launch_bn<128>(args, grid, stream);
+    case 256: return launch_bn<256>(args, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace lgt

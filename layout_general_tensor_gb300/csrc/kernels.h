@@ -1,0 +1,73 @@
+// Kernel argument blocks and launchers shared between the C ABI (api.cu) and
+// the kernel translation units.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "intmath.h"
+
+namespace lgt {
+
+// MMA tile: 128 rows on the P side (the operand whose rows map to TMEM
+// lanes), BN rows on the Q side, 64 elements of K per pipeline stage.
+constexpr int TILE_P = 128;
+constexpr int TILE_K = 64;
+
+// Instruction descriptor, kind::f16, fp32 accumulator, dense.
+//   bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (0 = f16,
+//   1 = bf16); 15 / 16 A / B major (0 = K-major, 1 = MN-major);
+//   17-22 N >> 3; 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_bf16, uint32_t a_mn, uint32_t b_mn, uint32_t M,
+                                                 uint32_t N) {
+  return (1u << 4) | (ab_bf16 << 7) | (ab_bf16 << 10) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
+}
+
+// Status word written by kernels that give up a bounded wait.
+struct DeviceStatus {
+  int32_t code;   // 0 or GEMM_ERR_TIMEOUT
+  int32_t where;  // role * 16 + barrier kind of the first wait that gave up
+};
+
+// Tensor-core GEMM over (tile, split) work units.  P is the MMA's M-side
+// operand, Q its N-side operand.  Normal mode: P = A (rows m), Q = B
+// (rows n).  Swapped mode (skinny M): P = B (rows n), Q = A (rows m), and the
+// accumulator holds C^T.
+struct TcArgs {
+  CUtensorMap tm_p;
+  CUtensorMap tm_q;
+  void* c;
+  float* ws;            // fp32 partial sums [M][N] (split > 1)
+  int32_t* counters;    // per-tile arrival counters (split > 1)
+  DeviceStatus* status;
+  uint64_t wait_limit_ns;
+  int64_t ldc;
+  int32_t M, N, K;
+  int32_t tiles_p, tiles_q;
+  int32_t split, kb_per_split, kb_total;
+  int32_t num_units;
+  MagicDiv div_split;    // unit -> (tile, split)
+  MagicDiv div_tiles_p;  // tile -> (tile_p, tile_q)
+  int32_t p_mn, q_mn;    // 1: operand tile is MN-major in shared memory
+  int32_t swap;
+  int32_t c_bf16;
+  int32_t c_vec;         // C rows allow 16-byte vector stores
+  int32_t ws_vec;        // workspace rows allow 16-byte vector reductions
+  uint32_t idesc;
+};
+
+// Returns a cudaError_t; `bn` selects the kernel instance.
+cudaError_t launch_tc_gemm(const TcArgs& args, int bn, int grid, cudaStream_t stream);
+size_t tc_gemm_smem_bytes(int bn);
+
+// Copy `rows` rows of `row_bytes` bytes from a source with row pitch
+// `src_pitch` (any 2-byte alignment) into a destination with a 16-byte
+// aligned pitch `dst_pitch`.
+cudaError_t launch_repack_rows(const void* src, int64_t src_pitch, void* dst, int64_t dst_pitch, int64_t rows,
+                               int64_t row_bytes, cudaStream_t stream);
+
+cudaError_t launch_magic_divmod(const uint32_t* n, size_t count, MagicDiv m, uint32_t* q, uint32_t* r,
+                                cudaStream_t stream);
+
+}  // namespace lgt

@@ -1,0 +1,182 @@
+"""CPU tests of the C-ABI library: it loads, exports every entry point the
+header declares, and its host-side integer logic (split-K rule, perpDim
+permutation, magic division, planner decisions, argument validation) agrees
+bit-exactly with the oracle and with plain integer division.  No GPU work."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from layout_general_tensor_gb300 import build
+    build.build()
+    import layout_general_tensor_gb300 as m
+    return m
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(gemm_[a-z0-9_]+)\s*\(", text, re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert {"gemm_create", "gemm_run", "gemm_destroy", "gemm_workspace_size"} <= declared
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for name in sorted(declared):
+        assert hasattr(raw, name), f"libgemm.so does not export {name}"
+    assert set(lib.EXPORTS) == declared
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.gemm_status_string(code).startswith("GEMM_")
+
+
+def test_splitk_rule_matches_oracle(lib, golden_dir):
+    rng = np.random.default_rng(3)
+    for _ in range(5000):
+        M, N, K = (int(x) for x in rng.integers(1, 70000, 3))
+        sms = int(rng.integers(1, 300))
+        bm, bn = int(rng.choice([64, 128, 256])), int(rng.choice([64, 128, 256]))
+        bk = int(rng.choice([32, 64, 128]))
+        assert lib.gemm_splitk_auto(M, N, K, bm, bn, bk, sms, 0.05) == \
+            oracle.splitk_factor(M, N, K, bm, bn, bk, sms, 0.05)
+    for line in open(os.path.join(golden_dir, "splitk_traces.txt")):
+        if line.strip() and not line.startswith("#"):
+            head, want = line.split("->")
+            M, N, K, sms = map(int, head.split()[:4])
+            assert lib.gemm_splitk_auto(M, N, K, 128, 128, 64, sms, 0.05) == int(want)
+
+
+def test_perm_matches_oracle(lib):
+    for B in range(1, 129):
+        for S in range(1, B + 1):
+            if B % S:
+                continue
+            count = 3 * B + B // 2          # two full blocks and a partial tail
+            want = oracle.perm_apply(count, B, S)
+            got = [lib.gemm_perm_fwd(i, count, B, S) for i in range(count)]
+            assert got == want, (B, S)
+            assert [lib.gemm_perm_inv(v, count, B, S) for v in got] == list(range(count))
+
+
+def test_magic_division_bit_exact(lib):
+    divisors = [1, 2, 3, 5, 7, 31, 64, 128, 148, 152, 1000, 3000, 4095, 65537, 1 << 20, (1 << 31) - 1, 1 << 30,
+                12345679]
+    rng = np.random.default_rng(9)
+    top = 1 << 31
+    for d in divisors:
+        parts = [np.arange(0, 1 << 20, dtype=np.uint32),
+                 np.arange(top - (1 << 20), top, dtype=np.uint32),
+                 rng.integers(0, top, 1 << 20, dtype=np.uint32)]
+        ks = np.arange(1, min(top // d, 1 << 16), dtype=np.uint64) if d > 1 else np.arange(1, 10, dtype=np.uint64)
+        edges = np.concatenate([ks * d - 1, ks * d, ks * d + 1])
+        parts.append(edges[edges < top].astype(np.uint32))
+        n = np.concatenate(parts)
+        q, r = lib.gemm_magic_divmod_host(n, d)
+        assert np.array_equal(q, n // np.uint32(d)), d
+        assert np.array_equal(r, n % np.uint32(d)), d
+    # exhaustive over the full 31-bit range for one small divisor, in chunks
+    d = 148
+    for start in range(0, top, 1 << 27):
+        n = np.arange(start, start + (1 << 27), dtype=np.uint32)
+        q, r = lib.gemm_magic_divmod_host(n, d)
+        assert np.array_equal(q, n // np.uint32(d))
+
+
+def test_magic_division_rejects_out_of_range(lib):
+    with pytest.raises(lib.GemmError):
+        lib.gemm_magic_divmod_host(np.array([1 << 31], dtype=np.uint32), 3)
+    with pytest.raises(lib.GemmError):
+        lib.gemm_magic_divmod_host(np.array([5], dtype=np.uint32), 0)
+
+
+def _plan_for(lib, case, num_sms=148):
+    lda, ldb, ldc = case.dense_ld()
+    desc = lib.make_desc(case.M, case.N, case.K, case.a_layout, case.b_layout, case.a_dtype, case.b_dtype,
+                         case.c_dtype, lda=case.lda, ldb=case.ldb, ldc=case.ldc, split_k=case.split_k,
+                         num_sms=num_sms)
+    st, h = lib.gemm_create_status(desc)
+    return st, h
+
+
+@pytest.mark.parametrize("case", [c for c in wl.WORKLOADS if c.b_dtype != wl.INT4], ids=lambda c: c.name)
+def test_planner_decisions(lib, case):
+    st, h = _plan_for(lib, case)
+    assert st == lib.GEMM_OK
+    try:
+        info = lib.gemm_query(h)
+        want_split = case.split_k or oracle.splitk_factor(case.M, case.N, case.K, 128, 128, 64, 148)
+        assert info.split_k == want_split
+        assert info.swap_ab == (1 if case.M <= 64 else 0)
+        lda, ldb, _ = case.dense_ld()
+        assert info.repack_a == ((lda * 2) % 16 != 0)
+        assert info.repack_b == ((ldb * 2) % 16 != 0)
+        ws = lib.gemm_workspace_size(h)
+        if info.split_k > 1:
+            assert ws >= case.M * case.N * 4
+        if info.repack_a:
+            assert ws >= (case.K * ((case.M + 7) // 8 * 8) * 2 if case.a_layout == wl.MN_CONTIG
+                          else case.M * ((case.K + 7) // 8 * 8) * 2)
+        # K blocks per split follow Ks = ceil(K / (f * 64)) * 64
+        assert info.k_per_split == -(-case.K // (info.split_k * 64)) * 64
+    finally:
+        lib.gemm_destroy(h)
+
+
+def test_planner_skinny_and_irregular_factors(lib):
+    # the SM-waste rule's values at 148 SMs for the skinny bf16 and int4-shaped problems
+    desc = lib.make_desc(64, 4096, 16384, split_k=0, num_sms=148)
+    h = lib.gemm_create(desc)
+    assert lib.gemm_query(h).split_k == 128
+    lib.gemm_destroy(h)
+    desc = lib.make_desc(4095, 3000, 2880, wl.MN_CONTIG, wl.MN_CONTIG, split_k=0, num_sms=160)
+    h = lib.gemm_create(desc)
+    assert lib.gemm_query(h).split_k == 4
+    lib.gemm_destroy(h)
+
+
+def test_invalid_arguments(lib):
+    bad = [
+        lib.make_desc(-1, 4, 4, num_sms=148),
+        lib.make_desc(4, 4, 4, a_layout=2, num_sms=148),
+        lib.make_desc(4, 4, 4, lda=3, num_sms=148),
+        lib.make_desc(4, 4, 4, a_dtype=lib.GEMM_F16, b_dtype=lib.GEMM_BF16, num_sms=148),
+        lib.make_desc(4, 4, 4, c_dtype=lib.GEMM_F32, num_sms=148),
+        lib.make_desc(4, 4, 4, flags=1, num_sms=148),
+        lib.make_desc(4, 4, 4, split_k=-2, num_sms=148),
+        lib.make_desc(4, 4, 4, a_dtype=lib.GEMM_BF16, b_dtype=lib.GEMM_INT4, c_dtype=lib.GEMM_F16, num_sms=148),
+    ]
+    for d in bad:
+        st, h = lib.gemm_create_status(d)
+        assert st == lib.GEMM_ERR_INVALID_ARG and h is None
+    assert lib._lib.gemm_create(None, None) == lib.GEMM_ERR_INVALID_ARG
+    assert lib._lib.gemm_query(None, None) == lib.GEMM_ERR_INVALID_ARG
+
+
+def test_no_device_paths(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    st, h = lib.gemm_create_status(lib.make_desc(128, 128, 128, num_sms=0))
+    assert st == lib.GEMM_ERR_CUDA and h is None
+    h = lib.gemm_create(lib.make_desc(128, 128, 128, num_sms=148))
+    assert lib.gemm_run(h, 16, 16, 16) == lib.GEMM_ERR_CUDA
+    lib.gemm_destroy(h)
