@@ -59,7 +59,7 @@ class gemm_info_t(ctypes.Structure):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m layout_general_tensor_gb300.build` "
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python layout_general_tensor_gb300/build.py` "
                           "(there is no CPU fallback)")
     lib = ctypes.CDLL(LIB_PATH)
     P = ctypes.c_void_p

@@ -2,7 +2,9 @@
 
 Each translation unit compiles in parallel; the shared library links against
 the CUDA runtime only (driver entry points are resolved at run time).  Run as
-``python -m layout_general_tensor_gb300.build`` or call :func:`build`.
+``python layout_general_tensor_gb300/build.py`` or call :func:`build` (the
+package itself loads the built library on import, so this file is loaded by
+path).
 """
 from __future__ import annotations
 

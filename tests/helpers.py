@@ -8,8 +8,8 @@ import workloads as wl
 
 
 def lib():
-    from layout_general_tensor_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import layout_general_tensor_gb300 as m
     return m
 

@@ -17,10 +17,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
-    from layout_general_tensor_gb300 import build
-    build.build()
-    import layout_general_tensor_gb300 as m
-    return m
+    import helpers
+    return helpers.lib()
 
 
 def _declared_functions():
