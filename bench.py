@@ -1,0 +1,434 @@
+"""Benchmark of the any-layout GEMM through its C ABI.
+
+A step is one gemm_run of the headline workload (bf16 4096 x 4096 x 4096,
+A K-contiguous, B N-contiguous, fp32 accumulation) on inputs resident in HBM;
+L2 is flushed (a 256 MiB write) between timed steps, outside the timed
+events.  The same run also measures the other workloads (fp16 256^3 in four
+layouts, the skinny split-K GEMM, the irregular GEMM) and reports them under
+"configs".  One JSON line on stdout (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the GEMM
+has no exchange step); value = FLOPs of all ranks / max-over-ranks time.
+--impl reference times the CPU oracle (fp64, numpy) on the host cores on a
+bounded row-block sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s & % dense-BF16 peak per shape/layout; GB/s & % HBM (skinny/int4)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["layout_general_tensor_gb300/csrc/gemm_tc.cu", "layout_general_tensor_gb300/csrc/ptx.cuh",
+                  "layout_general_tensor_gb300/csrc/kernels.h"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,utilization.gpu,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.dev)], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[4:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r[2] > 0] or rows
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in loaded:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def algorithmic_bytes(case):
+    import workloads as wl
+    esz = 2
+    a = case.M * case.K * esz
+    b = (case.N * case.K // 2) if case.b_dtype == wl.INT4 else case.N * case.K * esz
+    c = case.M * case.N * esz
+    extra = 0
+    if case.b_dtype == wl.INT4:
+        g = case.K // case.group_size
+        extra = case.N * g * 2 * (2 if case.zero_value is not None else 1)
+    return a + b + c + extra
+
+
+class DeviceCase:
+    """Inputs of one workload resident on the device plus its plan."""
+
+    def __init__(self, case, seed=0):
+        import torch
+        import workloads as wl
+        import layout_general_tensor_gb300 as lgt
+        self.case = case
+        inp = wl.make_inputs(case, seed)
+        self.host = inp
+        self.A = inp.A.cuda()
+        self.B = inp.B.cuda()
+        self.C = torch.empty(case.M * inp.ldc, dtype=wl.TORCH_DTYPE[case.c_dtype], device="cuda")
+        self.scales = inp.scales.cuda() if inp.scales is not None else None
+        self.zeros = inp.zeros.cuda() if inp.zeros is not None else None
+        lda, ldb, ldc = case.dense_ld()
+        desc = lgt.make_desc(case.M, case.N, case.K, case.a_layout, case.b_layout, case.a_dtype, case.b_dtype,
+                             case.c_dtype, lda=lda, ldb=0 if case.b_dtype == wl.INT4 else ldb, ldc=ldc,
+                             split_k=case.split_k, group_size=case.group_size if case.b_dtype == wl.INT4 else 0,
+                             num_sms=148)
+        self.g = lgt.Gemm(desc)
+        self.launches_per_run = 1 + int(self.g.info.repack_a) + int(self.g.info.repack_b)
+
+    def run(self):
+        self.g.run(self.A, self.B, self.C, self.scales, self.zeros)
+
+
+def time_steps(fn, steps, warmup, flush):
+    """Per-step CUDA-event timing on the current stream; L2 flushed before
+    every step outside the events.  Returns the list of step times in ms."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in evs:
+        flush()
+        s.record()
+        fn()
+        e.record()
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+def cpu_cores():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            n = min(n, int(v))
+    return n
+
+
+def oracle_row_block(case, inp, rows):
+    """The oracle on the first `rows` rows of C (A is K-contiguous, so those
+    rows of A are a prefix of its storage)."""
+    import oracle
+    import workloads as wl
+    assert case.a_layout == wl.K_CONTIG
+    return oracle.gemm(rows, case.N, case.K, inp.A[: rows * inp.lda], case.a_layout, inp.lda, case.a_dtype,
+                       inp.B, case.b_layout, inp.ldb, case.b_dtype, scales=inp.scales, zeros=inp.zeros,
+                       group=case.group_size)
+
+
+def cpu_baseline(case, inp, budget_s=10.0, rows=512):
+    """Time the oracle on row blocks of the workload for about `budget_s`."""
+    done = 0
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle_row_block(case, inp, rows)
+        done += 2 * rows * case.N * case.K
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    return {"value": done / el / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{reps} x oracle.gemm on rows 0..{rows - 1} of C ({rows}x{case.N}x{case.K}, fp64 numpy "
+                      f"matmul after per-layout gather), {el:.1f} s"}
+
+
+# ------------------------------------------------------------------ arms
+
+def reference_arm(args, case):
+    import workloads as wl
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inp = wl.make_inputs(case, seed=0)
+    rows = 256
+    for _ in range(args.warmup):
+        oracle_row_block(case, inp, rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_row_block(case, inp, rows)
+        times.append(time.perf_counter() - t0)
+    flops = 2 * rows * case.N * case.K
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    sample = f"each step: oracle.gemm on rows 0..{rows - 1} of C ({rows}x{case.N}x{case.K}, fp64 numpy matmul)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K, "sample_rows": rows},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def gpu_arm(args, headline):
+    import torch
+    import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    peaks, peak_src = load_peaks()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    dc = DeviceCase(headline)
+    sampler = ClockSampler(local)
+    sampler.start()
+    # warm-up (also lets the clock sampler see the GPU under load)
+    t_soak = time.perf_counter()
+    for _ in range(max(args.warmup, 3)):
+        flush()
+        dc.run()
+    torch.cuda.synchronize()
+    while time.perf_counter() - t_soak < args.soak_seconds:
+        dc.run()
+        torch.cuda.synchronize()
+    st = dc.g.sync_status()
+    assert st == 0, f"device status {st}"
+
+    barrier()
+    times = time_steps(dc.run, args.steps, 0, flush)
+    barrier()
+    clocks = sampler.stop()
+    total_ms = sum(times)
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops = headline.flops()
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    avg_launch_ms = total_ms / args.steps
+    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+
+    # end to end through the C ABI with host buffers: pinned H2D of A and B,
+    # the GEMM, D2H of C, all inside the timed events.
+    A_h = dc.host.A.pin_memory()
+    B_h = dc.host.B.pin_memory()
+    C_h = torch.empty(dc.C.numel(), dtype=dc.C.dtype).pin_memory()
+
+    def e2e_step():
+        dc.A.copy_(A_h, non_blocking=True)
+        dc.B.copy_(B_h, non_blocking=True)
+        dc.run()
+        C_h.copy_(dc.C, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_times = time_steps(e2e_step, e2e_steps, 2, flush)
+    e2e_total = sum(e2e_times)
+    if dist is not None:
+        t = torch.tensor([e2e_total], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = world * flops * e2e_steps / (e2e_total * 1e-3) / 1e12
+
+    # the other workloads, same timing discipline
+    configs = {}
+    for case in wl.WORKLOADS:
+        if case.name == headline.name:
+            continue
+        if case.b_dtype == wl.INT4:
+            configs[case.name] = {"status": "not measured: the int4 path is not built"}
+            continue
+        d = DeviceCase(case)
+        ts = time_steps(d.run, max(args.steps, 20), max(args.warmup, 3), flush)
+        ms = statistics.median(ts)
+        tf = case.flops() / (ms * 1e-3) / 1e12
+        gbs = algorithmic_bytes(case) / (ms * 1e-3) / 1e9
+        configs[case.name] = {"ms_median": ms, "tflops": tf, "pct_bf16_peak": 100 * tf / peaks["bf16_tflops"],
+                              "gbs": gbs, "pct_hbm": 100 * gbs / peaks["hbm_gbs"], "split_k": d.g.info.split_k,
+                              "swap_ab": d.g.info.swap_ab, "launches_per_run": d.launches_per_run,
+                              "algorithmic_bytes": algorithmic_bytes(case), "flop": case.flops()}
+        st = d.g.sync_status()
+        assert st == 0, f"device status {st} on {case.name}"
+        d.g.close()
+        del d
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(headline, dc.host, budget_s=args.cpu_seconds)
+
+    traffic = recorded_traffic(headline.name)
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": headline.name, "M": headline.M, "N": headline.N, "K": headline.K,
+                   "a_layout": "K-contiguous", "b_layout": "N-contiguous", "accumulate": "fp32",
+                   "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+                   "inputs": "seeded synthetic N(0,1) bf16", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": f"tc_gemm_kernel<{dc.g.info.tile_n}>",
+                     "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
+                     else "fallback 1.9 PFLOP/s bf16 burst"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": A_h.numel() * 2 + B_h.numel() * 2,
+                "d2h_bytes_per_step": C_h.numel() * 2, "steps": e2e_steps},
+        "gpu_launches": args.steps * dc.launches_per_run,
+        "clocks": clocks,
+        "configs": configs,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dc.g.close()
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def profile_case(args):
+    import torch
+    import workloads as wl
+    import __graft_entry__
+    __graft_entry__.build()
+    case = {c.name: c for c in wl.WORKLOADS}[args.profile_case]
+    d = DeviceCase(case)
+    for _ in range(args.steps):
+        d.run()
+    torch.cuda.synchronize()
+    st = d.g.sync_status()
+    print(json.dumps({"profile_case": case.name, "runs": args.steps, "status": st}))
+    return 0 if st == 0 else 1
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--soak-seconds", type=float, default=1.0,
+                    help="untimed load before the timed steps, so the clock samples see the GPU busy")
+    ap.add_argument("--profile-case", default=None,
+                    help="run only this workload --steps times, untimed (for profiler captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    import workloads as wl
+    headline = wl.SQUARE_BF16
+    if args.profile_case:
+        return profile_case(args)
+    if args.impl == "reference":
+        return reference_arm(args, headline)
+    return gpu_arm(args, headline)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
