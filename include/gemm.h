@@ -109,6 +109,33 @@ gemm_status_t gemm_query(const gemm_plan_t* plan, gemm_info_t* info);
 gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C, const void* scales,
                        const void* zeros, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Run a plan without any caller-provided device memory.  (No counterpart on
+ * the source pages: this is an interface addition of this library.)
+ *
+ * For callers that cannot allocate device memory when they run the GEMM --
+ * e.g. an inference-engine plugin whose enqueue call must not allocate, a
+ * serving loop that cannot afford a cudaMalloc / cudaFree stall, or code that
+ * runs after another allocator has reserved all free device memory -- and so
+ * cannot hand gemm_run a workspace.  The split-K partial sums and tile
+ * counters then live in a fixed 8 MiB array in the library's own device
+ * memory, held on every GPU that loads the library until the process exits.
+ *
+ * - Nothing is allocated by this call (no cudaMalloc / cudaFree); the plan
+ *   itself is made beforehand with gemm_create.
+ * - The first call on a device resolves the array's address on that device
+ *   (cudaGetSymbolAddress), so make that first call before any stream
+ *   capture.  The plan's device must be current.
+ * - Plans whose split-K region (M*N*4 bytes plus the tile counters) exceeds
+ *   8 MiB are rejected with GEMM_ERR_WORKSPACE.  Plans that need a realigned
+ *   operand copy (a leading dimension that is not a multiple of 16 bytes) or
+ *   operands not 16-byte aligned are rejected with GEMM_ERR_UNSUPPORTED.
+ * - All calls on a device share the array; each call clears the part it uses
+ *   (cudaMemsetAsync on `stream`) before its kernel.  Calls whose work
+ *   overlaps on the GPU (different streams, no ordering between them) race
+ *   on the array and give wrong results.
+ * - A device-side timeout is reported by gemm_sync_status, as for gemm_run. */
+gemm_status_t gemm_run_static_scratch(const gemm_plan_t* plan, const void* A, const void* B, void* C, void* stream);
+
 /* Wait for `stream`, then read and clear the plan's device status word:
  * GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel of this plan gave up a wait. */
 gemm_status_t gemm_sync_status(gemm_plan_t* plan, void* stream);

@@ -31,7 +31,8 @@ GEMM_F32 = 3
 
 # Every entry point include/gemm.h declares.
 EXPORTS = (
-    "gemm_create", "gemm_workspace_size", "gemm_query", "gemm_run", "gemm_sync_status", "gemm_destroy",
+    "gemm_create", "gemm_workspace_size", "gemm_query", "gemm_run", "gemm_run_static_scratch",
+    "gemm_sync_status", "gemm_destroy",
     "gemm_splitk_auto", "gemm_perm_fwd", "gemm_perm_inv", "gemm_magic_divmod_host",
     "gemm_magic_divmod_device", "gemm_status_string",
 )
@@ -68,6 +69,7 @@ def _load():
         "gemm_workspace_size": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_size_t)]),
         "gemm_query": (ctypes.c_int, [P, ctypes.POINTER(gemm_info_t)]),
         "gemm_run": (ctypes.c_int, [P, P, P, P, P, P, P, ctypes.c_size_t, P]),
+        "gemm_run_static_scratch": (ctypes.c_int, [P, P, P, P, P]),
         "gemm_sync_status": (ctypes.c_int, [P, P]),
         "gemm_destroy": (ctypes.c_int, [P]),
         "gemm_splitk_auto": (ctypes.c_int32, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
@@ -135,6 +137,13 @@ def gemm_run(plan: int, A: int, B: int, C: int, scales: int = 0, zeros: int = 0,
     """Raw entry point: integer device addresses; returns the status code."""
     return _lib.gemm_run(plan, A or None, B or None, C or None, scales or None, zeros or None, workspace or None,
                          workspace_bytes, stream or None)
+
+
+def gemm_run_static_scratch(plan: int, A: int, B: int, C: int, stream: int = 0) -> int:
+    """Run `plan` using the library's fixed device scratch instead of a
+    caller workspace (for callers that cannot allocate device memory when
+    they run the GEMM).  Integer device addresses; returns the status."""
+    return _lib.gemm_run_static_scratch(plan, A or None, B or None, C or None, stream or None)
 
 
 def gemm_sync_status(plan: int, stream: int = 0) -> int:

@@ -12,30 +12,10 @@
 
 #include "../../include/gemm.h"
 #include "kernels.h"
+#include "plan.h"
 
 using lgt::MagicDiv;
 
-struct gemm_plan {
-  gemm_desc_t d;
-  int device;        // device current at create time, -1 if none was queried
-  int sms_rule;      // SM count fed to the split-K rule
-  int sms_grid;      // persistent grid size (device SMs), 0 without a device
-  int kernel;        // 0: tensor-core any-layout
-  int swap;
-  int bn;
-  int split, kb_per_split, kb_total;
-  int tiles_p, tiles_q, num_units;
-  int64_t lda, ldb, ldc;
-  int a_mn, b_mn;
-  // operand repacking (leading dimension not a multiple of 16 bytes)
-  int repack_a, repack_b;
-  int64_t a_rows, a_row_elems, b_rows, b_row_elems;  // storage rows of each operand
-  int64_t a_pack_ld, b_pack_ld;
-  size_t off_partial, off_counters, off_pack_a, off_pack_b, ws_bytes;
-  size_t ws_bytes_misaligned;
-  lgt::DeviceStatus* d_status;
-  uint64_t wait_limit_ns;
-};
 
 namespace {
 
@@ -62,36 +42,6 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   });
   return fn;
-}
-
-// 2-D tensor map over a 16-bit operand.  K-major: dims {K, rows}, box
-// {64, box_rows}.  MN-major: dims {mn, K}, box {64, 64}.  128-byte swizzle,
-// zero fill outside the tensor (ragged M / N / K tails).
-bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major, int64_t rows_or_mn, int64_t K,
-                    int64_t ld, int box_rows) {
-  auto enc = get_encoder();
-  if (!enc) return false;
-  const CUtensorMapDataType dt =
-      dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  cuuint64_t dims[2];
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2];
-  cuuint32_t estr[2] = {1, 1};
-  if (!mn_major) {
-    dims[0] = static_cast<cuuint64_t>(K);
-    dims[1] = static_cast<cuuint64_t>(rows_or_mn);
-    box[0] = kBlockK;
-    box[1] = static_cast<cuuint32_t>(box_rows);
-  } else {
-    dims[0] = static_cast<cuuint64_t>(rows_or_mn);
-    dims[1] = static_cast<cuuint64_t>(K);
-    box[0] = 64;
-    box[1] = kBlockK;
-  }
-  CUresult r = enc(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
 }
 
 bool is_half(int t) { return t == GEMM_F16 || t == GEMM_BF16; }
@@ -132,6 +82,40 @@ uint64_t wait_limit_from_env() {
 }
 
 }  // namespace
+
+namespace lgt {
+
+// 2-D tensor map over a 16-bit operand.  K-major: dims {K, rows}, box
+// {64, box_rows}.  MN-major: dims {mn, K}, box {64, 64}.  128-byte swizzle,
+// zero fill outside the tensor (ragged M / N / K tails).
+bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major, int64_t rows_or_mn, int64_t K,
+                    int64_t ld, int box_rows) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  const CUtensorMapDataType dt =
+      dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[2];
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2];
+  cuuint32_t estr[2] = {1, 1};
+  if (!mn_major) {
+    dims[0] = static_cast<cuuint64_t>(K);
+    dims[1] = static_cast<cuuint64_t>(rows_or_mn);
+    box[0] = kBlockK;
+    box[1] = static_cast<cuuint32_t>(box_rows);
+  } else {
+    dims[0] = static_cast<cuuint64_t>(rows_or_mn);
+    dims[1] = static_cast<cuuint64_t>(K);
+    box[0] = 64;
+    box[1] = kBlockK;
+  }
+  CUresult r = enc(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace lgt
 
 extern "C" {
 
@@ -372,8 +356,8 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   const int64_t q_ext = a_is_p ? d.N : d.M;
   const int64_t p_ld = a_is_p ? lda : ldb;
   const int64_t q_ld = a_is_p ? ldb : lda;
-  if (!encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, lgt::TILE_P)) return GEMM_ERR_CUDA;
-  if (!encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, plan->bn)) return GEMM_ERR_CUDA;
+  if (!lgt::encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, lgt::TILE_P)) return GEMM_ERR_CUDA;
+  if (!lgt::encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, plan->bn)) return GEMM_ERR_CUDA;
 
   args.c = C;
   args.ldc = plan->ldc;

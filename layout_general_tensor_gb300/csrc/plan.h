@@ -1,0 +1,41 @@
+// Host-side plan of the GEMM (the object behind gemm_plan_t) and helpers
+// shared by the C-ABI translation units.
+#pragma once
+#include <cuda.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/gemm.h"
+#include "kernels.h"
+
+struct gemm_plan {
+  gemm_desc_t d;
+  int device;        // device current at create time, -1 if none was queried
+  int sms_rule;      // SM count fed to the split-K rule
+  int sms_grid;      // persistent grid size (device SMs), 0 without a device
+  int kernel;        // 0: tensor-core any-layout
+  int swap;
+  int bn;
+  int split, kb_per_split, kb_total;
+  int tiles_p, tiles_q, num_units;
+  int64_t lda, ldb, ldc;
+  int a_mn, b_mn;
+  // operand repacking (leading dimension not a multiple of 16 bytes)
+  int repack_a, repack_b;
+  int64_t a_rows, a_row_elems, b_rows, b_row_elems;  // storage rows of each operand
+  int64_t a_pack_ld, b_pack_ld;
+  size_t off_partial, off_counters, off_pack_a, off_pack_b, ws_bytes;
+  size_t ws_bytes_misaligned;
+  lgt::DeviceStatus* d_status;
+  uint64_t wait_limit_ns;
+};
+
+
+namespace lgt {
+
+// Encode a 2-D TMA map over a 16-bit operand (see api.cu).
+bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major, int64_t rows_or_mn, int64_t K,
+                    int64_t ld, int box_rows);
+
+}  // namespace lgt
