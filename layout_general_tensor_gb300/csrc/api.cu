@@ -206,8 +206,20 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   p.swap = (d.M <= 64 && d.N > d.M) ? 1 : 0;
   const bool q_mn = p.swap ? p.a_mn : p.b_mn;
   const int64_t q_extent = p.swap ? d.M : d.N;
+  // 256-wide tiles halve the L2 -> shared-memory bytes per FLOP of 128-wide
+  // ones; narrow problems use the smallest power of two covering them.
+  // They are used only while the problem still has a tile for every SM.
+  const int64_t p_tiles = ceil_div(p.swap ? d.N : d.M, lgt::TILE_P);
+  const int sms = p.sms_grid > 0 ? p.sms_grid : p.sms_rule;
   int bn = q_extent >= 128 ? 128 : next_pow2_at_least16(q_extent);
+  if (q_extent >= 256 && p_tiles * ceil_div(q_extent, 256) >= sms) bn = 256;
   if (q_mn && bn < 64) bn = 64;  // MN-major tiles come in 64-element swizzle atoms
+  if (!p.swap) {
+    // tuning override of the tile width for large problems
+    const char* e = std::getenv("LGT_GEMM_BN");
+    const int o = e ? std::atoi(e) : 0;
+    if ((o == 64 || o == 128 || o == 192 || o == 256) && q_extent >= o) bn = o;
+  }
   p.bn = bn;
   p.tiles_p = static_cast<int>(ceil_div(p.swap ? d.N : d.M, lgt::TILE_P));
   p.tiles_q = static_cast<int>(ceil_div(q_extent, bn));

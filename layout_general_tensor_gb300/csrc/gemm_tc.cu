@@ -49,7 +49,9 @@ struct Cfg {
   static constexpr uint32_t STAGE_BYTES = kP_BYTES + Q_BYTES;
   static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
-  static constexpr uint32_t TMEM_COLS = (2 * BN) < 32 ? 32 : 2 * BN;
+  // two accumulator buffers of BN fp32 columns, rounded up to a power of two
+  static constexpr uint32_t TMEM_COLS = (2 * BN) <= 32 ? 32 : (2 * BN) <= 64 ? 64 : (2 * BN) <= 128 ? 128
+                                        : (2 * BN) <= 256 ? 256 : 512;
   static constexpr int CH = BN < 32 ? BN : 32;          // accumulator columns per tcgen05.ld
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2], teardown
   static constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
@@ -148,6 +150,69 @@ __device__ __forceinline__ void tile_ranges(const TcArgs& a, int32_t tile, int b
     m0 = tq * bn;
     n1 = min(a.N, n0 + TILE_P);
     m1 = min(a.M, m0 + bn);
+  }
+}
+
+// Last arriver of a split tile: read the fp32 sum from the workspace (L2),
+// convert once, store C and zero the workspace region again.  Rows are
+// walked in 4-float vectors with several loads in flight per thread.
+__device__ __noinline__ void finish_tile(const TcArgs& a, int m0, int m1, int n0, int n1, int et) {
+  const int rows = m1 - m0, cols = n1 - n0;
+  uint16_t* cbase = reinterpret_cast<uint16_t*>(a.c);
+  if (a.ws_vec && a.c_vec && (cols & 3) == 0) {
+    // c_vec: C rows and n0 are 16-byte aligned, so 4-element (8-byte) stores are aligned too
+    const int cols4 = cols >> 2;
+    const int total = rows * cols4;
+    constexpr int U = 8;
+    for (int i0 = et; i0 < total; i0 += kEpiThreads * U) {
+      float4 v[U];
+      float4* w[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * kEpiThreads;
+        w[u] = nullptr;
+        if (i < total) {
+          const int r = i / cols4, c4 = i - r * cols4;
+          w[u] = reinterpret_cast<float4*>(a.ws + static_cast<int64_t>(m0 + r) * a.N + n0) + c4;
+          v[u] = __ldcg(w[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * kEpiThreads;
+        if (i < total) {
+          const int r = i / cols4, c4 = i - r * cols4;
+          __stcg(w[u], make_float4(0.f, 0.f, 0.f, 0.f));
+          uint2 o;
+          o.x = pack2(v[u].x, v[u].y, a.c_bf16);
+          o.y = pack2(v[u].z, v[u].w, a.c_bf16);
+          *reinterpret_cast<uint2*>(cbase + static_cast<int64_t>(m0 + r) * a.ldc + n0 + 4 * c4) = o;
+        }
+      }
+    }
+    return;
+  }
+  const int total = rows * cols;
+  constexpr int U = 8;
+  for (int i0 = et; i0 < total; i0 += kEpiThreads * U) {
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * kEpiThreads;
+      if (i < total) {
+        const int r = i / cols, cidx = i - r * cols;
+        v[u] = __ldcg(a.ws + static_cast<int64_t>(m0 + r) * a.N + (n0 + cidx));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * kEpiThreads;
+      if (i < total) {
+        const int r = i / cols, cidx = i - r * cols;
+        __stcg(a.ws + static_cast<int64_t>(m0 + r) * a.N + (n0 + cidx), 0.0f);
+        cbase[static_cast<int64_t>(m0 + r) * a.ldc + (n0 + cidx)] = cvt1(v[u], a.c_bf16);
+      }
+    }
   }
 }
 
@@ -403,15 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         }
         if (named_bar_or(1, kEpiThreads, mine_last)) {
           __threadfence();
-          const int rows = m1 - m0, cols = n1 - n0;
-          const int total = rows * cols;
-          for (int i = et; i < total; i += kEpiThreads) {
-            const int r = i / cols, cidx = i - r * cols;
-            float* w = a.ws + static_cast<int64_t>(m0 + r) * a.N + (n0 + cidx);
-            const float s = __ldcg(w);
-            __stcg(w, 0.0f);
-            reinterpret_cast<uint16_t*>(a.c)[static_cast<int64_t>(m0 + r) * a.ldc + (n0 + cidx)] = cvt1(s, a.c_bf16);
-          }
+          finish_tile(a, m0, m1, n0, n1, et);
           named_bar_sync(1, kEpiThreads);
           if (et == 0) a.counters[g.tile] = 0;
         }
@@ -460,6 +517,7 @@ size_t tc_gemm_smem_bytes(int bn) {
     case 32: return Cfg<32>::SMEM_ALLOC;
     case 64: return Cfg<64>::SMEM_ALLOC;
     case 128: return Cfg<128>::SMEM_ALLOC;
+    case 192: return Cfg<192>::SMEM_ALLOC;
     case 256: return Cfg<256>::SMEM_ALLOC;
     default: return 0;
   }
@@ -471,6 +529,7 @@ cudaError_t launch_tc_gemm(const TcArgs& args, int bn, int grid, cudaStream_t st
     case 32: return launch_bn<32>(args, grid, stream);
     case 64: return launch_bn<64>(args, grid, stream);
     case 128: return launch_bn<128>(args, grid, stream);
+    case 192: return launch_bn<192>(args, grid, stream);
     case 256: return launch_bn<256>(args, grid, stream);
     default: return cudaErrorInvalidValue;
   }
