@@ -349,9 +349,6 @@ def gpu_arm(args, headline):
     for case in wl.WORKLOADS:
         if case.name == headline.name:
             continue
-        if case.b_dtype == wl.INT4:
-            configs[case.name] = {"status": "not measured: the int4 path is not built"}
-            continue
         d = DeviceCase(case)
         ts = time_steps(d.run, max(args.steps, 20), max(args.warmup, 3))
         ms = statistics.median(ts)

@@ -115,6 +115,23 @@ bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major,
   return r == CUDA_SUCCESS;
 }
 
+// Packed int4 weights: N rows of `ld_bytes` bytes (K/2 used), box 32 bytes
+// (64 codes) x 128 rows, 32-byte swizzle so that each thread's two 16-byte
+// row reads fall in different bank groups.
+bool encode_int4_weights(CUtensorMap* map, const void* ptr, int64_t N, int64_t ld_bytes) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  (void)N;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(ld_bytes), static_cast<cuuint64_t>(N)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_bytes)};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(TILE_P)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace lgt
 
 extern "C" {
@@ -170,7 +187,16 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   if (!desc) return GEMM_ERR_INVALID_ARG;
   const gemm_status_t v = validate(*desc);
   if (v != GEMM_OK) return v;
-  if (desc->b_dtype == GEMM_INT4) return GEMM_ERR_UNSUPPORTED;
+  const bool int4 = desc->b_dtype == GEMM_INT4;
+  if (int4) {
+    // group: a multiple of the 64-deep K block that divides K; rows of packed
+    // bytes must be TMA-addressable (16-byte multiples)
+    const int64_t g = desc->group_size ? desc->group_size : 128;
+    if (g % kBlockK != 0 || desc->K % g != 0 || desc->K % 2 != 0) return GEMM_ERR_INVALID_ARG;
+    const int64_t ldb = desc->ldb ? desc->ldb : desc->K / 2;
+    if (ldb < desc->K / 2) return GEMM_ERR_INVALID_ARG;
+    if (ldb % 16 != 0) return GEMM_ERR_UNSUPPORTED;
+  }
 
   gemm_plan p;
   std::memset(&p, 0, sizeof(p));
@@ -200,10 +226,15 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   if (p.ldc == 0) p.ldc = 1;
   p.a_mn = d.a_layout == GEMM_MN_CONTIG;
   p.b_mn = d.b_layout == GEMM_MN_CONTIG;
+  if (int4) {
+    p.kernel = 1;
+    p.group = d.group_size ? d.group_size : 128;
+    p.ldb = d.ldb ? d.ldb : d.K / 2;  // bytes
+  }
 
   // Tile shape.  Skinny M runs swapped: the 128-row MMA side walks N and the
   // MMA's N extent covers all of M.
-  p.swap = (d.M <= 64 && d.N > d.M) ? 1 : 0;
+  p.swap = ((d.M <= 64 && d.N > d.M) || int4) ? 1 : 0;
   const bool q_mn = p.swap ? p.a_mn : p.b_mn;
   const int64_t q_extent = p.swap ? d.M : d.N;
   // 256-wide tiles halve the L2 -> shared-memory bytes per FLOP of 128-wide
@@ -213,6 +244,7 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   const int sms = p.sms_grid > 0 ? p.sms_grid : p.sms_rule;
   int bn = q_extent >= 128 ? 128 : next_pow2_at_least16(q_extent);
   if (q_extent >= 256 && p_tiles * ceil_div(q_extent, 256) >= sms) bn = 256;
+  if (int4 && bn > 128) bn = 128;  // the int4 kernel keeps 256 TMEM columns for the dequantised weight
   if (q_mn && bn < 64) bn = 64;  // MN-major tiles come in 64-element swizzle atoms
   if (!p.swap) {
     // tuning override of the tile width for large problems
@@ -245,7 +277,7 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   p.b_rows = p.b_mn ? d.K : d.N;
   p.b_row_elems = p.b_mn ? d.N : d.K;
   p.repack_a = (p.lda * 2) % 16 != 0;
-  p.repack_b = (p.ldb * 2) % 16 != 0;
+  p.repack_b = !int4 && (p.ldb * 2) % 16 != 0;
   p.a_pack_ld = align_up(static_cast<size_t>(p.a_row_elems), 8);
   p.b_pack_ld = align_up(static_cast<size_t>(p.b_row_elems), 8);
 
@@ -257,7 +289,7 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
     off = align_up(off + static_cast<size_t>(p.tiles_p) * p.tiles_q * sizeof(int32_t), 256);
   }
   const size_t pack_a_bytes = align_up(static_cast<size_t>(p.a_rows) * p.a_pack_ld * 2, 256);
-  const size_t pack_b_bytes = align_up(static_cast<size_t>(p.b_rows) * p.b_pack_ld * 2, 256);
+  const size_t pack_b_bytes = int4 ? 0 : align_up(static_cast<size_t>(p.b_rows) * p.b_pack_ld * 2, 256);
   size_t off_aligned = off;
   p.off_pack_a = off;
   if (p.repack_a) off_aligned += pack_a_bytes;
@@ -323,9 +355,16 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   }
   if (!A || !B) return GEMM_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(A) % 2 || reinterpret_cast<uintptr_t>(B) % 2) return GEMM_ERR_ALIGNMENT;
+  const bool int4 = plan->kernel == 1;
+  if (int4) {
+    // packed weights are read by TMA in place; scales (and zeros) are fp16
+    if (reinterpret_cast<uintptr_t>(B) % 16) return GEMM_ERR_ALIGNMENT;
+    if (!scales) return GEMM_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(scales) % 2 || reinterpret_cast<uintptr_t>(zeros) % 2) return GEMM_ERR_ALIGNMENT;
+  }
 
   const bool a_mis = reinterpret_cast<uintptr_t>(A) % 16 != 0;
-  const bool b_mis = reinterpret_cast<uintptr_t>(B) % 16 != 0;
+  const bool b_mis = !int4 && reinterpret_cast<uintptr_t>(B) % 16 != 0;
   const bool pack_a = plan->repack_a || a_mis;
   const bool pack_b = plan->repack_b || b_mis;
   const size_t need = (a_mis || b_mis) ? plan->ws_bytes_misaligned : plan->ws_bytes;
@@ -368,7 +407,8 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   const int64_t q_ext = a_is_p ? d.N : d.M;
   const int64_t p_ld = a_is_p ? lda : ldb;
   const int64_t q_ld = a_is_p ? ldb : lda;
-  if (!lgt::encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, lgt::TILE_P)) return GEMM_ERR_CUDA;
+  if (!int4 && !lgt::encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, lgt::TILE_P))
+    return GEMM_ERR_CUDA;
   if (!lgt::encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, plan->bn)) return GEMM_ERR_CUDA;
 
   args.c = C;
@@ -396,9 +436,22 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   args.c_bf16 = d.c_dtype == GEMM_BF16;
   args.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (plan->ldc % 8 == 0);
   args.ws_vec = (d.N % 4 == 0);
+  const int grid = plan->num_units < plan->sms_grid ? plan->num_units : plan->sms_grid;
+  if (int4) {
+    // MMA A operand: the dequantised weight in TMEM (K-major); B: the activation
+    args.idesc = lgt::idesc_f16(0u, 0u, static_cast<uint32_t>(q_mn), lgt::TILE_P, static_cast<uint32_t>(plan->bn));
+    lgt::Int4Args a4;
+    std::memset(&a4, 0, sizeof(a4));
+    a4.t = args;
+    if (!lgt::encode_int4_weights(&a4.tm_w, B, d.N, plan->ldb)) return GEMM_ERR_CUDA;
+    a4.scales = static_cast<const uint16_t*>(scales);
+    a4.zeros = static_cast<const uint16_t*>(zeros);
+    a4.groups = static_cast<int32_t>(d.K / plan->group);
+    a4.div_kb_per_group = lgt::magic_encode(static_cast<uint32_t>(plan->group / kBlockK));
+    return lgt::launch_int4_gemm(a4, plan->bn, grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
   args.idesc = lgt::idesc_f16(d.a_dtype == GEMM_BF16 ? 1u : 0u, static_cast<uint32_t>(p_mn),
                               static_cast<uint32_t>(q_mn), lgt::TILE_P, static_cast<uint32_t>(plan->bn));
-  const int grid = plan->num_units < plan->sms_grid ? plan->num_units : plan->sms_grid;
   return lgt::launch_tc_gemm(args, plan->bn, grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

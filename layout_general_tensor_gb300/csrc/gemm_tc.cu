@@ -32,16 +32,15 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace lgt {
 namespace {
 
 constexpr int kThreads = 192;
 constexpr int kEpiWarp0 = 2;
-constexpr int kEpiThreads = 128;
 constexpr uint32_t kP_BYTES = TILE_P * TILE_K * 2;   // 16 KiB
 constexpr uint32_t kMnChunkBytes = 64 * TILE_K * 2;  // one 64-wide MN box, 64 K rows: 8 KiB
-constexpr int kTimeoutCode = 6;                      // GEMM_ERR_TIMEOUT
 
 template <int BN>
 struct Cfg {
@@ -62,159 +61,6 @@ struct Cfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
   static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM allocation");
 };
-
-struct Group {
-  int32_t tile;
-  int32_t s0, s1;    // splits [s0, s1) of the tile
-  int32_t kb0, nkb;  // K blocks
-};
-
-// Work assignment.  split == 1: units are tiles, taken round-robin.
-// split > 1: CTA b takes the contiguous unit range
-// [b*U/G, (b+1)*U/G) and a group is a maximal run of one tile's splits.
-struct Sched {
-  int32_t u, u_end, step;
-  __device__ Sched(const TcArgs& a) {
-    const int32_t G = gridDim.x, b = blockIdx.x;
-    if (a.split == 1) {
-      u = b;
-      u_end = a.num_units;
-      step = G;
-    } else {
-      u = static_cast<int32_t>((static_cast<int64_t>(b) * a.num_units) / G);
-      u_end = static_cast<int32_t>((static_cast<int64_t>(b + 1) * a.num_units) / G);
-      step = 0;
-    }
-  }
-  __device__ bool next(const TcArgs& a, Group& g) {
-    if (u >= u_end) return false;
-    if (step) {
-      g.tile = u;
-      g.s0 = 0;
-      g.s1 = 1;
-      u += step;
-    } else {
-      uint32_t tile, s;
-      magic_divmod(static_cast<uint32_t>(u), a.div_split, tile, s);
-      const int32_t avail = u_end - u;
-      const int32_t s1 = min(a.split, static_cast<int32_t>(s) + avail);
-      g.tile = static_cast<int32_t>(tile);
-      g.s0 = static_cast<int32_t>(s);
-      g.s1 = s1;
-      u += s1 - static_cast<int32_t>(s);
-    }
-    g.kb0 = g.s0 * a.kb_per_split;
-    const int32_t kb1 = min(a.kb_total, g.s1 * a.kb_per_split);
-    g.nkb = kb1 > g.kb0 ? kb1 - g.kb0 : 0;
-    return true;
-  }
-};
-
-__device__ __forceinline__ void record_timeout(const TcArgs& a, volatile int* abort_flag, int where) {
-  *abort_flag = 1;
-  if (atomicCAS(&a.status->code, 0, kTimeoutCode) == 0) a.status->where = where;
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
-  if (bf16) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint16_t cvt1(float v, int bf16) {
-  if (bf16) {
-    __nv_bfloat16 h = __float2bfloat16_rn(v);
-    return *reinterpret_cast<uint16_t*>(&h);
-  }
-  __half h = __float2half_rn(v);
-  return *reinterpret_cast<uint16_t*>(&h);
-}
-
-// (m, n) ranges of a tile in C coordinates.
-__device__ __forceinline__ void tile_ranges(const TcArgs& a, int32_t tile, int bn, int32_t& tp, int32_t& tq,
-                                            int32_t& m0, int32_t& m1, int32_t& n0, int32_t& n1) {
-  uint32_t q, r;
-  magic_divmod(static_cast<uint32_t>(tile), a.div_tiles_p, q, r);
-  tp = static_cast<int32_t>(r);
-  tq = static_cast<int32_t>(q);
-  if (!a.swap) {
-    m0 = tp * TILE_P;
-    n0 = tq * bn;
-    m1 = min(a.M, m0 + TILE_P);
-    n1 = min(a.N, n0 + bn);
-  } else {
-    n0 = tp * TILE_P;
-    m0 = tq * bn;
-    n1 = min(a.N, n0 + TILE_P);
-    m1 = min(a.M, m0 + bn);
-  }
-}
-
-// Last arriver of a split tile: read the fp32 sum from the workspace (L2),
-// convert once, store C and zero the workspace region again.  Rows are
-// walked in 4-float vectors with several loads in flight per thread.
-__device__ __noinline__ void finish_tile(const TcArgs& a, int m0, int m1, int n0, int n1, int et) {
-  const int rows = m1 - m0, cols = n1 - n0;
-  uint16_t* cbase = reinterpret_cast<uint16_t*>(a.c);
-  if (a.ws_vec && a.c_vec && (cols & 3) == 0) {
-    // c_vec: C rows and n0 are 16-byte aligned, so 4-element (8-byte) stores are aligned too
-    const int cols4 = cols >> 2;
-    const int total = rows * cols4;
-    constexpr int U = 8;
-    for (int i0 = et; i0 < total; i0 += kEpiThreads * U) {
-      float4 v[U];
-      float4* w[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * kEpiThreads;
-        w[u] = nullptr;
-        if (i < total) {
-          const int r = i / cols4, c4 = i - r * cols4;
-          w[u] = reinterpret_cast<float4*>(a.ws + static_cast<int64_t>(m0 + r) * a.N + n0) + c4;
-          v[u] = __ldcg(w[u]);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * kEpiThreads;
-        if (i < total) {
-          const int r = i / cols4, c4 = i - r * cols4;
-          __stcg(w[u], make_float4(0.f, 0.f, 0.f, 0.f));
-          uint2 o;
-          o.x = pack2(v[u].x, v[u].y, a.c_bf16);
-          o.y = pack2(v[u].z, v[u].w, a.c_bf16);
-          *reinterpret_cast<uint2*>(cbase + static_cast<int64_t>(m0 + r) * a.ldc + n0 + 4 * c4) = o;
-        }
-      }
-    }
-    return;
-  }
-  const int total = rows * cols;
-  constexpr int U = 8;
-  for (int i0 = et; i0 < total; i0 += kEpiThreads * U) {
-    float v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = i0 + u * kEpiThreads;
-      if (i < total) {
-        const int r = i / cols, cidx = i - r * cols;
-        v[u] = __ldcg(a.ws + static_cast<int64_t>(m0 + r) * a.N + (n0 + cidx));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = i0 + u * kEpiThreads;
-      if (i < total) {
-        const int r = i / cols, cidx = i - r * cols;
-        __stcg(a.ws + static_cast<int64_t>(m0 + r) * a.N + (n0 + cidx), 0.0f);
-        cbase[static_cast<int64_t>(m0 + r) * a.ldc + (n0 + cidx)] = cvt1(v[u], a.c_bf16);
-      }
-    }
-  }
-}
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcArgs a) {
@@ -366,112 +212,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else {
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;                  // TMEM lane quadrant this warp may access
-    const int row = q4 * 32 + lane;           // accumulator row (TMEM lane)
     const int et = threadIdx.x - kEpiWarp0 * 32;
     Sched sched(a);
     Group g;
     int acc_iter = 0;
     bool ok = true;
     while (ok && sched.next(a, g)) {
-      int32_t tp, tq, m0, m1, n0, n1;
-      tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
-      const bool full_tile = (g.s0 == 0 && g.s1 == a.split);
-      if (g.nkb > 0) {
-        const int buf = acc_iter & 1;
-        const uint32_t acc_phase = (acc_iter >> 1) & 1;
-        const bool got = mbar_wait_bounded(accf_bar(buf), acc_phase, a.wait_limit_ns, abort_flag);
-        if (!got && !*abort_flag) record_timeout(a, abort_flag, 2 * 16 + 2);
-        // all epilogue threads leave together if any of them gave up
-        if (named_bar_or(1, kEpiThreads, !got)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(buf * BN);
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += C::CH) {
-          uint32_t v[C::CH];
-          if constexpr (C::CH == 32) {
-            tc_ld_32x32b_x32(t_row + c0, v);
-          } else {
-            tc_ld_32x32b_x16(t_row + c0, v);
-          }
-          tc_wait_ld();
-          if (!a.swap) {
-            const int m = m0 + row;
-            const int nb = n0 + c0;
-            if (m < m1) {
-              if (full_tile) {
-                uint16_t* crow = reinterpret_cast<uint16_t*>(a.c) + static_cast<int64_t>(m) * a.ldc;
-                if (a.c_vec && nb + C::CH <= n1) {
-#pragma unroll
-                  for (int j = 0; j < C::CH; j += 8) {
-                    st_global_v4(crow + nb + j, pack2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), a.c_bf16),
-                                 pack2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), a.c_bf16),
-                                 pack2(__uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]), a.c_bf16),
-                                 pack2(__uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]), a.c_bf16));
-                  }
-                } else {
-#pragma unroll
-                  for (int j = 0; j < C::CH; ++j)
-                    if (nb + j < n1) crow[nb + j] = cvt1(__uint_as_float(v[j]), a.c_bf16);
-                }
-              } else {
-                float* wrow = a.ws + static_cast<int64_t>(m) * a.N;
-                if (a.ws_vec && nb + C::CH <= n1) {
-#pragma unroll
-                  for (int j = 0; j < C::CH; j += 4)
-                    red_add_v4_f32(wrow + nb + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                   __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-                } else {
-#pragma unroll
-                  for (int j = 0; j < C::CH; ++j)
-                    if (nb + j < n1) red_add_f32(wrow + nb + j, __uint_as_float(v[j]));
-                }
-              }
-            }
-          } else {
-            const int n = n0 + row;
-            if (n < n1) {
-              if (full_tile) {
-                uint16_t* cc = reinterpret_cast<uint16_t*>(a.c) + n;
-#pragma unroll
-                for (int j = 0; j < C::CH; ++j) {
-                  const int m = m0 + c0 + j;
-                  if (m < m1) cc[static_cast<int64_t>(m) * a.ldc] = cvt1(__uint_as_float(v[j]), a.c_bf16);
-                }
-              } else {
-                float* wc = a.ws + n;
-#pragma unroll
-                for (int j = 0; j < C::CH; ++j) {
-                  const int m = m0 + c0 + j;
-                  if (m < m1) red_add_f32(wc + static_cast<int64_t>(m) * a.N, __uint_as_float(v[j]));
-                }
-              }
-            }
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acce_bar(buf));
-        ++acc_iter;
-      }
-      if (!full_tile) {
-        // Publish this run's partial, count its splits, and let the CTA that
-        // completes the count convert the tile.
-        __threadfence();
-        named_bar_sync(1, kEpiThreads);
-        bool mine_last = false;
-        if (et == 0) {
-          const int old = atomicAdd(&a.counters[g.tile], g.s1 - g.s0);
-          mine_last = (old + (g.s1 - g.s0) == a.split);
-        }
-        if (named_bar_or(1, kEpiThreads, mine_last)) {
-          __threadfence();
-          finish_tile(a, m0, m1, n0, n1, et);
-          named_bar_sync(1, kEpiThreads);
-          if (et == 0) a.counters[g.tile] = 0;
-        }
+      if (!epilogue_group<BN, C::CH>(a, g, tmem_base, accf_bar(0), acce_bar(0), acc_iter, abort_flag, q4, lane, et)) {
+        ok = false;
+        break;
       }
     }
   }

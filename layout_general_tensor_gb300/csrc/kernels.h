@@ -57,6 +57,20 @@ struct TcArgs {
   uint32_t idesc;
 };
 
+// int4-weight GEMM (always swapped: P = the weight rows n, Q = the activation
+// rows m).  `t` carries the scheduler, activation map (tm_q) and epilogue
+// fields; tm_p is unused.
+struct Int4Args {
+  TcArgs t;
+  CUtensorMap tm_w;          // packed weight bytes: dims {ldb bytes, N}, box {32, 128}, 32-byte swizzle
+  const uint16_t* scales;    // fp16 [N][groups]
+  const uint16_t* zeros;     // fp16 [N][groups], or null for z = 8
+  int32_t groups;
+  MagicDiv div_kb_per_group; // 64-deep K block -> quantisation group
+};
+
+cudaError_t launch_int4_gemm(const Int4Args& args, int bn, int grid, cudaStream_t stream);
+
 // Returns a cudaError_t; `bn` selects the kernel instance.
 cudaError_t launch_tc_gemm(const TcArgs& args, int bn, int grid, cudaStream_t stream);
 size_t tc_gemm_smem_bytes(int bn);

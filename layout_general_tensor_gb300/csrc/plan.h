@@ -14,7 +14,8 @@ struct gemm_plan {
   int device;        // device current at create time, -1 if none was queried
   int sms_rule;      // SM count fed to the split-K rule
   int sms_grid;      // persistent grid size (device SMs), 0 without a device
-  int kernel;        // 0: tensor-core any-layout
+  int kernel;        // 0: tensor-core any-layout, 1: int4 dequant
+  int group;         // int4 quantisation group along K
   int swap;
   int bn;
   int split, kb_per_split, kb_total;
@@ -37,5 +38,8 @@ namespace lgt {
 // Encode a 2-D TMA map over a 16-bit operand (see api.cu).
 bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major, int64_t rows_or_mn, int64_t K,
                     int64_t ld, int box_rows);
+
+// Encode the TMA map over packed int4 weights (see api.cu).
+bool encode_int4_weights(CUtensorMap* map, const void* ptr, int64_t N, int64_t ld_bytes);
 
 }  // namespace lgt

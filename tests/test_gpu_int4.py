@@ -1,0 +1,120 @@
+"""GPU parity of the int4-weight GEMM (dequantisation inside the mainloop)
+against the fp64 oracle, through the C ABI.  Same tolerances as the dense
+path; the dequantised weight is rounded once to fp16 on the GPU, which the
+oracle does not do (it is the exact definition)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import assert_close, lib, oracle_full, oracle_sample, run_case
+
+pytestmark = pytest.mark.gpu
+
+K, MN = wl.K_CONTIG, wl.MN_CONTIG
+
+
+def _case(M, N, Kd, al=K, split=1, group=128, zero=8.0, scale=("uniform", 0.005, 0.02), name=""):
+    nm = f"int4_m{M}_n{N}_k{Kd}_{'a-kcontig' if al == K else 'a-mcontig'}_g{group}_s{split}{name}"
+    return wl.GemmCase(nm, M, N, Kd, al, K, wl.F16, wl.INT4, wl.F16, ("normal", 1.0), ("bytes",), split_k=split,
+                       group_size=group, zero_value=zero, scale_dist=scale)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    lib()
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 33])
+@pytest.mark.parametrize("N,Kd", [(128, 128), (300, 640), (1000, 256)])
+def test_int4_small(M, N, Kd):
+    for zero in (8.0, None):
+        case = _case(M, N, Kd, zero=zero)
+        inp = wl.make_inputs(case, seed=M + N)
+        c, g, _ = run_case(case, inp)
+        assert g.info.kernel == 1 and g.info.swap_ab == 1
+        assert_close(c, oracle_full(case, inp), case.name)
+        g.close()
+
+
+@pytest.mark.parametrize("split", [2, 3, 8, 0])
+def test_int4_split_k(split):
+    case = _case(16, 700, 4096, split=split)
+    inp = wl.make_inputs(case, seed=split + 1)
+    c, g, _ = run_case(case, inp, reps=2)
+    if split:
+        assert g.info.split_k == split
+    assert_close(c, oracle_full(case, inp), case.name)
+    g.close()
+
+
+@pytest.mark.parametrize("group", [64, 256])
+def test_int4_group_sizes(group):
+    case = _case(9, 260, 1024, group=group, split=2)
+    inp = wl.make_inputs(case, seed=group)
+    c, g, _ = run_case(case, inp)
+    assert_close(c, oracle_full(case, inp), case.name)
+    g.close()
+
+
+def test_int4_activation_m_contiguous():
+    case = _case(40, 512, 512, al=MN, split=2)
+    inp = wl.make_inputs(case, seed=3)
+    c, g, _ = run_case(case, inp)
+    assert_close(c, oracle_full(case, inp), case.name)
+    g.close()
+
+
+def test_int4_general_dequant_path():
+    """Non-integer zero points and scales too small for an exact s/16 in fp16
+    take the kernel's general path; it must round each weight the same way."""
+    case = _case(8, 384, 512, split=1, zero=7.5, scale=("uniform", 2e-4, 9e-4))
+    inp = wl.make_inputs(case, seed=9)
+    c, g, _ = run_case(case, inp)
+    ref = oracle_full(case, inp)
+    assert_close(c, ref, case.name)
+    # and each weight was rounded once: compare with the oracle on fp16-rounded weights
+    a, b = oracle.logical_operands(case.M, case.N, case.K, inp.A, case.a_layout, inp.lda, case.a_dtype, inp.B,
+                                   case.b_layout, 0, wl.INT4, inp.scales, inp.zeros, case.group_size)
+    ref_rounded_w = a @ oracle.round_to(b, oracle.F16)
+    assert_close(c, ref_rounded_w, case.name + " (rounded weights)")
+    g.close()
+
+
+def test_int4_closed_forms():
+    m = lib()
+    M, N, Kd = 4, 256, 256
+    A = torch.empty(M * Kd, dtype=torch.float16).uniform_(-1, 1)
+    a64 = oracle.decode(A, oracle.F16).reshape(M, Kd)
+    desc = m.make_desc(M, N, Kd, a_dtype=m.GEMM_F16, b_dtype=m.GEMM_INT4, c_dtype=m.GEMM_F16, split_k=1,
+                       num_sms=148)
+    g = m.Gemm(desc)
+    C = torch.empty(M * N, dtype=torch.float16, device="cuda")
+    Ad = A.cuda()
+    # all codes 8 with zero point 8 -> exactly zero
+    W = torch.full((N * Kd // 2,), 0x88, dtype=torch.uint8, device="cuda")
+    s = torch.full((N, Kd // 128), 0.01, dtype=torch.float16, device="cuda")
+    g.run(Ad, W, C, s, None)
+    assert g.sync_status() == 0
+    assert torch.count_nonzero(C).item() == 0
+    # all codes 9, scale 1/64 -> C[m, n] = sum_k a[m, k] / 64
+    W.fill_(0x99)
+    s.fill_(1.0 / 64)
+    g.run(Ad, W, C, s, None)
+    assert g.sync_status() == 0
+    got = oracle.decode(C.cpu(), oracle.F16).reshape(M, N)
+    want = np.repeat((a64.sum(axis=1) / 64)[:, None], N, axis=1)
+    assert_close(got, want, "codes 9")
+    g.close()
+
+
+def test_int4_full_size_sampled():
+    case = wl.INT4_DEQUANT
+    inp = wl.make_inputs(case, seed=0)
+    c, g, _ = run_case(case, inp, reps=2)
+    assert g.info.split_k == oracle.splitk_factor(case.M, case.N, case.K, 128, 128, 64, 148)
+    rows, cols = wl.sample_indices(case.M, case.N, 1500, seed=2)
+    assert_close(c[rows, cols], oracle_sample(case, inp, rows, cols), case.name)
+    assert np.all(np.isfinite(c))
+    g.close()

@@ -139,6 +139,28 @@ def test_planner_decisions(lib, case):
         lib.gemm_destroy(h)
 
 
+def test_planner_int4(lib):
+    case = wl.INT4_DEQUANT
+    desc = lib.make_desc(case.M, case.N, case.K, a_dtype=lib.GEMM_F16, b_dtype=lib.GEMM_INT4, c_dtype=lib.GEMM_F16,
+                         split_k=0, group_size=128, num_sms=148)
+    h = lib.gemm_create(desc)
+    info = lib.gemm_query(h)
+    assert info.kernel == 1 and info.swap_ab == 1 and info.split_k == 32
+    assert info.tile_m == 16 and info.tile_n == 128 and info.k_per_split == 512
+    assert lib.gemm_workspace_size(h) >= case.M * case.N * 4
+    lib.gemm_destroy(h)
+    bad = [dict(group_size=96), dict(group_size=512, K=768), dict(a_dtype=lib.GEMM_BF16)]
+    for kw in bad:
+        args = dict(M=16, N=256, K=1024, a_dtype=lib.GEMM_F16, b_dtype=lib.GEMM_INT4, c_dtype=lib.GEMM_F16,
+                    num_sms=148)
+        args.update(kw)
+        st, h = lib.gemm_create_status(lib.make_desc(**args))
+        assert st == lib.GEMM_ERR_INVALID_ARG, kw
+    st, h = lib.gemm_create_status(lib.make_desc(16, 256, 1024, a_dtype=lib.GEMM_F16, b_dtype=lib.GEMM_INT4,
+                                                 c_dtype=lib.GEMM_F16, ldb=520, num_sms=148))
+    assert st == lib.GEMM_ERR_UNSUPPORTED
+
+
 def test_planner_skinny_and_irregular_factors(lib):
     # the SM-waste rule's values at 148 SMs for the skinny bf16 and int4-shaped problems
     desc = lib.make_desc(64, 4096, 16384, split_k=0, num_sms=148)
