@@ -10,7 +10,7 @@
 #include <mutex>
 #include <new>
 
-#include "../../include/gemm.h"
+#include "gemm.h"
 #include "kernels.h"
 #include "plan.h"
 
@@ -115,19 +115,19 @@ bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major,
   return r == CUDA_SUCCESS;
 }
 
-// Packed int4 weights: N rows of `ld_bytes` bytes (K/2 used), box 32 bytes
-// (64 codes) x 128 rows, 32-byte swizzle so that each thread's two 16-byte
-// row reads fall in different bank groups.
+// Packed int4 weights: N rows of `ld_bytes` bytes (K/2 used), box 128 bytes
+// (256 codes) x 128 rows, 128-byte swizzle so that the threads' 16-byte row
+// reads fall in different bank groups.
 bool encode_int4_weights(CUtensorMap* map, const void* ptr, int64_t N, int64_t ld_bytes) {
   auto enc = get_encoder();
   if (!enc) return false;
   (void)N;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(ld_bytes), static_cast<cuuint64_t>(N)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_bytes)};
-  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(TILE_P)};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(TILE_P)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -235,7 +235,8 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   // Tile shape.  Skinny M runs swapped: the 128-row MMA side walks N and the
   // MMA's N extent covers all of M.
   p.swap = ((d.M <= 64 && d.N > d.M) || int4) ? 1 : 0;
-  const bool q_mn = p.swap ? p.a_mn : p.b_mn;
+  // (the int4 path reads a prepared K-contiguous copy of the activation)
+  const bool q_mn = int4 ? false : (p.swap ? p.a_mn : p.b_mn);
   const int64_t q_extent = p.swap ? d.M : d.N;
   // 256-wide tiles halve the L2 -> shared-memory bytes per FLOP of 128-wide
   // ones; narrow problems use the smallest power of two covering them.
@@ -244,7 +245,7 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   const int sms = p.sms_grid > 0 ? p.sms_grid : p.sms_rule;
   int bn = q_extent >= 128 ? 128 : next_pow2_at_least16(q_extent);
   if (q_extent >= 256 && p_tiles * ceil_div(q_extent, 256) >= sms) bn = 256;
-  if (int4 && bn > 128) bn = 128;  // the int4 kernel keeps 256 TMEM columns for the dequantised weight
+  if (int4 && bn > 64) bn = 64;  // the int4 epilogue holds a tile row's fp32 sums in registers
   if (q_mn && bn < 64) bn = 64;  // MN-major tiles come in 64-element swizzle atoms
   if (!p.swap) {
     // tuning override of the tile width for large problems
@@ -276,7 +277,7 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   p.a_row_elems = p.a_mn ? d.M : d.K;
   p.b_rows = p.b_mn ? d.K : d.N;
   p.b_row_elems = p.b_mn ? d.N : d.K;
-  p.repack_a = (p.lda * 2) % 16 != 0;
+  p.repack_a = !int4 && (p.lda * 2) % 16 != 0;
   p.repack_b = !int4 && (p.ldb * 2) % 16 != 0;
   p.a_pack_ld = align_up(static_cast<size_t>(p.a_row_elems), 8);
   p.b_pack_ld = align_up(static_cast<size_t>(p.b_row_elems), 8);
@@ -298,6 +299,14 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   p.ws_bytes = off_aligned;
   // When a base pointer is not 16-byte aligned the operand is repacked too.
   p.ws_bytes_misaligned = off + pack_a_bytes + pack_b_bytes;
+  if (int4) {
+    p.asum_ld = p.tiles_q * p.bn;
+    p.off_aprep = off;
+    p.off_asum = align_up(off + static_cast<size_t>(d.M) * d.K * 2, 256);
+    p.off_gsum = align_up(p.off_asum + static_cast<size_t>(p.kb_total) * p.asum_ld * sizeof(float), 256);
+    p.ws_bytes = align_up(p.off_gsum + static_cast<size_t>(d.K / p.group) * p.asum_ld * sizeof(float), 256);
+    p.ws_bytes_misaligned = p.ws_bytes;
+  }
 
   if (p.device >= 0) {
     if (cudaMalloc(&p.d_status, sizeof(lgt::DeviceStatus)) != cudaSuccess) return GEMM_ERR_CUDA;
@@ -363,7 +372,7 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     if (reinterpret_cast<uintptr_t>(scales) % 2 || reinterpret_cast<uintptr_t>(zeros) % 2) return GEMM_ERR_ALIGNMENT;
   }
 
-  const bool a_mis = reinterpret_cast<uintptr_t>(A) % 16 != 0;
+  const bool a_mis = !int4 && reinterpret_cast<uintptr_t>(A) % 16 != 0;
   const bool b_mis = !int4 && reinterpret_cast<uintptr_t>(B) % 16 != 0;
   const bool pack_a = plan->repack_a || a_mis;
   const bool pack_b = plan->repack_b || b_mis;
@@ -407,9 +416,20 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   const int64_t q_ext = a_is_p ? d.N : d.M;
   const int64_t p_ld = a_is_p ? lda : ldb;
   const int64_t q_ld = a_is_p ? ldb : lda;
-  if (!int4 && !lgt::encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, lgt::TILE_P))
-    return GEMM_ERR_CUDA;
-  if (!lgt::encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, plan->bn)) return GEMM_ERR_CUDA;
+  if (int4) {
+    // prepared activation: K-contiguous, pitch K, in the workspace
+    void* ap = ws + plan->off_aprep;
+    float* asum = reinterpret_cast<float*>(ws + plan->off_asum);
+    float* gsum = reinterpret_cast<float*>(ws + plan->off_gsum);
+    if (lgt::launch_int4_prep(A, plan->lda, plan->a_mn, static_cast<int>(d.M), static_cast<int>(d.K), plan->group, ap,
+                              asum, gsum, plan->asum_ld, plan->sms_grid, stream) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    if (!lgt::encode_operand(&args.tm_q, ap, GEMM_F16, false, d.M, d.K, d.K, plan->bn)) return GEMM_ERR_CUDA;
+  } else {
+    if (!lgt::encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, lgt::TILE_P))
+      return GEMM_ERR_CUDA;
+    if (!lgt::encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, plan->bn)) return GEMM_ERR_CUDA;
+  }
 
   args.c = C;
   args.ldc = plan->ldc;
@@ -439,7 +459,8 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   const int grid = plan->num_units < plan->sms_grid ? plan->num_units : plan->sms_grid;
   if (int4) {
     // MMA A operand: the dequantised weight in TMEM (K-major); B: the activation
-    args.idesc = lgt::idesc_f16(0u, 0u, static_cast<uint32_t>(q_mn), lgt::TILE_P, static_cast<uint32_t>(plan->bn));
+    args.q_mn = 0;
+    args.idesc = lgt::idesc_f16(0u, 0u, 0u, lgt::TILE_P, static_cast<uint32_t>(plan->bn));
     lgt::Int4Args a4;
     std::memset(&a4, 0, sizeof(a4));
     a4.t = args;
@@ -448,6 +469,11 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     a4.zeros = static_cast<const uint16_t*>(zeros);
     a4.groups = static_cast<int32_t>(d.K / plan->group);
     a4.div_kb_per_group = lgt::magic_encode(static_cast<uint32_t>(plan->group / kBlockK));
+    a4.asum = reinterpret_cast<const float*>(ws + plan->off_asum);
+    a4.gsum = reinterpret_cast<const float*>(ws + plan->off_gsum);
+    a4.vec_sz = (a4.groups % 8 == 0) && reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
+                reinterpret_cast<uintptr_t>(zeros) % 16 == 0;
+    a4.asum_ld = plan->asum_ld;
     return lgt::launch_int4_gemm(a4, plan->bn, grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
   args.idesc = lgt::idesc_f16(d.a_dtype == GEMM_BF16 ? 1u : 0u, static_cast<uint32_t>(p_mn),

@@ -167,6 +167,27 @@ __device__ __noinline__ void finish_tile(const TcArgs& a, int m0, int m1, int n0
   }
 }
 
+// After the 128 epilogue threads have added a run's fp32 partial into the
+// workspace: count the run's splits on the tile's arrival counter, and if
+// this arrival completes the tile, convert it (the CTA that arrives last
+// reads the full sum from L2), then reset the counter.
+__device__ __forceinline__ void arrive_split_tile(const TcArgs& a, const Group& g, int m0, int m1, int n0, int n1,
+                                                  int et) {
+  __threadfence();
+  named_bar_sync(1, kEpiThreads);
+  bool mine_last = false;
+  if (et == 0) {
+    const int old = atomicAdd(&a.counters[g.tile], g.s1 - g.s0);
+    mine_last = (old + (g.s1 - g.s0) == a.split);
+  }
+  if (named_bar_or(1, kEpiThreads, mine_last)) {
+    __threadfence();
+    finish_tile(a, m0, m1, n0, n1, et);
+    named_bar_sync(1, kEpiThreads);
+    if (et == 0) a.counters[g.tile] = 0;
+  }
+}
+
 // The epilogue of one group, run by the 128 epilogue threads (TMEM lane
 // quadrant q4, lane `lane`, index `et` among the 128).  Reads the fp32
 // accumulator buffer of the group from TMEM and either converts and stores
@@ -258,23 +279,7 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
     if (lane == 0) mbar_arrive(acce_bar0 + 8u * buf);
     ++acc_iter;
   }
-  if (!full_tile) {
-    // Publish this run's partial, count its splits, and let the CTA that
-    // completes the count convert the tile.
-    __threadfence();
-    named_bar_sync(1, kEpiThreads);
-    bool mine_last = false;
-    if (et == 0) {
-      const int old = atomicAdd(&a.counters[g.tile], g.s1 - g.s0);
-      mine_last = (old + (g.s1 - g.s0) == a.split);
-    }
-    if (named_bar_or(1, kEpiThreads, mine_last)) {
-      __threadfence();
-      finish_tile(a, m0, m1, n0, n1, et);
-      named_bar_sync(1, kEpiThreads);
-      if (et == 0) a.counters[g.tile] = 0;
-    }
-  }
+  if (!full_tile) arrive_split_tile(a, g, m0, m1, n0, n1, et);
   return true;
 }
 

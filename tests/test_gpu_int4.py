@@ -1,7 +1,7 @@
 """GPU parity of the int4-weight GEMM (dequantisation inside the mainloop)
 against the fp64 oracle, through the C ABI.  Same tolerances as the dense
-path; the dequantised weight is rounded once to fp16 on the GPU, which the
-oracle does not do (it is the exact definition)."""
+path.  The kernel accumulates (1024 + q) * a on the tensor cores and applies
+each (row, group)'s scale and zero point once, in fp32."""
 import numpy as np
 import pytest
 import torch
@@ -67,14 +67,15 @@ def test_int4_activation_m_contiguous():
 
 
 def test_int4_general_dequant_path():
-    """Non-integer zero points and scales too small for an exact s/16 in fp16
-    take the kernel's general path; it must round each weight the same way."""
+    """Non-integer zero points and very small scales: the scale and zero
+    point are applied once per (row, group) in fp32, so the result must match
+    the exact oracle and also the oracle on fp16-rounded weights."""
     case = _case(8, 384, 512, split=1, zero=7.5, scale=("uniform", 2e-4, 9e-4))
     inp = wl.make_inputs(case, seed=9)
     c, g, _ = run_case(case, inp)
     ref = oracle_full(case, inp)
     assert_close(c, ref, case.name)
-    # and each weight was rounded once: compare with the oracle on fp16-rounded weights
+    # and it is within tolerance of the oracle on fp16-rounded weights too
     a, b = oracle.logical_operands(case.M, case.N, case.K, inp.A, case.a_layout, inp.lda, case.a_dtype, inp.B,
                                    case.b_layout, 0, wl.INT4, inp.scales, inp.zeros, case.group_size)
     ref_rounded_w = a @ oracle.round_to(b, oracle.F16)
@@ -92,12 +93,14 @@ def test_int4_closed_forms():
     g = m.Gemm(desc)
     C = torch.empty(M * N, dtype=torch.float16, device="cuda")
     Ad = A.cuda()
-    # all codes 8 with zero point 8 -> exactly zero
+    # all codes 8 with zero point 8 -> zero.  The kernel forms
+    # s * (sum (1024 + q) a - (1024 + z) sum a) in fp32, so the two terms
+    # cancel to within fp32 rounding of the ~1024 * sum(a) magnitude.
     W = torch.full((N * Kd // 2,), 0x88, dtype=torch.uint8, device="cuda")
     s = torch.full((N, Kd // 128), 0.01, dtype=torch.float16, device="cuda")
     g.run(Ad, W, C, s, None)
     assert g.sync_status() == 0
-    assert torch.count_nonzero(C).item() == 0
+    assert torch.max(torch.abs(C.float())).item() <= 1e-4
     # all codes 9, scale 1/64 -> C[m, n] = sum_k a[m, k] / 64
     W.fill_(0x99)
     s.fill_(1.0 / 64)
