@@ -79,7 +79,8 @@ typedef struct {
   int32_t num_units;   /* (tile, split) work units */
   int32_t k_per_split; /* Ks in elements */
   int32_t repack_a, repack_b; /* operand copied into the workspace first (stride TMA cannot express) */
-  int32_t kernel;      /* 0 = tensor-core any-layout, 1 = int4 dequant */
+  int32_t kernel;      /* 0 = tensor-core any-layout, 1 = int4 dequant,
+                          2 = tensor-core any-layout on CTA pairs (256 x 256 tiles) */
 } gemm_info_t;
 
 typedef struct gemm_plan gemm_plan_t;

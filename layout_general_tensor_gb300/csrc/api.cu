@@ -72,6 +72,29 @@ gemm_status_t validate(const gemm_desc_t& d) {
   return GEMM_OK;
 }
 
+// Resident clusters of the CTA-pair kernel on each device (queried once).
+int pair_clusters(int device) {
+  constexpr int kMaxDevices = 64;
+  static int cached[kMaxDevices];
+  static std::once_flag once[kMaxDevices];
+  if (device < 0 || device >= kMaxDevices) return 0;
+  std::call_once(once[device], [device] {
+    int c = 0;
+    if (lgt::tc_gemm_pair_max_clusters(&c) != cudaSuccess) {
+      cudaGetLastError();
+      c = 0;
+    }
+    cached[device] = c;
+  });
+  return cached[device];
+}
+
+bool env_flag(const char* name, bool dflt) {
+  const char* s = std::getenv(name);
+  if (!s || !*s) return dflt;
+  return std::atoi(s) != 0;
+}
+
 uint64_t wait_limit_from_env() {
   const char* s = std::getenv("LGT_GEMM_WAIT_LIMIT_MS");
   if (s && *s) {
@@ -130,6 +153,56 @@ bool encode_int4_weights(CUtensorMap* map, const void* ptr, int64_t N, int64_t l
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                           float* partial, int32_t* counters, cudaStream_t stream) {
+  const gemm_desc_t& d = plan->d;
+  TcArgs args;
+  std::memset(&args, 0, sizeof(args));
+  // P operand: the MMA's M side (128-row tiles, 256 for a CTA pair whose
+  // CTAs load 128 each).  Q operand: bn-row tiles (128 per CTA for a pair).
+  const bool a_is_p = !plan->swap;
+  const void* p_ptr = a_is_p ? A : B;
+  const void* q_ptr = a_is_p ? B : A;
+  const int p_mn = a_is_p ? plan->a_mn : plan->b_mn;
+  const int q_mn = a_is_p ? plan->b_mn : plan->a_mn;
+  const int64_t p_ext = a_is_p ? d.M : d.N;
+  const int64_t q_ext = a_is_p ? d.N : d.M;
+  const int64_t p_ld = a_is_p ? lda : ldb;
+  const int64_t q_ld = a_is_p ? ldb : lda;
+  const int q_box = plan->pair ? TILE_P : plan->bn;
+  if (!encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, TILE_P)) return GEMM_ERR_CUDA;
+  if (!encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, q_box)) return GEMM_ERR_CUDA;
+  args.c = C;
+  args.ldc = plan->ldc;
+  args.ws = partial;
+  args.counters = counters;
+  args.status = plan->d_status;
+  args.wait_limit_ns = plan->wait_limit_ns;
+  args.M = static_cast<int32_t>(d.M);
+  args.N = static_cast<int32_t>(d.N);
+  args.K = static_cast<int32_t>(d.K);
+  args.tiles_p = plan->tiles_p;
+  args.tiles_q = plan->tiles_q;
+  args.split = plan->split;
+  args.kb_per_split = plan->kb_per_split;
+  args.kb_total = plan->kb_total;
+  args.num_units = plan->num_units;
+  args.div_split = magic_encode(static_cast<uint32_t>(plan->split));
+  args.div_tiles_p = magic_encode(static_cast<uint32_t>(plan->tiles_p));
+  args.p_mn = p_mn;
+  args.q_mn = q_mn;
+  args.swap = plan->swap;
+  args.c_bf16 = d.c_dtype == GEMM_BF16;
+  args.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (plan->ldc % 8 == 0);
+  args.ws_vec = (d.N % 4 == 0);
+  args.pair = plan->pair;
+  args.idesc = idesc_f16(d.a_dtype == GEMM_BF16 ? 1u : 0u, static_cast<uint32_t>(p_mn), static_cast<uint32_t>(q_mn),
+                         static_cast<uint32_t>(TILE_P << plan->pair), static_cast<uint32_t>(plan->bn));
+  const cudaError_t e = plan->pair ? launch_tc_gemm_pair(args, plan->grid, stream)
+                                   : launch_tc_gemm(args, plan->bn, plan->grid, stream);
+  return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 }  // namespace lgt
@@ -253,8 +326,15 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
     const int o = e ? std::atoi(e) : 0;
     if ((o == 64 || o == 128 || o == 192 || o == 256) && q_extent >= o) bn = o;
   }
+  // Where 256-wide tiles are chosen, a CTA pair shares a 256 x 256 tile (one
+  // cta_group::2 MMA) if the device can co-schedule pairs; LGT_GEMM_PAIR=0
+  // keeps the single-CTA kernel.
+  p.pair = 0;
+  if (!int4 && !p.swap && bn == 256 && p.device >= 0 && env_flag("LGT_GEMM_PAIR", true) &&
+      pair_clusters(p.device) > 0)
+    p.pair = 1;
   p.bn = bn;
-  p.tiles_p = static_cast<int>(ceil_div(p.swap ? d.N : d.M, lgt::TILE_P));
+  p.tiles_p = static_cast<int>(ceil_div(p.swap ? d.N : d.M, lgt::TILE_P << p.pair));
   p.tiles_q = static_cast<int>(ceil_div(q_extent, bn));
 
   // Split-K factor: the SM-waste rule on the logical M x N with 128 x 128 x 64
@@ -271,6 +351,13 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   const int64_t units = static_cast<int64_t>(p.tiles_p) * p.tiles_q * p.split;
   if (units >= (1ll << 31)) return GEMM_ERR_UNSUPPORTED;
   p.num_units = static_cast<int>(units);
+  p.num_counters = p.tiles_p * p.tiles_q * (1 + p.pair);
+  if (p.pair) {
+    const int clusters = pair_clusters(p.device);
+    p.grid = 2 * (p.num_units < clusters ? p.num_units : clusters);
+  } else {
+    p.grid = p.num_units < p.sms_grid ? p.num_units : p.sms_grid;
+  }
 
   // Storage rows of each operand and whether TMA can address them in place.
   p.a_rows = p.a_mn ? d.K : d.M;
@@ -287,7 +374,7 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
     p.off_partial = off;
     off = align_up(off + static_cast<size_t>(d.M) * d.N * sizeof(float), 256);
     p.off_counters = off;
-    off = align_up(off + static_cast<size_t>(p.tiles_p) * p.tiles_q * sizeof(int32_t), 256);
+    off = align_up(off + static_cast<size_t>(p.num_counters) * sizeof(int32_t), 256);
   }
   const size_t pack_a_bytes = align_up(static_cast<size_t>(p.a_rows) * p.a_pack_ld * 2, 256);
   const size_t pack_b_bytes = int4 ? 0 : align_up(static_cast<size_t>(p.b_rows) * p.b_pack_ld * 2, 256);
@@ -334,15 +421,15 @@ gemm_status_t gemm_query(const gemm_plan_t* plan, gemm_info_t* info) {
   if (!plan || !info) return GEMM_ERR_INVALID_ARG;
   std::memset(info, 0, sizeof(*info));
   info->split_k = plan->split;
-  info->tile_m = plan->swap ? plan->bn : lgt::TILE_P;
-  info->tile_n = plan->swap ? lgt::TILE_P : plan->bn;
+  info->tile_m = plan->swap ? plan->bn : (lgt::TILE_P << plan->pair);
+  info->tile_n = plan->swap ? (lgt::TILE_P << plan->pair) : plan->bn;
   info->tile_k = kBlockK;
   info->swap_ab = plan->swap;
   info->num_units = plan->num_units;
   info->k_per_split = plan->kb_per_split * kBlockK;
   info->repack_a = plan->repack_a;
   info->repack_b = plan->repack_b;
-  info->kernel = plan->kernel;
+  info->kernel = plan->kernel == 0 && plan->pair ? 2 : plan->kernel;
   return GEMM_OK;
 }
 
@@ -404,19 +491,13 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     ldb = plan->b_pack_ld;
   }
 
+  float* partial = plan->split > 1 ? reinterpret_cast<float*>(ws + plan->off_partial) : nullptr;
+  int32_t* counters = plan->split > 1 ? reinterpret_cast<int32_t*>(ws + plan->off_counters) : nullptr;
+  if (!int4) return lgt::launch_dense(plan, a_eff, lda, b_eff, ldb, C, partial, counters, stream);
+
   lgt::TcArgs args;
   std::memset(&args, 0, sizeof(args));
-  const bool a_is_p = !plan->swap;
-  // P operand: 128-row tiles.  Q operand: bn-row tiles.
-  const void* p_ptr = a_is_p ? a_eff : b_eff;
-  const void* q_ptr = a_is_p ? b_eff : a_eff;
-  const int p_mn = a_is_p ? plan->a_mn : plan->b_mn;
-  const int q_mn = a_is_p ? plan->b_mn : plan->a_mn;
-  const int64_t p_ext = a_is_p ? d.M : d.N;
-  const int64_t q_ext = a_is_p ? d.N : d.M;
-  const int64_t p_ld = a_is_p ? lda : ldb;
-  const int64_t q_ld = a_is_p ? ldb : lda;
-  if (int4) {
+  {
     // prepared activation: K-contiguous, pitch K, in the workspace
     void* ap = ws + plan->off_aprep;
     float* asum = reinterpret_cast<float*>(ws + plan->off_asum);
@@ -425,18 +506,11 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
                               asum, gsum, plan->asum_ld, plan->sms_grid, stream) != cudaSuccess)
       return GEMM_ERR_CUDA;
     if (!lgt::encode_operand(&args.tm_q, ap, GEMM_F16, false, d.M, d.K, d.K, plan->bn)) return GEMM_ERR_CUDA;
-  } else {
-    if (!lgt::encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, lgt::TILE_P))
-      return GEMM_ERR_CUDA;
-    if (!lgt::encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, plan->bn)) return GEMM_ERR_CUDA;
   }
-
   args.c = C;
   args.ldc = plan->ldc;
-  if (plan->split > 1) {
-    args.ws = reinterpret_cast<float*>(ws + plan->off_partial);
-    args.counters = reinterpret_cast<int32_t*>(ws + plan->off_counters);
-  }
+  args.ws = partial;
+  args.counters = counters;
   args.status = plan->d_status;
   args.wait_limit_ns = plan->wait_limit_ns;
   args.M = static_cast<int32_t>(d.M);
@@ -450,14 +524,11 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   args.num_units = plan->num_units;
   args.div_split = lgt::magic_encode(static_cast<uint32_t>(plan->split));
   args.div_tiles_p = lgt::magic_encode(static_cast<uint32_t>(plan->tiles_p));
-  args.p_mn = p_mn;
-  args.q_mn = q_mn;
   args.swap = plan->swap;
   args.c_bf16 = d.c_dtype == GEMM_BF16;
   args.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (plan->ldc % 8 == 0);
   args.ws_vec = (d.N % 4 == 0);
-  const int grid = plan->num_units < plan->sms_grid ? plan->num_units : plan->sms_grid;
-  if (int4) {
+  {
     // MMA A operand: the dequantised weight in TMEM (K-major); B: the activation
     args.q_mn = 0;
     args.idesc = lgt::idesc_f16(0u, 0u, 0u, lgt::TILE_P, static_cast<uint32_t>(plan->bn));
@@ -474,11 +545,8 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     a4.vec_sz = (a4.groups % 8 == 0) && reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
                 reinterpret_cast<uintptr_t>(zeros) % 16 == 0;
     a4.asum_ld = plan->asum_ld;
-    return lgt::launch_int4_gemm(a4, plan->bn, grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    return lgt::launch_int4_gemm(a4, plan->bn, plan->grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
-  args.idesc = lgt::idesc_f16(d.a_dtype == GEMM_BF16 ? 1u : 0u, static_cast<uint32_t>(p_mn),
-                              static_cast<uint32_t>(q_mn), lgt::TILE_P, static_cast<uint32_t>(plan->bn));
-  return lgt::launch_tc_gemm(args, plan->bn, grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 gemm_status_t gemm_sync_status(gemm_plan_t* plan, void* stream) {

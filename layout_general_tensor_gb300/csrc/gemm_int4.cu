@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
             if (m0 + j < m1) red_add_f32(wc + static_cast<int64_t>(m0 + j) * a.N, acc[j]);
         }
       }
-      if (!full_tile) arrive_split_tile(a, g, m0, m1, n0, n1, et);
+      if (!full_tile) arrive_split_tile(a, g, g.tile, m0, m1, n0, n1, et);
     }
   }
 

@@ -1,0 +1,272 @@
+// CTA-pair variant of the any-layout fp16 / bf16 GEMM (tcgen05 cta_group::2).
+//
+// Two CTAs of a cluster share a 256 x 256 output tile.  Each CTA loads 128
+// rows of the P operand and 128 rows of the Q operand per 64-deep K block;
+// one thread of the even CTA issues a 256 x 256 x 16 MMA that reads both
+// CTAs' shared memory and writes 128 accumulator rows into each CTA's TMEM.
+// Against the single-CTA 128 x 256 tile this moves a third fewer bytes from
+// L2 into shared memory per FLOP and frees room for more pipeline stages.
+//
+// Roles (192 threads per CTA, in both CTAs):
+//   warp 0      TMA producer of this CTA's halves; the copies of both CTAs
+//               complete on the even CTA's stage barrier, which the even
+//               CTA's producer arms with the bytes of both.
+//   warp 1      TMEM allocation (both CTAs, jointly); in the even CTA one lane
+//               issues the MMAs and multicasts each commit to both CTAs'
+//               stage-free / accumulator-full barriers.
+//   warps 2..5  epilogue of the CTA's own 128 accumulator rows (shared code
+//               with the single-CTA kernel); each warp signals "buffer
+//               drained" on the even CTA's barrier.
+//
+// Operand layouts are handled exactly as in the single-CTA kernel (TMA box
+// along the contiguous dimension, 128-byte swizzle, K- or MN-major shared
+// memory descriptors), following the inThreadTranspose page's "Feature
+// description": no operand is transposed by threads.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace lgt {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kEpiWarp0 = 2;
+constexpr int kBN = PAIR_TILE;                        // MMA N: Q rows of a pair tile
+constexpr int kHalf = 128;                            // P rows and Q rows per CTA
+constexpr uint32_t kHalfBytes = kHalf * TILE_K * 2;   // 16 KiB
+constexpr uint32_t kStageBytes = 2 * kHalfBytes;      // this CTA's P half + Q half
+constexpr uint32_t kMnChunkBytes = 64 * TILE_K * 2;   // one 64-wide MN box, 64 K rows: 8 KiB
+constexpr uint32_t kSmemLimit = 227 * 1024;
+constexpr uint32_t kNumBarsFor = 5;                   // accf[2], acce[2], teardown (+ 2 per stage)
+constexpr int kStages = static_cast<int>((kSmemLimit - 1024 - 64 - 8 * kNumBarsFor) / (kStageBytes + 16));
+constexpr uint32_t kBarOff = kStages * kStageBytes;
+constexpr uint32_t kNumBars = 2 * kStages + kNumBarsFor;
+constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+constexpr uint32_t kSmemAlloc = kMiscOff + 64 + 1024;  // slack for 1024-byte alignment
+constexpr uint32_t kTmemCols = 2 * kBN;               // two accumulator buffers: all 512 columns
+constexpr int kCH = 32;
+static_assert(kSmemAlloc <= kSmemLimit, "shared memory budget");
+static_assert(kStages >= 4, "pipeline depth");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_base);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+  const bool leader = rank == 0;
+  const uint32_t bar0 = base + kBarOff;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+  const uint32_t teardown_bar = bar0 + 8u * (2 * kStages + 4);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);   // the even CTA's producer arms it with both CTAs' bytes
+      mbar_init(empty_bar(s), 1);  // multicast MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);                   // multicast MMA commit
+      mbar_init(acce_bar(b), 2 * kEpiThreads / 32);  // epilogue warps of both CTAs
+    }
+    mbar_init(teardown_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&a.tm_p);
+    tma_prefetch_desc(&a.tm_q);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  // Both CTAs' barriers are initialised and TMEM is allocated before any
+  // cross-CTA traffic.
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // The even CTA's barriers in the cluster's shared window.
+  const uint32_t full_bar_leader0 = mapa_shared(full_bar(0), 0);
+  const uint32_t acce_bar_leader0 = mapa_shared(acce_bar(0), 0);
+
+  int issued = 0;  // producer lane: K blocks whose loads were issued
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      Sched sched(a);
+      Group g;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      while (ok && sched.next(a, g)) {
+        int32_t tp, tq, m0, m1, n0, n1;
+        tile_ranges(a, g.tile, kBN, tp, tq, m0, m1, n0, n1);
+        const int32_t prow = tp * kBN + static_cast<int32_t>(rank) * kHalf;
+        const int32_t qrow = tq * kBN + static_cast<int32_t>(rank) * kHalf;
+        for (int kb = 0; kb < g.nkb; ++kb) {
+          if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, a.wait_limit_ns, abort_flag)) {
+            if (!*abort_flag) record_timeout(a, abort_flag, 0 * 16 + 1);
+            ok = false;
+            break;
+          }
+          const uint32_t sp = base + stage * kStageBytes;
+          const uint32_t sq = sp + kHalfBytes;
+          const uint32_t fb = full_bar_leader0 + 8u * stage;
+          const int32_t k0 = (g.kb0 + kb) * TILE_K;
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes);
+          if (!a.p_mn) {
+            tma_load_2d_pair(sp, &a.tm_p, fb, k0, prow);
+          } else {
+            tma_load_2d_pair(sp, &a.tm_p, fb, prow, k0);
+            tma_load_2d_pair(sp + kMnChunkBytes, &a.tm_p, fb, prow + 64, k0);
+          }
+          if (!a.q_mn) {
+            tma_load_2d_pair(sq, &a.tm_q, fb, k0, qrow);
+          } else {
+            tma_load_2d_pair(sq, &a.tm_q, fb, qrow, k0);
+            tma_load_2d_pair(sq + kMnChunkBytes, &a.tm_q, fb, qrow + 64, k0);
+          }
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Wait until the MMAs have released the last stages this CTA filled, so
+      // that no multicast commit targets this CTA after it exits.
+      const int first = issued > kStages ? issued - kStages : 0;
+      for (int it = first; it < issued && !*abort_flag; ++it)
+        if (!mbar_wait_bounded_cluster(empty_bar(it % kStages), (it / kStages) & 1, a.wait_limit_ns, abort_flag) &&
+            !*abort_flag)
+          record_timeout(a, abort_flag, 0 * 16 + 4);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (leader && lane == 0) {
+      Sched sched(a);
+      Group g;
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc_iter = 0;
+      bool ok = true;
+      // Per-MMA (K = 16) start-address advance inside a stage, as in the
+      // single-CTA kernel: K-major 128-byte rows (+32 B per 16 elements),
+      // MN-major 128-byte rows per k (+2 KiB per 16 k), 64-wide chunks 8 KiB apart.
+      const uint32_t p_step = a.p_mn ? 2048u : 32u;
+      const uint32_t q_step = a.q_mn ? 2048u : 32u;
+      const uint32_t p_lbo = a.p_mn ? kMnChunkBytes : 16u;
+      const uint32_t q_lbo = a.q_mn ? kMnChunkBytes : 16u;
+      while (ok && sched.next(a, g)) {
+        if (g.nkb == 0) continue;
+        const int buf = acc_iter & 1;
+        const uint32_t acc_phase = (acc_iter >> 1) & 1;
+        if (!mbar_wait_bounded_cluster(acce_bar(buf), acc_phase ^ 1u, a.wait_limit_ns, abort_flag)) {
+          if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 3);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kBN);
+        for (int kb = 0; kb < g.nkb; ++kb) {
+          if (!mbar_wait_bounded_cluster(full_bar(stage), phase, a.wait_limit_ns, abort_flag)) {
+            if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 0);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sp = base + stage * kStageBytes;
+          const uint32_t sq = sp + kHalfBytes;
+#pragma unroll
+          for (int k = 0; k < TILE_K / 16; ++k) {
+            const uint64_t pd = sw128_desc(sp + k * p_step, p_lbo, 1024u);
+            const uint64_t qd = sw128_desc(sq + k * q_step, q_lbo, 1024u);
+            tc_mma_f16_ss_pair(d_tmem, pd, qd, a.idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(empty_bar(stage), 0x3);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(accf_bar(buf), 0x3);
+        ++acc_iter;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;
+    const int et = threadIdx.x - kEpiWarp0 * 32;
+    Sched sched(a);
+    Group g;
+    int acc_iter = 0;
+    while (sched.next(a, g)) {
+      if (!epilogue_group<kBN, kCH, true>(a, g, tmem_base, accf_bar(0), acce_bar_leader0, acc_iter, abort_flag, q4,
+                                          lane, et, static_cast<int>(rank)))
+        break;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  if (*abort_flag) {
+    // Copies this CTA issued may still be landing (their stage barrier lives
+    // in the even CTA and may never complete): give them time to arrive.
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+  }
+  if (leader && warp == 1 && lane == 0) {
+    // Wait until every MMA of the pair has completed.
+    volatile int no_abort = 0;
+    tc_commit_pair_mc(teardown_bar, 0x1);
+    mbar_wait_bounded(teardown_bar, 0, a.wait_limit_ns, &no_abort);
+  }
+  tc_fence_before();
+  __syncthreads();
+  // Neither CTA leaves while the other may still touch its shared memory.
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm_pair(const TcArgs& args, int grid, cudaStream_t stream) {
+  if (grid < 2 || (grid & 1) || !args.pair) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemAlloc));
+  if (e != cudaSuccess) return e;
+  tc_gemm_pair_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(args);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_gemm_pair_max_clusters(int* clusters) {
+  *clusters = 0;
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemAlloc));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  return cudaOccupancyMaxActiveClusters(clusters, tc_gemm_pair_kernel, &cfg);
+}
+
+}  // namespace lgt

@@ -54,6 +54,7 @@ struct TcArgs {
   int32_t c_bf16;
   int32_t c_vec;         // C rows allow 16-byte vector stores
   int32_t ws_vec;        // workspace rows allow 16-byte vector reductions
+  int32_t pair;          // 1: CTA-pair kernel, 256-row P tiles split over the pair
   uint32_t idesc;
 };
 
@@ -86,6 +87,14 @@ cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K,
 // Returns a cudaError_t; `bn` selects the kernel instance.
 cudaError_t launch_tc_gemm(const TcArgs& args, int bn, int grid, cudaStream_t stream);
 size_t tc_gemm_smem_bytes(int bn);
+
+// CTA-pair kernel (clusters of two CTAs, one cta_group::2 MMA per pair):
+// tiles of 256 P rows x 256 Q rows; `grid` CTAs (even).  args.pair must be 1.
+constexpr int PAIR_TILE = 256;
+cudaError_t launch_tc_gemm_pair(const TcArgs& args, int grid, cudaStream_t stream);
+// Clusters of the pair kernel that can be resident at once on the current
+// device (0 if it cannot run there).
+cudaError_t tc_gemm_pair_max_clusters(int* clusters);
 
 // Copy `rows` rows of `row_bytes` bytes from a source with row pitch
 // `src_pitch` (any 2-byte alignment) into a destination with a 16-byte

@@ -77,8 +77,8 @@ extern "C" gemm_status_t gemm_run_static_scratch(const gemm_plan_t* plan, const 
     return GEMM_ERR_UNSUPPORTED;
 
   // Scratch layout: [tile counters][fp32 partial sums M x N].
-  const size_t tiles = static_cast<size_t>(plan->tiles_p) * plan->tiles_q;
-  const size_t counters_bytes = plan->split > 1 ? align256(tiles * sizeof(int32_t)) : 0;
+  const size_t counters_bytes =
+      plan->split > 1 ? align256(static_cast<size_t>(plan->num_counters) * sizeof(int32_t)) : 0;
   const size_t partial_bytes = plan->split > 1 ? static_cast<size_t>(d.M) * d.N * sizeof(float) : 0;
   if (counters_bytes + partial_bytes > kStaticScratchBytes) return GEMM_ERR_WORKSPACE;
 
@@ -90,46 +90,7 @@ extern "C" gemm_status_t gemm_run_static_scratch(const gemm_plan_t* plan, const 
     if (cudaMemsetAsync(scratch, 0, counters_bytes + partial_bytes, stream) != cudaSuccess) return GEMM_ERR_CUDA;
   }
 
-  lgt::TcArgs args;
-  std::memset(&args, 0, sizeof(args));
-  const bool a_is_p = !plan->swap;
-  const void* p_ptr = a_is_p ? A : B;
-  const void* q_ptr = a_is_p ? B : A;
-  const int p_mn = a_is_p ? plan->a_mn : plan->b_mn;
-  const int q_mn = a_is_p ? plan->b_mn : plan->a_mn;
-  const int64_t p_ext = a_is_p ? d.M : d.N;
-  const int64_t q_ext = a_is_p ? d.N : d.M;
-  const int64_t p_ld = a_is_p ? plan->lda : plan->ldb;
-  const int64_t q_ld = a_is_p ? plan->ldb : plan->lda;
-  if (!lgt::encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, lgt::TILE_P)) return GEMM_ERR_CUDA;
-  if (!lgt::encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, plan->bn)) return GEMM_ERR_CUDA;
-  args.c = C;
-  args.ldc = plan->ldc;
-  if (plan->split > 1) {
-    args.counters = reinterpret_cast<int32_t*>(scratch);
-    args.ws = reinterpret_cast<float*>(scratch + counters_bytes);
-  }
-  args.status = plan->d_status;
-  args.wait_limit_ns = plan->wait_limit_ns;
-  args.M = static_cast<int32_t>(d.M);
-  args.N = static_cast<int32_t>(d.N);
-  args.K = static_cast<int32_t>(d.K);
-  args.tiles_p = plan->tiles_p;
-  args.tiles_q = plan->tiles_q;
-  args.split = plan->split;
-  args.kb_per_split = plan->kb_per_split;
-  args.kb_total = plan->kb_total;
-  args.num_units = plan->num_units;
-  args.div_split = lgt::magic_encode(static_cast<uint32_t>(plan->split));
-  args.div_tiles_p = lgt::magic_encode(static_cast<uint32_t>(plan->tiles_p));
-  args.p_mn = p_mn;
-  args.q_mn = q_mn;
-  args.swap = plan->swap;
-  args.c_bf16 = d.c_dtype == GEMM_BF16;
-  args.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (plan->ldc % 8 == 0);
-  args.ws_vec = (d.N % 4 == 0);
-  args.idesc = lgt::idesc_f16(d.a_dtype == GEMM_BF16 ? 1u : 0u, static_cast<uint32_t>(p_mn),
-                              static_cast<uint32_t>(q_mn), lgt::TILE_P, static_cast<uint32_t>(plan->bn));
-  const int grid = plan->num_units < plan->sms_grid ? plan->num_units : plan->sms_grid;
-  return lgt::launch_tc_gemm(args, plan->bn, grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  float* partial = plan->split > 1 ? reinterpret_cast<float*>(scratch + counters_bytes) : nullptr;
+  int32_t* counters = plan->split > 1 ? reinterpret_cast<int32_t*>(scratch) : nullptr;
+  return lgt::launch_dense(plan, A, plan->lda, B, plan->ldb, C, partial, counters, stream);
 }

@@ -18,6 +18,9 @@ struct gemm_plan {
   int group;         // int4 quantisation group along K
   int swap;
   int bn;
+  int pair;          // 1: CTA-pair kernel (256 x 256 tiles, clusters of two CTAs)
+  int grid;          // CTAs launched by the tensor-core kernels
+  int num_counters;  // split-K arrival counters (one per tile, per half-tile for pairs)
   int split, kb_per_split, kb_total;
   int tiles_p, tiles_q, num_units;
   int64_t lda, ldb, ldc;
@@ -43,5 +46,12 @@ bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major,
 
 // Encode the TMA map over packed int4 weights (see api.cu).
 bool encode_int4_weights(CUtensorMap* map, const void* ptr, int64_t N, int64_t ld_bytes);
+
+// Launch the dense tensor-core kernel of `plan` on operands TMA can address
+// in place (16-byte aligned bases and pitches `lda` / `ldb` in elements),
+// with the split-K partial sums and counters at `partial` / `counters`
+// (zero-filled; unused when split == 1).
+gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                           float* partial, int32_t* counters, cudaStream_t stream);
 
 }  // namespace lgt

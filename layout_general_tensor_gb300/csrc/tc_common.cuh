@@ -21,12 +21,13 @@ struct Group {
 };
 
 // Work assignment.  split == 1: units are tiles, taken round-robin.
-// split > 1: CTA b takes the contiguous unit range
+// split > 1: worker b takes the contiguous unit range
 // [b*U/G, (b+1)*U/G) and a group is a maximal run of one tile's splits.
+// A worker is a CTA, or a CTA pair (both CTAs walk the same units).
 struct Sched {
   int32_t u, u_end, step;
   __device__ Sched(const TcArgs& a) {
-    const int32_t G = gridDim.x, b = blockIdx.x;
+    const int32_t G = gridDim.x >> a.pair, b = blockIdx.x >> a.pair;
     if (a.split == 1) {
       u = b;
       u_end = a.num_units;
@@ -84,23 +85,38 @@ __device__ __forceinline__ uint16_t cvt1(float v, int bf16) {
   return *reinterpret_cast<uint16_t*>(&h);
 }
 
-// (m, n) ranges of a tile in C coordinates.
+// (m, n) ranges of a tile in C coordinates.  A pair tile is 256 rows high
+// on the P side.
 __device__ __forceinline__ void tile_ranges(const TcArgs& a, int32_t tile, int bn, int32_t& tp, int32_t& tq,
                                             int32_t& m0, int32_t& m1, int32_t& n0, int32_t& n1) {
   uint32_t q, r;
   magic_divmod(static_cast<uint32_t>(tile), a.div_tiles_p, q, r);
   tp = static_cast<int32_t>(r);
   tq = static_cast<int32_t>(q);
+  const int32_t pt = TILE_P << a.pair;
   if (!a.swap) {
-    m0 = tp * TILE_P;
+    m0 = tp * pt;
     n0 = tq * bn;
-    m1 = min(a.M, m0 + TILE_P);
+    m1 = min(a.M, m0 + pt);
     n1 = min(a.N, n0 + bn);
   } else {
-    n0 = tp * TILE_P;
+    n0 = tp * pt;
     m0 = tq * bn;
-    n1 = min(a.N, n0 + TILE_P);
+    n1 = min(a.N, n0 + pt);
     m1 = min(a.M, m0 + bn);
+  }
+}
+
+// The 128 P-side rows of a pair tile that CTA `half` of the pair holds in its
+// TMEM (may be empty at a ragged edge).
+__device__ __forceinline__ void narrow_to_half(const TcArgs& a, int half, int32_t& m0, int32_t& m1, int32_t& n0,
+                                               int32_t& n1) {
+  if (!a.swap) {
+    m0 += half * TILE_P;
+    m1 = max(m0, min(m1, m0 + TILE_P));
+  } else {
+    n0 += half * TILE_P;
+    n1 = max(n0, min(n1, n0 + TILE_P));
   }
 }
 
@@ -171,20 +187,20 @@ __device__ __noinline__ void finish_tile(const TcArgs& a, int m0, int m1, int n0
 // workspace: count the run's splits on the tile's arrival counter, and if
 // this arrival completes the tile, convert it (the CTA that arrives last
 // reads the full sum from L2), then reset the counter.
-__device__ __forceinline__ void arrive_split_tile(const TcArgs& a, const Group& g, int m0, int m1, int n0, int n1,
-                                                  int et) {
+__device__ __forceinline__ void arrive_split_tile(const TcArgs& a, const Group& g, int counter, int m0, int m1, int n0,
+                                                  int n1, int et) {
   __threadfence();
   named_bar_sync(1, kEpiThreads);
   bool mine_last = false;
   if (et == 0) {
-    const int old = atomicAdd(&a.counters[g.tile], g.s1 - g.s0);
+    const int old = atomicAdd(&a.counters[counter], g.s1 - g.s0);
     mine_last = (old + (g.s1 - g.s0) == a.split);
   }
   if (named_bar_or(1, kEpiThreads, mine_last)) {
     __threadfence();
     finish_tile(a, m0, m1, n0, n1, et);
     named_bar_sync(1, kEpiThreads);
-    if (et == 0) a.counters[g.tile] = 0;
+    if (et == 0) a.counters[counter] = 0;
   }
 }
 
@@ -194,13 +210,16 @@ __device__ __forceinline__ void arrive_split_tile(const TcArgs& a, const Group& 
 // the tile of C, or adds it to the split-K workspace and, for the CTA whose
 // arrival completes the tile, converts the total.  Returns false when the CTA
 // is aborting; all 128 threads return the same value.
-template <int BN, int CH>
+// PAIR: the CTA holds P-side half `half` of a pair tile, and the buffer-free
+// arrival goes to the pair's MMA CTA (acce_bar0 is a shared::cluster address).
+template <int BN, int CH, bool PAIR = false>
 __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, uint32_t tmem_base, uint32_t accf_bar0,
                                                uint32_t acce_bar0, int& acc_iter, volatile int* abort_flag, int q4,
-                                               int lane, int et) {
+                                               int lane, int et, int half = 0) {
   const int row = q4 * 32 + lane;  // accumulator row (TMEM lane)
   int32_t tp, tq, m0, m1, n0, n1;
   tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
+  if (PAIR) narrow_to_half(a, half, m0, m1, n0, n1);
   const bool full_tile = (g.s0 == 0 && g.s1 == a.split);
   if (g.nkb > 0) {
     const int buf = acc_iter & 1;
@@ -276,10 +295,15 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(acce_bar0 + 8u * buf);
+    if (lane == 0) {
+      if (PAIR)
+        mbar_arrive_cluster(acce_bar0 + 8u * buf);
+      else
+        mbar_arrive(acce_bar0 + 8u * buf);
+    }
     ++acc_iter;
   }
-  if (!full_tile) arrive_split_tile(a, g, m0, m1, n0, n1, et);
+  if (!full_tile) arrive_split_tile(a, g, PAIR ? 2 * g.tile + half : g.tile, m0, m1, n0, n1, et);
   return true;
 }
 
