@@ -68,8 +68,12 @@ typedef struct {
   int32_t split_k;            /* 0 = SM-waste rule; >= 1 explicit factor */
   int32_t group_size;         /* int4 quantisation group along K (0 = 128); must divide K and the split length */
   int32_t num_sms;            /* SM count the split-K rule uses: 0 = the current device's */
-  int32_t flags;              /* reserved, must be 0 */
+  int32_t flags;              /* 0 or GEMM_FLAG_DETERMINISTIC */
 } gemm_desc_t;
+
+/* Bitwise-reproducible results: no stream-K tail (below).  Split-K factors
+ * above 1 are rejected with GEMM_ERR_UNSUPPORTED under this flag. */
+#define GEMM_FLAG_DETERMINISTIC 1
 
 /* What a plan decided. */
 typedef struct {
@@ -81,11 +85,21 @@ typedef struct {
   int32_t repack_a, repack_b; /* operand copied into the workspace first (stride TMA cannot express) */
   int32_t kernel;      /* 0 = tensor-core any-layout, 1 = int4 dequant,
                           2 = tensor-core any-layout on CTA pairs (256 x 256 tiles) */
+  int32_t streamk_tiles; /* tiles of the stream-K tail (0 = none), see gemm_create */
 } gemm_info_t;
 
 typedef struct gemm_plan gemm_plan_t;
 
 /* Validate `desc`, choose tiles and the split factor, and return a plan.
+ *
+ * Stream-K tail.  With split factor 1 (given, or from the rule) the tiles
+ * are dealt to the persistent CTAs in whole waves; when the last wave would
+ * leave at least a quarter of the CTAs idle, the K blocks of its tiles are
+ * spread evenly over all CTAs instead and their fp32 partial sums reduced as
+ * split-K partials are (so those tiles' rounding order depends on timing).
+ * The workspace then holds an M x N fp32 region.  GEMM_FLAG_DETERMINISTIC
+ * turns it off; gemm_info_t.streamk_tiles reports it.
+ *
  * Needs a CUDA device only when desc->num_sms == 0 (to count its SMs); the
  * plan's kernels run on the device current at gemm_create.  The plan is
  * immutable and may be used from several streams, each with its own

@@ -21,6 +21,8 @@ GEMM_ERR_WORKSPACE = 4
 GEMM_ERR_CUDA = 5
 GEMM_ERR_TIMEOUT = 6
 
+GEMM_FLAG_DETERMINISTIC = 1
+
 GEMM_K_CONTIG = 0
 GEMM_MN_CONTIG = 1
 
@@ -55,6 +57,7 @@ class gemm_info_t(ctypes.Structure):
         ("tile_k", ctypes.c_int32), ("swap_ab", ctypes.c_int32), ("num_units", ctypes.c_int32),
         ("k_per_split", ctypes.c_int32), ("repack_a", ctypes.c_int32), ("repack_b", ctypes.c_int32),
         ("kernel", ctypes.c_int32),
+        ("streamk_tiles", ctypes.c_int32),
     ]
 
 

@@ -58,7 +58,8 @@ gemm_status_t validate(const gemm_desc_t& d) {
   } else if (!is_half(d.a_dtype) || d.a_dtype != d.b_dtype) {
     return GEMM_ERR_INVALID_ARG;
   }
-  if (d.split_k < 0 || d.split_k > 65536 || d.num_sms < 0 || d.group_size < 0 || d.flags != 0)
+  if (d.split_k < 0 || d.split_k > 65536 || d.num_sms < 0 || d.group_size < 0 ||
+      (d.flags & ~GEMM_FLAG_DETERMINISTIC) != 0)
     return GEMM_ERR_INVALID_ARG;
   if (d.lda < 0 || d.ldb < 0 || d.ldc < 0) return GEMM_ERR_INVALID_ARG;
   const int64_t a_min = d.a_layout == GEMM_K_CONTIG ? d.K : d.M;
@@ -89,11 +90,32 @@ int pair_clusters(int device) {
   return cached[device];
 }
 
-bool env_flag(const char* name, bool dflt) {
+// Integer value of an environment variable, or `dflt` when unset / empty.
+int env_int(const char* name, int dflt) {
   const char* s = std::getenv(name);
   if (!s || !*s) return dflt;
-  return std::atoi(s) != 0;
+  return std::atoi(s);
 }
+
+// Time model of a persistent tile kernel (relative units: microseconds of a
+// 4096-deep K loop on this GPU).  A full wave is paced by the operand stream
+// from L2 into shared memory: measured 18.2 us for pair tiles of width 128,
+// 21.2 us for width 256 (about w + 650 column-units), 25.2 us for single-CTA
+// 128 x 256 tiles.  A partial last wave competes with fewer CTAs and runs
+// faster, but a tile never beats its pure MMA time (17 us for 256 columns).
+double waves_cost(int64_t tiles, int64_t workers, double wave_us, double mma_us) {
+  const int64_t full = tiles / workers, rest = tiles % workers;
+  double t = static_cast<double>(full) * wave_us;
+  if (rest) {
+    const double frac = static_cast<double>(rest) / static_cast<double>(workers) * wave_us;
+    t += frac > mma_us ? frac : mma_us;
+  }
+  return t;
+}
+double pair_wave_us(int w) { return (w + 650.0) / 906.0 * 21.2; }
+double mma_tile_us(int w) { return w / 256.0 * 17.0; }
+constexpr double kSingleWave256Us = 25.2;
+constexpr int kPairWidths[] = {256, 224, 192, 160, 128};
 
 uint64_t wait_limit_from_env() {
   const char* s = std::getenv("LGT_GEMM_WAIT_LIMIT_MS");
@@ -138,6 +160,26 @@ bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major,
   return r == CUDA_SUCCESS;
 }
 
+// Output-side maps for the staged epilogue: a row-major rows x cols matrix
+// (row pitch `pitch_bytes`), box 32 x 32.  fp32 partials use the 128-byte
+// swizzle (32 floats = one 128-byte row); 16-bit C is unswizzled.
+bool encode_output(CUtensorMap* map, void* ptr, bool fp32, int c_dtype, int64_t rows, int64_t cols,
+                   int64_t pitch_bytes) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  const CUtensorMapDataType dt = fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                      : (c_dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(EPI_BOX), static_cast<cuuint32_t>(EPI_BOX)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Packed int4 weights: N rows of `ld_bytes` bytes (K/2 used), box 128 bytes
 // (256 codes) x 128 rows, 128-byte swizzle so that the threads' 16-byte row
 // reads fall in different bank groups.
@@ -171,7 +213,7 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
   const int64_t q_ext = a_is_p ? d.N : d.M;
   const int64_t p_ld = a_is_p ? lda : ldb;
   const int64_t q_ld = a_is_p ? ldb : lda;
-  const int q_box = plan->pair ? TILE_P : plan->bn;
+  const int q_box = plan->pair ? plan->bn / 2 : plan->bn;
   if (!encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, TILE_P)) return GEMM_ERR_CUDA;
   if (!encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, q_box)) return GEMM_ERR_CUDA;
   args.c = C;
@@ -189,6 +231,8 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
   args.kb_per_split = plan->kb_per_split;
   args.kb_total = plan->kb_total;
   args.num_units = plan->num_units;
+  args.rr_tiles = plan->rr_tiles;
+  args.tail_tiles = plan->tail_tiles;
   args.div_split = magic_encode(static_cast<uint32_t>(plan->split));
   args.div_tiles_p = magic_encode(static_cast<uint32_t>(plan->tiles_p));
   args.p_mn = p_mn;
@@ -198,11 +242,30 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
   args.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (plan->ldc % 8 == 0);
   args.ws_vec = (d.N % 4 == 0);
   args.pair = plan->pair;
+  // Staged epilogue: whole-line bulk stores of C and bulk reductions of the
+  // fp32 partials, where the pointers and pitches allow them (16 bytes).
+  if (!plan->swap && env_int("LGT_GEMM_TMA_EPI", 1) != 0) {
+    args.tma_c = args.c_vec && encode_output(&args.tm_c, C, false, d.c_dtype, d.M, d.N, plan->ldc * 2);
+    args.tma_ws = partial && (d.N % 4 == 0) && encode_output(&args.tm_ws, partial, true, 0, d.M, d.N, d.N * 4);
+  }
   args.idesc = idesc_f16(d.a_dtype == GEMM_BF16 ? 1u : 0u, static_cast<uint32_t>(p_mn), static_cast<uint32_t>(q_mn),
                          static_cast<uint32_t>(TILE_P << plan->pair), static_cast<uint32_t>(plan->bn));
-  const cudaError_t e = plan->pair ? launch_tc_gemm_pair(args, plan->grid, stream)
+  const cudaError_t e = plan->pair ? launch_tc_gemm_pair(args, plan->bn, plan->grid, stream)
                                    : launch_tc_gemm(args, plan->bn, plan->grid, stream);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_plan plan_without_tail(const gemm_plan& p) {
+  gemm_plan q = p;
+  if (!q.tail_tiles) return q;
+  q.split = 1;
+  q.kb_per_split = q.kb_total;
+  q.rr_tiles = q.tiles_p * q.tiles_q;
+  q.tail_tiles = 0;
+  q.num_units = q.rr_tiles;
+  const int workers = q.pair ? q.grid / 2 : q.sms_grid;
+  q.grid = (q.pair ? 2 : 1) * (q.num_units < workers ? q.num_units : workers);
+  return q;
 }
 
 }  // namespace lgt
@@ -326,13 +389,32 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
     const int o = e ? std::atoi(e) : 0;
     if ((o == 64 || o == 128 || o == 192 || o == 256) && q_extent >= o) bn = o;
   }
-  // Where 256-wide tiles are chosen, a CTA pair shares a 256 x 256 tile (one
-  // cta_group::2 MMA) if the device can co-schedule pairs; LGT_GEMM_PAIR=0
-  // keeps the single-CTA kernel.
+  // CTA pairs (one cta_group::2 MMA over a 256 x w tile, w in 128..256):
+  // where the single-CTA plan has at least a wave of 256-wide tiles, take the
+  // pair width with the lowest modelled time if it beats the single-CTA plan.
+  // LGT_GEMM_PAIR=0 / 1 disables / forces pairs, LGT_GEMM_PAIR_BN forces w.
   p.pair = 0;
-  if (!int4 && !p.swap && bn == 256 && p.device >= 0 && env_flag("LGT_GEMM_PAIR", true) &&
-      pair_clusters(p.device) > 0)
-    p.pair = 1;
+  const int clusters = (!int4 && !p.swap && p.device >= 0) ? pair_clusters(p.device) : 0;
+  if (clusters > 0) {
+    const int mode = env_int("LGT_GEMM_PAIR", -1);
+    const int forced_w = env_int("LGT_GEMM_PAIR_BN", 0);
+    const int64_t pair_rows = ceil_div(d.M, 2 * lgt::TILE_P);
+    int best_w = 0;
+    double best = 0;
+    for (int w : kPairWidths) {
+      if (forced_w && w != forced_w) continue;
+      const double c = waves_cost(pair_rows * ceil_div(q_extent, w), clusters, pair_wave_us(w), mma_tile_us(w));
+      if (!best_w || c < best) {
+        best_w = w;
+        best = c;
+      }
+    }
+    const double single = waves_cost(p_tiles * ceil_div(q_extent, bn), sms, kSingleWave256Us, mma_tile_us(bn));
+    if (best_w && (mode == 1 || (mode != 0 && bn == 256 && best < single))) {
+      p.pair = 1;
+      bn = best_w;
+    }
+  }
   p.bn = bn;
   p.tiles_p = static_cast<int>(ceil_div(p.swap ? d.N : d.M, lgt::TILE_P << p.pair));
   p.tiles_q = static_cast<int>(ceil_div(q_extent, bn));
@@ -347,14 +429,36 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   } else {
     p.split = d.split_k;
   }
+  if ((d.flags & GEMM_FLAG_DETERMINISTIC) && p.split > 1) return GEMM_ERR_UNSUPPORTED;
+  p.split_req = p.split;
   p.kb_per_split = p.kb_total > 0 ? static_cast<int>(ceil_div(p.kb_total, p.split)) : 0;
-  const int64_t units = static_cast<int64_t>(p.tiles_p) * p.tiles_q * p.split;
-  if (units >= (1ll << 31)) return GEMM_ERR_UNSUPPORTED;
-  p.num_units = static_cast<int>(units);
-  p.num_counters = p.tiles_p * p.tiles_q * (1 + p.pair);
+  const int64_t tiles = static_cast<int64_t>(p.tiles_p) * p.tiles_q;
+  if (tiles * (p.kb_total > 0 ? p.kb_total : 1) >= (1ll << 31)) return GEMM_ERR_UNSUPPORTED;
+  const int workers = p.pair ? pair_clusters(p.device) : p.sms_grid;
+  p.rr_tiles = p.split == 1 ? static_cast<int>(tiles) : 0;
+  p.tail_tiles = 0;
+  // Stream-K tail: with no K split, whole waves of tiles run as they are and
+  // the K blocks of a last partial wave (at most 3/4 full) are spread evenly
+  // over all workers, their fp32 partials reduced like split-K partials.
+  // Off with GEMM_FLAG_DETERMINISTIC or LGT_GEMM_STREAMK=0.
+  if (!int4 && !p.swap && p.split == 1 && !(d.flags & GEMM_FLAG_DETERMINISTIC) && p.kb_total >= 2 && workers > 0 &&
+      env_int("LGT_GEMM_STREAMK", 1) != 0) {
+    const int64_t full = tiles / workers, rest = tiles % workers;
+    // (at least three whole waves: the tail's conversion runs behind the
+    // whole tiles that follow it and needs two of them to stay hidden)
+    if (full >= 3 && rest > 0 && rest * 4 <= static_cast<int64_t>(workers) * 3) {
+      p.rr_tiles = static_cast<int>(full * workers);
+      p.tail_tiles = static_cast<int>(rest);
+      p.split = p.kb_total;  // a tail tile's units are its single K blocks
+      p.kb_per_split = 1;
+    }
+  }
+  p.num_units = static_cast<int>(tiles * p.split);
+  // arrival counters per tile (per half-tile for pairs); a stream-K tail
+  // also keeps a finished-rows counter per half-tile after them
+  p.num_counters = static_cast<int>(tiles) * (1 + p.pair) * (p.tail_tiles ? 2 : 1);
   if (p.pair) {
-    const int clusters = pair_clusters(p.device);
-    p.grid = 2 * (p.num_units < clusters ? p.num_units : clusters);
+    p.grid = 2 * (p.num_units < workers ? p.num_units : workers);
   } else {
     p.grid = p.num_units < p.sms_grid ? p.num_units : p.sms_grid;
   }
@@ -420,13 +524,14 @@ gemm_status_t gemm_workspace_size(const gemm_plan_t* plan, size_t* bytes) {
 gemm_status_t gemm_query(const gemm_plan_t* plan, gemm_info_t* info) {
   if (!plan || !info) return GEMM_ERR_INVALID_ARG;
   std::memset(info, 0, sizeof(*info));
-  info->split_k = plan->split;
+  info->split_k = plan->split_req;
   info->tile_m = plan->swap ? plan->bn : (lgt::TILE_P << plan->pair);
-  info->tile_n = plan->swap ? (lgt::TILE_P << plan->pair) : plan->bn;
+  info->tile_n = plan->swap ? lgt::TILE_P : plan->bn;
   info->tile_k = kBlockK;
   info->swap_ab = plan->swap;
   info->num_units = plan->num_units;
-  info->k_per_split = plan->kb_per_split * kBlockK;
+  info->k_per_split = static_cast<int32_t>(ceil_div(plan->kb_total, plan->split_req) * kBlockK);
+  info->streamk_tiles = plan->tail_tiles;
   info->repack_a = plan->repack_a;
   info->repack_b = plan->repack_b;
   info->kernel = plan->kernel == 0 && plan->pair ? 2 : plan->kernel;
@@ -522,6 +627,7 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   args.kb_per_split = plan->kb_per_split;
   args.kb_total = plan->kb_total;
   args.num_units = plan->num_units;
+  args.rr_tiles = plan->rr_tiles;
   args.div_split = lgt::magic_encode(static_cast<uint32_t>(plan->split));
   args.div_tiles_p = lgt::magic_encode(static_cast<uint32_t>(plan->tiles_p));
   args.swap = plan->swap;

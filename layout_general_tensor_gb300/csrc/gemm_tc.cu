@@ -8,6 +8,8 @@
 //   warps 2..5  epilogue: tcgen05.ld the accumulator, then either convert and
 //               store C, or add the fp32 partial into the workspace and let the
 //               last-arriving CTA of the tile convert and store.
+//   warps 6..9  stream-K fixup: convert this CTA's share of the tail tiles
+//               once their partial sums are complete (idle without a tail).
 //
 // Operand layouts.  The Triton inThreadTranspose page ("Feature description")
 // fixes the problem: a dot operand that is not contiguous along K must still
@@ -37,7 +39,8 @@
 namespace lgt {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // 6 warps + 4 stream-K fixup warps
+constexpr int kFixWarp0 = 6;
 constexpr int kEpiWarp0 = 2;
 constexpr uint32_t kP_BYTES = TILE_P * TILE_K * 2;   // 16 KiB
 constexpr uint32_t kMnChunkBytes = 64 * TILE_K * 2;  // one 64-wide MN box, 64 K rows: 8 KiB
@@ -46,20 +49,22 @@ template <int BN>
 struct Cfg {
   static constexpr uint32_t Q_BYTES = BN * TILE_K * 2;
   static constexpr uint32_t STAGE_BYTES = kP_BYTES + Q_BYTES;
-  static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES_RAW = (194 * 1024) / STAGE_BYTES;  // leaves room for the epilogue staging
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
   // two accumulator buffers of BN fp32 columns, rounded up to a power of two
   static constexpr uint32_t TMEM_COLS = (2 * BN) <= 32 ? 32 : (2 * BN) <= 64 ? 64 : (2 * BN) <= 128 ? 128
                                         : (2 * BN) <= 256 ? 256 : 512;
   static constexpr int CH = BN < 32 ? BN : 32;          // accumulator columns per tcgen05.ld
+  static constexpr uint32_t EPI_OFF = STAGES * STAGE_BYTES;  // 1024-aligned (stages are 2 KiB multiples)
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2], teardown
-  static constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr uint32_t BAR_OFF = EPI_OFF + EPI_STAGING_BYTES;
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_USED = MISC_OFF + 64;
   static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
   static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM allocation");
+  static_assert(EPI_OFF % 1024 == 0 && SMEM_ALLOC <= 227 * 1024, "shared memory layout");
 };
 
 template <int BN>
@@ -209,6 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       }
       *consumed_slot = consumed;
     }
+  } else if (warp >= kFixWarp0) {
+    // ------------------------------------------------------------ stream-K fixup
+    if (a.tail_tiles) finish_tail<BN>(a, abort_flag, threadIdx.x - kFixWarp0 * 32);
   } else {
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;                  // TMEM lane quadrant this warp may access
@@ -216,13 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     Sched sched(a);
     Group g;
     int acc_iter = 0;
-    bool ok = true;
-    while (ok && sched.next(a, g)) {
-      if (!epilogue_group<BN, C::CH>(a, g, tmem_base, accf_bar(0), acce_bar(0), acc_iter, abort_flag, q4, lane, et)) {
-        ok = false;
+    int ring = 0;
+    const uint32_t stage_smem = base + C::EPI_OFF + static_cast<uint32_t>(warp - kEpiWarp0) * 8192u;
+    while (sched.next(a, g)) {
+      if (!epilogue_group<BN, C::CH>(a, g, tmem_base, accf_bar(0), acce_bar(0), acc_iter, abort_flag, q4, lane, et,
+                                     0, stage_smem, ring))
         break;
-      }
     }
+    if (lane == 0) bulk_wait_group<0>();  // staged stores finished before the CTA exits
   }
 
   // ------------------------------------------------------------ teardown
@@ -254,8 +263,19 @@ cudaError_t launch_bn(const TcArgs& args, int grid, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM_ALLOC));
   if (e != cudaSuccess) return e;
-  tc_gemm_kernel<BN><<<grid, kThreads, C::SMEM_ALLOC, stream>>>(args);
-  return cudaGetLastError();
+  // A stream-K tail makes CTAs wait for each other's partial sums: launch
+  // cooperatively so that all CTAs are resident together.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = args.tail_tiles ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN>, args);
 }
 
 }  // namespace

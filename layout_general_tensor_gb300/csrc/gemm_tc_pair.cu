@@ -1,13 +1,15 @@
 // CTA-pair variant of the any-layout fp16 / bf16 GEMM (tcgen05 cta_group::2).
 //
-// Two CTAs of a cluster share a 256 x 256 output tile.  Each CTA loads 128
-// rows of the P operand and 128 rows of the Q operand per 64-deep K block;
-// one thread of the even CTA issues a 256 x 256 x 16 MMA that reads both
-// CTAs' shared memory and writes 128 accumulator rows into each CTA's TMEM.
-// Against the single-CTA 128 x 256 tile this moves a third fewer bytes from
-// L2 into shared memory per FLOP and frees room for more pipeline stages.
+// Two CTAs of a cluster share a 256 x BN output tile (BN in 128..256).  Each
+// CTA loads 128 rows of the P operand and BN/2 rows of the Q operand per
+// 64-deep K block; one thread of the even CTA issues a 256 x BN x 16 MMA
+// that reads both CTAs' shared memory and writes 128 accumulator rows into
+// each CTA's TMEM.  Against the single-CTA 128 x 256 tile this moves a third
+// fewer bytes from L2 into shared memory per FLOP and frees room for more
+// pipeline stages.  The planner picks BN so that the tiles fill whole waves
+// of CTA pairs.
 //
-// Roles (192 threads per CTA, in both CTAs):
+// Roles (320 threads per CTA, in both CTAs):
 //   warp 0      TMA producer of this CTA's halves; the copies of both CTAs
 //               complete on the even CTA's stage barrier, which the even
 //               CTA's producer arms with the bytes of both.
@@ -17,6 +19,7 @@
 //   warps 2..5  epilogue of the CTA's own 128 accumulator rows (shared code
 //               with the single-CTA kernel); each warp signals "buffer
 //               drained" on the even CTA's barrier.
+//   warps 6..9  stream-K fixup of this CTA's share of the tail tiles.
 //
 // Operand layouts are handled exactly as in the single-CTA kernel (TMA box
 // along the contiguous dimension, 128-byte swizzle, K- or MN-major shared
@@ -32,27 +35,33 @@
 namespace lgt {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // 6 warps + 4 stream-K fixup warps
+constexpr int kFixWarp0 = 6;
 constexpr int kEpiWarp0 = 2;
-constexpr int kBN = PAIR_TILE;                        // MMA N: Q rows of a pair tile
-constexpr int kHalf = 128;                            // P rows and Q rows per CTA
-constexpr uint32_t kHalfBytes = kHalf * TILE_K * 2;   // 16 KiB
+constexpr int kHalf = 128;                            // P rows per CTA
+constexpr uint32_t kHalfBytes = kHalf * TILE_K * 2;   // 16 KiB: the P half, and room for the Q half
 constexpr uint32_t kStageBytes = 2 * kHalfBytes;      // this CTA's P half + Q half
 constexpr uint32_t kMnChunkBytes = 64 * TILE_K * 2;   // one 64-wide MN box, 64 K rows: 8 KiB
 constexpr uint32_t kSmemLimit = 227 * 1024;
 constexpr uint32_t kNumBarsFor = 5;                   // accf[2], acce[2], teardown (+ 2 per stage)
-constexpr int kStages = static_cast<int>((kSmemLimit - 1024 - 64 - 8 * kNumBarsFor) / (kStageBytes + 16));
-constexpr uint32_t kBarOff = kStages * kStageBytes;
+constexpr int kStages = static_cast<int>((kSmemLimit - EPI_STAGING_BYTES - 1024 - 64 - 8 * kNumBarsFor) /
+                                         (kStageBytes + 16));
+constexpr uint32_t kEpiOff = kStages * kStageBytes;
+constexpr uint32_t kBarOff = kEpiOff + EPI_STAGING_BYTES;
 constexpr uint32_t kNumBars = 2 * kStages + kNumBarsFor;
 constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
 constexpr uint32_t kSmemAlloc = kMiscOff + 64 + 1024;  // slack for 1024-byte alignment
-constexpr uint32_t kTmemCols = 2 * kBN;               // two accumulator buffers: all 512 columns
+constexpr uint32_t kTmemCols = 512;                   // two accumulator buffers of BN <= 256 columns
 constexpr int kCH = 32;
 static_assert(kSmemAlloc <= kSmemLimit, "shared memory budget");
 static_assert(kStages >= 4, "pipeline depth");
 
+template <int kBN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcArgs a) {
+  static_assert(kBN % 32 == 0 && kBN >= 128 && kBN <= 256, "pair tile width");
+  constexpr int kQHalf = kBN / 2;                   // Q rows per CTA
+  constexpr int kQChunks = (kQHalf + 63) / 64;      // 64-wide boxes of an MN-major Q half
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -111,11 +120,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // Bytes of both CTAs' copies per stage (an MN-major Q half is loaded in
+      // whole 64-wide boxes).
+      const uint32_t q_bytes = a.q_mn ? kQChunks * kMnChunkBytes : kQHalf * TILE_K * 2;
+      const uint32_t pair_bytes = 2 * (kHalfBytes + q_bytes);
       while (ok && sched.next(a, g)) {
         int32_t tp, tq, m0, m1, n0, n1;
         tile_ranges(a, g.tile, kBN, tp, tq, m0, m1, n0, n1);
-        const int32_t prow = tp * kBN + static_cast<int32_t>(rank) * kHalf;
-        const int32_t qrow = tq * kBN + static_cast<int32_t>(rank) * kHalf;
+        const int32_t prow = tp * (2 * kHalf) + static_cast<int32_t>(rank) * kHalf;
+        const int32_t qrow = tq * kBN + static_cast<int32_t>(rank) * kQHalf;
         for (int kb = 0; kb < g.nkb; ++kb) {
           if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, a.wait_limit_ns, abort_flag)) {
             if (!*abort_flag) record_timeout(a, abort_flag, 0 * 16 + 1);
@@ -126,7 +139,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t sq = sp + kHalfBytes;
           const uint32_t fb = full_bar_leader0 + 8u * stage;
           const int32_t k0 = (g.kb0 + kb) * TILE_K;
-          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes);
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
           if (!a.p_mn) {
             tma_load_2d_pair(sp, &a.tm_p, fb, k0, prow);
           } else {
@@ -136,8 +149,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!a.q_mn) {
             tma_load_2d_pair(sq, &a.tm_q, fb, k0, qrow);
           } else {
-            tma_load_2d_pair(sq, &a.tm_q, fb, qrow, k0);
-            tma_load_2d_pair(sq + kMnChunkBytes, &a.tm_q, fb, qrow + 64, k0);
+#pragma unroll
+            for (int j = 0; j < kQChunks; ++j)
+              tma_load_2d_pair(sq + j * kMnChunkBytes, &a.tm_q, fb, qrow + 64 * j, k0);
           }
           ++issued;
           if (++stage == kStages) {
@@ -206,6 +220,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ++acc_iter;
       }
     }
+  } else if (warp >= kFixWarp0) {
+    // ------------------------------------------------------------ stream-K fixup
+    if (a.tail_tiles) finish_tail<kBN>(a, abort_flag, threadIdx.x - kFixWarp0 * 32);
   } else {
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;
@@ -213,11 +230,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     Sched sched(a);
     Group g;
     int acc_iter = 0;
+    int ring = 0;
+    const uint32_t stage_smem = base + kEpiOff + static_cast<uint32_t>(warp - kEpiWarp0) * 8192u;
     while (sched.next(a, g)) {
       if (!epilogue_group<kBN, kCH, true>(a, g, tmem_base, accf_bar(0), acce_bar_leader0, acc_iter, abort_flag, q4,
-                                          lane, et, static_cast<int>(rank)))
+                                          lane, et, static_cast<int>(rank), stage_smem, ring))
         break;
     }
+    if (lane == 0) bulk_wait_group<0>();  // staged stores finished before the CTA exits
   }
 
   // ------------------------------------------------------------ teardown
@@ -243,20 +263,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
-}  // namespace
-
-cudaError_t launch_tc_gemm_pair(const TcArgs& args, int grid, cudaStream_t stream) {
-  if (grid < 2 || (grid & 1) || !args.pair) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int BN>
+cudaError_t launch_bn(const TcArgs& args, int grid, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemAlloc));
   if (e != cudaSuccess) return e;
-  tc_gemm_pair_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(args);
-  return cudaGetLastError();
+  // A stream-K tail makes CTAs wait for each other's partial sums: launch
+  // cooperatively so that all CTAs are resident together.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = args.tail_tiles ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN>, args);
+}
+
+}  // namespace
+
+bool tc_gemm_pair_supports(int bn) { return bn == 128 || bn == 160 || bn == 192 || bn == 224 || bn == 256; }
+
+cudaError_t launch_tc_gemm_pair(const TcArgs& args, int bn, int grid, cudaStream_t stream) {
+  if (grid < 2 || (grid & 1) || !args.pair) return cudaErrorInvalidValue;
+  switch (bn) {
+    case 128: return launch_bn<128>(args, grid, stream);
+    case 160: return launch_bn<160>(args, grid, stream);
+    case 192: return launch_bn<192>(args, grid, stream);
+    case 224: return launch_bn<224>(args, grid, stream);
+    case 256: return launch_bn<256>(args, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t tc_gemm_pair_max_clusters(int* clusters) {
   *clusters = 0;
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // every width has the same block size and shared memory
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemAlloc));
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -266,7 +312,7 @@ cudaError_t tc_gemm_pair_max_clusters(int* clusters) {
   cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemAlloc;
-  return cudaOccupancyMaxActiveClusters(clusters, tc_gemm_pair_kernel, &cfg);
+  return cudaOccupancyMaxActiveClusters(clusters, tc_gemm_pair_kernel<256>, &cfg);
 }
 
 }  // namespace lgt

@@ -14,6 +14,11 @@ namespace lgt {
 constexpr int TILE_P = 128;
 constexpr int TILE_K = 64;
 
+// Epilogue staging in shared memory: per epilogue warp, two 4 KiB buffers of
+// one 32-row x 32-column output block (fp32 partials or 16-bit C).
+constexpr int EPI_BOX = 32;
+constexpr uint32_t EPI_STAGING_BYTES = 4 * 2 * 4096;
+
 // Instruction descriptor, kind::f16, fp32 accumulator, dense.
 //   bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (0 = f16,
 //   1 = bf16); 15 / 16 A / B major (0 = K-major, 1 = MN-major);
@@ -37,6 +42,8 @@ struct DeviceStatus {
 struct TcArgs {
   CUtensorMap tm_p;
   CUtensorMap tm_q;
+  CUtensorMap tm_c;     // C, box 32 x 32, for bulk tile stores (valid if tma_c)
+  CUtensorMap tm_ws;    // fp32 partial sums, box 32 x 32, for bulk reductions (valid if tma_ws)
   void* c;
   float* ws;            // fp32 partial sums [M][N] (split > 1)
   int32_t* counters;    // per-tile arrival counters (split > 1)
@@ -47,6 +54,8 @@ struct TcArgs {
   int32_t tiles_p, tiles_q;
   int32_t split, kb_per_split, kb_total;
   int32_t num_units;
+  int32_t rr_tiles;      // tiles dealt whole, round-robin, after the contiguous unit ranges
+  int32_t tail_tiles;    // stream-K tail tiles [rr_tiles, rr_tiles + tail_tiles): finished by all CTAs at the end
   MagicDiv div_split;    // unit -> (tile, split)
   MagicDiv div_tiles_p;  // tile -> (tile_p, tile_q)
   int32_t p_mn, q_mn;    // 1: operand tile is MN-major in shared memory
@@ -55,6 +64,8 @@ struct TcArgs {
   int32_t c_vec;         // C rows allow 16-byte vector stores
   int32_t ws_vec;        // workspace rows allow 16-byte vector reductions
   int32_t pair;          // 1: CTA-pair kernel, 256-row P tiles split over the pair
+  int32_t tma_c;         // full tiles leave through shared memory and bulk tile stores
+  int32_t tma_ws;        // partial tiles leave through shared memory and bulk reductions
   uint32_t idesc;
 };
 
@@ -89,9 +100,9 @@ cudaError_t launch_tc_gemm(const TcArgs& args, int bn, int grid, cudaStream_t st
 size_t tc_gemm_smem_bytes(int bn);
 
 // CTA-pair kernel (clusters of two CTAs, one cta_group::2 MMA per pair):
-// tiles of 256 P rows x 256 Q rows; `grid` CTAs (even).  args.pair must be 1.
-constexpr int PAIR_TILE = 256;
-cudaError_t launch_tc_gemm_pair(const TcArgs& args, int grid, cudaStream_t stream);
+// tiles of 256 P rows x `bn` Q rows; `grid` CTAs (even).  args.pair must be 1.
+bool tc_gemm_pair_supports(int bn);
+cudaError_t launch_tc_gemm_pair(const TcArgs& args, int bn, int grid, cudaStream_t stream);
 // Clusters of the pair kernel that can be resident at once on the current
 // device (0 if it cannot run there).
 cudaError_t tc_gemm_pair_max_clusters(int* clusters);

@@ -76,7 +76,13 @@ extern "C" gemm_status_t gemm_run_static_scratch(const gemm_plan_t* plan, const 
       reinterpret_cast<uintptr_t>(B) % 16)
     return GEMM_ERR_UNSUPPORTED;
 
-  // Scratch layout: [tile counters][fp32 partial sums M x N].
+  // Scratch layout: [tile counters][fp32 partial sums M x N].  A stream-K
+  // tail that does not fit is dropped (whole tiles only).
+  const gemm_plan no_tail = lgt::plan_without_tail(*plan);
+  if (plan->tail_tiles &&
+      align256(static_cast<size_t>(plan->num_counters) * sizeof(int32_t)) + static_cast<size_t>(d.M) * d.N * 4 >
+          kStaticScratchBytes)
+    plan = &no_tail;
   const size_t counters_bytes =
       plan->split > 1 ? align256(static_cast<size_t>(plan->num_counters) * sizeof(int32_t)) : 0;
   const size_t partial_bytes = plan->split > 1 ? static_cast<size_t>(d.M) * d.N * sizeof(float) : 0;

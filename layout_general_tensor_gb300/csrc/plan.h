@@ -21,7 +21,10 @@ struct gemm_plan {
   int pair;          // 1: CTA-pair kernel (256 x 256 tiles, clusters of two CTAs)
   int grid;          // CTAs launched by the tensor-core kernels
   int num_counters;  // split-K arrival counters (one per tile, per half-tile for pairs)
-  int split, kb_per_split, kb_total;
+  int split, kb_per_split, kb_total;  // split: units per tile in the kernel's unit space
+  int split_req;     // split-K factor of the SM-waste rule or of the caller
+  int rr_tiles;      // tiles dealt whole before the contiguous unit ranges
+  int tail_tiles;    // stream-K tail: tiles whose K blocks are spread over all workers
   int tiles_p, tiles_q, num_units;
   int64_t lda, ldb, ldc;
   int a_mn, b_mn;
@@ -51,6 +54,9 @@ bool encode_int4_weights(CUtensorMap* map, const void* ptr, int64_t N, int64_t l
 // in place (16-byte aligned bases and pitches `lda` / `ldb` in elements),
 // with the split-K partial sums and counters at `partial` / `counters`
 // (zero-filled; unused when split == 1).
+// A copy of `p` that runs every tile whole (no stream-K tail).
+gemm_plan plan_without_tail(const gemm_plan& p);
+
 gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                            float* partial, int32_t* counters, cudaStream_t stream);
 

@@ -20,32 +20,44 @@ struct Group {
   int32_t kb0, nkb;  // K blocks
 };
 
-// Work assignment.  split == 1: units are tiles, taken round-robin.
-// split > 1: worker b takes the contiguous unit range
-// [b*U/G, (b+1)*U/G) and a group is a maximal run of one tile's splits.
+// Work assignment.  Two kinds of groups:
+//  - round-robin tiles [0, rr_tiles): worker b takes tiles b, b+G, b+2G, ...
+//    each as one whole group (all of its K blocks);
+//  - contiguous units [rr_tiles * split, num_units), unit u = tile * split + s:
+//    worker b takes [b*U/G, (b+1)*U/G) of the U units; a group is a maximal
+//    run of one tile's units.
+// Order for one worker: its first round-robin tile, then its contiguous
+// units, then its other round-robin tiles.  split == 1 has round-robin tiles
+// only; an explicit split > 1 has contiguous units only (consecutive splits
+// of one tile then accumulate in TMEM).  The stream-K tail has both, with
+// split = the K blocks of a tile: one whole wave first warms L2 with the
+// operands, then the tail units run and their partial sums complete early,
+// so that their conversion (by the fixup warps) overlaps the later waves.
 // A worker is a CTA, or a CTA pair (both CTAs walk the same units).
 struct Sched {
-  int32_t u, u_end, step;
+  int32_t u, u_end;          // contiguous-unit cursor
+  int32_t r, r_end, r_step;  // round-robin cursor
+  bool first;                // the first round-robin tile is still to come
   __device__ Sched(const TcArgs& a) {
     const int32_t G = gridDim.x >> a.pair, b = blockIdx.x >> a.pair;
-    if (a.split == 1) {
-      u = b;
-      u_end = a.num_units;
-      step = G;
-    } else {
-      u = static_cast<int32_t>((static_cast<int64_t>(b) * a.num_units) / G);
-      u_end = static_cast<int32_t>((static_cast<int64_t>(b + 1) * a.num_units) / G);
-      step = 0;
-    }
+    r = b;
+    r_end = a.rr_tiles;
+    r_step = G;
+    first = true;
+    const int64_t u0 = static_cast<int64_t>(a.rr_tiles) * a.split;
+    const int64_t U = static_cast<int64_t>(a.num_units) - u0;
+    u = static_cast<int32_t>(u0 + (static_cast<int64_t>(b) * U) / G);
+    u_end = static_cast<int32_t>(u0 + (static_cast<int64_t>(b + 1) * U) / G);
   }
   __device__ bool next(const TcArgs& a, Group& g) {
-    if (u >= u_end) return false;
-    if (step) {
-      g.tile = u;
+    const bool rr_now = r < r_end && (first || u >= u_end);
+    first = false;
+    if (rr_now) {
+      g.tile = r;
       g.s0 = 0;
-      g.s1 = 1;
-      u += step;
-    } else {
+      g.s1 = a.split;
+      r += r_step;
+    } else if (u < u_end) {
       uint32_t tile, s;
       magic_divmod(static_cast<uint32_t>(u), a.div_split, tile, s);
       const int32_t avail = u_end - u;
@@ -54,6 +66,8 @@ struct Sched {
       g.s0 = static_cast<int32_t>(s);
       g.s1 = s1;
       u += s1 - static_cast<int32_t>(s);
+    } else {
+      return false;
     }
     g.kb0 = g.s0 * a.kb_per_split;
     const int32_t kb1 = min(a.kb_total, g.s1 * a.kb_per_split);
@@ -120,9 +134,12 @@ __device__ __forceinline__ void narrow_to_half(const TcArgs& a, int half, int32_
   }
 }
 
-// Last arriver of a split tile: read the fp32 sum from the workspace (L2),
-// convert once, store C and zero the workspace region again.  Rows are
-// walked in 4-float vectors with several loads in flight per thread.
+// Convert the fp32 sums of C rows [m0, m1) x columns [n0, n1) from the
+// workspace (L2), store them to C and zero the workspace region again.  The
+// 128 epilogue threads walk the region in 4-float vectors with U loads in
+// flight per thread: a round trip to L2 costs microseconds on this GPU, so
+// the loads of a whole region should be in flight together.
+template <int U>
 __device__ __noinline__ void finish_tile(const TcArgs& a, int m0, int m1, int n0, int n1, int et) {
   const int rows = m1 - m0, cols = n1 - n0;
   uint16_t* cbase = reinterpret_cast<uint16_t*>(a.c);
@@ -130,18 +147,14 @@ __device__ __noinline__ void finish_tile(const TcArgs& a, int m0, int m1, int n0
     // c_vec: C rows and n0 are 16-byte aligned, so 4-element (8-byte) stores are aligned too
     const int cols4 = cols >> 2;
     const int total = rows * cols4;
-    constexpr int U = 8;
     for (int i0 = et; i0 < total; i0 += kEpiThreads * U) {
       float4 v[U];
-      float4* w[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u * kEpiThreads;
-        w[u] = nullptr;
         if (i < total) {
           const int r = i / cols4, c4 = i - r * cols4;
-          w[u] = reinterpret_cast<float4*>(a.ws + static_cast<int64_t>(m0 + r) * a.N + n0) + c4;
-          v[u] = __ldcg(w[u]);
+          v[u] = __ldcg(reinterpret_cast<const float4*>(a.ws + static_cast<int64_t>(m0 + r) * a.N + n0) + c4);
         }
       }
 #pragma unroll
@@ -149,7 +162,8 @@ __device__ __noinline__ void finish_tile(const TcArgs& a, int m0, int m1, int n0
         const int i = i0 + u * kEpiThreads;
         if (i < total) {
           const int r = i / cols4, c4 = i - r * cols4;
-          __stcg(w[u], make_float4(0.f, 0.f, 0.f, 0.f));
+          __stcg(reinterpret_cast<float4*>(a.ws + static_cast<int64_t>(m0 + r) * a.N + n0) + c4,
+                 make_float4(0.f, 0.f, 0.f, 0.f));
           uint2 o;
           o.x = pack2(v[u].x, v[u].y, a.c_bf16);
           o.y = pack2(v[u].z, v[u].w, a.c_bf16);
@@ -160,11 +174,11 @@ __device__ __noinline__ void finish_tile(const TcArgs& a, int m0, int m1, int n0
     return;
   }
   const int total = rows * cols;
-  constexpr int U = 8;
-  for (int i0 = et; i0 < total; i0 += kEpiThreads * U) {
-    float v[U];
+  constexpr int U1 = U < 8 ? U : 8;
+  for (int i0 = et; i0 < total; i0 += kEpiThreads * U1) {
+    float v[U1];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int u = 0; u < U1; ++u) {
       const int i = i0 + u * kEpiThreads;
       if (i < total) {
         const int r = i / cols, cidx = i - r * cols;
@@ -172,7 +186,7 @@ __device__ __noinline__ void finish_tile(const TcArgs& a, int m0, int m1, int n0
       }
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int u = 0; u < U1; ++u) {
       const int i = i0 + u * kEpiThreads;
       if (i < total) {
         const int r = i / cols, cidx = i - r * cols;
@@ -191,6 +205,12 @@ __device__ __forceinline__ void arrive_split_tile(const TcArgs& a, const Group& 
                                                   int n1, int et) {
   __threadfence();
   named_bar_sync(1, kEpiThreads);
+  if (a.tail_tiles) {
+    // stream-K tail: count the arrival only; every CTA finishes a share of
+    // the tail tiles at the end (finish_tail)
+    if (et == 0) atomicAdd(&a.counters[counter], g.s1 - g.s0);
+    return;
+  }
   bool mine_last = false;
   if (et == 0) {
     const int old = atomicAdd(&a.counters[counter], g.s1 - g.s0);
@@ -198,10 +218,72 @@ __device__ __forceinline__ void arrive_split_tile(const TcArgs& a, const Group& 
   }
   if (named_bar_or(1, kEpiThreads, mine_last)) {
     __threadfence();
-    finish_tile(a, m0, m1, n0, n1, et);
+    finish_tile<8>(a, m0, m1, n0, n1, et);
     named_bar_sync(1, kEpiThreads);
     if (et == 0) a.counters[counter] = 0;
   }
+}
+
+// Finish of the stream-K tail by the 128 fixup threads of every CTA (their
+// own warps, named barrier 2), concurrent with the main loops of the whole
+// tiles.  The tail tiles' 128-row strips (two per pair tile) are laid end to
+// end and CTA c converts rows [c*R/G, (c+1)*R/G) of them: for each strip it
+// meets, it waits until all of the strip's K blocks have arrived (tail units
+// run after the first wave, early in the kernel), converts and stores its rows
+// of C, zeroes them in the workspace, and counts them on the strip's second
+// counter; the CTA completing a strip resets both counters for the next
+// run.  Spreading the reads over all SMs matters: one CTA reading a whole
+// tile competes with its own main loop for the SM's L2 bandwidth.
+template <int BN>
+__device__ __noinline__ bool finish_tail(const TcArgs& a, volatile int* abort_flag, int et) {
+  constexpr int kBar = 2;
+  const int halves = 1 + a.pair;
+  const int64_t R = static_cast<int64_t>(a.tail_tiles) * halves * TILE_P;
+  const int64_t G = gridDim.x;
+  int64_t row = (static_cast<int64_t>(blockIdx.x) * R) / G;
+  const int64_t row_end = (static_cast<int64_t>(blockIdx.x + 1) * R) / G;
+  int32_t* done = a.counters + static_cast<int64_t>(a.tiles_p) * a.tiles_q * halves;
+  while (row < row_end) {
+    const int strip = static_cast<int>(row / TILE_P);
+    const int r0 = static_cast<int>(row - static_cast<int64_t>(strip) * TILE_P);
+    const int r1 = static_cast<int>(min(static_cast<int64_t>(TILE_P), row_end - static_cast<int64_t>(strip) * TILE_P));
+    const int tile = a.rr_tiles + strip / halves;
+    const int half = strip % halves;
+    const int cidx = tile * halves + half;
+    int32_t tp, tq, m0, m1, n0, n1;
+    tile_ranges(a, tile, BN, tp, tq, m0, m1, n0, n1);
+    m0 += half * TILE_P;
+    const int ma = min(a.M, m0 + r0), mb = min(a.M, m0 + r1);
+    bool ok = true;
+    if (et == 0) {
+      volatile int32_t* c = a.counters + cidx;
+      if (*c < a.split) {
+        const uint64_t t0 = global_timer_ns();
+        while (*c < a.split) {
+          if (*abort_flag || global_timer_ns() - t0 > a.wait_limit_ns) {
+            ok = false;
+            break;
+          }
+          __nanosleep(256);
+        }
+      }
+      if (!ok && !*abort_flag) record_timeout(a, abort_flag, 2 * 16 + 5);
+      __threadfence();
+    }
+    if (named_bar_or(kBar, kEpiThreads, !ok)) return false;
+    if (mb > ma) finish_tile<8>(a, ma, mb, n0, n1, et);
+    __threadfence();
+    named_bar_sync(kBar, kEpiThreads);
+    if (et == 0) {
+      const int old = atomicAdd(&done[cidx], r1 - r0);
+      if (old + (r1 - r0) == TILE_P) {
+        a.counters[cidx] = 0;
+        done[cidx] = 0;
+      }
+    }
+    row += r1 - r0;
+  }
+  return true;
 }
 
 // The epilogue of one group, run by the 128 epilogue threads (TMEM lane
@@ -212,10 +294,17 @@ __device__ __forceinline__ void arrive_split_tile(const TcArgs& a, const Group& 
 // is aborting; all 128 threads return the same value.
 // PAIR: the CTA holds P-side half `half` of a pair tile, and the buffer-free
 // arrival goes to the pair's MMA CTA (acce_bar0 is a shared::cluster address).
+//
+// Unswapped tiles with a.tma_c / a.tma_ws leave through shared memory: each
+// warp writes its 32 rows x 32 columns into one of its two 4 KiB staging
+// buffers (`stage_smem`, 1024-aligned; `ring` counts the blocks it has
+// issued) and one lane hands the block to a bulk tile store (C) or bulk
+// tile reduction (fp32 partials), so whole lines reach L2.  Otherwise each
+// thread stores its own row directly.
 template <int BN, int CH, bool PAIR = false>
 __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, uint32_t tmem_base, uint32_t accf_bar0,
                                                uint32_t acce_bar0, int& acc_iter, volatile int* abort_flag, int q4,
-                                               int lane, int et, int half = 0) {
+                                               int lane, int et, int half, uint32_t stage_smem, int& ring) {
   const int row = q4 * 32 + lane;  // accumulator row (TMEM lane)
   int32_t tp, tq, m0, m1, n0, n1;
   tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
@@ -230,8 +319,59 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
     if (named_bar_or(1, kEpiThreads, !got)) return false;
     tc_fence_after();
     const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(buf * BN);
+    const bool staged = (BN % EPI_BOX == 0) && !a.swap && (full_tile ? a.tma_c : a.tma_ws);
+    if (staged) {
+      const int32_t ybox = m0 + q4 * 32;  // first C row of this warp's blocks
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += CH) {
+      for (int c0 = 0; c0 < BN; c0 += EPI_BOX) {
+        uint32_t v[EPI_BOX];
+        tc_ld_32x32b_x32(t_row + c0, v);
+        tc_wait_ld();
+        const int32_t xbox = n0 + c0;
+        if (ybox >= m1 || xbox >= n1) continue;  // block wholly outside C (warp-uniform)
+        const uint32_t sbuf = stage_smem + static_cast<uint32_t>(ring & 1) * 4096u;
+        if (ring >= 2) {
+          // the block issued two steps ago has been read out of this buffer
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+        }
+        if (full_tile) {
+          // 16-bit C: row `lane` of the block is 64 bytes, no swizzle
+          const uint32_t r = sbuf + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            st_shared_v4(r + 16u * j, pack2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1]), a.c_bf16),
+                         pack2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]), a.c_bf16),
+                         pack2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]), a.c_bf16),
+                         pack2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]), a.c_bf16));
+        } else {
+          // fp32 partials: row `lane` is 128 bytes in the 128-byte swizzle
+          // (16-byte chunk j stored at chunk j ^ (row & 7)), conflict-free
+          const uint32_t r = sbuf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(r + 16u * static_cast<uint32_t>(j ^ (lane & 7)), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                         v[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (full_tile)
+            tma_store_2d(&a.tm_c, sbuf, xbox, ybox);
+          else
+            tma_reduce_add_2d(&a.tm_ws, sbuf, xbox, ybox);
+          bulk_commit_group();
+        }
+        ++ring;
+      }
+      if (!full_tile && lane == 0) {
+        // the partial sums must be in L2 before the tile's arrival is counted
+        bulk_wait_group<0>();
+        fence_proxy_async_global();
+      }
+    }
+#pragma unroll 1
+    for (int c0 = 0; c0 < (staged ? 0 : BN); c0 += CH) {
       uint32_t v[CH];
       if constexpr (CH == 32) {
         tc_ld_32x32b_x32(t_row + c0, v);

@@ -1,9 +1,10 @@
-"""GPU parity of the CTA-pair kernel (two CTAs of a cluster share a 256 x 256
-tile through one cta_group::2 MMA) against the fp64 oracle.  The planner
-uses it for large problems; here LGT_GEMM_BN=256 selects it on small and
-ragged shapes too, so that pair tiles whose second half is partly or wholly
-outside the matrix, ragged K, split-K through per-half counters and every
-operand layout are all exercised."""
+"""GPU parity of the CTA-pair kernel (two CTAs of a cluster share a 256 x w
+tile, w in 128..256, through one cta_group::2 MMA) against the fp64 oracle.
+The planner uses it for large problems; here LGT_GEMM_PAIR=1 selects it on
+small and ragged shapes too (LGT_GEMM_PAIR_BN picks w), so that pair tiles
+whose second half is partly or wholly outside the matrix, ragged K, split-K
+through per-half counters, every tile width and every operand layout are
+all exercised."""
 import numpy as np
 import pytest
 import torch
@@ -18,11 +19,15 @@ K, MN = wl.K_CONTIG, wl.MN_CONTIG
 F16, BF16 = wl.F16, wl.BF16
 
 
+WIDTHS = [256, 224, 192, 160, 128]
+
+
 @pytest.fixture(autouse=True)
-def _wide_tiles(monkeypatch):
+def _pairs(monkeypatch):
     lib()
-    monkeypatch.setenv("LGT_GEMM_BN", "256")
-    monkeypatch.delenv("LGT_GEMM_PAIR", raising=False)
+    monkeypatch.setenv("LGT_GEMM_PAIR", "1")
+    monkeypatch.setenv("LGT_GEMM_PAIR_BN", "256")
+    monkeypatch.delenv("LGT_GEMM_BN", raising=False)
 
 
 def _case(M, N, Kd, al, bl, dt=BF16, split=1, dist=("uniform", -1.0, 1.0)):
@@ -30,10 +35,10 @@ def _case(M, N, Kd, al, bl, dt=BF16, split=1, dist=("uniform", -1.0, 1.0)):
     return wl.GemmCase(name, M, N, Kd, al, bl, dt, dt, dt, dist, dist, split_k=split)
 
 
-def _run(case, seed=0, reps=1):
+def _run(case, seed=0, reps=1, width=256):
     inp = wl.make_inputs(case, seed=seed)
     c, g, _ = run_case(case, inp, reps=reps)
-    assert g.info.kernel == 2 and g.info.tile_m == 256 and g.info.tile_n == 256, "pair kernel not selected"
+    assert g.info.kernel == 2 and g.info.tile_m == 256 and g.info.tile_n == width, "pair kernel not selected"
     return inp, c, g
 
 
@@ -43,6 +48,18 @@ def _run(case, seed=0, reps=1):
 def test_pair_layouts(al, bl, dt):
     case = _case(512, 512, 512, al, bl, dt)
     inp, c, g = _run(case)
+    assert_close(c, oracle_full(case, inp), case.name)
+    g.close()
+
+
+@pytest.mark.parametrize("width", WIDTHS)
+@pytest.mark.parametrize("al", [K, MN])
+@pytest.mark.parametrize("bl", [K, MN])
+def test_pair_widths(width, al, bl, monkeypatch):
+    # N spans two tiles and a ragged third for every width
+    monkeypatch.setenv("LGT_GEMM_PAIR_BN", str(width))
+    case = _case(384, 2 * width + 40, 328, al, bl)
+    inp, c, g = _run(case, seed=width, width=width)
     assert_close(c, oracle_full(case, inp), case.name)
     g.close()
 
@@ -96,6 +113,7 @@ def test_pair_matches_single_cta_kernel(monkeypatch):
     inp, c_pair, g = _run(case, seed=11)
     g.close()
     monkeypatch.setenv("LGT_GEMM_PAIR", "0")
+    monkeypatch.setenv("LGT_GEMM_BN", "256")
     c_single, g1, _ = run_case(case, inp)
     assert g1.info.kernel == 0 and g1.info.tile_m == 128
     g1.close()
@@ -123,10 +141,19 @@ def test_pair_static_scratch():
     g.close()
 
 
-def test_full_size_square_uses_pairs(monkeypatch):
-    """The 4096^3 workload is planned onto CTA pairs without any override."""
-    monkeypatch.delenv("LGT_GEMM_BN")
+def test_planner_choice_without_overrides(monkeypatch):
+    """Without overrides: the large workloads go to CTA pairs with a width
+    that fills whole waves; a problem with about one wave of 128 x 256 tiles
+    stays on the single-CTA kernel (pairs would need two waves)."""
+    monkeypatch.delenv("LGT_GEMM_PAIR")
+    monkeypatch.delenv("LGT_GEMM_PAIR_BN")
     m = lib()
-    g = m.Gemm(desc_for(m, wl.SQUARE_BF16))
-    assert g.info.kernel == 2 and g.info.split_k == 1
+    for case in (wl.SQUARE_BF16, wl.IRREGULAR):
+        g = m.Gemm(desc_for(m, case))
+        assert g.info.kernel == 2 and g.info.split_k == 1 and g.info.tile_n in WIDTHS
+        g.close()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    one_wave = _case(128 * sms // 8, 256 * 8, 512, K, K)
+    g = m.Gemm(desc_for(m, one_wave))
+    assert g.info.kernel == 0 and g.info.tile_n == 256
     g.close()

@@ -180,7 +180,7 @@ def test_invalid_arguments(lib):
         lib.make_desc(4, 4, 4, lda=3, num_sms=148),
         lib.make_desc(4, 4, 4, a_dtype=lib.GEMM_F16, b_dtype=lib.GEMM_BF16, num_sms=148),
         lib.make_desc(4, 4, 4, c_dtype=lib.GEMM_F32, num_sms=148),
-        lib.make_desc(4, 4, 4, flags=1, num_sms=148),
+        lib.make_desc(4, 4, 4, flags=2, num_sms=148),
         lib.make_desc(4, 4, 4, split_k=-2, num_sms=148),
         lib.make_desc(4, 4, 4, a_dtype=lib.GEMM_BF16, b_dtype=lib.GEMM_INT4, c_dtype=lib.GEMM_F16, num_sms=148),
     ]
@@ -189,6 +189,18 @@ def test_invalid_arguments(lib):
         assert st == lib.GEMM_ERR_INVALID_ARG and h is None
     assert lib._lib.gemm_create(None, None) == lib.GEMM_ERR_INVALID_ARG
     assert lib._lib.gemm_query(None, None) == lib.GEMM_ERR_INVALID_ARG
+
+
+def test_deterministic_flag(lib):
+    # accepted with no K split; a split factor above 1 cannot be reproducible
+    # bit for bit (fp32 atomics), so it is refused under the flag
+    h = lib.gemm_create(lib.make_desc(512, 512, 512, flags=lib.GEMM_FLAG_DETERMINISTIC, num_sms=148))
+    info = lib.gemm_query(h)
+    assert info.split_k == 1 and info.streamk_tiles == 0
+    lib.gemm_destroy(h)
+    st, h = lib.gemm_create_status(lib.make_desc(512, 512, 4096, split_k=4, flags=lib.GEMM_FLAG_DETERMINISTIC,
+                                                 num_sms=148))
+    assert st == lib.GEMM_ERR_UNSUPPORTED and h is None
 
 
 def test_no_device_paths(lib):
