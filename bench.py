@@ -31,8 +31,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GEMM TFLOP/s & % dense-BF16 peak per shape/layout; GB/s & % HBM (skinny/int4)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["layout_general_tensor_gb300/csrc/gemm_tc.cu", "layout_general_tensor_gb300/csrc/ptx.cuh",
-                  "layout_general_tensor_gb300/csrc/kernels.h"]
+KERNEL_SOURCES = ["layout_general_tensor_gb300/csrc/" + f for f in
+                  ("api.cu", "gemm_tc.cu", "gemm_tc_pair.cu", "tc_common.cuh", "ptx.cuh", "kernels.h")]
 
 
 def load_peaks():
@@ -51,6 +51,15 @@ def kernel_source_hash():
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def kernel_name(info):
+    """Name of the main kernel a plan launches (as profilers list it)."""
+    if info.kernel == 2:
+        return f"tc_gemm_pair_kernel<{info.tile_n}>"
+    if info.kernel == 1:
+        return f"int4_gemm_kernel<{info.tile_m}>"
+    return f"tc_gemm_kernel<{info.tile_m if info.swap_ab else info.tile_n}>"
 
 
 def recorded_traffic(workload):
@@ -358,6 +367,7 @@ def gpu_arm(args, headline):
                               "pct_bf16_peak": 100 * tf / peaks["bf16_tflops"], "operand_sets": d.n_sets,
                               "gbs": gbs, "pct_hbm": 100 * gbs / peaks["hbm_gbs"], "split_k": d.g.info.split_k,
                               "swap_ab": d.g.info.swap_ab, "launches_per_run": d.launches_per_run,
+                              "kernel": kernel_name(d.g.info), "streamk_tiles": d.g.info.streamk_tiles,
                               "algorithmic_bytes": algorithmic_bytes(case), "flop": case.flops()}
         st = d.g.sync_status()
         assert st == 0, f"device status {st} on {case.name}"
@@ -381,7 +391,7 @@ def gpu_arm(args, headline):
                    "inputs": "seeded synthetic N(0,1) bf16", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": f"tc_gemm_kernel<{dc.g.info.tile_n}>",
+                     "kernel": kernel_name(dc.g.info),
                      "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 1.9 PFLOP/s bf16 burst"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": A_h.numel() * 2 + B_h.numel() * 2,
