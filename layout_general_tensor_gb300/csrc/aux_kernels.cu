@@ -11,9 +11,12 @@ namespace {
 // of the hipBLASLt DTL page's generalised loads ("Add support for
 // non-power of 2 MT when TLU=1" / "generalized NLC=1"): any number of
 // elements per row, offsets split with a magic-number division by the
-// (static) chunks-per-row count.  Each thread gathers eight 2-byte elements
-// (consecutive threads read consecutive addresses, so a warp's loads
-// coalesce) and writes one aligned 16-byte vector.
+// (static) chunks-per-row count.  Each thread produces eight 2-byte elements
+// as one aligned 16-byte store: it loads the one or two aligned 16-byte words
+// that hold them (consecutive threads read consecutive words, so a warp's
+// loads coalesce) and realigns them with funnel shifts.  Every word read
+// holds at least one of the thread's elements, so it lies in the same page as
+// valid data.
 __global__ void repack_rows_kernel(const uint16_t* __restrict__ src, int64_t src_pitch, uint16_t* __restrict__ dst,
                                    int64_t dst_pitch, int64_t rows, int64_t row_elems, MagicDiv chunks_div,
                                    int64_t total_chunks) {
@@ -33,10 +36,25 @@ __global__ void repack_rows_kernel(const uint16_t* __restrict__ src, int64_t src
     const uint16_t* s = src + r * src_pitch + e0;
     uint16_t* d = dst + r * dst_pitch + e0;
     if (e0 + 8 <= row_elems) {
-      uint32_t w[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) w[j] = static_cast<uint32_t>(s[2 * j]) | (static_cast<uint32_t>(s[2 * j + 1]) << 16);
-      *reinterpret_cast<uint4*>(d) = make_uint4(w[0], w[1], w[2], w[3]);
+      const uintptr_t addr = reinterpret_cast<uintptr_t>(s);
+      const uint4* p = reinterpret_cast<const uint4*>(addr & ~static_cast<uintptr_t>(15));
+      const uint32_t off = static_cast<uint32_t>(addr & 15);  // even: 2-byte elements
+      const uint4 a = __ldg(p);
+      uint4 out = a;
+      if (off) {
+        const uint4 b = __ldg(p + 1);
+        uint32_t x0, x1, x2, x3, x4;
+        switch (off >> 2) {
+          case 0: x0 = a.x; x1 = a.y; x2 = a.z; x3 = a.w; x4 = b.x; break;
+          case 1: x0 = a.y; x1 = a.z; x2 = a.w; x3 = b.x; x4 = b.y; break;
+          case 2: x0 = a.z; x1 = a.w; x2 = b.x; x3 = b.y; x4 = b.z; break;
+          default: x0 = a.w; x1 = b.x; x2 = b.y; x3 = b.z; x4 = b.w; break;
+        }
+        const uint32_t sh = (off & 3u) * 8u;  // 0 or 16 bits
+        out = make_uint4(__funnelshift_r(x0, x1, sh), __funnelshift_r(x1, x2, sh), __funnelshift_r(x2, x3, sh),
+                         __funnelshift_r(x3, x4, sh));
+      }
+      *reinterpret_cast<uint4*>(d) = out;
     } else {
       for (int64_t j = 0; e0 + j < row_elems; ++j) d[j] = s[j];
     }

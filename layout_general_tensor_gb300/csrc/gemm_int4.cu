@@ -584,6 +584,67 @@ __global__ void int4_prep_kernel(const uint16_t* __restrict__ A, int64_t lda, in
   }
 }
 
+// Activation pre-pass for a K-contiguous activation: one thread per
+// 8-element chunk (m, c), c fastest, so that loads and stores are coalesced
+// 16-byte vectors (scalar loads when the rows are not 16-byte aligned).  The
+// chunk is stored with its elements reordered to (0,4,1,5,2,6,3,7); the 8
+// chunks of a 64-deep block sit in 8 adjacent lanes (K is a multiple of 64)
+// and their sum is reduced by shuffles into asum[kb][m]; when a quantisation
+// group spans 8, 16 or 32 lanes (64, 128 or 256 elements), the group sum
+// gsum[g][m] is reduced the same way (lanes_per_group = 0: not here).
+__global__ void __launch_bounds__(256) int4_prep_kmajor_kernel(const uint16_t* __restrict__ A, int64_t lda, int vec,
+                                                               int M, int K, uint16_t* __restrict__ Ap,
+                                                               float* __restrict__ asum, float* __restrict__ gsum,
+                                                               int asum_ld, int lanes_per_group) {
+  const int chunks = K / 8;
+  const int64_t total = static_cast<int64_t>(M) * chunks;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // base is a multiple of the block size: warps cover 32 consecutive chunks
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x; base < total; base += step) {
+    const int64_t i = base + threadIdx.x;
+    const bool act = i < total;
+    int m = 0, c = 0;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (act) {
+      m = static_cast<int>(i / chunks);
+      c = static_cast<int>(i - static_cast<int64_t>(m) * chunks);
+      const uint16_t* src = A + static_cast<int64_t>(m) * lda + 8 * c;
+      if (vec) {
+        const uint4 q = *reinterpret_cast<const uint4*>(src);
+        w[0] = q.x;
+        w[1] = q.y;
+        w[2] = q.z;
+        w[3] = q.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = static_cast<uint32_t>(src[2 * e]) | (static_cast<uint32_t>(src[2 * e + 1]) << 16);
+      }
+    }
+    // elements e = 0..7 are the halves of w[e / 2]; the stored order is 0,4 | 1,5 | 2,6 | 3,7
+    uint4 o;
+    o.x = (w[0] & 0xFFFFu) | (w[2] << 16);
+    o.y = (w[0] >> 16) | (w[2] & 0xFFFF0000u);
+    o.z = (w[1] & 0xFFFFu) | (w[3] << 16);
+    o.w = (w[1] >> 16) | (w[3] & 0xFFFF0000u);
+    float s = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __half2 h = *reinterpret_cast<const __half2*>(&w[e]);
+      const float2 f = __half22float2(h);
+      s += f.x + f.y;
+    }
+    if (act) *reinterpret_cast<uint4*>(Ap + static_cast<int64_t>(m) * K + 8 * c) = o;
+    s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+    s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+    s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
+    if (act && (c & 7) == 0) asum[static_cast<int64_t>(c >> 3) * asum_ld + m] = s;
+    if (lanes_per_group >= 16) s += __shfl_xor_sync(0xFFFFFFFFu, s, 8);
+    if (lanes_per_group >= 32) s += __shfl_xor_sync(0xFFFFFFFFu, s, 16);
+    if (lanes_per_group && act && c % lanes_per_group == 0)
+      gsum[static_cast<int64_t>(c / lanes_per_group) * asum_ld + m] = s;
+  }
+}
+
 // Per-group row sums from the per-block ones: gsum[g][m] = sum of asum over
 // the group's 64-deep blocks (same fp32 values the epilogue would add).
 __global__ void int4_group_sum_kernel(const float* __restrict__ asum, float* __restrict__ gsum, int asum_ld, int M,
@@ -615,13 +676,27 @@ cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K,
                              float* gsum, int asum_ld, int sms, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(K / TILE_K) * M;
   if (total == 0) return cudaSuccess;
+  if (!a_mn) {
+    const int lanes = group / 8;
+    const int lpg = (lanes == 8 || lanes == 16 || lanes == 32) ? lanes : 0;
+    const int vec = (lda % 8 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
+    const int64_t chunks = static_cast<int64_t>(M) * (K / 8);
+    int64_t blocks = (chunks + 255) / 256;
+    if (blocks > static_cast<int64_t>(sms) * 8) blocks = static_cast<int64_t>(sms) * 8;
+    int4_prep_kmajor_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(A), lda, vec, M, K, static_cast<uint16_t*>(Ap), asum, gsum, asum_ld, lpg);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || lpg) return e;
+  }
   const int threads = 128;
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
-  int4_prep_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(static_cast<const uint16_t*>(A), lda, a_mn, M,
-                                                                     K, static_cast<uint16_t*>(Ap), asum, asum_ld);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (a_mn) {
+    int4_prep_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(static_cast<const uint16_t*>(A), lda, a_mn, M,
+                                                                       K, static_cast<uint16_t*>(Ap), asum, asum_ld);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const int groups = K / group;
   const int64_t gtotal = static_cast<int64_t>(groups) * M;
   int64_t gblocks = (gtotal + threads - 1) / threads;
