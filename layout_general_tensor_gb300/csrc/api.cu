@@ -232,7 +232,7 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
   args.kb_total = plan->kb_total;
   args.num_units = plan->num_units;
   args.rr_tiles = plan->rr_tiles;
-  args.tail_tiles = plan->tail_tiles;
+  args.tail_tiles = plan->fin_tiles;
   args.div_split = magic_encode(static_cast<uint32_t>(plan->split));
   args.div_tiles_p = magic_encode(static_cast<uint32_t>(plan->tiles_p));
   args.p_mn = p_mn;
@@ -244,7 +244,7 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
   args.pair = plan->pair;
   // Staged epilogue: whole-line bulk stores of C and bulk reductions of the
   // fp32 partials, where the pointers and pitches allow them (16 bytes).
-  if (!plan->swap && env_int("LGT_GEMM_TMA_EPI", 1) != 0) {
+  if (env_int("LGT_GEMM_TMA_EPI", 1) != 0) {
     args.tma_c = args.c_vec && encode_output(&args.tm_c, C, false, d.c_dtype, d.M, d.N, plan->ldc * 2);
     args.tma_ws = partial && (d.N % 4 == 0) && encode_output(&args.tm_ws, partial, true, 0, d.M, d.N, d.N * 4);
   }
@@ -262,6 +262,7 @@ gemm_plan plan_without_tail(const gemm_plan& p) {
   q.kb_per_split = q.kb_total;
   q.rr_tiles = q.tiles_p * q.tiles_q;
   q.tail_tiles = 0;
+  q.fin_tiles = 0;
   q.num_units = q.rr_tiles;
   const int workers = q.pair ? q.grid / 2 : q.sms_grid;
   q.grid = (q.pair ? 2 : 1) * (q.num_units < workers ? q.num_units : workers);
@@ -454,9 +455,13 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
     }
   }
   p.num_units = static_cast<int>(tiles * p.split);
-  // arrival counters per tile (per half-tile for pairs); a stream-K tail
-  // also keeps a finished-rows counter per half-tile after them
-  p.num_counters = static_cast<int>(tiles) * (1 + p.pair) * (p.tail_tiles ? 2 : 1);
+  // Split tiles of the tensor-core kernels are converted at the end by all
+  // CTAs together (their fixup warps), not by each tile's last arriver: a
+  // single CTA converting a whole tile is bound by its own L2 round trips.
+  p.fin_tiles = int4 ? 0 : (p.tail_tiles ? p.tail_tiles : (p.split > 1 ? static_cast<int>(tiles) : 0));
+  // arrival counters per tile (per half-tile for pairs); converted tiles
+  // also keep a finished-rows counter per strip after them
+  p.num_counters = static_cast<int>(tiles) * (1 + p.pair) * (p.fin_tiles ? 2 : 1);
   if (p.pair) {
     p.grid = 2 * (p.num_units < workers ? p.num_units : workers);
   } else {

@@ -17,9 +17,28 @@ namespace {
 // loads coalesce) and realigns them with funnel shifts.  Every word read
 // holds at least one of the thread's elements, so it lies in the same page as
 // valid data.
-__global__ void repack_rows_kernel(const uint16_t* __restrict__ src, int64_t src_pitch, uint16_t* __restrict__ dst,
-                                   int64_t dst_pitch, int64_t rows, int64_t row_elems, MagicDiv chunks_div,
-                                   int64_t total_chunks) {
+// Eight 2-byte elements starting at byte offset `off` (even, < 16) of the
+// aligned 16-byte word pair (a, b).
+__device__ __forceinline__ uint4 realign8(const uint4& a, const uint4& b, uint32_t off) {
+  if (!off) return a;
+  uint32_t x0, x1, x2, x3, x4;
+  switch (off >> 2) {
+    case 0: x0 = a.x; x1 = a.y; x2 = a.z; x3 = a.w; x4 = b.x; break;
+    case 1: x0 = a.y; x1 = a.z; x2 = a.w; x3 = b.x; x4 = b.y; break;
+    case 2: x0 = a.z; x1 = a.w; x2 = b.x; x3 = b.y; x4 = b.z; break;
+    default: x0 = a.w; x1 = b.x; x2 = b.y; x3 = b.z; x4 = b.w; break;
+  }
+  const uint32_t sh = (off & 3u) * 8u;  // 0 or 16 bits
+  return make_uint4(__funnelshift_r(x0, x1, sh), __funnelshift_r(x1, x2, sh), __funnelshift_r(x2, x3, sh),
+                    __funnelshift_r(x3, x4, sh));
+}
+
+// One chunk per thread over a grid that covers all chunks (measured faster
+// than grid-stride loops with several chunks in flight per thread).
+__global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t* __restrict__ src, int64_t src_pitch,
+                                                          uint16_t* __restrict__ dst, int64_t dst_pitch,
+                                                          int64_t row_elems, MagicDiv chunks_div,
+                                                          int64_t total_chunks) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_chunks; i += stride) {
     int64_t r, c;
@@ -40,21 +59,8 @@ __global__ void repack_rows_kernel(const uint16_t* __restrict__ src, int64_t src
       const uint4* p = reinterpret_cast<const uint4*>(addr & ~static_cast<uintptr_t>(15));
       const uint32_t off = static_cast<uint32_t>(addr & 15);  // even: 2-byte elements
       const uint4 a = __ldg(p);
-      uint4 out = a;
-      if (off) {
-        const uint4 b = __ldg(p + 1);
-        uint32_t x0, x1, x2, x3, x4;
-        switch (off >> 2) {
-          case 0: x0 = a.x; x1 = a.y; x2 = a.z; x3 = a.w; x4 = b.x; break;
-          case 1: x0 = a.y; x1 = a.z; x2 = a.w; x3 = b.x; x4 = b.y; break;
-          case 2: x0 = a.z; x1 = a.w; x2 = b.x; x3 = b.y; x4 = b.z; break;
-          default: x0 = a.w; x1 = b.x; x2 = b.y; x3 = b.z; x4 = b.w; break;
-        }
-        const uint32_t sh = (off & 3u) * 8u;  // 0 or 16 bits
-        out = make_uint4(__funnelshift_r(x0, x1, sh), __funnelshift_r(x1, x2, sh), __funnelshift_r(x2, x3, sh),
-                         __funnelshift_r(x3, x4, sh));
-      }
-      *reinterpret_cast<uint4*>(d) = out;
+      const uint4 b = off ? __ldg(p + 1) : a;
+      *reinterpret_cast<uint4*>(d) = realign8(a, b, off);
     } else {
       for (int64_t j = 0; e0 + j < row_elems; ++j) d[j] = s[j];
     }
@@ -90,9 +96,10 @@ cudaError_t launch_repack_rows(const void* src, int64_t src_pitch, void* dst, in
   const int64_t total = rows * chunks;
   const MagicDiv cd = magic_encode(static_cast<uint32_t>(chunks));
   const int threads = 256;
-  repack_rows_kernel<<<grid_for(total, threads), threads, 0, stream>>>(
-      static_cast<const uint16_t*>(src), src_pitch / 2, static_cast<uint16_t*>(dst), dst_pitch / 2, rows, row_elems,
-      cd, total);
+  const int64_t blocks = (total + threads - 1) / threads;
+  repack_rows_kernel<<<static_cast<int>(blocks < (1ll << 31) - 1 ? blocks : (1ll << 31) - 1), threads, 0, stream>>>(
+      static_cast<const uint16_t*>(src), src_pitch / 2, static_cast<uint16_t*>(dst), dst_pitch / 2, row_elems, cd,
+      total);
   return cudaGetLastError();
 }
 

@@ -55,7 +55,8 @@ struct TcArgs {
   int32_t split, kb_per_split, kb_total;
   int32_t num_units;
   int32_t rr_tiles;      // tiles dealt whole, round-robin, after the contiguous unit ranges
-  int32_t tail_tiles;    // stream-K tail tiles [rr_tiles, rr_tiles + tail_tiles): finished by all CTAs at the end
+  int32_t tail_tiles;    // split tiles [rr_tiles, rr_tiles + tail_tiles) converted by the fixup warps of all CTAs
+                         // (a stream-K tail, or every tile of a split-K plan); 0: the last arriver converts
   MagicDiv div_split;    // unit -> (tile, split)
   MagicDiv div_tiles_p;  // tile -> (tile_p, tile_q)
   int32_t p_mn, q_mn;    // 1: operand tile is MN-major in shared memory

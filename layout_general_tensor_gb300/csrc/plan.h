@@ -25,6 +25,7 @@ struct gemm_plan {
   int split_req;     // split-K factor of the SM-waste rule or of the caller
   int rr_tiles;      // tiles dealt whole before the contiguous unit ranges
   int tail_tiles;    // stream-K tail: tiles whose K blocks are spread over all workers
+  int fin_tiles;     // split tiles converted by the fixup warps of all CTAs (the tail, or all tiles when split > 1)
   int tiles_p, tiles_q, num_units;
   int64_t lda, ldb, ldc;
   int a_mn, b_mn;

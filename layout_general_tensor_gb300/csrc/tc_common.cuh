@@ -201,6 +201,8 @@ __device__ __noinline__ void finish_tile(const TcArgs& a, int m0, int m1, int n0
 // workspace: count the run's splits on the tile's arrival counter, and if
 // this arrival completes the tile, convert it (the CTA that arrives last
 // reads the full sum from L2), then reset the counter.
+// FU: loads in flight per thread in the conversion (registers permitting).
+template <int FU = 8>
 __device__ __forceinline__ void arrive_split_tile(const TcArgs& a, const Group& g, int counter, int m0, int m1, int n0,
                                                   int n1, int et) {
   __threadfence();
@@ -218,18 +220,21 @@ __device__ __forceinline__ void arrive_split_tile(const TcArgs& a, const Group& 
   }
   if (named_bar_or(1, kEpiThreads, mine_last)) {
     __threadfence();
-    finish_tile<8>(a, m0, m1, n0, n1, et);
+    finish_tile<FU>(a, m0, m1, n0, n1, et);
     named_bar_sync(1, kEpiThreads);
     if (et == 0) a.counters[counter] = 0;
   }
 }
 
-// Finish of the stream-K tail by the 128 fixup threads of every CTA (their
-// own warps, named barrier 2), concurrent with the main loops of the whole
-// tiles.  The tail tiles' 128-row strips (two per pair tile) are laid end to
-// end and CTA c converts rows [c*R/G, (c+1)*R/G) of them: for each strip it
-// meets, it waits until all of the strip's K blocks have arrived (tail units
-// run after the first wave, early in the kernel), converts and stores its rows
+// Conversion of split tiles by the 128 fixup threads of every CTA (their own
+// warps, named barrier 2): the tiles [rr_tiles, rr_tiles + tail_tiles) --
+// a stream-K tail, or every tile of a split-K plan.  Each tile is cut into
+// strips (the two halves of a pair tile; the tile itself otherwise) of
+// C rows (128, or BN when swapped), shared among the CTAs (see below): for
+// each strip it serves, a CTA waits until all of the strip's K blocks have
+// arrived (for a
+// stream-K tail early in the kernel, behind the whole tiles' main loops;
+// for split-K at the end, all CTAs at once), converts and stores its rows
 // of C, zeroes them in the workspace, and counts them on the strip's second
 // counter; the CTA completing a strip resets both counters for the next
 // run.  Spreading the reads over all SMs matters: one CTA reading a whole
@@ -238,33 +243,49 @@ template <int BN>
 __device__ __noinline__ bool finish_tail(const TcArgs& a, volatile int* abort_flag, int et) {
   constexpr int kBar = 2;
   const int halves = 1 + a.pair;
-  const int64_t R = static_cast<int64_t>(a.tail_tiles) * halves * TILE_P;
-  const int64_t G = gridDim.x;
-  int64_t row = (static_cast<int64_t>(blockIdx.x) * R) / G;
-  const int64_t row_end = (static_cast<int64_t>(blockIdx.x + 1) * R) / G;
+  const int strip_rows = a.swap ? BN : TILE_P;
+  const int S = a.tail_tiles * halves;  // strips
+  const int G = gridDim.x, c = blockIdx.x;
+  // With at least as many CTAs as strips every CTA serves one strip (a
+  // group of CTAs shares each strip's rows evenly); otherwise each CTA
+  // serves whole strips.
+  int s_begin, s_end;
+  if (G >= S) {
+    s_begin = static_cast<int>((static_cast<int64_t>(c) * S) / G);
+    s_end = s_begin + 1;
+  } else {
+    s_begin = static_cast<int>((static_cast<int64_t>(c) * S) / G);
+    s_end = static_cast<int>((static_cast<int64_t>(c + 1) * S) / G);
+  }
   int32_t* done = a.counters + static_cast<int64_t>(a.tiles_p) * a.tiles_q * halves;
-  while (row < row_end) {
-    const int strip = static_cast<int>(row / TILE_P);
-    const int r0 = static_cast<int>(row - static_cast<int64_t>(strip) * TILE_P);
-    const int r1 = static_cast<int>(min(static_cast<int64_t>(TILE_P), row_end - static_cast<int64_t>(strip) * TILE_P));
+  for (int strip = s_begin; strip < s_end; ++strip) {
+    int r0 = 0, r1 = strip_rows;
+    if (G >= S) {
+      // CTAs [first, last) share this strip: first = ceil(strip*G/S)
+      const int first = static_cast<int>((static_cast<int64_t>(strip) * G + S - 1) / S);
+      const int last = static_cast<int>((static_cast<int64_t>(strip + 1) * G + S - 1) / S);
+      const int k = last - first, j = c - first;
+      r0 = (j * strip_rows) / k;
+      r1 = ((j + 1) * strip_rows) / k;
+    }
     const int tile = a.rr_tiles + strip / halves;
     const int half = strip % halves;
     const int cidx = tile * halves + half;
     int32_t tp, tq, m0, m1, n0, n1;
     tile_ranges(a, tile, BN, tp, tq, m0, m1, n0, n1);
-    m0 += half * TILE_P;
+    if (!a.swap) m0 += half * TILE_P;  // pair halves are P rows = C rows
     const int ma = min(a.M, m0 + r0), mb = min(a.M, m0 + r1);
     bool ok = true;
     if (et == 0) {
-      volatile int32_t* c = a.counters + cidx;
-      if (*c < a.split) {
+      volatile int32_t* cnt = a.counters + cidx;
+      if (*cnt < a.split) {
         const uint64_t t0 = global_timer_ns();
-        while (*c < a.split) {
+        while (*cnt < a.split) {
           if (*abort_flag || global_timer_ns() - t0 > a.wait_limit_ns) {
             ok = false;
             break;
           }
-          __nanosleep(256);
+          __nanosleep(64);
         }
       }
       if (!ok && !*abort_flag) record_timeout(a, abort_flag, 2 * 16 + 5);
@@ -274,14 +295,13 @@ __device__ __noinline__ bool finish_tail(const TcArgs& a, volatile int* abort_fl
     if (mb > ma) finish_tile<8>(a, ma, mb, n0, n1, et);
     __threadfence();
     named_bar_sync(kBar, kEpiThreads);
-    if (et == 0) {
+    if (et == 0 && r1 > r0) {
       const int old = atomicAdd(&done[cidx], r1 - r0);
-      if (old + (r1 - r0) == TILE_P) {
+      if (old + (r1 - r0) == strip_rows) {
         a.counters[cidx] = 0;
         done[cidx] = 0;
       }
     }
-    row += r1 - r0;
   }
   return true;
 }
@@ -295,12 +315,13 @@ __device__ __noinline__ bool finish_tail(const TcArgs& a, volatile int* abort_fl
 // PAIR: the CTA holds P-side half `half` of a pair tile, and the buffer-free
 // arrival goes to the pair's MMA CTA (acce_bar0 is a shared::cluster address).
 //
-// Unswapped tiles with a.tma_c / a.tma_ws leave through shared memory: each
-// warp writes its 32 rows x 32 columns into one of its two 4 KiB staging
-// buffers (`stage_smem`, 1024-aligned; `ring` counts the blocks it has
-// issued) and one lane hands the block to a bulk tile store (C) or bulk
-// tile reduction (fp32 partials), so whole lines reach L2.  Otherwise each
-// thread stores its own row directly.
+// With a.tma_c / a.tma_ws (and BN a multiple of 32) tiles leave through
+// shared memory: each warp writes a 32 x 32 block of C (its 32 TMEM lanes
+// by 32 accumulator columns; rows are m, or n when swapped) into one of its
+// two 4 KiB staging buffers (`stage_smem`, 1024-aligned; `ring` counts the
+// blocks it has issued) and one lane hands the block to a bulk tile store
+// (C) or bulk tile reduction (fp32 partials), so whole lines reach L2.
+// Otherwise each thread stores its own values directly.
 template <int BN, int CH, bool PAIR = false>
 __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, uint32_t tmem_base, uint32_t accf_bar0,
                                                uint32_t acce_bar0, int& acc_iter, volatile int* abort_flag, int q4,
@@ -319,8 +340,51 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
     if (named_bar_or(1, kEpiThreads, !got)) return false;
     tc_fence_after();
     const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(buf * BN);
-    const bool staged = (BN % EPI_BOX == 0) && !a.swap && (full_tile ? a.tma_c : a.tma_ws);
-    if (staged) {
+    const bool staged = (BN % EPI_BOX == 0) && (full_tile ? a.tma_c : a.tma_ws);
+    if (staged && a.swap) {
+      // Swapped: TMEM lane = n, column = m.  Block rows are m, each holding
+      // the warp's 32 n; this lane writes column `lane` of every row.
+      const int32_t xbox = n0 + q4 * 32;  // first n of this warp's blocks
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += EPI_BOX) {
+        uint32_t v[EPI_BOX];
+        tc_ld_32x32b_x32(t_row + c0, v);
+        tc_wait_ld();
+        const int32_t ybox = m0 + c0;
+        if (xbox >= n1 || ybox >= m1) continue;  // block wholly outside C (warp-uniform)
+        const uint32_t sbuf = stage_smem + static_cast<uint32_t>(ring & 1) * 4096u;
+        if (ring >= 2) {
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+        }
+        if (full_tile) {
+          // 16-bit C: 64-byte rows, no swizzle
+#pragma unroll
+          for (int j = 0; j < EPI_BOX; ++j)
+            st_shared_u16(sbuf + 64u * j + 2u * lane, cvt1(__uint_as_float(v[j]), a.c_bf16));
+        } else {
+          // fp32: 128-byte rows in the 128-byte swizzle (16-byte chunk index XOR row & 7)
+#pragma unroll
+          for (int j = 0; j < EPI_BOX; ++j)
+            st_shared_f32(sbuf + 128u * j + ((static_cast<uint32_t>(lane >> 2) ^ (j & 7)) << 4) + 4u * (lane & 3),
+                          __uint_as_float(v[j]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (full_tile)
+            tma_store_2d(&a.tm_c, sbuf, xbox, ybox);
+          else
+            tma_reduce_add_2d(&a.tm_ws, sbuf, xbox, ybox);
+          bulk_commit_group();
+        }
+        ++ring;
+      }
+      if (!full_tile && lane == 0) {
+        bulk_wait_group<0>();
+        fence_proxy_async_global();
+      }
+    } else if (staged) {
       const int32_t ybox = m0 + q4 * 32;  // first C row of this warp's blocks
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += EPI_BOX) {
@@ -443,7 +507,7 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
     }
     ++acc_iter;
   }
-  if (!full_tile) arrive_split_tile(a, g, PAIR ? 2 * g.tile + half : g.tile, m0, m1, n0, n1, et);
+  if (!full_tile) arrive_split_tile<16>(a, g, PAIR ? 2 * g.tile + half : g.tile, m0, m1, n0, n1, et);
   return true;
 }
 
