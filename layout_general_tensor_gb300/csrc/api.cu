@@ -496,11 +496,9 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   // When a base pointer is not 16-byte aligned the operand is repacked too.
   p.ws_bytes_misaligned = off + pack_a_bytes + pack_b_bytes;
   if (int4) {
-    p.asum_ld = p.tiles_q * p.bn;
+    // the prepared (K-contiguous, pair-ordered) activation follows the split-K region
     p.off_aprep = off;
-    p.off_asum = align_up(off + static_cast<size_t>(d.M) * d.K * 2, 256);
-    p.off_gsum = align_up(p.off_asum + static_cast<size_t>(p.kb_total) * p.asum_ld * sizeof(float), 256);
-    p.ws_bytes = align_up(p.off_gsum + static_cast<size_t>(d.K / p.group) * p.asum_ld * sizeof(float), 256);
+    p.ws_bytes = align_up(off + static_cast<size_t>(d.M) * d.K * 2, 256);
     p.ws_bytes_misaligned = p.ws_bytes;
   }
 
@@ -610,10 +608,8 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   {
     // prepared activation: K-contiguous, pitch K, in the workspace
     void* ap = ws + plan->off_aprep;
-    float* asum = reinterpret_cast<float*>(ws + plan->off_asum);
-    float* gsum = reinterpret_cast<float*>(ws + plan->off_gsum);
-    if (lgt::launch_int4_prep(A, plan->lda, plan->a_mn, static_cast<int>(d.M), static_cast<int>(d.K), plan->group, ap,
-                              asum, gsum, plan->asum_ld, plan->sms_grid, stream) != cudaSuccess)
+    if (lgt::launch_int4_prep(A, plan->lda, plan->a_mn, static_cast<int>(d.M), static_cast<int>(d.K), ap,
+                              plan->sms_grid, stream) != cudaSuccess)
       return GEMM_ERR_CUDA;
     if (!lgt::encode_operand(&args.tm_q, ap, GEMM_F16, false, d.M, d.K, d.K, plan->bn)) return GEMM_ERR_CUDA;
   }
@@ -651,11 +647,8 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     a4.zeros = static_cast<const uint16_t*>(zeros);
     a4.groups = static_cast<int32_t>(d.K / plan->group);
     a4.div_kb_per_group = lgt::magic_encode(static_cast<uint32_t>(plan->group / kBlockK));
-    a4.asum = reinterpret_cast<const float*>(ws + plan->off_asum);
-    a4.gsum = reinterpret_cast<const float*>(ws + plan->off_gsum);
     a4.vec_sz = (a4.groups % 8 == 0) && reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
                 reinterpret_cast<uintptr_t>(zeros) % 16 == 0;
-    a4.asum_ld = plan->asum_ld;
     return lgt::launch_int4_gemm(a4, plan->bn, plan->grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
 }

@@ -3,52 +3,39 @@
 //   C[m,n] = sum_k A[m,k] * w(k,n),  w(k,n) = (q(n,k) - z(n,g)) * s(n,g),
 //   g = k / group_size, codes two per byte (low nibble = even k).
 //
-// Within one quantisation group the scale and zero point are constants of the
-// weight row, so the sum splits per group g:
-//   sum_{k in g} A[m,k] (q(n,k) - z) s = s * ( D_g[n,m] - (1024 + z) * S_g[m] ),
-//   D_g[n,m] = sum_{k in g} (1024 + q(n,k)) * A[m,k],  S_g[m] = sum_{k in g} A[m,k].
-// 1024 + q is exactly the fp16 number whose bits are 0x6400 | q, so the
-// mainloop expands nibbles to fp16 with one LOP3 per pair of codes and no
-// floating-point work; the tensor cores form D_g (exact products, fp32 sums)
-// and the epilogue applies s and z once per (row, group) in fp32.
-//
 // The weight is the large operand and the activation the skinny one, so the
 // MMA runs swapped: 128 weight rows (n) on the MMA's M side, the activation
-// rows (m) on its N side, the accumulator holding C^T in TMEM.
+// rows (m) on its N side, the accumulator holding C^T in TMEM.  The expanded
+// weight tile is the MMA's A operand *in TMEM*; the activation its B operand
+// in shared memory.
 //
-// A small pre-pass (int4_prep_kernel) copies the activation into the
-// workspace K-contiguous, with the eight elements of every 8-element group
-// of K reordered to match the order in which one 32-bit word of codes
-// expands (codes 0,4 | 1,5 | 2,6 | 3,7), and writes the per-64-K row sums
-// S used above.
+// Expansion.  A 32-bit word of codes q0..q7 gives the fp16 pairs (1024 + q)
+// of codes (0,4), (1,5), (2,6), (3,7) with one LOP3 each (1024 + q is exactly
+// the fp16 number with bits 0x6400 | q); two packed subtractions and one
+// packed multiply then form (q - z) * s, rounded once to fp16.  q - z is exact
+// for an integer zero point, so a weight equal to its zero point is exactly 0.
+// The activation is copied once, K-contiguous, with every 8-element group of
+// K reordered to that pair order (0,4,1,5,2,6,3,7) by a small pre-pass
+// (int4_prep_kmajor_kernel / int4_prep_kernel), so no code is moved in the
+// mainloop.  The dequantise copy of the BitBLAS TileLang page (the
+// thread-level listing in "Relevant Issues") vectorises its loads of packed
+// weights; here the TMA box does the addressing and every thread's shared
+// loads are 128-bit.
 //
 // A pipeline stage is up to four 64-deep K blocks of one run: the packed
-// weight arrives as one TMA box of 128 rows x 128 bytes (128-byte swizzle; wide
-// row segments keep the TMA stream near the HBM rate, 32-byte ones cap it at a
-// third of it) plus one activation box per K block.
+// weight as one TMA box of 128 rows x 128 bytes (128-byte swizzle; 128-byte
+// row segments keep the TMA stream near the HBM rate) plus one activation box
+// per K block.  The accumulator of a run is double-buffered in TMEM, so the
+// epilogue of one run overlaps the next; a run's epilogue (C, or the split-K
+// partial and the arrival protocol) is the one of the dense kernels.
 //
-// Warp roles of the main kernel (480 threads):
+// Warp roles (448 threads):
 //   warp 0       TMA producer.
-//   warp 1       MMA issuer (and TMEM allocator): the expanded weight tile is
-//                the MMA's A operand *in TMEM*, the activation its B operand in
-//                shared memory; one TMEM accumulator per group segment.
-//   warps 2..9   expanders: two warps per TMEM lane quadrant, alternating
-//                stages.  Each thread owns one weight row: eight 16-byte shared
-//                loads (conflict-free thanks to the swizzle), 3 shifts and 4
-//                LOP3 per 8 codes, one tcgen05.st of 32 columns per K block.
-//   warps 10..13 epilogue: per group segment, tcgen05.ld the accumulator and
-//                fold in s and z; at the end of a run, store C or add the fp32
-//                partial to the split-K workspace (shared arrival protocol).
-//   warp 14      waiter: performs every mbarrier wait the MMA issuer needs and
-//                hands it each ready stage through a named barrier.  An
-//                mbarrier wait executed while MMAs are in flight stalls until
-//                they drain; the named barrier does not, so the issuer only
-//                issues MMAs and commits and the tensor core stays fed.
-//
-// The dequantise copy of the BitBLAS TileLang page (the thread-level TIR
-// listing in "Relevant Issues") decomposes a flat index into (vj, vk, vjj, vkk)
-// to vectorise loads of the packed weight; here the TMA box does that
-// addressing and each thread's loads are 128-bit.
+//   warp 1       TMEM allocator and MMA issuer: waits for an expanded slot,
+//                issues the stage's MMAs, frees the stage and the slot.
+//   warps 2..5   epilogue (TMEM lane quadrant warp % 4).
+//   warps 6..13  expanders: two warps per TMEM lane quadrant, alternating
+//                stages; each thread owns one weight row of the tile.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc_common.cuh"
@@ -56,16 +43,13 @@
 namespace lgt {
 namespace {
 
-constexpr int kThreads4 = 480;
-constexpr int kDequantWarp0 = 2;
-constexpr int kEpiWarp04 = 10;
-constexpr int kWaiterWarp = 14;
+constexpr int kThreads4 = 448;
+constexpr int kEpiWarp04 = 2;
+constexpr int kExpWarp0 = 6;
 constexpr int kQuadK = 4;                     // K blocks per stage
 constexpr uint32_t kRawBytes = TILE_P * 128;  // 128 rows x 128 bytes (256 codes)
 constexpr int kTSlots = 3;                    // TMEM A slots of 128 columns
-constexpr uint32_t kASlotCol0 = 128;          // A slots at [128, 512); segment accumulators below
-constexpr uint32_t kBarStage = 2;             // named barrier: waiter warp <-> MMA warp
-constexpr int kGsumChunk = 64;                // groups of activation row sums staged in shared memory
+constexpr uint32_t kASlotCol0 = 128;          // A slots at [128, 512); the accumulators below
 
 template <int BN>
 struct Cfg4 {
@@ -73,23 +57,34 @@ struct Cfg4 {
   static constexpr uint32_t STAGE_BYTES = kRawBytes + kQuadK * ACT_TILE;
   static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static constexpr int NSEG = (128 / BN) > 8 ? 8 : (128 / BN);  // segment accumulators in TMEM
-  // barriers: full[S], sfree[S], a_full[T], tfree[T], d_full[NSEG], d_empty[NSEG], teardown
-  static constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * kTSlots + 2 * NSEG + 1;
+  // barriers: full[S], sfree[S], a_full[T], tfree[T], accf[2], acce[2], teardown
+  static constexpr uint32_t EPI_OFF = STAGES * STAGE_BYTES;
+  static constexpr uint32_t BAR_OFF = EPI_OFF + EPI_STAGING_BYTES;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * kTSlots + 5;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
-  static constexpr uint32_t GSUM_OFF = ((MISC_OFF + 64 + 15) / 16) * 16;  // staged group row sums
-  static constexpr uint32_t SMEM_ALLOC = GSUM_OFF + kGsumChunk * BN * 4 + 1024;
+  static constexpr uint32_t SMEM_ALLOC = MISC_OFF + 64 + 1024;  // slack for 1024-byte alignment
   static_assert(STAGE_BYTES % 1024 == 0 && ACT_TILE % 1024 == 0, "swizzled buffers stay 1024-byte aligned");
   static_assert(STAGES >= 2, "at least two shared-memory stages");
-  static_assert(NSEG * BN <= static_cast<int>(kASlotCol0), "accumulators fit below the A slots");
+  static_assert(2 * BN <= static_cast<int>(kASlotCol0), "accumulators fit below the A slots");
   static_assert(kASlotCol0 + kTSlots * 128 <= 512, "A slots fit in the TMEM allocation");
-  static_assert(BN <= 64, "per-thread fp32 accumulators: at most 64 activation rows per tile");
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
@@ -118,14 +113,6 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
-// End (exclusive) of the run's K blocks that share the quantisation group of
-// block kb.
-__device__ __forceinline__ int segment_end(const Int4Args& A4, const Group& g, int kb) {
-  const uint32_t grp = magic_div(static_cast<uint32_t>(g.kb0 + kb), A4.div_kb_per_group);
-  const int next_group_kb = static_cast<int>((grp + 1) * A4.div_kb_per_group.d) - g.kb0;
-  return min(g.nkb, next_group_kb);
-}
-
 // Stages of this CTA's runs, in order: up to kQuadK K blocks of one run each
 // (runs without K blocks are skipped).
 struct StageIter {
@@ -149,23 +136,57 @@ struct StageIter {
   }
 };
 
-// Group segments of the K blocks, in order: which TMEM accumulator buffer a
-// block accumulates into and whether it opens / closes its segment.
-template <int NSEG>
-struct SegTracker {
-  int seg_end = 0, nseg = 0, buf = 0;
-  __device__ void new_run() { seg_end = 0; }
-  __device__ void step(const Int4Args& A4, const Group& g, int kb, bool& start, bool& last, int& b, uint32_t& ph) {
-    start = (kb == seg_end);
-    ph = 0;
-    if (start) {
-      seg_end = segment_end(A4, g, kb);
-      buf = nseg % NSEG;
-      ph = static_cast<uint32_t>((nseg / NSEG) & 1);
-      ++nseg;
+// One weight row's scales and zero points, eight groups (16 bytes) at a time,
+// the next eight loaded while the current ones are in use.
+struct RowScales {
+  const uint16_t* srow = nullptr;
+  const uint16_t* zrow = nullptr;
+  int groups = 0, win = -1;
+  bool vec = true;  // rows readable 16 bytes at a time; otherwise one load per group
+  uint4 s_cur, z_cur, s_nxt, z_nxt;
+  __device__ void fetch(int w, uint4& sv, uint4& zv) const {
+    if (w * 8 < groups) {
+      sv = __ldg(reinterpret_cast<const uint4*>(srow) + w);
+      if (zrow) zv = __ldg(reinterpret_cast<const uint4*>(zrow) + w);
     }
-    b = buf;
-    last = (kb + 1 == seg_end);
+  }
+  __device__ void reset(const uint16_t* s, const uint16_t* z, int ngroups, int first_group, bool vectors) {
+    srow = s;
+    zrow = z;
+    groups = ngroups;
+    vec = vectors;
+    const uint4 eight = make_uint4(0x48004800u, 0x48004800u, 0x48004800u, 0x48004800u);  // fp16 8.0
+    s_cur = s_nxt = make_uint4(0u, 0u, 0u, 0u);
+    z_cur = z_nxt = eight;
+    win = first_group >> 3;
+    if (srow && vec) {
+      fetch(win, s_cur, z_cur);
+      fetch(win + 1, s_nxt, z_nxt);
+    }
+  }
+  // fp16 bits of (s, z) of group g (g >= the previous call's group)
+  __device__ void get(int g, uint16_t& sb, uint16_t& zb) {
+    if (!vec) {
+      sb = srow ? __ldg(srow + g) : static_cast<uint16_t>(0);
+      zb = zrow ? __ldg(zrow + g) : (srow ? static_cast<uint16_t>(0x4800) : static_cast<uint16_t>(0));
+      return;
+    }
+    const int w = g >> 3;
+    if (w != win && srow) {
+      if (w == win + 1) {
+        s_cur = s_nxt;
+        z_cur = z_nxt;
+      } else {
+        fetch(w, s_cur, z_cur);
+      }
+      win = w;
+      fetch(w + 1, s_nxt, z_nxt);
+    }
+    const int j = g & 7;
+    const uint32_t sw = (j >> 1) == 0 ? s_cur.x : (j >> 1) == 1 ? s_cur.y : (j >> 1) == 2 ? s_cur.z : s_cur.w;
+    const uint32_t zw = (j >> 1) == 0 ? z_cur.x : (j >> 1) == 1 ? z_cur.y : (j >> 1) == 2 ? z_cur.z : z_cur.w;
+    sb = static_cast<uint16_t>((j & 1) ? (sw >> 16) : (sw & 0xFFFFu));
+    zb = static_cast<uint16_t>((j & 1) ? (zw >> 16) : (zw & 0xFFFFu));
   }
 };
 
@@ -182,18 +203,20 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   const int lane = threadIdx.x & 31;
   const uint32_t bar0 = base + C::BAR_OFF;
   // full[s]: stage s's TMA bytes landed.  sfree[s]: stage s may be refilled
-  // (its raw bytes were read by the expanders and the MMAs that read its
-  // activation completed).  a_full[t]: the expanders wrote the stage's weights
-  // into TMEM A slot t.  tfree[t]: the MMAs reading slot t completed.
+  // (the expanders read its raw bytes and the MMAs that read its activation
+  // completed).  a_full[t]: the expanders wrote a stage's weights into TMEM
+  // A slot t.  tfree[t]: the MMAs reading slot t completed.  accf / acce:
+  // accumulator buffer full / drained.
   auto full_bar = [&](int i) { return bar0 + 8u * i; };
   auto sfree_bar = [&](int i) { return bar0 + 8u * (C::STAGES + i); };
   auto a_full = [&](int t) { return bar0 + 8u * (2 * C::STAGES + t); };
   auto tfree_bar = [&](int t) { return bar0 + 8u * (2 * C::STAGES + kTSlots + t); };
-  auto d_full = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 * kTSlots + b); };
-  auto d_empty = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 * kTSlots + C::NSEG + b); };
-  const uint32_t teardown_bar = bar0 + 8u * (2 * C::STAGES + 2 * kTSlots + 2 * C::NSEG);
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 * kTSlots + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 * kTSlots + 2 + b); };
+  const uint32_t teardown_bar = bar0 + 8u * (2 * C::STAGES + 2 * kTSlots + 4);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  volatile int* consumed_slot = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 8);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
@@ -204,12 +227,13 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
       mbar_init(a_full(t), 4);
       mbar_init(tfree_bar(t), 1);
     }
-    for (int b = 0; b < C::NSEG; ++b) {
-      mbar_init(d_full(b), 1);
-      mbar_init(d_empty(b), kEpiThreads / 32);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), kEpiThreads / 32);
     }
     mbar_init(teardown_bar, 1);
     *abort_flag = 0;
+    *consumed_slot = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
     tma_prefetch_desc(&A4.tm_w);
@@ -224,7 +248,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  int issued = 0;
+  int issued = 0;  // producer lane: stages whose loads were issued
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -252,96 +276,69 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    StageIter it(a);
-    SegTracker<C::NSEG> sg;
-    int kb0, nk, st = 0;
-    bool nr;
-    while (it.next(a, kb0, nk, nr)) {
-      // the waiter warp has checked every barrier of this stage
-      if (named_bar_or(kBarStage, 64, false)) break;
-      if (lane == 0) {
-        if (nr) sg.new_run();
+    if (lane == 0) {
+      StageIter it(a);
+      int kb0, nk, st = 0, acc_iter = -1;
+      bool nr, ok = true;
+      uint32_t d_tmem = tmem_base;
+      while (ok && it.next(a, kb0, nk, nr)) {
         const int s = st % C::STAGES, t = st % kTSlots;
-        // operands of the stage's K blocks first, then the MMAs back to back
-        // and the commits after them (segment hand-offs at the end of the
-        // stage are only a few hundred cycles later)
+        if (nr) {
+          ++acc_iter;
+          const int buf = acc_iter & 1;
+          if (!mbar_wait_bounded(acce_bar(buf), ((acc_iter >> 1) & 1) ^ 1u, a.wait_limit_ns, abort_flag)) {
+            if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 3);
+            break;
+          }
+          d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        }
+        if (!mbar_wait_bounded(a_full(t), (st / kTSlots) & 1, a.wait_limit_ns, abort_flag)) {
+          if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 0);
+          break;
+        }
+        *consumed_slot = st + 1;
+        tc_fence_after();
         const uint64_t bd0 = sw128_desc(base + s * C::STAGE_BYTES + kRawBytes, 16u, 1024u);
         const uint32_t a0 = tmem_base + kASlotCol0 + static_cast<uint32_t>(t * 128);
-        uint32_t dcol[kQuadK];
-        uint32_t first = 0, closes = 0;  // bit j: K block j opens / closes its segment
-#pragma unroll
-        for (int j = 0; j < kQuadK; ++j) {
-          if (j < nk) {
-            bool start, last;
-            int buf;
-            uint32_t ph;
-            sg.step(A4, it.g, kb0 + j, start, last, buf, ph);
-            dcol[j] = static_cast<uint32_t>(buf * BN);
-            first |= (start ? 1u : 0u) << j;
-            closes |= (last ? 1u : 0u) << j;
-          } else {
-            dcol[j] = 0;
-          }
-        }
-        tc_fence_after();
 #pragma unroll
         for (int j = 0; j < kQuadK; ++j) {
           if (j < nk) {
             const uint64_t bd = bd0 + static_cast<uint64_t>((j * C::ACT_TILE) >> 4);
             const uint32_t at = a0 + static_cast<uint32_t>(j * 32);
-            const uint32_t d_tmem = tmem_base + dcol[j];
-            tc_mma_f16_ts(d_tmem, at, bd, a.idesc, ((first >> j) & 1u) ? 0u : 1u);
+            // columns 8 per K = 16 (fp16 pairs), descriptor +32 bytes per K = 16
+            tc_mma_f16_ts(d_tmem, at, bd, a.idesc, (kb0 + j) != 0 ? 1u : 0u);
             tc_mma_f16_ts(d_tmem, at + 8, bd + 2, a.idesc, 1u);
             tc_mma_f16_ts(d_tmem, at + 16, bd + 4, a.idesc, 1u);
             tc_mma_f16_ts(d_tmem, at + 24, bd + 6, a.idesc, 1u);
           }
         }
-#pragma unroll
-        for (int j = 0; j < kQuadK; ++j)
-          if (j < nk && ((closes >> j) & 1u)) tc_commit(d_full(static_cast<int>(dcol[j] / BN)));
         tc_commit(sfree_bar(s));
         tc_commit(tfree_bar(t));
+        if (kb0 + nk == it.g.nkb) tc_commit(accf_bar(acc_iter & 1));
+        ++st;
       }
-      ++st;
+      (void)ok;
     }
-  } else if (warp == kWaiterWarp) {
-    // ------------------------------------------------------------ waiter
-    StageIter it(a);
-    SegTracker<C::NSEG> sg;
-    int kb0, nk, st = 0;
-    bool nr;
-    bool failed = false;
-    while (it.next(a, kb0, nk, nr)) {
-      if (lane == 0 && !failed) {
-        if (nr) sg.new_run();
-        const int t = st % kTSlots;
-        bool ok = mbar_wait_bounded(a_full(t), (st / kTSlots) & 1, a.wait_limit_ns, abort_flag);
-        for (int j = 0; j < nk && ok; ++j) {
-          bool start, last;
-          int buf;
-          uint32_t ph;
-          sg.step(A4, it.g, kb0 + j, start, last, buf, ph);
-          if (start) ok = mbar_wait_bounded(d_empty(buf), ph ^ 1u, a.wait_limit_ns, abort_flag);
-        }
-        if (!ok) {
-          if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 0);
-          failed = true;
-        }
-      }
-      // a_full implies the stage's TMA bytes landed: the expanders observed
-      // full[s] before publishing a_full[t]
-      if (named_bar_or(kBarStage, 64, failed)) break;
-      ++st;
-    }
-  } else if (warp < kEpiWarp04) {
+  } else if (warp >= kExpWarp0) {
     // ------------------------------------------------------------ expanders
     const int q4 = warp & 3;
-    const int h = (warp - kDequantWarp0) >> 2;  // stages with index % 2 == h
-    const int r = q4 * 32 + lane;               // weight row within the tile (TMEM lane)
+    const int h = (warp - kExpWarp0) >> 2;  // stages with index % 2 == h
+    const int r = q4 * 32 + lane;           // weight row within the tile (TMEM lane)
     StageIter it(a);
+    RowScales rs;
     int kb0, nk, st = 0;
     bool nr;
     while (it.next(a, kb0, nk, nr)) {
+      if (nr) {
+        int32_t tp, tq, m0, m1, n0, n1;
+        tile_ranges(a, it.g.tile, BN, tp, tq, m0, m1, n0, n1);
+        const int n = n0 + r;
+        const bool row_ok = n < n1;
+        const int g0 = static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0), A4.div_kb_per_group));
+        rs.reset(row_ok ? A4.scales + static_cast<int64_t>(n) * A4.groups : nullptr,
+                 (row_ok && A4.zeros) ? A4.zeros + static_cast<int64_t>(n) * A4.groups : nullptr, A4.groups, g0,
+                 A4.vec_sz != 0);
+      }
       if ((st & 1) == h) {
         const int s = st % C::STAGES, t = st % kTSlots;
         const bool got =
@@ -361,17 +358,24 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         const uint32_t slot = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + kASlotCol0 +
                               static_cast<uint32_t>(t * 128);
         for (int j = 0; j < nk; ++j) {
+          const int grp =
+              static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + kb0 + j), A4.div_kb_per_group));
+          uint16_t sb, zb;
+          rs.get(grp, sb, zb);
+          const uint32_t s2 = static_cast<uint32_t>(sb) * 0x10001u;
+          const uint32_t z2 = static_cast<uint32_t>(zb) * 0x10001u;
           const uint32_t words[8] = {raw[2 * j].x, raw[2 * j].y, raw[2 * j].z, raw[2 * j].w,
                                      raw[2 * j + 1].x, raw[2 * j + 1].y, raw[2 * j + 1].z, raw[2 * j + 1].w};
           uint32_t vals[32];
 #pragma unroll
           for (int w8 = 0; w8 < 8; ++w8) {
-            // codes (0,4), (1,5), (2,6), (3,7) of the word as fp16 pairs 1024 + q
             const uint32_t w = words[w8];
-            vals[4 * w8 + 0] = lop3_and_or(w, 0x000F000Fu, 0x64006400u);
-            vals[4 * w8 + 1] = lop3_and_or(w >> 4, 0x000F000Fu, 0x64006400u);
-            vals[4 * w8 + 2] = lop3_and_or(w >> 8, 0x000F000Fu, 0x64006400u);
-            vals[4 * w8 + 3] = lop3_and_or(w >> 12, 0x000F000Fu, 0x64006400u);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              // codes (p, p + 4) of the word as the fp16 pair 1024 + q, then (q - z) * s
+              const uint32_t x = lop3_and_or(w >> (4 * p), 0x000F000Fu, 0x64006400u);
+              vals[4 * w8 + p] = hmul2(hsub2(hsub2(x, 0x64006400u), z2), s2);
+            }
           }
           tc_st_32x32b_x32(slot + static_cast<uint32_t>(j * 32), vals);
         }
@@ -386,158 +390,24 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;
     const int et = threadIdx.x - kEpiWarp04 * 32;
-    const int r = q4 * 32 + lane;
-    float* gs_smem = reinterpret_cast<float*>(smem + C::GSUM_OFF);  // [kGsumChunk][BN]
-    const int kpg = static_cast<int>(A4.div_kb_per_group.d);
     Sched sched(a);
     Group g;
-    int seg = 0;
-    bool ok = true;
-    int gs_first = -(1 << 30), gs_m0 = -1;  // staged chunk: groups [gs_first, +kGsumChunk) of rows m0..
-    while (ok && sched.next(a, g)) {
-      int32_t tp, tq, m0, m1, n0, n1;
-      tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
-      const int n = n0 + r;
-      const bool row_ok = n < n1;
-      const uint16_t* srow = A4.scales + static_cast<int64_t>(row_ok ? n : 0) * A4.groups;
-      const uint16_t* zrow = A4.zeros ? A4.zeros + static_cast<int64_t>(row_ok ? n : 0) * A4.groups : nullptr;
-      float acc[BN];
-#pragma unroll
-      for (int j = 0; j < BN; ++j) acc[j] = 0.0f;
-      // This row's scales and zero points, 8 groups (16 bytes) per load, the
-      // next window loaded while the current one is in use.
-      int win = -1, win_nxt = -1;
-      uint4 s_cur = make_uint4(0, 0, 0, 0), s_nxt = s_cur;
-      uint4 z_cur = make_uint4(0x48004800u, 0x48004800u, 0x48004800u, 0x48004800u), z_nxt = z_cur;  // fp16 8.0
-      auto fetch_window = [&](int w, uint4& sv, uint4& zv) {
-        if (row_ok && w * 8 < A4.groups) {
-          sv = __ldg(reinterpret_cast<const uint4*>(srow) + w);
-          if (zrow) zv = __ldg(reinterpret_cast<const uint4*>(zrow) + w);
-        }
-      };
-      int kb = 0;
-      while (kb < g.nkb) {
-        const int end = segment_end(A4, g, kb);
-        const uint32_t grp = magic_div(static_cast<uint32_t>(g.kb0 + kb), A4.div_kb_per_group);
-        // scale and zero point of (row, group)
-        uint16_t sb = 0, zb = 0x4800;
-        if (A4.vec_sz) {
-          const int w = static_cast<int>(grp >> 3);
-          if (w != win) {
-            if (w == win_nxt) {
-              s_cur = s_nxt;
-              z_cur = z_nxt;
-            } else {
-              fetch_window(w, s_cur, z_cur);
-            }
-            win = w;
-            win_nxt = w + 1;
-            fetch_window(win_nxt, s_nxt, z_nxt);
-          }
-          const uint32_t jj = grp & 7;
-          const uint32_t sw = jj < 2 ? s_cur.x : jj < 4 ? s_cur.y : jj < 6 ? s_cur.z : s_cur.w;
-          const uint32_t zw = jj < 2 ? z_cur.x : jj < 4 ? z_cur.y : jj < 6 ? z_cur.z : z_cur.w;
-          sb = static_cast<uint16_t>((jj & 1) ? (sw >> 16) : (sw & 0xFFFFu));
-          if (zrow) zb = static_cast<uint16_t>((jj & 1) ? (zw >> 16) : (zw & 0xFFFFu));
-        } else if (row_ok) {
-          sb = __ldg(srow + grp);
-          if (zrow) zb = __ldg(zrow + grp);
-        }
-        const float sf = row_ok ? __half2float(*reinterpret_cast<const __half*>(&sb)) : 0.0f;
-        const float zf = __half2float(*reinterpret_cast<const __half*>(&zb));
-        // activation row sums of the segment
-        float ssum[BN];
-        const bool whole = (end - kb == kpg) && (static_cast<int>(grp) * kpg == g.kb0 + kb);
-        if (whole) {
-          if (static_cast<int>(grp) >= gs_first + kGsumChunk || static_cast<int>(grp) < gs_first || gs_m0 != m0) {
-            // stage the next chunk of group sums (uniform across the 128 threads)
-            named_bar_sync(1, kEpiThreads);
-            gs_first = static_cast<int>(grp);
-            gs_m0 = m0;
-            const int cnt = min(kGsumChunk, A4.groups - gs_first) * BN;
-            for (int i = et; i < cnt; i += kEpiThreads) {
-              const int gi = i / BN, j = i - gi * BN;
-              gs_smem[i] = A4.gsum[static_cast<int64_t>(gs_first + gi) * A4.asum_ld + m0 + j];
-            }
-            named_bar_sync(1, kEpiThreads);
-          }
-          const float4* sp = reinterpret_cast<const float4*>(gs_smem + (static_cast<int>(grp) - gs_first) * BN);
-#pragma unroll
-          for (int j4 = 0; j4 < BN / 4; ++j4) {
-            const float4 f = sp[j4];
-            ssum[4 * j4 + 0] = f.x;
-            ssum[4 * j4 + 1] = f.y;
-            ssum[4 * j4 + 2] = f.z;
-            ssum[4 * j4 + 3] = f.w;
-          }
-        } else {
-          // a split boundary cuts this group: add the per-block sums
-#pragma unroll
-          for (int j = 0; j < BN; ++j) ssum[j] = 0.0f;
-          for (int k = kb; k < end; ++k) {
-            const float4* sp =
-                reinterpret_cast<const float4*>(A4.asum + static_cast<int64_t>(g.kb0 + k) * A4.asum_ld + m0);
-#pragma unroll
-            for (int j4 = 0; j4 < BN / 4; ++j4) {
-              const float4 f = __ldg(sp + j4);
-              ssum[4 * j4 + 0] += f.x;
-              ssum[4 * j4 + 1] += f.y;
-              ssum[4 * j4 + 2] += f.z;
-              ssum[4 * j4 + 3] += f.w;
-            }
-          }
-        }
-        const int buf = seg % C::NSEG;
-        const bool got = mbar_wait_bounded(d_full(buf), (seg / C::NSEG) & 1, a.wait_limit_ns, abort_flag);
-        if (!got && !*abort_flag) record_timeout(a, abort_flag, 2 * 16 + 2);
-        if (named_bar_or(1, kEpiThreads, !got)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float bias = sf * (1024.0f + zf);
-        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(buf * BN);
-#pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          uint32_t v[16];
-          tc_ld_32x32b_x16(t_row + c0, v);
-          tc_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            acc[c0 + j] = fmaf(sf, __uint_as_float(v[j]), fmaf(-bias, ssum[c0 + j], acc[c0 + j]));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(d_empty(buf));
-        ++seg;
-        kb = end;
-      }
-      if (!ok) break;
-      const bool full_tile = (g.s0 == 0 && g.s1 == a.split);
-      if (row_ok && g.nkb > 0) {
-        if (full_tile) {
-          uint16_t* cc = reinterpret_cast<uint16_t*>(a.c) + n;
-#pragma unroll
-          for (int j = 0; j < BN; ++j)
-            if (m0 + j < m1) cc[static_cast<int64_t>(m0 + j) * a.ldc] = cvt1(acc[j], a.c_bf16);
-        } else {
-          float* wc = a.ws + n;
-#pragma unroll
-          for (int j = 0; j < BN; ++j)
-            if (m0 + j < m1) red_add_f32(wc + static_cast<int64_t>(m0 + j) * a.N, acc[j]);
-        }
-      }
-      if (!full_tile) arrive_split_tile(a, g, g.tile, m0, m1, n0, n1, et);
+    int acc_iter = 0, ring = 0;
+    const uint32_t stage_smem = base + C::EPI_OFF + static_cast<uint32_t>(warp - kEpiWarp04) * 8192u;
+    while (sched.next(a, g)) {
+      if (!epilogue_group<BN, (BN < 32 ? BN : 32)>(a, g, tmem_base, accf_bar(0), acce_bar(0), acc_iter, abort_flag,
+                                                   q4, lane, et, 0, stage_smem, ring))
+        break;
     }
+    if (lane == 0) bulk_wait_group<0>();
   }
 
   // ------------------------------------------------------------ teardown
   __syncthreads();
   if (*abort_flag && warp == 0 && lane == 0) {
-    // Let the last loads issued into each stage land before the CTA exits.
+    // Let the loads still in flight land before the CTA exits.
     volatile int no_abort = 0;
-    const int first = issued > C::STAGES ? issued - C::STAGES : 0;
-    for (int c = first; c < issued; ++c)
+    for (int c = *consumed_slot; c < issued; ++c)
       mbar_wait_bounded(full_bar(c % C::STAGES), (c / C::STAGES) & 1, a.wait_limit_ns, &no_abort);
   }
   if (warp == 1 && lane == 0) {
@@ -551,74 +421,29 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
-// Activation pre-pass: one thread per (64-deep K block, row m).  Writes the
-// row's 64 values to Ap (K-contiguous, pitch K) with each 8-element group
-// reordered to (0,4,1,5,2,6,3,7), and their fp32 sum to asum[kb][m].
-__global__ void int4_prep_kernel(const uint16_t* __restrict__ A, int64_t lda, int a_mn, int M, int K,
-                                 uint16_t* __restrict__ Ap, float* __restrict__ asum, int asum_ld) {
-  const int kb_count = K / TILE_K;
-  const int64_t total = static_cast<int64_t>(kb_count) * M;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int m = static_cast<int>(i % M);
-    const int kb = static_cast<int>(i / M);
-    float sum = 0.0f;
-#pragma unroll 2
-    for (int j = 0; j < TILE_K / 8; ++j) {
-      const int k0 = kb * TILE_K + 8 * j;
-      uint16_t v[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int64_t idx = a_mn ? static_cast<int64_t>(k0 + e) * lda + m : static_cast<int64_t>(m) * lda + k0 + e;
-        v[e] = A[idx];
-        sum += __half2float(*reinterpret_cast<const __half*>(&v[e]));
-      }
-      uint4 o;
-      o.x = static_cast<uint32_t>(v[0]) | (static_cast<uint32_t>(v[4]) << 16);
-      o.y = static_cast<uint32_t>(v[1]) | (static_cast<uint32_t>(v[5]) << 16);
-      o.z = static_cast<uint32_t>(v[2]) | (static_cast<uint32_t>(v[6]) << 16);
-      o.w = static_cast<uint32_t>(v[3]) | (static_cast<uint32_t>(v[7]) << 16);
-      *reinterpret_cast<uint4*>(Ap + static_cast<int64_t>(m) * K + k0) = o;
-    }
-    asum[static_cast<int64_t>(kb) * asum_ld + m] = sum;
-  }
-}
-
-// Activation pre-pass for a K-contiguous activation: one thread per
-// 8-element chunk (m, c), c fastest, so that loads and stores are coalesced
-// 16-byte vectors (scalar loads when the rows are not 16-byte aligned).  The
-// chunk is stored with its elements reordered to (0,4,1,5,2,6,3,7); the 8
-// chunks of a 64-deep block sit in 8 adjacent lanes (K is a multiple of 64)
-// and their sum is reduced by shuffles into asum[kb][m]; when a quantisation
-// group spans 8, 16 or 32 lanes (64, 128 or 256 elements), the group sum
-// gsum[g][m] is reduced the same way (lanes_per_group = 0: not here).
+// Activation pre-pass, K-contiguous activation: one thread per 8-element
+// chunk (m, c), c fastest, so that loads and stores are coalesced 16-byte
+// vectors (scalar loads when the rows are not 16-byte aligned); the chunk is
+// stored with its elements reordered to (0,4,1,5,2,6,3,7).
 __global__ void __launch_bounds__(256) int4_prep_kmajor_kernel(const uint16_t* __restrict__ A, int64_t lda, int vec,
-                                                               int M, int K, uint16_t* __restrict__ Ap,
-                                                               float* __restrict__ asum, float* __restrict__ gsum,
-                                                               int asum_ld, int lanes_per_group) {
+                                                               int M, int K, uint16_t* __restrict__ Ap) {
   const int chunks = K / 8;
   const int64_t total = static_cast<int64_t>(M) * chunks;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  // base is a multiple of the block size: warps cover 32 consecutive chunks
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x; base < total; base += step) {
-    const int64_t i = base + threadIdx.x;
-    const bool act = i < total;
-    int m = 0, c = 0;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (act) {
-      m = static_cast<int>(i / chunks);
-      c = static_cast<int>(i - static_cast<int64_t>(m) * chunks);
-      const uint16_t* src = A + static_cast<int64_t>(m) * lda + 8 * c;
-      if (vec) {
-        const uint4 q = *reinterpret_cast<const uint4*>(src);
-        w[0] = q.x;
-        w[1] = q.y;
-        w[2] = q.z;
-        w[3] = q.w;
-      } else {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += step) {
+    const int m = static_cast<int>(i / chunks);
+    const int c = static_cast<int>(i - static_cast<int64_t>(m) * chunks);
+    const uint16_t* src = A + static_cast<int64_t>(m) * lda + 8 * c;
+    uint32_t w[4];
+    if (vec) {
+      const uint4 q = *reinterpret_cast<const uint4*>(src);
+      w[0] = q.x;
+      w[1] = q.y;
+      w[2] = q.z;
+      w[3] = q.w;
+    } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) w[e] = static_cast<uint32_t>(src[2 * e]) | (static_cast<uint32_t>(src[2 * e + 1]) << 16);
-      }
+      for (int e = 0; e < 4; ++e) w[e] = static_cast<uint32_t>(src[2 * e]) | (static_cast<uint32_t>(src[2 * e + 1]) << 16);
     }
     // elements e = 0..7 are the halves of w[e / 2]; the stored order is 0,4 | 1,5 | 2,6 | 3,7
     uint4 o;
@@ -626,37 +451,29 @@ __global__ void __launch_bounds__(256) int4_prep_kmajor_kernel(const uint16_t* _
     o.y = (w[0] >> 16) | (w[2] & 0xFFFF0000u);
     o.z = (w[1] & 0xFFFFu) | (w[3] << 16);
     o.w = (w[1] >> 16) | (w[3] & 0xFFFF0000u);
-    float s = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __half2 h = *reinterpret_cast<const __half2*>(&w[e]);
-      const float2 f = __half22float2(h);
-      s += f.x + f.y;
-    }
-    if (act) *reinterpret_cast<uint4*>(Ap + static_cast<int64_t>(m) * K + 8 * c) = o;
-    s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
-    s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
-    s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
-    if (act && (c & 7) == 0) asum[static_cast<int64_t>(c >> 3) * asum_ld + m] = s;
-    if (lanes_per_group >= 16) s += __shfl_xor_sync(0xFFFFFFFFu, s, 8);
-    if (lanes_per_group >= 32) s += __shfl_xor_sync(0xFFFFFFFFu, s, 16);
-    if (lanes_per_group && act && c % lanes_per_group == 0)
-      gsum[static_cast<int64_t>(c / lanes_per_group) * asum_ld + m] = s;
+    *reinterpret_cast<uint4*>(Ap + static_cast<int64_t>(m) * K + 8 * c) = o;
   }
 }
 
-// Per-group row sums from the per-block ones: gsum[g][m] = sum of asum over
-// the group's 64-deep blocks (same fp32 values the epilogue would add).
-__global__ void int4_group_sum_kernel(const float* __restrict__ asum, float* __restrict__ gsum, int asum_ld, int M,
-                                      int groups, int kb_per_group) {
-  const int64_t total = static_cast<int64_t>(groups) * M;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int m = static_cast<int>(i % M);
-    const int g = static_cast<int>(i / M);
-    float s = 0.0f;
-    for (int k = 0; k < kb_per_group; ++k) s += asum[static_cast<int64_t>(g * kb_per_group + k) * asum_ld + m];
-    gsum[static_cast<int64_t>(g) * asum_ld + m] = s;
+// Same for an M-contiguous activation: one thread per (8-element K chunk, m),
+// m fastest, so that each of the eight loads is coalesced across the warp.
+__global__ void __launch_bounds__(256) int4_prep_mmajor_kernel(const uint16_t* __restrict__ A, int64_t lda, int M,
+                                                               int K, uint16_t* __restrict__ Ap) {
+  const int chunks = K / 8;
+  const int64_t total = static_cast<int64_t>(M) * chunks;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += step) {
+    const int c = static_cast<int>(i / M);
+    const int m = static_cast<int>(i - static_cast<int64_t>(c) * M);
+    uint16_t v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = A[static_cast<int64_t>(8 * c + e) * lda + m];
+    uint4 o;
+    o.x = static_cast<uint32_t>(v[0]) | (static_cast<uint32_t>(v[4]) << 16);
+    o.y = static_cast<uint32_t>(v[1]) | (static_cast<uint32_t>(v[5]) << 16);
+    o.z = static_cast<uint32_t>(v[2]) | (static_cast<uint32_t>(v[6]) << 16);
+    o.w = static_cast<uint32_t>(v[3]) | (static_cast<uint32_t>(v[7]) << 16);
+    *reinterpret_cast<uint4*>(Ap + static_cast<int64_t>(m) * K + 8 * c) = o;
   }
 }
 
@@ -672,37 +489,20 @@ cudaError_t launch4(const Int4Args& args, int grid, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K, int group, void* Ap, float* asum,
-                             float* gsum, int asum_ld, int sms, cudaStream_t stream) {
-  const int64_t total = static_cast<int64_t>(K / TILE_K) * M;
-  if (total == 0) return cudaSuccess;
+cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K, void* Ap, int sms,
+                             cudaStream_t stream) {
+  const int64_t chunks = static_cast<int64_t>(M) * (K / 8);
+  if (chunks == 0) return cudaSuccess;
+  int64_t blocks = (chunks + 255) / 256;
+  if (blocks > static_cast<int64_t>(sms) * 8) blocks = static_cast<int64_t>(sms) * 8;
   if (!a_mn) {
-    const int lanes = group / 8;
-    const int lpg = (lanes == 8 || lanes == 16 || lanes == 32) ? lanes : 0;
     const int vec = (lda % 8 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
-    const int64_t chunks = static_cast<int64_t>(M) * (K / 8);
-    int64_t blocks = (chunks + 255) / 256;
-    if (blocks > static_cast<int64_t>(sms) * 8) blocks = static_cast<int64_t>(sms) * 8;
-    int4_prep_kmajor_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(A), lda, vec, M, K, static_cast<uint16_t*>(Ap), asum, gsum, asum_ld, lpg);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || lpg) return e;
+    int4_prep_kmajor_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<const uint16_t*>(A), lda, vec,
+                                                                          M, K, static_cast<uint16_t*>(Ap));
+  } else {
+    int4_prep_mmajor_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<const uint16_t*>(A), lda, M,
+                                                                          K, static_cast<uint16_t*>(Ap));
   }
-  const int threads = 128;
-  int64_t blocks = (total + threads - 1) / threads;
-  if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
-  if (a_mn) {
-    int4_prep_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(static_cast<const uint16_t*>(A), lda, a_mn, M,
-                                                                       K, static_cast<uint16_t*>(Ap), asum, asum_ld);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  const int groups = K / group;
-  const int64_t gtotal = static_cast<int64_t>(groups) * M;
-  int64_t gblocks = (gtotal + threads - 1) / threads;
-  if (gblocks > static_cast<int64_t>(sms) * 16) gblocks = static_cast<int64_t>(sms) * 16;
-  int4_group_sum_kernel<<<static_cast<int>(gblocks), threads, 0, stream>>>(asum, gsum, asum_ld, M, groups,
-                                                                           group / TILE_K);
   return cudaGetLastError();
 }
 

@@ -75,12 +75,9 @@ struct TcArgs {
 // (tm_q, K-major) and the epilogue fields; tm_p is unused.
 struct Int4Args {
   TcArgs t;
-  CUtensorMap tm_w;          // packed weight bytes: dims {ldb bytes, N}, box {32, 128}, 32-byte swizzle
+  CUtensorMap tm_w;          // packed weight bytes: dims {ldb bytes, N}, box {128, 128}, 128-byte swizzle
   const uint16_t* scales;    // fp16 [N][groups]
   const uint16_t* zeros;     // fp16 [N][groups], or null for z = 8
-  const float* asum;         // activation row sums per 64-deep K block: [K/64][asum_ld]
-  const float* gsum;         // activation row sums per quantisation group: [groups][asum_ld]
-  int32_t asum_ld;
   int32_t groups;
   MagicDiv div_kb_per_group; // 64-deep K block -> quantisation group
   int32_t vec_sz;            // scale / zero rows readable 8 groups (16 bytes) at a time
@@ -89,12 +86,10 @@ struct Int4Args {
 cudaError_t launch_int4_gemm(const Int4Args& args, int bn, int grid, cudaStream_t stream);
 
 // Activation pre-pass of the int4 GEMM: K-contiguous copy of A (M x K, any
-// layout, 2-byte aligned) into Ap with each 8-element group of K reordered to
-// (0,4,1,5,2,6,3,7), the fp32 row sums of every 64-deep K block into
-// asum[kb * asum_ld + m], and of every quantisation group into
-// gsum[g * asum_ld + m].  K and `group` must be multiples of 64.
-cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K, int group, void* Ap, float* asum,
-                             float* gsum, int asum_ld, int sms, cudaStream_t stream);
+// layout, 2-byte aligned) into Ap (pitch K) with each 8-element group of K
+// reordered to (0,4,1,5,2,6,3,7).  K must be a multiple of 64.
+cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K, void* Ap, int sms,
+                             cudaStream_t stream);
 
 // Returns a cudaError_t; `bn` selects the kernel instance.
 cudaError_t launch_tc_gemm(const TcArgs& args, int bn, int grid, cudaStream_t stream);

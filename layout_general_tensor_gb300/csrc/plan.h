@@ -35,8 +35,7 @@ struct gemm_plan {
   int64_t a_pack_ld, b_pack_ld;
   size_t off_partial, off_counters, off_pack_a, off_pack_b, ws_bytes;
   size_t ws_bytes_misaligned;
-  size_t off_aprep, off_asum, off_gsum;  // int4: prepared activation, its 64-K and per-group row sums
-  int asum_ld;
+  size_t off_aprep;  // int4: the prepared activation
   lgt::DeviceStatus* d_status;
   uint64_t wait_limit_ns;
 };
