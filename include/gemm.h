@@ -71,8 +71,12 @@ typedef struct {
   int32_t flags;              /* 0 or GEMM_FLAG_DETERMINISTIC */
 } gemm_desc_t;
 
-/* Bitwise-reproducible results: no stream-K tail (below).  Split-K factors
- * above 1 are rejected with GEMM_ERR_UNSUPPORTED under this flag. */
+/* Bitwise-reproducible results.  No stream-K tail (below); with a split-K
+ * factor above 1 each run of consecutive splits stores its fp32 partial sum
+ * into a slot of its own (no atomics) and the tile's slots are added in a
+ * fixed order before the conversion.  The workspace then holds the slots
+ * instead of an M x N region.  gemm_run_static_scratch does not support
+ * this mode with a split factor above 1 (GEMM_ERR_UNSUPPORTED). */
 #define GEMM_FLAG_DETERMINISTIC 1
 
 /* What a plan decided. */

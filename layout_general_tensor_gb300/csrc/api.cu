@@ -233,6 +233,9 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
   args.num_units = plan->num_units;
   args.rr_tiles = plan->rr_tiles;
   args.tail_tiles = plan->fin_tiles;
+  args.det = plan->det;
+  args.max_runs = plan->max_runs;
+  if (plan->det) args.slots = partial;
   args.div_split = magic_encode(static_cast<uint32_t>(plan->split));
   args.div_tiles_p = magic_encode(static_cast<uint32_t>(plan->tiles_p));
   args.p_mn = p_mn;
@@ -246,7 +249,8 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
   // fp32 partials, where the pointers and pitches allow them (16 bytes).
   if (env_int("LGT_GEMM_TMA_EPI", 1) != 0) {
     args.tma_c = args.c_vec && encode_output(&args.tm_c, C, false, d.c_dtype, d.M, d.N, plan->ldc * 2);
-    args.tma_ws = partial && (d.N % 4 == 0) && encode_output(&args.tm_ws, partial, true, 0, d.M, d.N, d.N * 4);
+    args.tma_ws = partial && !plan->det && (d.N % 4 == 0) &&
+                  encode_output(&args.tm_ws, partial, true, 0, d.M, d.N, d.N * 4);
   }
   args.idesc = idesc_f16(d.a_dtype == GEMM_BF16 ? 1u : 0u, static_cast<uint32_t>(p_mn), static_cast<uint32_t>(q_mn),
                          static_cast<uint32_t>(TILE_P << plan->pair), static_cast<uint32_t>(plan->bn));
@@ -430,7 +434,7 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   } else {
     p.split = d.split_k;
   }
-  if ((d.flags & GEMM_FLAG_DETERMINISTIC) && p.split > 1) return GEMM_ERR_UNSUPPORTED;
+  p.det = (d.flags & GEMM_FLAG_DETERMINISTIC) && p.split > 1;
   p.split_req = p.split;
   p.kb_per_split = p.kb_total > 0 ? static_cast<int>(ceil_div(p.kb_total, p.split)) : 0;
   const int64_t tiles = static_cast<int64_t>(p.tiles_p) * p.tiles_q;
@@ -478,10 +482,32 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   p.a_pack_ld = align_up(static_cast<size_t>(p.a_row_elems), 8);
   p.b_pack_ld = align_up(static_cast<size_t>(p.b_row_elems), 8);
 
+  if (p.det) {
+    // Deterministic split-K: the tiles' runs (one per worker a tile's units
+    // meet) each own a tile-shaped fp32 slot; max_runs is the most runs of
+    // any tile.  Worker b owns units [b*U/G, (b+1)*U/G).
+    p.fin_tiles = 0;
+    const int64_t G = p.pair ? p.grid / 2 : p.grid;
+    const int64_t U = static_cast<int64_t>(p.num_units);
+    auto owner = [&](int64_t v) {
+      int64_t b = G > 0 ? (v * G) / U : 0;
+      while (b + 1 < G && ((b + 1) * U) / G <= v) ++b;
+      while (b > 0 && (b * U) / G > v) --b;
+      return b;
+    };
+    p.max_runs = 1;
+    for (int64_t t = 0; G > 0 && t < tiles; ++t) {
+      const int64_t r = owner((t + 1) * p.split - 1) - owner(t * p.split) + 1;
+      if (r > p.max_runs) p.max_runs = static_cast<int>(r);
+    }
+  }
   size_t off = 0;
   if (p.split > 1) {
     p.off_partial = off;
-    off = align_up(off + static_cast<size_t>(d.M) * d.N * sizeof(float), 256);
+    const size_t region = p.det ? static_cast<size_t>(tiles) * (1 + p.pair) * p.max_runs * lgt::TILE_P * p.bn *
+                                      sizeof(float)
+                                : static_cast<size_t>(d.M) * d.N * sizeof(float);
+    off = align_up(off + region, 256);
     p.off_counters = off;
     off = align_up(off + static_cast<size_t>(p.num_counters) * sizeof(int32_t), 256);
   }
@@ -629,6 +655,9 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   args.kb_total = plan->kb_total;
   args.num_units = plan->num_units;
   args.rr_tiles = plan->rr_tiles;
+  args.det = plan->det;
+  args.max_runs = plan->max_runs;
+  if (plan->det) args.slots = partial;
   args.div_split = lgt::magic_encode(static_cast<uint32_t>(plan->split));
   args.div_tiles_p = lgt::magic_encode(static_cast<uint32_t>(plan->tiles_p));
   args.swap = plan->swap;

@@ -55,6 +55,9 @@ struct TcArgs {
   int32_t split, kb_per_split, kb_total;
   int32_t num_units;
   int32_t rr_tiles;      // tiles dealt whole, round-robin, after the contiguous unit ranges
+  float* slots;          // deterministic split-K: one fp32 partial slot per (strip, run); see det
+  int32_t det;           // 1: runs store partials into slots, summed in run order by the last arriver
+  int32_t max_runs;      // slots per strip
   int32_t tail_tiles;    // split tiles [rr_tiles, rr_tiles + tail_tiles) converted by the fixup warps of all CTAs
                          // (a stream-K tail, or every tile of a split-K plan); 0: the last arriver converts
   MagicDiv div_split;    // unit -> (tile, split)

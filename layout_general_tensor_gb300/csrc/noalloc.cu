@@ -72,6 +72,7 @@ extern "C" gemm_status_t gemm_run_static_scratch(const gemm_plan_t* plan, const 
   if (reinterpret_cast<uintptr_t>(A) % 2 || reinterpret_cast<uintptr_t>(B) % 2) return GEMM_ERR_ALIGNMENT;
   // Operands must be addressable by TMA in place: there is no room reserved
   // for realigned copies.
+  if (plan->det) return GEMM_ERR_UNSUPPORTED;  // per-run slots are not kept in the static array
   if (plan->repack_a || plan->repack_b || reinterpret_cast<uintptr_t>(A) % 16 ||
       reinterpret_cast<uintptr_t>(B) % 16)
     return GEMM_ERR_UNSUPPORTED;

@@ -197,6 +197,62 @@ __device__ __noinline__ void finish_tile(const TcArgs& a, int m0, int m1, int n0
   }
 }
 
+// Deterministic split-K.  The worker (CTA or CTA pair) that owns unit u of
+// the contiguous-unit phase: the largest b with floor(b*U/G) <= u - u0.
+__device__ __forceinline__ int unit_owner(const TcArgs& a, int64_t u) {
+  const int64_t G = gridDim.x >> a.pair;
+  const int64_t u0 = static_cast<int64_t>(a.rr_tiles) * a.split;
+  const int64_t U = static_cast<int64_t>(a.num_units) - u0;
+  const int64_t v = u - u0;
+  int64_t b = (v * G) / U;
+  while (b + 1 < G && ((b + 1) * U) / G <= v) ++b;
+  while (b > 0 && (b * U) / G > v) --b;
+  return static_cast<int>(b);
+}
+
+// Runs of tile `tile` (one per worker its units meet) and the slot index of
+// this worker's run.
+__device__ __forceinline__ void tile_runs(const TcArgs& a, int tile, int& first_owner, int& nruns) {
+  const int64_t u = static_cast<int64_t>(a.rr_tiles) * a.split + static_cast<int64_t>(tile - a.rr_tiles) * a.split;
+  first_owner = unit_owner(a, u);
+  nruns = unit_owner(a, u + a.split - 1) - first_owner + 1;
+}
+
+// Last arriver of a deterministic split tile: C = the sum of the tile's run
+// slots in run order (rows x cols of C at m0 / n0; slot element (i, j) at
+// i * cols_ld + j, i the C row within the strip).
+template <int U>
+__device__ __noinline__ void finish_tile_det(const TcArgs& a, const float* slot0, int64_t slot_elems, int nruns,
+                                             int m0, int m1, int n0, int n1, int cols_ld, int et) {
+  const int rows = m1 - m0, cols = n1 - n0;
+  uint16_t* cbase = reinterpret_cast<uint16_t*>(a.c);
+  const int total = rows * cols;
+  for (int i0 = et; i0 < total; i0 += kEpiThreads * U) {
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = 0.0f;
+    for (int r = 0; r < nruns; ++r) {
+      const float* slot = slot0 + static_cast<int64_t>(r) * slot_elems;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * kEpiThreads;
+        if (i < total) {
+          const int rr = i / cols, cc = i - rr * cols;
+          v[u] += __ldcg(slot + static_cast<int64_t>(rr) * cols_ld + cc);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * kEpiThreads;
+      if (i < total) {
+        const int rr = i / cols, cc = i - rr * cols;
+        cbase[static_cast<int64_t>(m0 + rr) * a.ldc + (n0 + cc)] = cvt1(v[u], a.c_bf16);
+      }
+    }
+  }
+}
+
 // After the 128 epilogue threads have added a run's fp32 partial into the
 // workspace: count the run's splits on the tile's arrival counter, and if
 // this arrival completes the tile, convert it (the CTA that arrives last
@@ -306,6 +362,34 @@ __device__ __noinline__ bool finish_tail(const TcArgs& a, volatile int* abort_fl
   return true;
 }
 
+// Deterministic split-K arrival: after the run's partial is in its slot,
+// count the run's splits; the CTA completing the count sums the strip's run
+// slots in run order (so the result does not depend on arrival order),
+// converts and stores C, then resets the counter.  Slots are tile-shaped
+// (TILE_P x BN fp32, rows = C rows of the strip) and are overwritten by every
+// run, so nothing needs zeroing.
+template <int BN>
+__device__ __noinline__ void arrive_split_tile_det(const TcArgs& a, const Group& g, int counter, int m0, int m1,
+                                                   int n0, int n1, int et) {
+  __threadfence();
+  named_bar_sync(1, kEpiThreads);
+  bool mine_last = false;
+  if (et == 0) {
+    const int old = atomicAdd(&a.counters[counter], g.s1 - g.s0);
+    mine_last = (old + (g.s1 - g.s0) == a.split);
+  }
+  if (named_bar_or(1, kEpiThreads, mine_last)) {
+    __threadfence();
+    int first, nruns;
+    tile_runs(a, g.tile, first, nruns);
+    constexpr int64_t kSlotElems = static_cast<int64_t>(TILE_P) * BN;
+    const float* slot0 = a.slots + static_cast<int64_t>(counter) * a.max_runs * kSlotElems;
+    finish_tile_det<8>(a, slot0, kSlotElems, nruns, m0, m1, n0, n1, a.swap ? TILE_P : BN, et);
+    named_bar_sync(1, kEpiThreads);
+    if (et == 0) a.counters[counter] = 0;
+  }
+}
+
 // The epilogue of one group, run by the 128 epilogue threads (TMEM lane
 // quadrant q4, lane `lane`, index `et` among the 128).  Reads the fp32
 // accumulator buffer of the group from TMEM and either converts and stores
@@ -331,6 +415,15 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
   tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
   if (PAIR) narrow_to_half(a, half, m0, m1, n0, n1);
   const bool full_tile = (g.s0 == 0 && g.s1 == a.split);
+  const int cidx = PAIR ? 2 * g.tile + half : g.tile;
+  // deterministic split-K: this run's slot (tile-shaped, rows = C rows)
+  float* det_slot = nullptr;
+  if (a.det && !full_tile) {
+    int first, nruns;
+    tile_runs(a, g.tile, first, nruns);
+    const int r = static_cast<int>(blockIdx.x >> a.pair) - first;
+    det_slot = a.slots + (static_cast<int64_t>(cidx) * a.max_runs + r) * (static_cast<int64_t>(TILE_P) * BN);
+  }
   if (g.nkb > 0) {
     const int buf = acc_iter & 1;
     const uint32_t acc_phase = (acc_iter >> 1) & 1;
@@ -340,7 +433,7 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
     if (named_bar_or(1, kEpiThreads, !got)) return false;
     tc_fence_after();
     const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(buf * BN);
-    const bool staged = (BN % EPI_BOX == 0) && (full_tile ? a.tma_c : a.tma_ws);
+    const bool staged = (BN % EPI_BOX == 0) && (full_tile ? a.tma_c : (a.tma_ws && !a.det));
     if (staged && a.swap) {
       // Swapped: TMEM lane = n, column = m.  Block rows are m, each holding
       // the warp's 32 n; this lane writes column `lane` of every row.
@@ -443,6 +536,18 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
         tc_ld_32x32b_x16(t_row + c0, v);
       }
       tc_wait_ld();
+      if (det_slot) {
+        // the run's fp32 partial into its slot (every row; the conversion clips)
+        if (!a.swap) {
+          float* srow = det_slot + static_cast<int64_t>(row) * BN + c0;
+#pragma unroll
+          for (int j = 0; j < CH; j += 4) st_global_v4(srow + j, v[j], v[j + 1], v[j + 2], v[j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < CH; ++j) det_slot[static_cast<int64_t>(c0 + j) * TILE_P + row] = __uint_as_float(v[j]);
+        }
+        continue;
+      }
       if (!a.swap) {
         const int m = m0 + row;
         const int nb = n0 + c0;
@@ -506,8 +611,16 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
         mbar_arrive(acce_bar0 + 8u * buf);
     }
     ++acc_iter;
+  } else if (det_slot) {
+    // a run of empty splits contributes zeros
+    for (int i = et; i < TILE_P * BN; i += kEpiThreads) det_slot[i] = 0.0f;
   }
-  if (!full_tile) arrive_split_tile<16>(a, g, PAIR ? 2 * g.tile + half : g.tile, m0, m1, n0, n1, et);
+  if (!full_tile) {
+    if (a.det)
+      arrive_split_tile_det<BN>(a, g, cidx, m0, m1, n0, n1, et);
+    else
+      arrive_split_tile<16>(a, g, cidx, m0, m1, n0, n1, et);
+  }
   return true;
 }
 

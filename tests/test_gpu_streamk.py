@@ -126,3 +126,46 @@ def test_streamk_full_size_square():
     assert_close(c[rows, cols], oracle_sample(case, inp, rows, cols), case.name)
     assert np.all(np.isfinite(c))
     g.close()
+
+
+@pytest.mark.parametrize("shape,split,pair", [((300, 700, 4000), 3, "0"), ((64, 4096, 16384), 0, "0"),
+                                              ((16, 700, 4000), 7, "0"), ((512, 512, 2048), 4, "1"),
+                                              ((129, 65, 777), 16, "0")],
+                         ids=lambda x: str(x))
+def test_deterministic_split_k(shape, split, pair, monkeypatch):
+    """GEMM_FLAG_DETERMINISTIC with a split factor above 1: per-run partial
+    slots summed in run order -- two runs are bitwise identical, and both
+    are within tolerance of the oracle and of the atomic-reduction plan."""
+    monkeypatch.setenv("LGT_GEMM_PAIR", pair)
+    m = lib()
+    M, N, Kd = shape
+    case = wl.GemmCase(wl.case_name(BF16, M, N, Kd, K, K, f"det_s{split}"), M, N, Kd, K, K, BF16, BF16, BF16,
+                       ("normal", 0.1), ("normal", 0.1), split_k=split)
+    inp = wl.make_inputs(case, seed=split + 3)
+    gd = m.Gemm(_desc(m, case, flags=m.GEMM_FLAG_DETERMINISTIC))
+    assert gd.info.split_k > 1
+    c1, _, C1 = run_case(case, inp, gemm=gd)
+    c2, _, C2 = run_case(case, inp, gemm=gd)
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+    gd.close()
+    c_at, g, _ = run_case(case, inp)
+    g.close()
+    ref = oracle_full(case, inp)
+    assert_close(c1, ref, "deterministic")
+    assert_close(c_at, ref, "atomic")
+
+
+def test_deterministic_int4_split_k():
+    m = lib()
+    case = wl.GemmCase("int4_det_m16_n700_k4096", 16, 700, 4096, K, K, F16, wl.INT4, F16, ("normal", 1.0), ("bytes",),
+                       split_k=8, group_size=128, zero_value=8.0)
+    inp = wl.make_inputs(case, seed=4)
+    l_a, l_b, l_c = case.dense_ld()
+    desc = m.make_desc(case.M, case.N, case.K, K, K, F16, wl.INT4, F16, lda=l_a, ldb=0, ldc=l_c, split_k=8,
+                       group_size=128, num_sms=148, flags=m.GEMM_FLAG_DETERMINISTIC)
+    gd = m.Gemm(desc)
+    c1, _, C1 = run_case(case, inp, gemm=gd)
+    c2, _, C2 = run_case(case, inp, gemm=gd)
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+    assert_close(c1, oracle_full(case, inp), case.name)
+    gd.close()

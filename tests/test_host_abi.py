@@ -192,15 +192,15 @@ def test_invalid_arguments(lib):
 
 
 def test_deterministic_flag(lib):
-    # accepted with no K split; a split factor above 1 cannot be reproducible
-    # bit for bit (fp32 atomics), so it is refused under the flag
+    # accepted with or without a K split (per-run partial slots replace the
+    # fp32 atomics); never a stream-K tail
     h = lib.gemm_create(lib.make_desc(512, 512, 512, flags=lib.GEMM_FLAG_DETERMINISTIC, num_sms=148))
     info = lib.gemm_query(h)
     assert info.split_k == 1 and info.streamk_tiles == 0
     lib.gemm_destroy(h)
-    st, h = lib.gemm_create_status(lib.make_desc(512, 512, 4096, split_k=4, flags=lib.GEMM_FLAG_DETERMINISTIC,
-                                                 num_sms=148))
-    assert st == lib.GEMM_ERR_UNSUPPORTED and h is None
+    h = lib.gemm_create(lib.make_desc(512, 512, 4096, split_k=4, flags=lib.GEMM_FLAG_DETERMINISTIC, num_sms=148))
+    assert lib.gemm_query(h).split_k == 4
+    lib.gemm_destroy(h)
 
 
 def test_no_device_paths(lib):
