@@ -9,11 +9,14 @@
 // weight tile is the MMA's A operand *in TMEM*; the activation its B operand
 // in shared memory.
 //
-// Expansion.  A 32-bit word of codes q0..q7 gives the fp16 pairs (1024 + q)
-// of codes (0,4), (1,5), (2,6), (3,7) with one LOP3 each (1024 + q is exactly
-// the fp16 number with bits 0x6400 | q); two packed subtractions and one
-// packed multiply then form (q - z) * s, rounded once to fp16.  q - z is exact
-// for an integer zero point, so a weight equal to its zero point is exactly 0.
+// Expansion.  A 32-bit word of codes q0..q7 (and the word shifted right by
+// 8) gives the fp16 pairs of codes (0,4), (1,5), (2,6), (3,7) with one LOP3
+// each: a code in bits 0..3 of a half ORed into 0x6400 is the fp16 number
+// 1024 + q, a code in bits 4..7 ORed into 0x5400 is 64 + q (the mantissa's
+// unit there is 1/16).  One packed subtraction of that offset gives q
+// exactly, and one packed FMA q * s + (-z * s) gives the weight: -z * s is
+// rounded to fp16 once per (row, group), the FMA rounds once more, so the
+// weight is within one fp16 rounding of z * s of (q - z) * s.
 // The activation is copied once, K-contiguous, with every 8-element group of
 // K reordered to that pair order (0,4,1,5,2,6,3,7) by a small pre-pass
 // (int4_prep_kmajor_kernel / int4_prep_kernel), so no code is moved in the
@@ -32,7 +35,7 @@
 // Warp roles (448 threads):
 //   warp 0       TMA producer.
 //   warp 1       TMEM allocator and MMA issuer: waits for an expanded slot,
-//                issues the stage's MMAs, frees the stage and the slot.
+//                issues the stage's MMAs, frees the slot.
 //   warps 2..5   epilogue (TMEM lane quadrant warp % 4).
 //   warps 6..13  expanders: two warps per TMEM lane quadrant, alternating
 //                stages; each thread owns one weight row of the tile.
@@ -64,7 +67,7 @@ struct Cfg4 {
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_ALLOC = MISC_OFF + 64 + 1024;  // slack for 1024-byte alignment
   static_assert(STAGE_BYTES % 1024 == 0 && ACT_TILE % 1024 == 0, "swizzled buffers stay 1024-byte aligned");
-  static_assert(STAGES >= 2, "at least two shared-memory stages");
+  static_assert(STAGES > kTSlots, "a stage buffer outlives the TMEM slot cycle (sfree protocol)");
   static_assert(2 * BN <= static_cast<int>(kASlotCol0), "accumulators fit below the A slots");
   static_assert(kASlotCol0 + kTSlots * 128 <= 512, "A slots fit in the TMEM allocation");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
@@ -85,6 +88,12 @@ __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 
@@ -203,10 +212,12 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   const int lane = threadIdx.x & 31;
   const uint32_t bar0 = base + C::BAR_OFF;
   // full[s]: stage s's TMA bytes landed.  sfree[s]: stage s may be refilled
-  // (the expanders read its raw bytes and the MMAs that read its activation
-  // completed).  a_full[t]: the expanders wrote a stage's weights into TMEM
-  // A slot t.  tfree[t]: the MMAs reading slot t completed.  accf / acce:
-  // accumulator buffer full / drained.
+  // (its expanders read its raw bytes, and the expanders of the stage that
+  // reuses its TMEM slot saw that slot freed, i.e. the MMAs that read its
+  // activation completed; that saves the MMA issuer a commit per stage).
+  // a_full[t]: the expanders wrote a stage's weights into TMEM A slot t.
+  // tfree[t]: the MMAs reading slot t completed.  accf / acce: accumulator
+  // buffer full / drained.
   auto full_bar = [&](int i) { return bar0 + 8u * i; };
   auto sfree_bar = [&](int i) { return bar0 + 8u * (C::STAGES + i); };
   auto a_full = [&](int t) { return bar0 + 8u * (2 * C::STAGES + t); };
@@ -221,7 +232,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(full_bar(i), 1);
-      mbar_init(sfree_bar(i), 4 + 1);  // the stage's four expander warps + the MMA's commit
+      mbar_init(sfree_bar(i), 4 + 4);  // the stage's four expander warps + the four of the stage 3 later
     }
     for (int t = 0; t < kTSlots; ++t) {
       mbar_init(a_full(t), 4);
@@ -312,7 +323,6 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
             tc_mma_f16_ts(d_tmem, at + 24, bd + 6, a.idesc, 1u);
           }
         }
-        tc_commit(sfree_bar(s));
         tc_commit(tfree_bar(t));
         if (kb0 + nk == it.g.nkb) tc_commit(accf_bar(acc_iter & 1));
         ++st;
@@ -348,6 +358,8 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         // the warp leaves together (tcgen05.st below needs every lane)
         if (!__all_sync(0xffffffffu, got)) break;
         tc_fence_after();
+        // the MMAs of stage st - kTSlots completed: its stage buffer may be refilled
+        if (st >= kTSlots && lane == 0) mbar_arrive(sfree_bar((st - kTSlots) % C::STAGES));
         // raw row r: eight 16-byte chunks, chunk c stored at c ^ (r mod 8) (128-byte swizzle)
         const uint8_t* rowp = smem + s * C::STAGE_BYTES + r * 128;
         uint4 raw[8];
@@ -363,19 +375,22 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
           uint16_t sb, zb;
           rs.get(grp, sb, zb);
           const uint32_t s2 = static_cast<uint32_t>(sb) * 0x10001u;
-          const uint32_t z2 = static_cast<uint32_t>(zb) * 0x10001u;
+          const uint32_t nzs2 = hmul2(static_cast<uint32_t>(zb) * 0x10001u, s2) ^ 0x80008000u;  // -z * s
           const uint32_t words[8] = {raw[2 * j].x, raw[2 * j].y, raw[2 * j].z, raw[2 * j].w,
                                      raw[2 * j + 1].x, raw[2 * j + 1].y, raw[2 * j + 1].z, raw[2 * j + 1].w};
           uint32_t vals[32];
 #pragma unroll
           for (int w8 = 0; w8 < 8; ++w8) {
-            const uint32_t w = words[w8];
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              // codes (p, p + 4) of the word as the fp16 pair 1024 + q, then (q - z) * s
-              const uint32_t x = lop3_and_or(w >> (4 * p), 0x000F000Fu, 0x64006400u);
-              vals[4 * w8 + p] = hmul2(hsub2(hsub2(x, 0x64006400u), z2), s2);
-            }
+            const uint32_t lo = words[w8], hi = lo >> 8;
+            // codes (p, p + 4) of the word for p = 0..3, then q * s - z * s
+            const uint32_t q0 = hsub2(lop3_and_or(lo, 0x000F000Fu, 0x64006400u), 0x64006400u);
+            const uint32_t q1 = hsub2(lop3_and_or(lo, 0x00F000F0u, 0x54005400u), 0x54005400u);
+            const uint32_t q2 = hsub2(lop3_and_or(hi, 0x000F000Fu, 0x64006400u), 0x64006400u);
+            const uint32_t q3 = hsub2(lop3_and_or(hi, 0x00F000F0u, 0x54005400u), 0x54005400u);
+            vals[4 * w8 + 0] = hfma2(q0, s2, nzs2);
+            vals[4 * w8 + 1] = hfma2(q1, s2, nzs2);
+            vals[4 * w8 + 2] = hfma2(q2, s2, nzs2);
+            vals[4 * w8 + 3] = hfma2(q3, s2, nzs2);
           }
           tc_st_32x32b_x32(slot + static_cast<uint32_t>(j * 32), vals);
         }

@@ -1,7 +1,8 @@
 """GPU parity of the int4-weight GEMM (dequantisation inside the mainloop)
 against the fp64 oracle, through the C ABI.  Same tolerances as the dense
-path.  The kernel accumulates (1024 + q) * a on the tensor cores and applies
-each (row, group)'s scale and zero point once, in fp32."""
+path.  The kernel expands each weight to fp16 as q * s + (-z * s) (the
+second term rounded to fp16 once per row and group) and accumulates in fp32
+on the tensor cores."""
 import numpy as np
 import pytest
 import torch
@@ -67,9 +68,9 @@ def test_int4_activation_m_contiguous():
 
 
 def test_int4_general_dequant_path():
-    """Non-integer zero points and very small scales: the scale and zero
-    point are applied once per (row, group) in fp32, so the result must match
-    the exact oracle and also the oracle on fp16-rounded weights."""
+    """Non-integer zero points and very small scales: the expanded weights
+    are fp16, so the result must match the exact oracle and also the oracle
+    on fp16-rounded weights."""
     case = _case(8, 384, 512, split=1, zero=7.5, scale=("uniform", 2e-4, 9e-4))
     inp = wl.make_inputs(case, seed=9)
     c, g, _ = run_case(case, inp)
@@ -93,9 +94,8 @@ def test_int4_closed_forms():
     g = m.Gemm(desc)
     C = torch.empty(M * N, dtype=torch.float16, device="cuda")
     Ad = A.cuda()
-    # all codes 8 with zero point 8 -> zero.  The kernel forms
-    # s * (sum (1024 + q) a - (1024 + z) sum a) in fp32, so the two terms
-    # cancel to within fp32 rounding of the ~1024 * sum(a) magnitude.
+    # all codes 8 with zero point 8 -> zero: 8 * s is exact in fp16, so each
+    # expanded weight 8 * s - 8 * s is exactly 0.
     W = torch.full((N * Kd // 2,), 0x88, dtype=torch.uint8, device="cuda")
     s = torch.full((N, Kd // 128), 0.01, dtype=torch.float16, device="cuda")
     g.run(Ad, W, C, s, None)
