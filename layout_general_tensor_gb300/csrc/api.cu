@@ -197,6 +197,23 @@ bool encode_int4_weights(CUtensorMap* map, const void* ptr, int64_t N, int64_t l
   return r == CUDA_SUCCESS;
 }
 
+// Prepared int4-path activation, K-block-major fp16 (element (m, k) at
+// ((k / 64) * M + m) * 64 + k % 64): a 3-D map {64, M, K / 64}, box
+// {64, bn, kb_box}, 128-byte swizzle, so one copy brings a stage's K blocks
+// as kb_box consecutive bn x 128-byte tiles.
+bool encode_int4_activation(CUtensorMap* map, const void* ptr, int64_t M, int64_t K, int bn, int kb_box) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(M) * 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(bn), static_cast<cuuint32_t>(kb_box)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                            float* partial, int32_t* counters, cudaStream_t stream) {
   const gemm_desc_t& d = plan->d;
@@ -522,9 +539,11 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   // When a base pointer is not 16-byte aligned the operand is repacked too.
   p.ws_bytes_misaligned = off + pack_a_bytes + pack_b_bytes;
   if (int4) {
-    // the prepared (K-contiguous, pair-ordered) activation follows the split-K region
+    // the prepared (K-block-major, pair-ordered) activation and its
+    // per-group sums follow the split-K region
     p.off_aprep = off;
-    p.ws_bytes = align_up(off + static_cast<size_t>(d.M) * d.K * 2, 256);
+    p.off_agsum = align_up(off + static_cast<size_t>(d.M) * d.K * 2, 256);
+    p.ws_bytes = align_up(p.off_agsum + static_cast<size_t>(d.M) * (d.K / p.group) * sizeof(float), 256);
     p.ws_bytes_misaligned = p.ws_bytes;
   }
 
@@ -631,13 +650,17 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
 
   lgt::TcArgs args;
   std::memset(&args, 0, sizeof(args));
+  const float* args_agsum = nullptr;
   {
-    // prepared activation: K-contiguous, pitch K, in the workspace
+    // prepared activation: K-block-major, in the workspace
     void* ap = ws + plan->off_aprep;
-    if (lgt::launch_int4_prep(A, plan->lda, plan->a_mn, static_cast<int>(d.M), static_cast<int>(d.K), ap,
-                              plan->sms_grid, stream) != cudaSuccess)
+    float* agsum = reinterpret_cast<float*>(ws + plan->off_agsum);
+    if (lgt::launch_int4_prep(A, plan->lda, plan->a_mn, static_cast<int>(d.M), static_cast<int>(d.K),
+                              static_cast<int>(plan->group), ap, agsum, plan->sms_grid, stream) != cudaSuccess)
       return GEMM_ERR_CUDA;
-    if (!lgt::encode_operand(&args.tm_q, ap, GEMM_F16, false, d.M, d.K, d.K, plan->bn)) return GEMM_ERR_CUDA;
+    args_agsum = agsum;
+    if (!lgt::encode_int4_activation(&args.tm_q, ap, d.M, d.K, plan->bn, d.K / 64 < 4 ? static_cast<int>(d.K / 64) : 4))
+      return GEMM_ERR_CUDA;
   }
   args.c = C;
   args.ldc = plan->ldc;
@@ -672,10 +695,12 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     std::memset(&a4, 0, sizeof(a4));
     a4.t = args;
     if (!lgt::encode_int4_weights(&a4.tm_w, B, d.N, plan->ldb)) return GEMM_ERR_CUDA;
+    a4.agsum = args_agsum;
     a4.scales = static_cast<const uint16_t*>(scales);
     a4.zeros = static_cast<const uint16_t*>(zeros);
     a4.groups = static_cast<int32_t>(d.K / plan->group);
     a4.div_kb_per_group = lgt::magic_encode(static_cast<uint32_t>(plan->group / kBlockK));
+    a4.x_box_kb = d.K / 64 < 4 ? static_cast<int32_t>(d.K / 64) : 4;
     a4.vec_sz = (a4.groups % 8 == 0) && reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
                 reinterpret_cast<uintptr_t>(zeros) % 16 == 0;
     return lgt::launch_int4_gemm(a4, plan->bn, plan->grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

@@ -27,18 +27,26 @@
 //
 // A pipeline stage is up to four 64-deep K blocks of one run: the packed
 // weight as one TMA box of 128 rows x 128 bytes (128-byte swizzle; 128-byte
-// row segments keep the TMA stream near the HBM rate) plus one activation box
-// per K block.  The accumulator of a run is double-buffered in TMEM, so the
+// row segments keep the TMA stream near the HBM rate) in the weight ring, and
+// one activation box per K block in the activation ring.  The weight ring is
+// freed as soon as the expanders have read a stage, so its depth is all in
+// flight.  The accumulators of a run are double-buffered in TMEM, so the
 // epilogue of one run overlaps the next; a run's epilogue (C, or the split-K
 // partial and the arrival protocol) is the one of the dense kernels.
 //
-// Warp roles (448 threads):
-//   warp 0       TMA producer.
-//   warp 1       TMEM allocator and MMA issuer: waits for an expanded slot,
-//                issues the stage's MMAs, frees the slot.
-//   warps 2..5   epilogue (TMEM lane quadrant warp % 4).
-//   warps 6..13  expanders: two warps per TMEM lane quadrant, alternating
-//                stages; each thread owns one weight row of the tile.
+// Warp roles (512 threads):
+//   warp 0       TMA producer for both rings.
+//   warps 1..3   MMA issuers (NI of them active, by accumulator width): each
+//                waits for an expanded slot and the stage's activation, issues
+//                its share of the stage's MMAs into its own accumulator, frees
+//                the slot and the activation buffer.  Warp 1 owns the TMEM.
+//   warps 4..7   epilogue (TMEM lane quadrant warp % 4), adds the NI
+//                accumulators.
+//   warps 8..15  expanders: two warps per TMEM lane quadrant, each taking two
+//                of every stage's four K blocks; each thread owns one weight
+//                row of the tile.
+#include <cuda_fp16.h>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc_common.cuh"
@@ -46,29 +54,43 @@
 namespace lgt {
 namespace {
 
-constexpr int kThreads4 = 448;
-constexpr int kEpiWarp04 = 2;
-constexpr int kExpWarp0 = 6;
+constexpr int kThreads4 = 512;
+constexpr int kIssWarp0 = 1;                  // MMA issuer warps 1..3
+constexpr int kMaxIssuers = 3;
+constexpr int kEpiWarp04 = 4;                 // epilogue warps 4..7
+constexpr int kExpWarp0 = 8;                  // expander warps 8..15
 constexpr int kQuadK = 4;                     // K blocks per stage
 constexpr uint32_t kRawBytes = TILE_P * 128;  // 128 rows x 128 bytes (256 codes)
+constexpr uint32_t kWStage = kRawBytes;       // packed-weight stage
 constexpr int kTSlots = 3;                    // TMEM A slots of 128 columns
 constexpr uint32_t kASlotCol0 = 128;          // A slots at [128, 512); the accumulators below
 
 template <int BN>
 struct Cfg4 {
+  // MMA issuers.  One thread keeps about one narrow (N <= 64) MMA in flight,
+  // so the tensor core runs several times faster when several threads issue
+  // into accumulators of their own, which the epilogue adds.
+  static constexpr int NI = BN == 16 ? 3 : (BN == 32 ? 2 : 1);
   static constexpr uint32_t ACT_TILE = BN * TILE_K * 2;  // one 64-deep activation box
-  static constexpr uint32_t STAGE_BYTES = kRawBytes + kQuadK * ACT_TILE;
-  static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  // barriers: full[S], sfree[S], a_full[T], tfree[T], accf[2], acce[2], teardown
-  static constexpr uint32_t EPI_OFF = STAGES * STAGE_BYTES;
-  static constexpr uint32_t BAR_OFF = EPI_OFF + EPI_STAGING_BYTES;
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * kTSlots + 5;
+  static constexpr uint32_t XSTAGE = kQuadK * ACT_TILE;  // a stage's activation
+  static constexpr int XST = BN == 64 ? 3 : 4;           // activation ring
+  // the tile's slice of the activation group sums, Ag[g][m0 .. m0 + BN),
+  // staged in shared memory for the zero-point term (BN = 16, up to 256 groups)
+  static constexpr uint32_t ZP_BYTES = BN == 16 ? 256 * BN * 4 : 0;
+  static constexpr uint32_t RING_BYTES = 224 * 1024 - ZP_BYTES;
+  static constexpr int WST_FIT = static_cast<int>((RING_BYTES - XST * XSTAGE) / kWStage);
+  static constexpr int WST = WST_FIT > 12 ? 12 : WST_FIT;  // packed-weight ring
+  static constexpr uint32_t X_OFF = WST * kWStage;
+  // barriers: full_w[W], wfree[W], full_x[X], xfree[X], a_full[T], tfree[T], accf[2], acce[2], teardown
+  static constexpr uint32_t ZP_OFF = X_OFF + XST * XSTAGE;
+  static constexpr uint32_t BAR_OFF = ZP_OFF + ZP_BYTES;
+  static constexpr uint32_t NUM_BARS = 2 * WST + 2 * XST + 2 * kTSlots + 5;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_ALLOC = MISC_OFF + 64 + 1024;  // slack for 1024-byte alignment
-  static_assert(STAGE_BYTES % 1024 == 0 && ACT_TILE % 1024 == 0, "swizzled buffers stay 1024-byte aligned");
-  static_assert(STAGES > kTSlots, "a stage buffer outlives the TMEM slot cycle (sfree protocol)");
-  static_assert(2 * BN <= static_cast<int>(kASlotCol0), "accumulators fit below the A slots");
+  static_assert(kWStage % 1024 == 0 && ACT_TILE % 1024 == 0, "swizzled buffers stay 1024-byte aligned");
+  static_assert(WST >= 4 && XST >= 2, "ring depths");
+  static_assert(NI <= kMaxIssuers && NI <= kQuadK * 4, "every issuer has an MMA in every stage");
+  static_assert(2 * NI * BN <= static_cast<int>(kASlotCol0), "accumulators fit below the A slots");
   static_assert(kASlotCol0 + kTSlots * 128 <= 512, "A slots fit in the TMEM allocation");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
@@ -79,16 +101,14 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
   return d;
 }
 
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t b) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(b)));
 }
 
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
@@ -122,6 +142,32 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
+// Issuer ISS's MMAs of one stage of NK K blocks (MMA m = 4 j + k: K block j,
+// 16-deep step k; the issuer's are those with m % NI == ISS), straight-line:
+// an MMA skipped by a runtime guard still costs its issue slot.
+template <int NI, int ISS, int NK, uint32_t ACT_TILE>
+__device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint32_t a0, uint64_t bd0, uint32_t idesc, uint32_t first) {
+#pragma unroll
+  for (int m = ISS; m < 4 * NK; m += NI) {
+    const int j = m >> 2, k = m & 3;
+    // A: 8 TMEM columns (16 fp16 pairs) per 16-deep step; B: +32 bytes per step
+    tc_mma_f16_ts(d_tmem, a0 + static_cast<uint32_t>(j * 32 + k * 8),
+                  bd0 + static_cast<uint64_t>((j * ACT_TILE) >> 4) + static_cast<uint64_t>(2 * k), idesc,
+                  (m == ISS && first) ? 0u : 1u);
+  }
+}
+
+template <int NI, int ISS, uint32_t ACT_TILE>
+__device__ __forceinline__ void issue_stage_nk(int nk, uint32_t d_tmem, uint32_t a0, uint64_t bd0, uint32_t idesc,
+                                               uint32_t first) {
+  switch (nk) {
+    case 4: issue_stage<NI, ISS, 4, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
+    case 3: issue_stage<NI, ISS, 3, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
+    case 2: issue_stage<NI, ISS, 2, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
+    default: issue_stage<NI, ISS, 1, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
+  }
+}
+
 // Stages of this CTA's runs, in order: up to kQuadK K blocks of one run each
 // (runs without K blocks are skipped).
 struct StageIter {
@@ -145,63 +191,137 @@ struct StageIter {
   }
 };
 
-// One weight row's scales and zero points, eight groups (16 bytes) at a time,
-// the next eight loaded while the current ones are in use.
-struct RowScales {
-  const uint16_t* srow = nullptr;
+// The zero-point term of a tile, subtracted from the run that starts at K
+// block 0 (its accumulator holds sum_k A[m, k] q(n, k) s(n, g(k)) for its
+// K blocks; the other runs' partials need no term): for this thread's row n,
+//   corr[m] = sum over all groups g of z(n, g) s(n, g) * Ag[g][m],
+// with Ag the activation's group sums.  z s is exact in fp32.  For BN = 16
+// the term is formed before the accumulator is ready, else per block of
+// columns when it is drained.
+template <int BN>
+struct ZpFix {
+  static constexpr int NC = BN <= 16 ? BN : 1;
+  const Int4Args* A4 = nullptr;
+  const uint16_t* srow = nullptr;  // null: no term (row beyond N)
   const uint16_t* zrow = nullptr;
-  int groups = 0, win = -1;
-  bool vec = true;  // rows readable 16 bytes at a time; otherwise one load per group
-  uint4 s_cur, z_cur, s_nxt, z_nxt;
-  __device__ void fetch(int w, uint4& sv, uint4& zv) const {
-    if (w * 8 < groups) {
-      sv = __ldg(reinterpret_cast<const uint4*>(srow) + w);
-      if (zrow) zv = __ldg(reinterpret_cast<const uint4*>(zrow) + w);
-    }
-  }
-  __device__ void reset(const uint16_t* s, const uint16_t* z, int ngroups, int first_group, bool vectors) {
-    srow = s;
-    zrow = z;
-    groups = ngroups;
-    vec = vectors;
-    const uint4 eight = make_uint4(0x48004800u, 0x48004800u, 0x48004800u, 0x48004800u);  // fp16 8.0
-    s_cur = s_nxt = make_uint4(0u, 0u, 0u, 0u);
-    z_cur = z_nxt = eight;
-    win = first_group >> 3;
-    if (srow && vec) {
-      fetch(win, s_cur, z_cur);
-      fetch(win + 1, s_nxt, z_nxt);
-    }
-  }
-  // fp16 bits of (s, z) of group g (g >= the previous call's group)
-  __device__ void get(int g, uint16_t& sb, uint16_t& zb) {
-    if (!vec) {
-      sb = srow ? __ldg(srow + g) : static_cast<uint16_t>(0);
-      zb = zrow ? __ldg(zrow + g) : (srow ? static_cast<uint16_t>(0x4800) : static_cast<uint16_t>(0));
-      return;
-    }
-    const int w = g >> 3;
-    if (w != win && srow) {
-      if (w == win + 1) {
-        s_cur = s_nxt;
-        z_cur = z_nxt;
-      } else {
-        fetch(w, s_cur, z_cur);
+  uint32_t ag_smem = 0;            // staged Ag slice (fp32 [g][BN]), or 0: read from global memory
+  int m0 = 0;
+  bool active = false;  // the current run is one that subtracts the term
+  float corr[NC];
+
+  template <int N>
+  __device__ __forceinline__ void term(int c0, float (&out)[N]) const {
+#pragma unroll
+    for (int j = 0; j < N; ++j) out[j] = 0.0f;
+    if (!srow) return;
+    const int M = A4->t.M, G = A4->groups;
+    const int mc = m0 + c0;
+    const bool full = mc + N <= M && (M & 3) == 0;
+    // group g's Ag[g][mc .. mc + N) times zs
+    auto add_group = [&](int g, float zs) {
+      if (ag_smem) {
+#pragma unroll
+        for (int j = 0; j < N; j += 4) {
+          const float4 v = ld_shared_f32x4(ag_smem + static_cast<uint32_t>((g * BN + c0 + j) * 4));
+          out[j] = fmaf(zs, v.x, out[j]);
+          out[j + 1] = fmaf(zs, v.y, out[j + 1]);
+          out[j + 2] = fmaf(zs, v.z, out[j + 2]);
+          out[j + 3] = fmaf(zs, v.w, out[j + 3]);
+        }
+        return;
       }
-      win = w;
-      fetch(w + 1, s_nxt, z_nxt);
+      const float* ag = A4->agsum + static_cast<int64_t>(g) * M + mc;
+      if (full) {
+#pragma unroll
+        for (int j = 0; j < N; j += 4) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(ag + j));
+          out[j] = fmaf(zs, v.x, out[j]);
+          out[j + 1] = fmaf(zs, v.y, out[j + 1]);
+          out[j + 2] = fmaf(zs, v.z, out[j + 2]);
+          out[j + 3] = fmaf(zs, v.w, out[j + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+          if (mc + j < M) out[j] = fmaf(zs, __ldg(ag + j), out[j]);
+      }
+    };
+    if (A4->vec_sz) {
+      // the row's scales and zero points 16 bytes (8 groups) per load, four
+      // loads of each in flight at a time
+      for (int gb = 0; gb < G; gb += 32) {
+        uint4 sw[4], zw[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          sw[w] = make_uint4(0u, 0u, 0u, 0u);
+          zw[w] = make_uint4(0x48004800u, 0x48004800u, 0x48004800u, 0x48004800u);  // fp16 8.0
+          if (gb + 8 * w < G) {
+            sw[w] = __ldg(reinterpret_cast<const uint4*>(srow + gb) + w);
+            if (zrow) zw[w] = __ldg(reinterpret_cast<const uint4*>(zrow + gb) + w);
+          }
+        }
+#pragma unroll 1
+        for (int w = 0; w < 4; ++w) {
+          if (gb + 8 * w >= G) break;
+          const uint32_t sv[4] = {sw[w].x, sw[w].y, sw[w].z, sw[w].w};
+          const uint32_t zv[4] = {zw[w].x, zw[w].y, zw[w].z, zw[w].w};
+#pragma unroll 2
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t sb = (e & 1) ? (sv[e >> 1] >> 16) : (sv[e >> 1] & 0xFFFFu);
+            const uint32_t zb = (e & 1) ? (zv[e >> 1] >> 16) : (zv[e >> 1] & 0xFFFFu);
+            add_group(gb + 8 * w + e, half_bits_to_float(zb) * half_bits_to_float(sb));
+          }
+        }
+      }
+    } else {
+      for (int g = 0; g < G; ++g)
+        add_group(g, (zrow ? half_bits_to_float(__ldg(zrow + g)) : 8.0f) * half_bits_to_float(__ldg(srow + g)));
     }
-    const int j = g & 7;
-    const uint32_t sw = (j >> 1) == 0 ? s_cur.x : (j >> 1) == 1 ? s_cur.y : (j >> 1) == 2 ? s_cur.z : s_cur.w;
-    const uint32_t zw = (j >> 1) == 0 ? z_cur.x : (j >> 1) == 1 ? z_cur.y : (j >> 1) == 2 ? z_cur.z : z_cur.w;
-    sb = static_cast<uint16_t>((j & 1) ? (sw >> 16) : (sw & 0xFFFFu));
-    zb = static_cast<uint16_t>((j & 1) ? (zw >> 16) : (zw & 0xFFFFu));
+  }
+
+  // Sets up (and for BN = 16 forms) the term of a run that starts a tile.
+  // All 128 epilogue threads call it together: with a staging buffer
+  // (`stage` != 0, BN = 16, at most 256 groups) they first copy the tile's
+  // Ag slice there, every load in flight at once.
+  __device__ void prepare(const Int4Args& a4, const Group& g, int n, int n1, int m0_, uint32_t stage, int et) {
+    A4 = &a4;
+    m0 = m0_;
+    ag_smem = 0;
+    if (stage && a4.groups <= 256) {
+      const int M = a4.t.M;
+      named_bar_sync(1, kEpiThreads);  // the previous slice is no longer read
+      for (int i = et; i < a4.groups * BN; i += kEpiThreads) {
+        const int gi = i / BN, m = m0 + i % BN;
+        st_shared_f32(stage + 4u * i, m < M ? __ldg(a4.agsum + static_cast<int64_t>(gi) * M + m) : 0.0f);
+      }
+      named_bar_sync(1, kEpiThreads);
+      ag_smem = stage;
+    }
+    srow = n < n1 ? a4.scales + static_cast<int64_t>(n) * a4.groups : nullptr;
+    zrow = (n < n1 && a4.zeros) ? a4.zeros + static_cast<int64_t>(n) * a4.groups : nullptr;
+    (void)g;
+    if constexpr (BN <= 16) term<NC>(0, corr);
+  }
+
+  template <int N>
+  __device__ __forceinline__ void operator()(int c0, uint32_t (&v)[N]) const {
+    if (!active || !srow) return;
+    if constexpr (BN <= 16) {
+#pragma unroll
+      for (int j = 0; j < N; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) - corr[c0 + j]);
+    } else {
+      float t[N];
+      term<N>(c0, t);
+#pragma unroll
+      for (int j = 0; j < N; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) - t[j]);
+    }
   }
 };
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_constant__ Int4Args A4) {
   using C = Cfg4<BN>;
+  constexpr int NI = C::NI;
   const TcArgs& a = A4.t;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -211,46 +331,51 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t bar0 = base + C::BAR_OFF;
-  // full[s]: stage s's TMA bytes landed.  sfree[s]: stage s may be refilled
-  // (its expanders read its raw bytes, and the expanders of the stage that
-  // reuses its TMEM slot saw that slot freed, i.e. the MMAs that read its
-  // activation completed; that saves the MMA issuer a commit per stage).
-  // a_full[t]: the expanders wrote a stage's weights into TMEM A slot t.
-  // tfree[t]: the MMAs reading slot t completed.  accf / acce: accumulator
-  // buffer full / drained.
-  auto full_bar = [&](int i) { return bar0 + 8u * i; };
-  auto sfree_bar = [&](int i) { return bar0 + 8u * (C::STAGES + i); };
-  auto a_full = [&](int t) { return bar0 + 8u * (2 * C::STAGES + t); };
-  auto tfree_bar = [&](int t) { return bar0 + 8u * (2 * C::STAGES + kTSlots + t); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 * kTSlots + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 * kTSlots + 2 + b); };
-  const uint32_t teardown_bar = bar0 + 8u * (2 * C::STAGES + 2 * kTSlots + 4);
+  // full_w[s] / full_x[s]: a packed-weight / activation stage landed.
+  // wfree[s]: the stage's eight expander warps read its packed weights.
+  // xfree[s]: the MMAs that read the activation stage completed (one commit
+  // per issuer).  a_full[t]: the expanders wrote a stage's weights into TMEM
+  // A slot t.  tfree[t]: the MMAs reading slot t completed (one commit per
+  // issuer).  accf / acce: accumulator buffer full (one commit per issuer) /
+  // drained by the epilogue.
+  constexpr int kB1 = 2 * C::WST + 2 * C::XST;
+  auto full_w = [&](int i) { return bar0 + 8u * i; };
+  auto wfree = [&](int i) { return bar0 + 8u * (C::WST + i); };
+  auto full_x = [&](int i) { return bar0 + 8u * (2 * C::WST + i); };
+  auto xfree = [&](int i) { return bar0 + 8u * (2 * C::WST + C::XST + i); };
+  auto a_full = [&](int t) { return bar0 + 8u * (kB1 + t); };
+  auto tfree_bar = [&](int t) { return bar0 + 8u * (kB1 + kTSlots + t); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (kB1 + 2 * kTSlots + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (kB1 + 2 * kTSlots + 2 + b); };
+  const uint32_t teardown_bar = bar0 + 8u * (kB1 + 2 * kTSlots + 4);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
-  volatile int* consumed_slot = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 8);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::STAGES; ++i) {
-      mbar_init(full_bar(i), 1);
-      mbar_init(sfree_bar(i), 4 + 4);  // the stage's four expander warps + the four of the stage 3 later
+    for (int i = 0; i < C::WST; ++i) {
+      mbar_init(full_w(i), 1);
+      mbar_init(wfree(i), 8);
+    }
+    for (int i = 0; i < C::XST; ++i) {
+      mbar_init(full_x(i), 1);
+      mbar_init(xfree(i), NI);
     }
     for (int t = 0; t < kTSlots; ++t) {
-      mbar_init(a_full(t), 4);
-      mbar_init(tfree_bar(t), 1);
+      mbar_init(a_full(t), 8);
+      mbar_init(tfree_bar(t), NI);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(accf_bar(b), 1);
+      mbar_init(accf_bar(b), NI);
       mbar_init(acce_bar(b), kEpiThreads / 32);
     }
-    mbar_init(teardown_bar, 1);
+    mbar_init(teardown_bar, NI);
     *abort_flag = 0;
-    *consumed_slot = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
     tma_prefetch_desc(&A4.tm_w);
     tma_prefetch_desc(&a.tm_q);
   }
-  if (warp == 1) {
+  if (warp == kIssWarp0) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
     tmem_relinquish();
   }
@@ -259,41 +384,84 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  int issued = 0;  // producer lane: stages whose loads were issued
+  int w_issued = 0, x_issued = 0;  // producer lane: stages whose loads were issued, per ring
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Two rings fed in stage order, each as soon as its next buffer is free:
+    // the packed weights (the HBM stream) never wait for an activation buffer.
     if (lane == 0) {
-      StageIter it(a);
-      int kb0, nk, st = 0;
-      bool nr;
-      while (it.next(a, kb0, nk, nr)) {
-        const int s = st % C::STAGES;
-        if (!mbar_wait_bounded(sfree_bar(s), ((st / C::STAGES) & 1) ^ 1u, a.wait_limit_ns, abort_flag)) {
-          if (!*abort_flag) record_timeout(a, abort_flag, 0 * 16 + 1);
+      StageIter itw(a), itx(a);
+      int wkb0 = 0, wnk = 0, xkb0 = 0, xnk = 0;
+      bool nr, whave = false, xhave = false, wdone = false, xdone = false;
+      uint64_t stall_t0 = 0;
+      while (true) {
+        if (!whave && !wdone) {
+          whave = itw.next(a, wkb0, wnk, nr);
+          wdone = !whave;
+        }
+        if (!xhave && !xdone) {
+          xhave = itx.next(a, xkb0, xnk, nr);
+          xdone = !xhave;
+        }
+        if (wdone && xdone) break;
+        bool progress = false;
+        if (whave) {
+          const int s = w_issued % C::WST;
+          if (mbar_test_wait(wfree(s), ((w_issued / C::WST) & 1) ^ 1u)) {
+            int32_t tp, tq, m0, m1, n0, n1;
+            tile_ranges(a, itw.g.tile, BN, tp, tq, m0, m1, n0, n1);
+            const int kb = itw.g.kb0 + wkb0;
+            mbar_arrive_expect_tx(full_w(s), kRawBytes);
+            tma_load_2d(base + s * kWStage, &A4.tm_w, full_w(s), kb * (TILE_K / 2), n0);
+            ++w_issued;
+            whave = false;
+            progress = true;
+          }
+        }
+        if (xhave) {
+          const int s = x_issued % C::XST;
+          if (mbar_test_wait(xfree(s), ((x_issued / C::XST) & 1) ^ 1u)) {
+            int32_t tp, tq, m0, m1, n0, n1;
+            tile_ranges(a, itx.g.tile, BN, tp, tq, m0, m1, n0, n1);
+            // one box: x_box_kb K blocks of bn rows (beyond the run's K blocks
+            // it reads neighbours or zero fill, which no MMA uses)
+            (void)xnk;
+            mbar_arrive_expect_tx(full_x(s), static_cast<uint32_t>(A4.x_box_kb) * C::ACT_TILE);
+            tma_load_3d(base + C::X_OFF + s * C::XSTAGE, &a.tm_q, full_x(s), 0, m0, itx.g.kb0 + xkb0);
+            ++x_issued;
+            xhave = false;
+            progress = true;
+          }
+        }
+        if (progress) {
+          stall_t0 = 0;
+          continue;
+        }
+        if (*abort_flag) break;
+        const uint64_t now = global_timer_ns();
+        if (stall_t0 == 0) {
+          stall_t0 = now;
+        } else if (now - stall_t0 > a.wait_limit_ns) {
+          record_timeout(a, abort_flag, 0 * 16 + 1);
           break;
         }
-        int32_t tp, tq, m0, m1, n0, n1;
-        tile_ranges(a, it.g.tile, BN, tp, tq, m0, m1, n0, n1);
-        const uint32_t sb = base + s * C::STAGE_BYTES;
-        const int32_t k0 = (it.g.kb0 + kb0) * TILE_K;
-        mbar_arrive_expect_tx(full_bar(s), kRawBytes + nk * C::ACT_TILE);
-        tma_load_2d(sb, &A4.tm_w, full_bar(s), k0 / 2, n0);
-        for (int j = 0; j < nk; ++j)
-          tma_load_2d(sb + kRawBytes + j * C::ACT_TILE, &a.tm_q, full_bar(s), k0 + j * TILE_K, m0);
-        ++issued;
-        ++st;
+        __nanosleep(32);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp < kIssWarp0 + kMaxIssuers) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer i takes the MMAs m = 4 j + k (K block j, 16-deep step k) of
+    // every stage with m % NI == i, into its own accumulator (every issuer
+    // has one in every stage: a stage has at least 4 MMAs).
+    const int iss = warp - kIssWarp0;
+    if (lane == 0 && iss < NI) {
       StageIter it(a);
       int kb0, nk, st = 0, acc_iter = -1;
-      bool nr, ok = true;
+      bool nr;
       uint32_t d_tmem = tmem_base;
-      while (ok && it.next(a, kb0, nk, nr)) {
-        const int s = st % C::STAGES, t = st % kTSlots;
+      while (it.next(a, kb0, nk, nr)) {
+        const int t = st % kTSlots, sx = st % C::XST;
         if (nr) {
           ++acc_iter;
           const int buf = acc_iter & 1;
@@ -301,41 +469,46 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
             if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 3);
             break;
           }
-          d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+          d_tmem = tmem_base + static_cast<uint32_t>((buf * NI + iss) * BN);
         }
-        if (!mbar_wait_bounded(a_full(t), (st / kTSlots) & 1, a.wait_limit_ns, abort_flag)) {
+        if (!mbar_wait_bounded(a_full(t), (st / kTSlots) & 1, a.wait_limit_ns, abort_flag) ||
+            !mbar_wait_bounded(full_x(sx), (st / C::XST) & 1, a.wait_limit_ns, abort_flag)) {
           if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 0);
           break;
         }
-        *consumed_slot = st + 1;
         tc_fence_after();
-        const uint64_t bd0 = sw128_desc(base + s * C::STAGE_BYTES + kRawBytes, 16u, 1024u);
+        const uint64_t bd0 = sw128_desc(base + C::X_OFF + sx * C::XSTAGE, 16u, 1024u);
         const uint32_t a0 = tmem_base + kASlotCol0 + static_cast<uint32_t>(t * 128);
-#pragma unroll
-        for (int j = 0; j < kQuadK; ++j) {
-          if (j < nk) {
-            const uint64_t bd = bd0 + static_cast<uint64_t>((j * C::ACT_TILE) >> 4);
-            const uint32_t at = a0 + static_cast<uint32_t>(j * 32);
-            // columns 8 per K = 16 (fp16 pairs), descriptor +32 bytes per K = 16
-            tc_mma_f16_ts(d_tmem, at, bd, a.idesc, (kb0 + j) != 0 ? 1u : 0u);
-            tc_mma_f16_ts(d_tmem, at + 8, bd + 2, a.idesc, 1u);
-            tc_mma_f16_ts(d_tmem, at + 16, bd + 4, a.idesc, 1u);
-            tc_mma_f16_ts(d_tmem, at + 24, bd + 6, a.idesc, 1u);
-          }
-        }
+        const uint32_t first = kb0 == 0 ? 1u : 0u;
+        if (iss == 0) issue_stage_nk<NI, 0, C::ACT_TILE>(nk, d_tmem, a0, bd0, a.idesc, first);
+        if constexpr (NI > 1) if (iss == 1) issue_stage_nk<NI, 1, C::ACT_TILE>(nk, d_tmem, a0, bd0, a.idesc, first);
+        if constexpr (NI > 2) if (iss == 2) issue_stage_nk<NI, 2, C::ACT_TILE>(nk, d_tmem, a0, bd0, a.idesc, first);
         tc_commit(tfree_bar(t));
+        tc_commit(xfree(sx));
         if (kb0 + nk == it.g.nkb) tc_commit(accf_bar(acc_iter & 1));
         ++st;
       }
-      (void)ok;
     }
   } else if (warp >= kExpWarp0) {
     // ------------------------------------------------------------ expanders
     const int q4 = warp & 3;
-    const int h = (warp - kExpWarp0) >> 2;  // stages with index % 2 == h
+    const int h = (warp - kExpWarp0) >> 2;  // K blocks 2h, 2h + 1 of every stage
     const int r = q4 * 32 + lane;           // weight row within the tile (TMEM lane)
     StageIter it(a);
-    RowScales rs;
+    // This row's scales and zero points, 8 groups (16 bytes) per window: the
+    // current window and the next in registers, the next loaded when the
+    // current one is entered and the one after prefetched into L2 then.
+    // (Rows not 16-byte aligned: one load per K block.)
+    const uint16_t* srow = nullptr;
+    int w_cur = 0, w_last = -1;
+    uint4 s_cur, s_nxt;
+    auto load_win = [&](int w, uint4& sv) {
+      sv = make_uint4(0u, 0u, 0u, 0u);  // a row beyond N: s = 0
+      if (srow && w <= w_last) sv = __ldg(reinterpret_cast<const uint4*>(srow) + w);
+    };
+    auto prefetch_win = [&](int w) {
+      if (srow && w <= w_last) prefetch_l2(srow + 8 * w);
+    };
     int kb0, nk, st = 0;
     bool nr;
     while (it.next(a, kb0, nk, nr)) {
@@ -343,54 +516,86 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         int32_t tp, tq, m0, m1, n0, n1;
         tile_ranges(a, it.g.tile, BN, tp, tq, m0, m1, n0, n1);
         const int n = n0 + r;
-        const bool row_ok = n < n1;
+        srow = n < n1 ? A4.scales + static_cast<int64_t>(n) * A4.groups : nullptr;
         const int g0 = static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0), A4.div_kb_per_group));
-        rs.reset(row_ok ? A4.scales + static_cast<int64_t>(n) * A4.groups : nullptr,
-                 (row_ok && A4.zeros) ? A4.zeros + static_cast<int64_t>(n) * A4.groups : nullptr, A4.groups, g0,
-                 A4.vec_sz != 0);
+        const int g1 =
+            static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + it.g.nkb - 1), A4.div_kb_per_group));
+        if (A4.vec_sz) {
+          w_cur = g0 >> 3;
+          w_last = g1 >> 3;
+          load_win(w_cur, s_cur);
+          load_win(w_cur + 1, s_nxt);
+          prefetch_win(w_cur + 2);
+        }
       }
-      if ((st & 1) == h) {
-        const int s = st % C::STAGES, t = st % kTSlots;
+      {
+        const int sw = st % C::WST, t = st % kTSlots;
         const bool got =
-            mbar_wait_bounded(full_bar(s), (st / C::STAGES) & 1, a.wait_limit_ns, abort_flag) &&
+            mbar_wait_bounded(full_w(sw), (st / C::WST) & 1, a.wait_limit_ns, abort_flag) &&
             mbar_wait_bounded(tfree_bar(t), ((st / kTSlots) & 1) ^ 1u, a.wait_limit_ns, abort_flag);
         if (!got && !*abort_flag) record_timeout(a, abort_flag, 3 * 16 + 0);
         // the warp leaves together (tcgen05.st below needs every lane)
         if (!__all_sync(0xffffffffu, got)) break;
         tc_fence_after();
-        // the MMAs of stage st - kTSlots completed: its stage buffer may be refilled
-        if (st >= kTSlots && lane == 0) mbar_arrive(sfree_bar((st - kTSlots) % C::STAGES));
-        // raw row r: eight 16-byte chunks, chunk c stored at c ^ (r mod 8) (128-byte swizzle)
-        const uint8_t* rowp = smem + s * C::STAGE_BYTES + r * 128;
-        uint4 raw[8];
+        // raw row r: eight 16-byte chunks, chunk c stored at c ^ (r mod 8)
+        // (128-byte swizzle); this warp's K blocks 2h, 2h + 1 are chunks 4h..4h+3
+        const uint8_t* rowp = smem + sw * kWStage + r * 128;
+        uint4 raw[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(rowp + ((c ^ (r & 7)) << 4));
+        for (int c = 0; c < 4; ++c) raw[c] = *reinterpret_cast<const uint4*>(rowp + (((4 * h + c) ^ (r & 7)) << 4));
+        // each K block's scale as an fp16 pair
+        uint32_t s2v[2];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * h + jj;
+          uint32_t s2 = 0;
+          if (j < nk) {
+            const int g = static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + kb0 + j), A4.div_kb_per_group));
+            if (A4.vec_sz) {
+              const int w = g >> 3;
+              if (w != w_cur) {  // groups only grow within a run
+                if (w == w_cur + 1)
+                  s_cur = s_nxt;
+                else
+                  load_win(w, s_cur);
+                w_cur = w;
+                load_win(w + 1, s_nxt);
+                prefetch_win(w + 2);
+              }
+              // group g % 8 of the window: its two bytes, in both halves
+              const uint32_t b0 = static_cast<uint32_t>(g & 3) * 2u;
+              const uint32_t sel = b0 * 0x1111u + 0x1010u;
+              const bool hi = (g & 4) != 0;
+              s2 = prmt(hi ? s_cur.z : s_cur.x, hi ? s_cur.w : s_cur.y, sel);
+            } else {
+              s2 = (srow ? static_cast<uint32_t>(__ldg(srow + g)) : 0u) * 0x10001u;
+            }
+          }
+          s2v[jj] = s2;
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(sfree_bar(s));
+        if (lane == 0) mbar_arrive(wfree(sw));
         const uint32_t slot = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + kASlotCol0 +
                               static_cast<uint32_t>(t * 128);
-        for (int j = 0; j < nk; ++j) {
-          const int grp =
-              static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + kb0 + j), A4.div_kb_per_group));
-          uint16_t sb, zb;
-          rs.get(grp, sb, zb);
-          const uint32_t s2 = static_cast<uint32_t>(sb) * 0x10001u;
-          const uint32_t nzs2 = hmul2(static_cast<uint32_t>(zb) * 0x10001u, s2) ^ 0x80008000u;  // -z * s
-          const uint32_t words[8] = {raw[2 * j].x, raw[2 * j].y, raw[2 * j].z, raw[2 * j].w,
-                                     raw[2 * j + 1].x, raw[2 * j + 1].y, raw[2 * j + 1].z, raw[2 * j + 1].w};
+        // unrolled, so that raw[] stays in registers (nk is warp-uniform)
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * h + jj;
+          if (j >= nk) break;
+          // -1024 s and -64 s: exact (power-of-two multiples)
+          const uint32_t s2 = s2v[jj], c1024 = hmul2(s2, 0xE400E400u), c64 = hmul2(s2, 0xD400D400u);
+          const uint32_t words[8] = {raw[2 * jj].x, raw[2 * jj].y, raw[2 * jj].z, raw[2 * jj].w,
+                                     raw[2 * jj + 1].x, raw[2 * jj + 1].y, raw[2 * jj + 1].z, raw[2 * jj + 1].w};
           uint32_t vals[32];
 #pragma unroll
           for (int w8 = 0; w8 < 8; ++w8) {
             const uint32_t lo = words[w8], hi = lo >> 8;
-            // codes (p, p + 4) of the word for p = 0..3, then q * s - z * s
-            const uint32_t q0 = hsub2(lop3_and_or(lo, 0x000F000Fu, 0x64006400u), 0x64006400u);
-            const uint32_t q1 = hsub2(lop3_and_or(lo, 0x00F000F0u, 0x54005400u), 0x54005400u);
-            const uint32_t q2 = hsub2(lop3_and_or(hi, 0x000F000Fu, 0x64006400u), 0x64006400u);
-            const uint32_t q3 = hsub2(lop3_and_or(hi, 0x00F000F0u, 0x54005400u), 0x54005400u);
-            vals[4 * w8 + 0] = hfma2(q0, s2, nzs2);
-            vals[4 * w8 + 1] = hfma2(q1, s2, nzs2);
-            vals[4 * w8 + 2] = hfma2(q2, s2, nzs2);
-            vals[4 * w8 + 3] = hfma2(q3, s2, nzs2);
+            // codes (p, p + 4) of the word for p = 0..3 as 1024 + q (p even)
+            // or 64 + q (p odd), then (1024 + q) s - 1024 s = q s, rounded once
+            vals[4 * w8 + 0] = hfma2(lop3_and_or(lo, 0x000F000Fu, 0x64006400u), s2, c1024);
+            vals[4 * w8 + 1] = hfma2(lop3_and_or(lo, 0x00F000F0u, 0x54005400u), s2, c64);
+            vals[4 * w8 + 2] = hfma2(lop3_and_or(hi, 0x000F000Fu, 0x64006400u), s2, c1024);
+            vals[4 * w8 + 3] = hfma2(lop3_and_or(hi, 0x00F000F0u, 0x54005400u), s2, c64);
           }
           tc_st_32x32b_x32(slot + static_cast<uint32_t>(j * 32), vals);
         }
@@ -403,45 +608,76 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // (warps 4..7: TMEM lane quadrant warp % 4; tiles leave by plain stores,
+    // so no staging buffer)
     const int q4 = warp & 3;
     const int et = threadIdx.x - kEpiWarp04 * 32;
     Sched sched(a);
     Group g;
     int acc_iter = 0, ring = 0;
-    const uint32_t stage_smem = base + C::EPI_OFF + static_cast<uint32_t>(warp - kEpiWarp04) * 8192u;
-    while (sched.next(a, g)) {
-      if (!epilogue_group<BN, (BN < 32 ? BN : 32)>(a, g, tmem_base, accf_bar(0), acce_bar(0), acc_iter, abort_flag,
-                                                   q4, lane, et, 0, stage_smem, ring))
+    // The zero-point term of this CTA's first run that starts a tile is
+    // formed now, while the pipeline fills; later ones when they come up.
+    ZpFix<BN> fix;
+    const uint32_t zp_stage = C::ZP_BYTES ? base + C::ZP_OFF : 0u;
+    int first_idx = -1;
+    {
+      Sched look(a);
+      Group gl;
+      for (int idx = 0; look.next(a, gl); ++idx) {
+        if (gl.s0 == 0 && gl.nkb > 0) {
+          int32_t tp, tq, m0, m1, n0, n1;
+          tile_ranges(a, gl.tile, BN, tp, tq, m0, m1, n0, n1);
+          fix.prepare(A4, gl, n0 + q4 * 32 + lane, n1, m0, zp_stage, et);
+          first_idx = idx;
+          break;
+        }
+      }
+    }
+    for (int idx = 0; sched.next(a, g); ++idx) {
+      fix.active = g.s0 == 0 && g.nkb > 0;
+      if (fix.active && idx != first_idx) {
+        int32_t tp, tq, m0, m1, n0, n1;
+        tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
+        fix.prepare(A4, g, n0 + q4 * 32 + lane, n1, m0, zp_stage, et);
+      }
+      if (!epilogue_group<BN, (BN < 32 ? BN : 32), false, NI, ZpFix<BN>>(
+              a, g, tmem_base, accf_bar(0), acce_bar(0), acc_iter, abort_flag, q4, lane, et, 0, 0u, ring, fix))
         break;
     }
-    if (lane == 0) bulk_wait_group<0>();
   }
 
   // ------------------------------------------------------------ teardown
   __syncthreads();
   if (*abort_flag && warp == 0 && lane == 0) {
-    // Let the loads still in flight land before the CTA exits.
+    // Let the loads still in flight land before the CTA exits: every use of a
+    // buffer before its last one landed (its consumer waited for it before
+    // freeing it), so only each ring's last round of uses can be pending.
     volatile int no_abort = 0;
-    for (int c = *consumed_slot; c < issued; ++c)
-      mbar_wait_bounded(full_bar(c % C::STAGES), (c / C::STAGES) & 1, a.wait_limit_ns, &no_abort);
+    for (int c = w_issued > C::WST ? w_issued - C::WST : 0; c < w_issued; ++c)
+      mbar_wait_bounded(full_w(c % C::WST), (c / C::WST) & 1, a.wait_limit_ns, &no_abort);
+    for (int c = x_issued > C::XST ? x_issued - C::XST : 0; c < x_issued; ++c)
+      mbar_wait_bounded(full_x(c % C::XST), (c / C::XST) & 1, a.wait_limit_ns, &no_abort);
   }
-  if (warp == 1 && lane == 0) {
+  // every issuer's MMAs completed before the TMEM is released
+  if (warp >= kIssWarp0 && warp < kIssWarp0 + NI && lane == 0) tc_commit(teardown_bar);
+  if (warp == kIssWarp0 && lane == 0) {
     volatile int no_abort = 0;
-    tc_commit(teardown_bar);
     mbar_wait_bounded(teardown_bar, 0, a.wait_limit_ns, &no_abort);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, 512);
+  if (warp == kIssWarp0) tmem_dealloc(tmem_base, 512);
 }
 
 // Activation pre-pass, K-contiguous activation: one thread per 8-element
 // chunk (m, c), c fastest, so that loads and stores are coalesced 16-byte
 // vectors (scalar loads when the rows are not 16-byte aligned); the chunk is
-// stored with its elements reordered to (0,4,1,5,2,6,3,7).
+// stored K-block-major (K block c / 8 of row m at (c / 8 * M + m) * 64) with
+// its elements reordered to (0,4,1,5,2,6,3,7).
 __global__ void __launch_bounds__(256) int4_prep_kmajor_kernel(const uint16_t* __restrict__ A, int64_t lda, int vec,
-                                                               int M, int K, uint16_t* __restrict__ Ap) {
+                                                               int M, int K, int gc, uint16_t* __restrict__ Ap,
+                                                               float* __restrict__ agsum) {
   const int chunks = K / 8;
   const int64_t total = static_cast<int64_t>(M) * chunks;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -466,7 +702,38 @@ __global__ void __launch_bounds__(256) int4_prep_kmajor_kernel(const uint16_t* _
     o.y = (w[0] >> 16) | (w[2] & 0xFFFF0000u);
     o.z = (w[1] & 0xFFFFu) | (w[3] << 16);
     o.w = (w[1] >> 16) | (w[3] & 0xFFFF0000u);
-    *reinterpret_cast<uint4*>(Ap + static_cast<int64_t>(m) * K + 8 * c) = o;
+    *reinterpret_cast<uint4*>(Ap + ((static_cast<int64_t>(c >> 3) * M + m) << 6) + 8 * (c & 7)) = o;
+    if (gc) {
+      // group sums: the gc (8, 16 or 32) chunks of a group are consecutive
+      // lanes of this warp (chunks per row and the grid are multiples of 32,
+      // so every lane is active); a butterfly gives each lane the same total
+      float sum = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sum += half_bits_to_float(w[e] & 0xFFFFu) + half_bits_to_float(w[e] >> 16);
+      for (int off = 1; off < gc; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (c % gc == 0) agsum[static_cast<int64_t>(c / gc) * M + m] = sum;
+    }
+  }
+}
+
+// Group sums of the prepared activation, one thread per (g, m), for the
+// shapes the pre-pass does not sum itself.
+__global__ void __launch_bounds__(256) int4_group_sum_kernel(const uint16_t* __restrict__ Ap, int M, int K, int group,
+                                                             float* __restrict__ agsum) {
+  const int G = K / group;
+  const int64_t total = static_cast<int64_t>(G) * M;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += step) {
+    const int g = static_cast<int>(i / M);
+    const int m = static_cast<int>(i - static_cast<int64_t>(g) * M);
+    float sum = 0.0f;
+    for (int k = g * group; k < (g + 1) * group; k += 8) {
+      const uint4 q = *reinterpret_cast<const uint4*>(Ap + ((static_cast<int64_t>(k >> 6) * M + m) << 6) + (k & 63));
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sum += half_bits_to_float(w[e] & 0xFFFFu) + half_bits_to_float(w[e] >> 16);
+    }
+    agsum[i] = sum;
   }
 }
 
@@ -488,7 +755,7 @@ __global__ void __launch_bounds__(256) int4_prep_mmajor_kernel(const uint16_t* _
     o.y = static_cast<uint32_t>(v[1]) | (static_cast<uint32_t>(v[5]) << 16);
     o.z = static_cast<uint32_t>(v[2]) | (static_cast<uint32_t>(v[6]) << 16);
     o.w = static_cast<uint32_t>(v[3]) | (static_cast<uint32_t>(v[7]) << 16);
-    *reinterpret_cast<uint4*>(Ap + static_cast<int64_t>(m) * K + 8 * c) = o;
+    *reinterpret_cast<uint4*>(Ap + ((static_cast<int64_t>(c >> 3) * M + m) << 6) + 8 * (c & 7)) = o;
   }
 }
 
@@ -504,19 +771,32 @@ cudaError_t launch4(const Int4Args& args, int grid, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K, void* Ap, int sms,
-                             cudaStream_t stream) {
+cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K, int group, void* Ap, float* agsum,
+                             int sms, cudaStream_t stream) {
   const int64_t chunks = static_cast<int64_t>(M) * (K / 8);
   if (chunks == 0) return cudaSuccess;
   int64_t blocks = (chunks + 255) / 256;
   if (blocks > static_cast<int64_t>(sms) * 8) blocks = static_cast<int64_t>(sms) * 8;
+  // the pre-pass sums groups itself when a group's chunks are 8, 16 or 32
+  // consecutive lanes of a warp: K-contiguous A, 32 | K / 8, and a grid of
+  // whole warps with every lane in range
+  const int gc = group / 8;
+  const bool fused = !a_mn && (gc == 8 || gc == 16 || gc == 32) && (K / 8) % 32 == 0;
   if (!a_mn) {
     const int vec = (lda % 8 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
     int4_prep_kmajor_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<const uint16_t*>(A), lda, vec,
-                                                                          M, K, static_cast<uint16_t*>(Ap));
+                                                                          M, K, fused ? gc : 0,
+                                                                          static_cast<uint16_t*>(Ap), agsum);
   } else {
     int4_prep_mmajor_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<const uint16_t*>(A), lda, M,
                                                                           K, static_cast<uint16_t*>(Ap));
+  }
+  if (!fused) {
+    const int64_t gm = static_cast<int64_t>(M) * (K / group);
+    int64_t gblocks = (gm + 255) / 256;
+    if (gblocks > static_cast<int64_t>(sms) * 8) gblocks = static_cast<int64_t>(sms) * 8;
+    int4_group_sum_kernel<<<static_cast<int>(gblocks), 256, 0, stream>>>(static_cast<const uint16_t*>(Ap), M, K,
+                                                                          group, agsum);
   }
   return cudaGetLastError();
 }

@@ -79,19 +79,25 @@ struct TcArgs {
 struct Int4Args {
   TcArgs t;
   CUtensorMap tm_w;          // packed weight bytes: dims {ldb bytes, N}, box {128, 128}, 128-byte swizzle
+  const float* agsum;        // per-group sums of the activation, fp32 [groups][M]
   const uint16_t* scales;    // fp16 [N][groups]
   const uint16_t* zeros;     // fp16 [N][groups], or null for z = 8
   int32_t groups;
   MagicDiv div_kb_per_group; // 64-deep K block -> quantisation group
+  int32_t x_box_kb;          // K blocks per activation box (min(4, K / 64)); t.tm_q is 3-D {64, M, K / 64}
   int32_t vec_sz;            // scale / zero rows readable 8 groups (16 bytes) at a time
 };
 
 cudaError_t launch_int4_gemm(const Int4Args& args, int bn, int grid, cudaStream_t stream);
 
-// Activation pre-pass of the int4 GEMM: K-contiguous copy of A (M x K, any
-// layout, 2-byte aligned) into Ap (pitch K) with each 8-element group of K
-// reordered to (0,4,1,5,2,6,3,7).  K must be a multiple of 64.
-cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K, void* Ap, int sms,
+// Activation pre-pass of the int4 GEMM: copy of A (M x K, any layout,
+// 2-byte aligned) into Ap, K-block-major: the 64 elements of row m in K block
+// kb at Ap + (kb * M + m) * 64, each 8-element group of K reordered to
+// (0,4,1,5,2,6,3,7); and agsum[g * M + m] = the fp32 sum (fixed order) of row
+// m's elements in group g (group elements of K).  K and group must be
+// multiples of 64.
+cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K, int group, void* Ap, float* agsum,
+                             int sms,
                              cudaStream_t stream);
 
 // Returns a cudaError_t; `bn` selects the kernel instance.

@@ -38,6 +38,7 @@ struct gemm_plan {
   size_t off_partial, off_counters, off_pack_a, off_pack_b, ws_bytes;
   size_t ws_bytes_misaligned;
   size_t off_aprep;  // int4: the prepared activation
+  size_t off_agsum;  // int4: per-group sums of the activation, fp32 [groups][M]
   lgt::DeviceStatus* d_status;
   uint64_t wait_limit_ns;
 };
@@ -51,6 +52,9 @@ bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major,
 
 // Encode the TMA map over packed int4 weights (see api.cu).
 bool encode_int4_weights(CUtensorMap* map, const void* ptr, int64_t N, int64_t ld_bytes);
+
+// Encode the 3-D TMA map over the prepared int4-path activation (see api.cu).
+bool encode_int4_activation(CUtensorMap* map, const void* ptr, int64_t M, int64_t K, int bn, int kb_box);
 
 // Launch the dense tensor-core kernel of `plan` on operands TMA can address
 // in place (16-byte aligned bases and pitches `lda` / `ldb` in elements),

@@ -392,9 +392,12 @@ __device__ __noinline__ void arrive_split_tile_det(const TcArgs& a, const Group&
 
 // The epilogue of one group, run by the 128 epilogue threads (TMEM lane
 // quadrant q4, lane `lane`, index `et` among the 128).  Reads the fp32
-// accumulator buffer of the group from TMEM and either converts and stores
-// the tile of C, or adds it to the split-K workspace and, for the CTA whose
-// arrival completes the tile, converts the total.  Returns false when the CTA
+// accumulator buffer of the group from TMEM (the sum of NACC partial
+// accumulators, buffer b of them at columns [b * NACC * BN, (b + 1) * NACC * BN))
+// and either converts and stores the tile of C, or adds it to the split-K
+// workspace and, for the CTA whose arrival completes the tile, converts the
+// total.  `fix(c0, v)` may adjust each block of accumulator values (columns
+// c0.. of this thread's row) before it leaves.  Returns false when the CTA
 // is aborting; all 128 threads return the same value.
 // PAIR: the CTA holds P-side half `half` of a pair tile, and the buffer-free
 // arrival goes to the pair's MMA CTA (acce_bar0 is a shared::cluster address).
@@ -406,10 +409,39 @@ __device__ __noinline__ void arrive_split_tile_det(const TcArgs& a, const Group&
 // blocks it has issued) and one lane hands the block to a bulk tile store
 // (C) or bulk tile reduction (fp32 partials), so whole lines reach L2.
 // Otherwise each thread stores its own values directly.
-template <int BN, int CH, bool PAIR = false>
+// The group's accumulator as NACC partial accumulators (one per MMA issuer,
+// ST columns apart, added in index order): N columns from taddr of each.
+template <int N, int NACC, int ST>
+__device__ __forceinline__ void ld_acc(uint32_t taddr, uint32_t (&v)[N]) {
+  static_assert(N == 16 || N == 32, "tcgen05.ld shapes used here");
+  if constexpr (N == 32) tc_ld_32x32b_x32(taddr, v); else tc_ld_32x32b_x16(taddr, v);
+  if constexpr (NACC > 1) {
+    uint32_t w[NACC - 1][N];
+#pragma unroll
+    for (int i = 1; i < NACC; ++i) {
+      if constexpr (N == 32) tc_ld_32x32b_x32(taddr + i * ST, w[i - 1]); else tc_ld_32x32b_x16(taddr + i * ST, w[i - 1]);
+    }
+    tc_wait_ld();
+#pragma unroll
+    for (int i = 1; i < NACC; ++i)
+#pragma unroll
+      for (int j = 0; j < N; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(w[i - 1][j]));
+  } else {
+    tc_wait_ld();
+  }
+}
+
+// No change to the accumulator values.
+struct NoFix {
+  template <int N>
+  __device__ __forceinline__ void operator()(int, uint32_t (&)[N]) const {}
+};
+
+template <int BN, int CH, bool PAIR = false, int NACC = 1, class Fix = NoFix>
 __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, uint32_t tmem_base, uint32_t accf_bar0,
                                                uint32_t acce_bar0, int& acc_iter, volatile int* abort_flag, int q4,
-                                               int lane, int et, int half, uint32_t stage_smem, int& ring) {
+                                               int lane, int et, int half, uint32_t stage_smem, int& ring,
+                                               const Fix& fix = Fix()) {
   const int row = q4 * 32 + lane;  // accumulator row (TMEM lane)
   int32_t tp, tq, m0, m1, n0, n1;
   tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
@@ -432,7 +464,7 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
     // all epilogue threads leave together if any of them gave up
     if (named_bar_or(1, kEpiThreads, !got)) return false;
     tc_fence_after();
-    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(buf * BN);
+    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(buf * BN * NACC);
     const bool staged = (BN % EPI_BOX == 0) && (full_tile ? a.tma_c : (a.tma_ws && !a.det));
     if (staged && a.swap) {
       // Swapped: TMEM lane = n, column = m.  Block rows are m, each holding
@@ -441,8 +473,8 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += EPI_BOX) {
         uint32_t v[EPI_BOX];
-        tc_ld_32x32b_x32(t_row + c0, v);
-        tc_wait_ld();
+        ld_acc<EPI_BOX, NACC, BN>(t_row + c0, v);
+        fix(c0, v);
         const int32_t ybox = m0 + c0;
         if (xbox >= n1 || ybox >= m1) continue;  // block wholly outside C (warp-uniform)
         const uint32_t sbuf = stage_smem + static_cast<uint32_t>(ring & 1) * 4096u;
@@ -482,8 +514,8 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += EPI_BOX) {
         uint32_t v[EPI_BOX];
-        tc_ld_32x32b_x32(t_row + c0, v);
-        tc_wait_ld();
+        ld_acc<EPI_BOX, NACC, BN>(t_row + c0, v);
+        fix(c0, v);
         const int32_t xbox = n0 + c0;
         if (ybox >= m1 || xbox >= n1) continue;  // block wholly outside C (warp-uniform)
         const uint32_t sbuf = stage_smem + static_cast<uint32_t>(ring & 1) * 4096u;
@@ -530,12 +562,8 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
 #pragma unroll 1
     for (int c0 = 0; c0 < (staged ? 0 : BN); c0 += CH) {
       uint32_t v[CH];
-      if constexpr (CH == 32) {
-        tc_ld_32x32b_x32(t_row + c0, v);
-      } else {
-        tc_ld_32x32b_x16(t_row + c0, v);
-      }
-      tc_wait_ld();
+      ld_acc<CH, NACC, BN>(t_row + c0, v);
+      fix(c0, v);
       if (det_slot) {
         // the run's fp32 partial into its slot (every row; the conversion clips)
         if (!a.swap) {
