@@ -1,6 +1,7 @@
 // Small HBM-bound helper kernels: the stride-realigning operand copy and the
 // device-side magic-division check.
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace lgt {
 namespace {
@@ -39,6 +40,8 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t* __rest
                                                           uint16_t* __restrict__ dst, int64_t dst_pitch,
                                                           int64_t row_elems, MagicDiv chunks_div,
                                                           int64_t total_chunks) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_chunks; i += stride) {
     int64_t r, c;
@@ -69,6 +72,8 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t* __rest
 
 __global__ void magic_divmod_kernel(const uint32_t* __restrict__ n, size_t count, MagicDiv m, uint32_t* q,
                                     uint32_t* r) {
+  pdl_launch_dependents();
+  pdl_wait();
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count; i += stride) {
     uint32_t qq, rr;
@@ -97,18 +102,18 @@ cudaError_t launch_repack_rows(const void* src, int64_t src_pitch, void* dst, in
   const MagicDiv cd = magic_encode(static_cast<uint32_t>(chunks));
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
-  repack_rows_kernel<<<static_cast<int>(blocks < (1ll << 31) - 1 ? blocks : (1ll << 31) - 1), threads, 0, stream>>>(
-      static_cast<const uint16_t*>(src), src_pitch / 2, static_cast<uint16_t*>(dst), dst_pitch / 2, row_elems, cd,
-      total);
-  return cudaGetLastError();
+  return launch_pdl(repack_rows_kernel,
+                    dim3(static_cast<unsigned>(blocks < (1ll << 31) - 1 ? blocks : (1ll << 31) - 1)), dim3(threads), 0,
+                    stream, static_cast<const uint16_t*>(src), src_pitch / 2, static_cast<uint16_t*>(dst),
+                    dst_pitch / 2, row_elems, cd, total);
 }
 
 cudaError_t launch_magic_divmod(const uint32_t* n, size_t count, MagicDiv m, uint32_t* q, uint32_t* r,
                                 cudaStream_t stream) {
   if (count == 0) return cudaSuccess;
   const int threads = 256;
-  magic_divmod_kernel<<<grid_for(static_cast<int64_t>(count), threads), threads, 0, stream>>>(n, count, m, q, r);
-  return cudaGetLastError();
+  return launch_pdl(magic_divmod_kernel, dim3(static_cast<unsigned>(grid_for(static_cast<int64_t>(count), threads))),
+                    dim3(threads), 0, stream, n, count, m, q, r);
 }
 
 }  // namespace lgt

@@ -320,6 +320,7 @@ struct ZpFix {
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_constant__ Int4Args A4) {
+  pdl_launch_dependents();
   using C = Cfg4<BN>;
   constexpr int NI = C::NI;
   const TcArgs& a = A4.t;
@@ -383,6 +384,8 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the pre-pass's output, C and the split-K workspace come from earlier kernels
+  pdl_wait();
 
   int w_issued = 0, x_issued = 0;  // producer lane: stages whose loads were issued, per ring
 
@@ -678,6 +681,8 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
 __global__ void __launch_bounds__(256) int4_prep_kmajor_kernel(const uint16_t* __restrict__ A, int64_t lda, int vec,
                                                                int M, int K, int gc, uint16_t* __restrict__ Ap,
                                                                float* __restrict__ agsum) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int chunks = K / 8;
   const int64_t total = static_cast<int64_t>(M) * chunks;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -720,6 +725,8 @@ __global__ void __launch_bounds__(256) int4_prep_kmajor_kernel(const uint16_t* _
 // shapes the pre-pass does not sum itself.
 __global__ void __launch_bounds__(256) int4_group_sum_kernel(const uint16_t* __restrict__ Ap, int M, int K, int group,
                                                              float* __restrict__ agsum) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int G = K / group;
   const int64_t total = static_cast<int64_t>(G) * M;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -741,6 +748,8 @@ __global__ void __launch_bounds__(256) int4_group_sum_kernel(const uint16_t* __r
 // m fastest, so that each of the eight loads is coalesced across the warp.
 __global__ void __launch_bounds__(256) int4_prep_mmajor_kernel(const uint16_t* __restrict__ A, int64_t lda, int M,
                                                                int K, uint16_t* __restrict__ Ap) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int chunks = K / 8;
   const int64_t total = static_cast<int64_t>(M) * chunks;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -762,11 +771,10 @@ __global__ void __launch_bounds__(256) int4_prep_mmajor_kernel(const uint16_t* _
 template <int BN>
 cudaError_t launch4(const Int4Args& args, int grid, cudaStream_t stream) {
   using C = Cfg4<BN>;
-  cudaError_t e = cudaFuncSetAttribute(int4_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(C::SMEM_ALLOC));
+  cudaError_t e = set_smem_once<int4_gemm_kernel<BN>>(static_cast<int>(C::SMEM_ALLOC));
   if (e != cudaSuccess) return e;
-  int4_gemm_kernel<BN><<<grid, kThreads4, C::SMEM_ALLOC, stream>>>(args);
-  return cudaGetLastError();
+  return launch_pdl(int4_gemm_kernel<BN>, dim3(static_cast<unsigned>(grid)), dim3(kThreads4), C::SMEM_ALLOC, stream,
+                    args);
 }
 
 }  // namespace
@@ -784,19 +792,22 @@ cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K,
   const bool fused = !a_mn && (gc == 8 || gc == 16 || gc == 32) && (K / 8) % 32 == 0;
   if (!a_mn) {
     const int vec = (lda % 8 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
-    int4_prep_kmajor_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<const uint16_t*>(A), lda, vec,
-                                                                          M, K, fused ? gc : 0,
-                                                                          static_cast<uint16_t*>(Ap), agsum);
+    cudaError_t e = launch_pdl(int4_prep_kmajor_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                               static_cast<const uint16_t*>(A), lda, vec, M, K, fused ? gc : 0,
+                               static_cast<uint16_t*>(Ap), agsum);
+    if (e != cudaSuccess) return e;
   } else {
-    int4_prep_mmajor_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<const uint16_t*>(A), lda, M,
-                                                                          K, static_cast<uint16_t*>(Ap));
+    cudaError_t e = launch_pdl(int4_prep_mmajor_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                               static_cast<const uint16_t*>(A), lda, M, K, static_cast<uint16_t*>(Ap));
+    if (e != cudaSuccess) return e;
   }
   if (!fused) {
     const int64_t gm = static_cast<int64_t>(M) * (K / group);
     int64_t gblocks = (gm + 255) / 256;
     if (gblocks > static_cast<int64_t>(sms) * 8) gblocks = static_cast<int64_t>(sms) * 8;
-    int4_group_sum_kernel<<<static_cast<int>(gblocks), 256, 0, stream>>>(static_cast<const uint16_t*>(Ap), M, K,
-                                                                          group, agsum);
+    cudaError_t e = launch_pdl(int4_group_sum_kernel, dim3(static_cast<unsigned>(gblocks)), dim3(256), 0, stream,
+                               static_cast<const uint16_t*>(Ap), M, K, group, agsum);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_base);
 
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t bar0 = base + C::BAR_OFF;
@@ -112,6 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // operands, C and the split-K workspace may be written by the previous kernel
+  pdl_wait();
 
   int issued = 0;  // producer lane: K blocks whose loads were issued
 
@@ -260,22 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 template <int BN>
 cudaError_t launch_bn(const TcArgs& args, int grid, cudaStream_t stream) {
   using C = Cfg<BN>;
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(C::SMEM_ALLOC));
+  cudaError_t e = set_smem_once<tc_gemm_kernel<BN>>(static_cast<int>(C::SMEM_ALLOC));
   if (e != cudaSuccess) return e;
-  // A stream-K tail makes CTAs wait for each other's partial sums: launch
-  // cooperatively so that all CTAs are resident together.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_ALLOC;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = args.tail_tiles ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN>, args);
+  // CTAs that convert split tiles wait for other CTAs' partial sums; they
+  // start waiting only after pdl_wait (the previous kernel has left every
+  // SM), and the grid never exceeds the CTAs the device holds at once.
+  return launch_pdl(tc_gemm_kernel<BN>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), C::SMEM_ALLOC, stream, args);
 }
 
 }  // namespace

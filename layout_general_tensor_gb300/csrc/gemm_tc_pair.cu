@@ -59,6 +59,7 @@ static_assert(kStages >= 4, "pipeline depth");
 template <int kBN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcArgs a) {
+  pdl_launch_dependents();
   static_assert(kBN % 32 == 0 && kBN >= 128 && kBN <= 256, "pair tile width");
   constexpr int kQHalf = kBN / 2;                   // Q rows per CTA
   constexpr int kQChunks = (kQHalf + 63) / 64;      // 64-wide boxes of an MN-major Q half
@@ -106,6 +107,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // operands, C and the split-K workspace may be written by the previous kernel
+  pdl_wait();
   // The even CTA's barriers in the cluster's shared window.
   const uint32_t full_bar_leader0 = mapa_shared(full_bar(0), 0);
   const uint32_t acce_bar_leader0 = mapa_shared(acce_bar(0), 0);
@@ -265,22 +268,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <int BN>
 cudaError_t launch_bn(const TcArgs& args, int grid, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_pair_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemAlloc));
+  cudaError_t e = set_smem_once<tc_gemm_pair_kernel<BN>>(static_cast<int>(kSmemAlloc));
   if (e != cudaSuccess) return e;
-  // A stream-K tail makes CTAs wait for each other's partial sums: launch
-  // cooperatively so that all CTAs are resident together.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemAlloc;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = args.tail_tiles ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<BN>, args);
+  // (the grid is at most the resident clusters; see the single-CTA launcher)
+  return launch_pdl(tc_gemm_pair_kernel<BN>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemAlloc, stream,
+                    args);
 }
 
 }  // namespace

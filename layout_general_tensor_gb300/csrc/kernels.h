@@ -2,12 +2,53 @@
 // the kernel translation units.
 #pragma once
 #include <cstdint>
+#include <cstdlib>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "intmath.h"
 
 namespace lgt {
+
+// cudaFuncAttributeMaxDynamicSharedMemorySize for `Kernel` on the current
+// device, set once per device (the attribute outlives the call).
+template <auto Kernel>
+cudaError_t set_smem_once(int bytes) {
+  static unsigned long long done = 0;  // one bit per device ordinal below 64
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) __atomic_fetch_or(&done, bit, __ATOMIC_RELEASE);
+  return e;
+}
+
+// Launch with programmatic stream serialization: the kernel's prologue
+// (barrier set-up, TMEM allocation, descriptor prefetch) overlaps the end of
+// the previous kernel in the stream; every kernel here calls pdl_wait()
+// before its first global-memory access.  LGT_GEMM_PDL=0 launches plainly.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  static const bool pdl = [] {
+    const char* v = std::getenv("LGT_GEMM_PDL");
+    return !(v && v[0] == '0');
+  }();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // MMA tile: 128 rows on the P side (the operand whose rows map to TMEM
 // lanes), BN rows on the Q side, 64 elements of K per pipeline stage.

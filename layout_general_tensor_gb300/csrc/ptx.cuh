@@ -21,6 +21,19 @@ __device__ __forceinline__ uint32_t elect_lane0() {
   return (threadIdx.x & 31u) == 0u;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel in its stream is still running.  `pdl_launch_dependents`
+// lets the next kernel be scheduled as this one's CTAs leave; `pdl_wait`
+// blocks until every kernel this one depends on has completed and its memory
+// is visible.  Both are no-ops for a kernel launched without the attribute.
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
