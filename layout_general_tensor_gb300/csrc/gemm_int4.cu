@@ -63,6 +63,8 @@ constexpr int kQuadK = 4;                     // K blocks per stage
 constexpr uint32_t kRawBytes = TILE_P * 128;  // 128 rows x 128 bytes (256 codes)
 constexpr uint32_t kWStage = kRawBytes;       // packed-weight stage
 constexpr int kTSlots = 3;                    // TMEM A slots of 128 columns
+constexpr int kScWins = 4;                    // scale windows per expander warp's ring
+constexpr uint32_t kScRingBytes = kScWins * 32 * 16;
 constexpr uint32_t kASlotCol0 = 128;          // A slots at [128, 512); the accumulators below
 
 template <int BN>
@@ -77,12 +79,15 @@ struct Cfg4 {
   // the tile's slice of the activation group sums, Ag[g][m0 .. m0 + BN),
   // staged in shared memory for the zero-point term (BN = 16, up to 256 groups)
   static constexpr uint32_t ZP_BYTES = BN == 16 ? 256 * BN * 4 : 0;
-  static constexpr uint32_t RING_BYTES = 224 * 1024 - ZP_BYTES;
+  // each expander warp's ring of scale windows (8 groups x 32 rows, 4 windows)
+  static constexpr uint32_t SC_BYTES = 8 * kScRingBytes;
+  static constexpr uint32_t RING_BYTES = 224 * 1024 - ZP_BYTES - SC_BYTES;
   static constexpr int WST_FIT = static_cast<int>((RING_BYTES - XST * XSTAGE) / kWStage);
   static constexpr int WST = WST_FIT > 12 ? 12 : WST_FIT;  // packed-weight ring
   static constexpr uint32_t X_OFF = WST * kWStage;
   // barriers: full_w[W], wfree[W], full_x[X], xfree[X], a_full[T], tfree[T], accf[2], acce[2], teardown
-  static constexpr uint32_t ZP_OFF = X_OFF + XST * XSTAGE;
+  static constexpr uint32_t SC_OFF = X_OFF + XST * XSTAGE;
+  static constexpr uint32_t ZP_OFF = SC_OFF + SC_BYTES;
   static constexpr uint32_t BAR_OFF = ZP_OFF + ZP_BYTES;
   static constexpr uint32_t NUM_BARS = 2 * WST + 2 * XST + 2 * kTSlots + 5;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
@@ -498,19 +503,18 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
     const int h = (warp - kExpWarp0) >> 2;  // K blocks 2h, 2h + 1 of every stage
     const int r = q4 * 32 + lane;           // weight row within the tile (TMEM lane)
     StageIter it(a);
-    // This row's scales and zero points, 8 groups (16 bytes) per window: the
-    // current window and the next in registers, the next loaded when the
-    // current one is entered and the one after prefetched into L2 then.
-    // (Rows not 16-byte aligned: one load per K block.)
+    // This row's scales, 8 groups (16 bytes) per window, copied with
+    // cp.async into this warp's ring of kScWins windows in shared memory,
+    // three windows ahead of the one in use: the copies queue behind the
+    // weight stream in HBM for microseconds, and nothing waits on them until
+    // their window comes up.  (Rows not 16-byte aligned: one load per K block.)
     const uint16_t* srow = nullptr;
-    int w_cur = 0, w_last = -1;
-    uint4 s_cur, s_nxt;
-    auto load_win = [&](int w, uint4& sv) {
-      sv = make_uint4(0u, 0u, 0u, 0u);  // a row beyond N: s = 0
-      if (srow && w <= w_last) sv = __ldg(reinterpret_cast<const uint4*>(srow) + w);
-    };
-    auto prefetch_win = [&](int w) {
-      if (srow && w <= w_last) prefetch_l2(srow + 8 * w);
+    int w_cur = 0, w_next = 0, w_last = -1;
+    const uint32_t sc_mine = base + C::SC_OFF + static_cast<uint32_t>(warp - kExpWarp0) * kScRingBytes +
+                             static_cast<uint32_t>(lane) * 16u;
+    auto issue_win = [&](int w) {
+      if (srow && w <= w_last) cp_async_16(sc_mine + static_cast<uint32_t>(w & (kScWins - 1)) * 512u, srow + 8 * w);
+      cp_async_commit();  // (an empty group for windows past the run keeps the count uniform)
     };
     int kb0, nk, st = 0;
     bool nr;
@@ -524,14 +528,45 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         const int g1 =
             static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + it.g.nkb - 1), A4.div_kb_per_group));
         if (A4.vec_sz) {
+          cp_async_wait<0>();  // the previous run's copies have landed before slots are reused
           w_cur = g0 >> 3;
           w_last = g1 >> 3;
-          load_win(w_cur, s_cur);
-          load_win(w_cur + 1, s_nxt);
-          prefetch_win(w_cur + 2);
+          issue_win(w_cur);
+          issue_win(w_cur + 1);
+          issue_win(w_cur + 2);
+          w_next = w_cur + 3;
+          cp_async_wait<2>();  // window w_cur is in place
         }
       }
       {
+        // each K block's scale as an fp16 pair, and -1024 s, -64 s (exact:
+        // power-of-two multiples); formed before the waits below, whose time
+        // hides the latency of the lookup
+        uint32_t s2v[2], c1024v[2], c64v[2];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * h + jj;
+          uint32_t s2 = 0;
+          if (j < nk) {
+            const int g = static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + kb0 + j), A4.div_kb_per_group));
+            if (A4.vec_sz) {
+              const int w = g >> 3;
+              while (w_cur < w) {  // groups only grow within a run
+                ++w_cur;
+                issue_win(w_next++);
+                cp_async_wait<3>();  // window w_cur is in place (the 3 newer ones may be pending)
+              }
+              if (srow)
+                s2 = ld_shared_u16(sc_mine + static_cast<uint32_t>(w & (kScWins - 1)) * 512u +
+                                   static_cast<uint32_t>(g & 7) * 2u) * 0x10001u;
+            } else {
+              s2 = (srow ? static_cast<uint32_t>(__ldg(srow + g)) : 0u) * 0x10001u;
+            }
+          }
+          s2v[jj] = s2;
+          c1024v[jj] = hmul2(s2, 0xE400E400u);
+          c64v[jj] = hmul2(s2, 0xD400D400u);
+        }
         const int sw = st % C::WST, t = st % kTSlots;
         const bool got =
             mbar_wait_bounded(full_w(sw), (st / C::WST) & 1, a.wait_limit_ns, abort_flag) &&
@@ -546,36 +581,6 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         uint4 raw[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) raw[c] = *reinterpret_cast<const uint4*>(rowp + (((4 * h + c) ^ (r & 7)) << 4));
-        // each K block's scale as an fp16 pair
-        uint32_t s2v[2];
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * h + jj;
-          uint32_t s2 = 0;
-          if (j < nk) {
-            const int g = static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + kb0 + j), A4.div_kb_per_group));
-            if (A4.vec_sz) {
-              const int w = g >> 3;
-              if (w != w_cur) {  // groups only grow within a run
-                if (w == w_cur + 1)
-                  s_cur = s_nxt;
-                else
-                  load_win(w, s_cur);
-                w_cur = w;
-                load_win(w + 1, s_nxt);
-                prefetch_win(w + 2);
-              }
-              // group g % 8 of the window: its two bytes, in both halves
-              const uint32_t b0 = static_cast<uint32_t>(g & 3) * 2u;
-              const uint32_t sel = b0 * 0x1111u + 0x1010u;
-              const bool hi = (g & 4) != 0;
-              s2 = prmt(hi ? s_cur.z : s_cur.x, hi ? s_cur.w : s_cur.y, sel);
-            } else {
-              s2 = (srow ? static_cast<uint32_t>(__ldg(srow + g)) : 0u) * 0x10001u;
-            }
-          }
-          s2v[jj] = s2;
-        }
         __syncwarp();
         if (lane == 0) mbar_arrive(wfree(sw));
         const uint32_t slot = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + kASlotCol0 +
@@ -585,8 +590,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         for (int jj = 0; jj < 2; ++jj) {
           const int j = 2 * h + jj;
           if (j >= nk) break;
-          // -1024 s and -64 s: exact (power-of-two multiples)
-          const uint32_t s2 = s2v[jj], c1024 = hmul2(s2, 0xE400E400u), c64 = hmul2(s2, 0xD400D400u);
+          const uint32_t s2 = s2v[jj], c1024 = c1024v[jj], c64 = c64v[jj];
           const uint32_t words[8] = {raw[2 * jj].x, raw[2 * jj].y, raw[2 * jj].z, raw[2 * jj].w,
                                      raw[2 * jj + 1].x, raw[2 * jj + 1].y, raw[2 * jj + 1].z, raw[2 * jj + 1].w};
           uint32_t vals[32];
@@ -609,6 +613,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
       }
       ++st;
     }
+    cp_async_wait<0>();  // no copy into shared memory outlives the CTA
   } else {
     // ------------------------------------------------------------ epilogue
     // (warps 4..7: TMEM lane quadrant warp % 4; tiles leave by plain stores,
