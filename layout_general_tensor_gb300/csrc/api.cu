@@ -73,19 +73,6 @@ gemm_status_t validate(const gemm_desc_t& d) {
   return GEMM_OK;
 }
 
-// K blocks of a CTA's first group the kernels prefetch into L2 before their
-// programmatic-launch wait, for split-K plans (LGT_GEMM_L2PF, default 4; 0
-// turns it off).  On whole-tile plans it measured neutral to slightly slower.
-int l2_prefetch_depth() {
-  static const int v = [] {
-    const char* e = std::getenv("LGT_GEMM_L2PF");
-    if (!e || !*e) return 4;
-    const int x = std::atoi(e);
-    return x < 0 ? 0 : (x > 16 ? 16 : x);
-  }();
-  return v;
-}
-
 // Resident clusters of the CTA-pair kernel on each device (queried once).
 int pair_clusters(int device) {
   constexpr int kMaxDevices = 64;
@@ -262,7 +249,6 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
   args.kb_total = plan->kb_total;
   args.num_units = plan->num_units;
   args.rr_tiles = plan->rr_tiles;
-  args.l2_prefetch = plan->split > 1 ? l2_prefetch_depth() : 0;  // measured: helps split-K streams only
   args.tail_tiles = plan->fin_tiles;
   args.det = plan->det;
   args.max_runs = plan->max_runs;
@@ -692,7 +678,6 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   args.kb_total = plan->kb_total;
   args.num_units = plan->num_units;
   args.rr_tiles = plan->rr_tiles;
-  args.l2_prefetch = plan->split > 1 ? l2_prefetch_depth() : 0;  // measured: helps split-K streams only
   args.det = plan->det;
   args.max_runs = plan->max_runs;
   if (plan->det) args.slots = partial;

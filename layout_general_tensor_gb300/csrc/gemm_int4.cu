@@ -389,18 +389,6 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
     fence_proxy_async_smem();
     tma_prefetch_desc(&A4.tm_w);
     tma_prefetch_desc(&a.tm_q);
-    // Warm L2 with the first stages' weights and activation before pdl_wait
-    // (a prefetch reads nothing into the kernel).
-    StageIter pf(a);
-    int kb0, nk;
-    bool nr;
-    for (int i = 0; i < a.l2_prefetch && pf.next(a, kb0, nk, nr); ++i) {
-      int32_t tp, tq, m0, m1, n0, n1;
-      tile_ranges(a, pf.g.tile, BN, tp, tq, m0, m1, n0, n1);
-      const int kb = pf.g.kb0 + kb0;
-      tma_prefetch_l2_2d(&A4.tm_w, kb * (TILE_K / 2), n0);
-      tma_prefetch_l2_3d(&a.tm_q, 0, m0, kb);
-    }
   }
   if (warp == kIssWarp0) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);

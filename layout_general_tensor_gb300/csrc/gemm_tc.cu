@@ -104,32 +104,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     fence_proxy_async_smem();
     tma_prefetch_desc(&a.tm_p);
     tma_prefetch_desc(&a.tm_q);
-    // Warm L2 with the first K blocks' operand tiles while the previous
-    // kernel in the stream may still be finishing (a prefetch reads nothing
-    // into this kernel, so it needs no pdl_wait); the loads after pdl_wait
-    // then start from L2.
-    Sched sched(a);
-    Group g;
-    if (sched.next(a, g)) {
-      int32_t tp, tq, m0, m1, n0, n1;
-      tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
-      const int32_t prow = tp * TILE_P, qrow = tq * BN;
-      const int npf = g.nkb < a.l2_prefetch ? g.nkb : a.l2_prefetch;
-      for (int kb = 0; kb < npf; ++kb) {
-        const int32_t k0 = (g.kb0 + kb) * TILE_K;
-        if (!a.p_mn) {
-          tma_prefetch_l2_2d(&a.tm_p, k0, prow);
-        } else {
-          tma_prefetch_l2_2d(&a.tm_p, prow, k0);
-          tma_prefetch_l2_2d(&a.tm_p, prow + 64, k0);
-        }
-        if (!a.q_mn) {
-          tma_prefetch_l2_2d(&a.tm_q, k0, qrow);
-        } else {
-          for (int j = 0; j < BN / 64; ++j) tma_prefetch_l2_2d(&a.tm_q, qrow + 64 * j, k0);
-        }
-      }
-    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);

@@ -96,31 +96,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     tma_prefetch_desc(&a.tm_p);
     tma_prefetch_desc(&a.tm_q);
-    // Warm L2 with this CTA's share of the first K blocks before pdl_wait
-    // (a prefetch reads nothing into the kernel).
-    Sched sched(a);
-    Group g;
-    if (sched.next(a, g)) {
-      int32_t tp, tq, m0, m1, n0, n1;
-      tile_ranges(a, g.tile, kBN, tp, tq, m0, m1, n0, n1);
-      const int32_t prow = tp * (2 * kHalf) + static_cast<int32_t>(rank) * kHalf;
-      const int32_t qrow = tq * kBN + static_cast<int32_t>(rank) * kQHalf;
-      const int npf = g.nkb < a.l2_prefetch ? g.nkb : a.l2_prefetch;
-      for (int kb = 0; kb < npf; ++kb) {
-        const int32_t k0 = (g.kb0 + kb) * TILE_K;
-        if (!a.p_mn) {
-          tma_prefetch_l2_2d(&a.tm_p, k0, prow);
-        } else {
-          tma_prefetch_l2_2d(&a.tm_p, prow, k0);
-          tma_prefetch_l2_2d(&a.tm_p, prow + 64, k0);
-        }
-        if (!a.q_mn) {
-          tma_prefetch_l2_2d(&a.tm_q, k0, qrow);
-        } else {
-          for (int j = 0; j < kQChunks; ++j) tma_prefetch_l2_2d(&a.tm_q, qrow + 64 * j, k0);
-        }
-      }
-    }
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);

@@ -100,7 +100,6 @@ struct TcArgs {
   int32_t det;           // 1: runs store partials into slots, summed in run order by the last arriver
   int32_t max_runs;      // slots per strip
   int32_t tail_tiles;    // split tiles [rr_tiles, rr_tiles + tail_tiles) converted by the fixup warps of all CTAs
-  int32_t l2_prefetch;   // K blocks (int4: stages) of a CTA's first group prefetched into L2 before pdl_wait
                          // (a stream-K tail, or every tile of a split-K plan); 0: the last arriver converts
   MagicDiv div_split;    // unit -> (tile, split)
   MagicDiv div_tiles_p;  // tile -> (tile_p, tile_q)
