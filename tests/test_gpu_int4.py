@@ -59,6 +59,44 @@ def test_int4_group_sizes(group):
     g.close()
 
 
+@pytest.mark.parametrize("N,Kd,group,split", [(384, 8192, 64, 3), (300, 4096, 128, 5), (256, 16384, 512, 0),
+                                                (640, 2048, 64, 7)])
+def test_int4_scale_windows(N, Kd, group, split):
+    """Scales copied by TMA in windows of 8 groups of a tile's rows: runs
+    that start and end inside a window, several runs per CTA (split 7 over
+    5 tiles), rows beyond N (zero-filled window rows), group 64 (a window
+    every two stages) and 512 (a window every eight)."""
+    case = _case(16, N, Kd, group=group, split=split)
+    inp = wl.make_inputs(case, seed=N + group)
+    c, g, _ = run_case(case, inp, reps=2)
+    assert_close(c, oracle_full(case, inp), case.name)
+    g.close()
+
+
+def test_int4_unaligned_scale_rows():
+    """A scale array that does not start on a 16-byte boundary cannot be
+    copied by TMA: the per-K-block load path gives the same result."""
+    case = _case(16, 384, 2048, group=64, split=2)
+    inp = wl.make_inputs(case, seed=21)
+    ref = oracle_full(case, inp)
+    c_al, g, _ = run_case(case, inp)
+    m = lib()
+    A, B = inp.A.cuda(), inp.B.cuda()
+    n_sc = inp.scales.numel()
+    big = torch.zeros(n_sc + 8, dtype=inp.scales.dtype, device="cuda")
+    big[1:1 + n_sc] = inp.scales.reshape(-1).cuda()
+    sc = big[1:1 + n_sc]
+    assert sc.data_ptr() % 16 != 0
+    zr = inp.zeros.cuda() if inp.zeros is not None else None
+    C = torch.full((case.M * inp.ldc,), float("nan"), dtype=wl.TORCH_DTYPE[case.c_dtype], device="cuda")
+    g.run(A, B, C, sc, zr)
+    assert g.sync_status() == m.GEMM_OK
+    c_un = oracle.decode(C.cpu(), case.c_dtype).reshape(case.M, inp.ldc)[:, : case.N]
+    assert_close(c_un, ref, case.name + " (unaligned scales)")
+    assert_close(c_al, ref, case.name)
+    g.close()
+
+
 def test_int4_activation_m_contiguous():
     case = _case(40, 512, 512, al=MN, split=2)
     inp = wl.make_inputs(case, seed=3)
