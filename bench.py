@@ -3,9 +3,12 @@
 A step is one gemm_run of the headline workload (bf16 4096 x 4096 x 4096,
 A K-contiguous, B N-contiguous, fp32 accumulation) on inputs resident in HBM;
 consecutive steps cycle through enough copies of the operands (more than
-2.5 x the 129 MB L2 in total) that no step finds its inputs in L2.  The same run also measures the other workloads (fp16 256^3 in four
-layouts, the skinny split-K GEMM, the irregular GEMM) and reports them under
-"configs".  One JSON line on stdout (rank 0).
+2.5 x the 129 MB L2 in total) that no step finds its inputs in L2.  The
+same run also measures the other workloads (fp16 256^3 in four layouts, the
+skinny split-K GEMM, the irregular GEMM, the int4-weight GEMM, and the fp32
+row reductions: the IREE page's 4096 -> 1 and 4 x 4096 -> 4, and a 1 GiB
+16384 x 16384 matrix for bandwidth) and reports them under "configs".  One
+JSON line on stdout (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -394,6 +397,9 @@ def gpu_arm(args, headline):
         d.g.close()
         del d
 
+    for rc in (wl.REDUCE_VEC, wl.REDUCE_ROWS, wl.REDUCE_LARGE):
+        configs[rc.name] = reduce_config(rc, args, peaks)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(headline, dc.host, budget_s=args.cpu_seconds)
@@ -433,11 +439,49 @@ def gpu_arm(args, headline):
     return 0
 
 
+class DeviceReduce:
+    """One row-reduction workload resident on the device.  The 1 GiB matrix
+    is larger than L2 on its own; the page's 16 KB cases are latency-bound
+    and run on one input."""
+
+    def __init__(self, rc, seed=0):
+        import torch
+        import workloads as wl
+        import layout_general_tensor_gb300 as lgt
+        self.rc = rc
+        self.x = wl.make_reduce_input(rc, seed).cuda()
+        self.out = torch.empty(rc.rows, dtype=torch.float32, device="cuda")
+        self.r = lgt.RowReduce(rc.rows, rc.cols)
+
+    def run(self):
+        self.r.run(self.x, self.out, ldx=self.rc.ldx)
+
+
+def reduce_config(rc, args, peaks):
+    d = DeviceReduce(rc)
+    n = max(args.steps, 20)
+    ms = time_batched(d.run, n, max(args.warmup, 3)) / n
+    nbytes = rc.rows * rc.cols * 4 + rc.rows * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms_per_step": ms, "us_per_step": ms * 1e3, "gbs": gbs, "pct_hbm": 100 * gbs / peaks["hbm_gbs"],
+            "algorithmic_bytes": nbytes, "workspace_bytes": d.r.ws_bytes, "kernel": "reduce_rows_kernel",
+            "launches_per_run": 1,
+            "l2": "input larger than L2" if nbytes > DeviceCase.L2_BYTES else "input resident in L2 (latency case)"}
+
+
 def profile_case(args):
     import torch
     import workloads as wl
     import __graft_entry__
     __graft_entry__.build()
+    reduces = {c.name: c for c in (wl.REDUCE_VEC, wl.REDUCE_ROWS, wl.REDUCE_LARGE)}
+    if args.profile_case in reduces:
+        d = DeviceReduce(reduces[args.profile_case])
+        for _ in range(args.steps):
+            d.run()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": args.profile_case, "runs": args.steps, "status": 0}))
+        return 0
     case = {c.name: c for c in wl.WORKLOADS}[args.profile_case]
     d = DeviceCase(case, rotate=False)
     for _ in range(args.steps):

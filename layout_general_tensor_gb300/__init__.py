@@ -1,4 +1,5 @@
-"""Python binding of the any-layout GEMM C ABI (``include/gemm.h``).
+"""Python binding of the any-layout GEMM C ABI (``include/gemm.h``) and the
+fp32 row reduction (``include/reduce.h``).
 
 Argument marshalling only: every function forwards to the entry point of the
 same name in ``_lib/libgemm.so``; all arithmetic runs in the library's CUDA
@@ -31,12 +32,13 @@ GEMM_BF16 = 1
 GEMM_INT4 = 2
 GEMM_F32 = 3
 
-# Every entry point include/gemm.h declares.
+# Every entry point include/gemm.h and include/reduce.h declare.
 EXPORTS = (
     "gemm_create", "gemm_workspace_size", "gemm_query", "gemm_run", "gemm_run_static_scratch",
     "gemm_sync_status", "gemm_destroy",
     "gemm_splitk_auto", "gemm_perm_fwd", "gemm_perm_inv", "gemm_magic_divmod_host",
     "gemm_magic_divmod_device", "gemm_status_string",
+    "reduce_rows_workspace_size", "reduce_rows_f32",
 )
 
 
@@ -82,6 +84,10 @@ def _load():
         "gemm_magic_divmod_host": (ctypes.c_int, [P, ctypes.c_size_t, ctypes.c_uint32, P, P]),
         "gemm_magic_divmod_device": (ctypes.c_int, [P, ctypes.c_size_t, ctypes.c_uint32, P, P, P]),
         "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "reduce_rows_workspace_size": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                                      ctypes.POINTER(ctypes.c_size_t)]),
+        "reduce_rows_f32": (ctypes.c_int, [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P,
+                                           ctypes.c_size_t, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -182,6 +188,39 @@ def gemm_magic_divmod_host(n_array, divisor):
 
 def gemm_magic_divmod_device(n_ptr, count, divisor, q_ptr, r_ptr, stream=0) -> int:
     return _lib.gemm_magic_divmod_device(n_ptr, count, divisor, q_ptr, r_ptr, stream or None)
+
+
+def reduce_rows_workspace_size(rows: int, cols: int, num_sms: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.reduce_rows_workspace_size(rows, cols, num_sms, ctypes.byref(n)), "reduce_rows_workspace_size")
+    return n.value
+
+
+def reduce_rows_f32(x: int, rows: int, cols: int, ldx: int, out: int, workspace: int = 0, workspace_bytes: int = 0,
+                    stream: int = 0) -> int:
+    """Raw entry point: integer device addresses; returns the status code."""
+    return _lib.reduce_rows_f32(x or None, rows, cols, ldx, out or None, workspace or None, workspace_bytes,
+                                stream or None)
+
+
+class RowReduce:
+    """out[r] = sum of row r of an fp32 matrix, with its (zero-filled) device
+    workspace.  Marshalling only: passes device addresses and the current
+    torch stream to reduce_rows_f32."""
+
+    def __init__(self, rows: int, cols: int, device=None):
+        import torch
+        self.rows, self.cols = rows, cols
+        self.ws_bytes = reduce_rows_workspace_size(rows, cols, 0)
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.workspace = torch.zeros(max(self.ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+    def run(self, x, out, ldx: int = 0, stream=None):
+        import torch
+        s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+        st = reduce_rows_f32(x.data_ptr(), self.rows, self.cols, ldx, out.data_ptr(),
+                             self.workspace.data_ptr() if self.ws_bytes else 0, self.ws_bytes, s)
+        _check(st, "reduce_rows_f32")
 
 
 def make_desc(M, N, K, a_layout=GEMM_K_CONTIG, b_layout=GEMM_K_CONTIG, a_dtype=GEMM_BF16, b_dtype=None,

@@ -20,7 +20,7 @@ OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libgemm.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_tc_pair.cu", "gemm_int4.cu", "aux_kernels.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_tc_pair.cu", "gemm_int4.cu", "aux_kernels.cu", "noalloc.cu", "reduce.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]
@@ -35,7 +35,7 @@ def nvcc_path():
 
 def _deps():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "gemm.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     files.append(os.path.abspath(__file__))
     return files
 

@@ -24,6 +24,14 @@ What it computes, and the passage each function follows:
   stride permutation of the hipBLASLt DTL page ("Add support for permuting
   perpDim": forward and inverse mappings).
 * :func:`round_to` -- round-to-nearest-even of fp64 values to fp16 / bf16.
+* :func:`reduce_rows` -- ``out[r] = sum_c x[r*ldx + c]`` in fp64, the
+  reduction of the IREE page ("[LLVMGPUVectorDistribute] Add support for
+  inter-subgroup multi_reduction": linalg.generic with arith.addf over the
+  inner dimension, initial value 0, on 4096 and 4 x 4096 f32 inputs);
+  :func:`reduce_rows_bound` is the first-order fp32 summation error bound a
+  result computed by any fixed order of pairwise additions with sequential
+  chains of at most ``chain`` terms and trees of total depth ``depth``
+  must meet.
 
 Readings taken where the pages are silent or garbled (all listed in the
 design notes): split-K grid counts use ceiling division (floor gives zero
@@ -297,6 +305,38 @@ def perm_apply(count, block, stride):
     """The forward map over 0..count-1 (trailing partial block = identity)."""
     full = (count // block) * block
     return [perm_forward(i, block, stride) if i < full else i for i in range(count)]
+
+
+# ---------------------------------------------------------------------------
+# row reduction (IREE page: inter-subgroup multi_reduction)
+# ---------------------------------------------------------------------------
+
+def reduce_rows(x, rows, cols, ldx=0) -> np.ndarray:
+    """out[r] = sum over c < cols of x[r*ldx + c], each fp32 input exact
+    in fp64 and the sum accumulated in fp64 (ldx = 0 means cols).  Elements
+    outside a row's first ``cols`` (padding) are never read."""
+    ldx = cols if ldx == 0 else ldx
+    vals = np.asarray(x.numpy() if hasattr(x, "numpy") else x, dtype=np.float32).astype(np.float64)
+    out = np.zeros(rows, dtype=np.float64)
+    for r in range(rows):
+        idx = r * ldx + np.arange(cols, dtype=np.int64)
+        out[r] = np.sum(vals[idx]) if cols else 0.0
+    return out
+
+
+def reduce_rows_abs(x, rows, cols, ldx=0) -> np.ndarray:
+    """sum over c of |x[r*ldx + c]| per row, in fp64 (the scale of the
+    rounding error of any fp32 summation of the row)."""
+    return reduce_rows(np.abs(np.asarray(x.numpy() if hasattr(x, "numpy") else x, dtype=np.float32)), rows, cols, ldx)
+
+
+def reduce_rows_bound(abs_sums, chain, depth):
+    """First-order bound on |fp32 sum - exact sum| for a summation whose
+    every term passes through at most ``chain`` sequential additions and
+    trees of total depth ``depth``: (chain + depth) * 2^-24 * sum |x|
+    (each addition rounds once with relative error at most 2^-24, and a term
+    is affected only by the additions on its path to the result)."""
+    return (chain + depth) * 2.0 ** -24 * np.asarray(abs_sums, dtype=np.float64)
 
 
 # ---------------------------------------------------------------------------

@@ -28,7 +28,7 @@ def _declared_functions():
             continue
         text = open(os.path.join(ROOT, "include", fn)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(gemm_[a-z0-9_]+)\s*\(", text, re.M):
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*((?:gemm|reduce)_[a-z0-9_]+)\s*\(", text, re.M):
             names.add(m.group(1))
     return names
 
@@ -212,3 +212,31 @@ def test_no_device_paths(lib):
     h = lib.gemm_create(lib.make_desc(128, 128, 128, num_sms=148))
     assert lib.gemm_run(h, 16, 16, 16) == lib.GEMM_ERR_CUDA
     lib.gemm_destroy(h)
+
+
+def test_reduce_host_checks(lib):
+    """Workspace sizing and argument checks of the row reduction (host only)."""
+    assert lib.reduce_rows_workspace_size(1, 4096, 148) == 0       # the IREE page's cases: one CTA a row
+    assert lib.reduce_rows_workspace_size(4, 4096, 148) == 0
+    assert lib.reduce_rows_workspace_size(16384, 16384, 148) == 0  # rows fill the GPU
+    n = lib.reduce_rows_workspace_size(1, 1 << 22, 148)            # one long row: split across CTAs
+    assert n >= 148 * 4 * 4 + 4
+    assert lib.reduce_rows_workspace_size(0, 5, 148) == 0
+    with pytest.raises(lib.GemmError):
+        lib.reduce_rows_workspace_size(-1, 5, 148)
+    F = lib.reduce_rows_f32
+    assert F(4096, -1, 4, 0, 4096) == lib.GEMM_ERR_INVALID_ARG
+    assert F(4096, 2, 8, 7, 4096) == lib.GEMM_ERR_INVALID_ARG       # ldx < cols
+    assert F(0, 2, 8, 0, 4096) == lib.GEMM_ERR_INVALID_ARG          # NULL x
+    assert F(4098, 2, 8, 0, 4096) == lib.GEMM_ERR_ALIGNMENT         # x not 4-byte aligned
+    assert F(4096, 2, 8, 0, 4097) == lib.GEMM_ERR_ALIGNMENT         # out not 4-byte aligned
+    assert F(4096, 0, 8, 0, 0) == lib.GEMM_OK                       # no rows: nothing to do
+
+
+def test_reduce_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert lib.reduce_rows_f32(4096, 2, 8, 0, 4096) == lib.GEMM_ERR_CUDA
+    st = lib._lib.reduce_rows_workspace_size(2, 8, 0, ctypes.byref(ctypes.c_size_t()))
+    assert st == lib.GEMM_ERR_CUDA

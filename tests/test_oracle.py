@@ -406,3 +406,88 @@ def test_check_close_catches_planted_errors():
     nan = ref.copy()
     nan[0, 0] = np.nan
     assert not oracle.check_close(nan, ref)[0]
+
+
+# ---------------------------------------------------------- row reduction
+
+def _exact_row_sums(vals, rows, cols, ldx):
+    """Exact rational row sums of fp32 storage (struct-decoded values)."""
+    import struct
+    from fractions import Fraction
+    raw = np.asarray(vals, dtype=np.float32).tobytes()
+    dec = struct.unpack(f"<{len(raw) // 4}f", raw)
+    return [sum((Fraction(dec[r * ldx + c]) for c in range(cols)), Fraction(0)) for r in range(rows)]
+
+
+def _reduce_pins_hold(fn):
+    """True when ``fn`` (a candidate for oracle.reduce_rows) meets every pin:
+    the IREE page's two cases on all-ones input (4096 -> 4096, 4 x 4096 ->
+    four 4096s), the arithmetic-series closed form, and exact rational brute
+    force on small padded matrices whose padding is NaN."""
+    if not np.array_equal(fn(np.ones(4096, np.float32), 1, 4096), [4096.0]):
+        return False
+    if not np.array_equal(fn(np.ones(4 * 4096, np.float32), 4, 4096), [4096.0] * 4):
+        return False
+    rows, cols = 3, 1000
+    x = (np.arange(cols, dtype=np.float32)[None, :] + np.arange(rows, dtype=np.float32)[:, None] * 7).ravel()
+    want = [cols * (cols - 1) / 2 + 7 * r * cols for r in range(rows)]
+    if not np.array_equal(fn(x, rows, cols), want):
+        return False
+    rng = np.random.default_rng(5)
+    for rows, cols, pad in [(1, 1, 0), (2, 3, 1), (5, 9, 4), (4, 17, 3), (3, 0, 2)]:
+        ldx = cols + pad
+        buf = np.full(rows * max(ldx, 1), np.nan, dtype=np.float32)
+        for r in range(rows):
+            buf[r * ldx:r * ldx + cols] = (rng.standard_normal(cols) * 10.0 ** rng.integers(-3, 4)).astype(np.float32)
+        got = fn(buf, rows, cols, ldx)
+        exact = _exact_row_sums(buf, rows, cols, ldx)
+        for r in range(rows):
+            scale = float(sum(abs(float(buf[r * ldx + c])) for c in range(cols)))
+            if not np.isfinite(got[r]) or abs(float(exact[r]) - got[r]) > (cols + 1) * 2.0 ** -53 * scale:
+                return False
+    return True
+
+
+def test_reduce_rows_pins():
+    assert _reduce_pins_hold(oracle.reduce_rows)
+
+
+def test_reduce_rows_planted_mistakes_are_caught():
+    def drop_last(x, rows, cols, ldx=0):
+        return oracle.reduce_rows(x, rows, max(cols - 1, 0), ldx or cols)
+
+    def dense_pitch(x, rows, cols, ldx=0):
+        return oracle.reduce_rows(x, rows, cols, 0)
+
+    def first_negated(x, rows, cols, ldx=0):
+        y = np.array(x, dtype=np.float32, copy=True)
+        p = ldx or cols
+        for r in range(rows):
+            if cols:
+                y[r * p] = -y[r * p]
+        return oracle.reduce_rows(y, rows, cols, ldx)
+
+    def in_fp32(x, rows, cols, ldx=0):
+        p = ldx or cols
+        v = np.asarray(x, dtype=np.float32)
+        return np.array([np.float32(np.cumsum(v[r * p:r * p + cols], dtype=np.float32)[-1]) if cols else 0.0
+                         for r in range(rows)], dtype=np.float64)
+
+    for bad in (drop_last, dense_pitch, first_negated, in_fp32):
+        assert not _reduce_pins_hold(bad), bad.__name__
+
+
+def test_reduce_rows_bound_holds_for_sequential_fp32():
+    """The textbook bound for n-term recursive summation, (n - 1) u sum|x|
+    (Higham, Accuracy and Stability of Numerical Algorithms, sec. 4.2), is
+    what reduce_rows_bound gives for chain = n, depth = 0 (one spare term);
+    a plain fp32 left-to-right sum stays inside it, and a sum with one term
+    dropped does not."""
+    rng = np.random.default_rng(7)
+    for n in (10, 1000, 100000):
+        x = rng.standard_normal(n).astype(np.float32)
+        seq = float(np.cumsum(x, dtype=np.float32)[-1])
+        exact = oracle.reduce_rows(x, 1, n)[0]
+        bound = oracle.reduce_rows_bound(oracle.reduce_rows_abs(x, 1, n), n, 0)[0]
+        assert abs(seq - exact) <= bound
+        assert abs(float(np.cumsum(x[:-1], dtype=np.float32)[-1]) - exact) > bound or abs(x[-1]) < bound

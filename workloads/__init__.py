@@ -123,6 +123,8 @@ def _draw(n, dist, dtype, gen):
         x = torch.randn(n, generator=gen, dtype=torch.float32) * dist[1]
     elif kind == "ones":
         x = torch.ones(n, dtype=torch.float32)
+    elif kind == "ints":
+        x = torch.randint(dist[1], dist[2] + 1, (n,), generator=gen).to(torch.float32)
     else:
         raise ValueError(f"unknown distribution {dist}")
     return x.to(TORCH_DTYPE[dtype])
@@ -203,4 +205,35 @@ def ceil_div(a, b):
 
 def storage_elems(rows, ld):
     return rows * ld
+
+
+# ---------------------------------------------------------------------------
+# fp32 row reductions (the IREE page's multi_reduction cases)
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class ReduceCase:
+    """out[r] = sum of row r of a rows x cols fp32 matrix (row pitch ldx,
+    0 = cols) with values drawn from ``dist``."""
+    name: str
+    rows: int
+    cols: int
+    dist: tuple = ("normal", 1.0)
+    ldx: int = 0
+
+    def pitch(self):
+        return self.ldx or self.cols
+
+
+# The IREE page's two verification cases (4096 -> 1 and 4 x 4096 -> 4), and
+# a 1 GiB matrix (larger than L2) for the bandwidth measurement.
+REDUCE_VEC = ReduceCase("reduce_f32_4096_to_1", 1, 4096)
+REDUCE_ROWS = ReduceCase("reduce_f32_4x4096_to_4", 4, 4096)
+REDUCE_LARGE = ReduceCase("reduce_f32_16384x16384_to_16384", 16384, 16384)
+
+
+def make_reduce_input(case: ReduceCase, seed: int = 0) -> torch.Tensor:
+    """Flat CPU fp32 storage of ``rows * pitch`` elements (NaN padding)."""
+    gen = torch.Generator().manual_seed(1_000_003 * seed + 29)
+    return strided_matrix(case.rows, case.cols, case.pitch(), case.dist, F32, gen)
 
