@@ -36,10 +36,12 @@
 //
 // Warp roles (512 threads):
 //   warp 0       TMA producer for both rings.
-//   warps 1..3   MMA issuers (NI of them active, by accumulator width): each
-//                waits for an expanded slot and the stage's activation, issues
-//                its share of the stage's MMAs into its own accumulator, frees
-//                the slot and the activation buffer.  Warp 1 owns the TMEM.
+//   warps 1..3   MMA issuers (NI of them active, by accumulator width): the
+//                CTA's stages are dealt round-robin to the issuers (stage s
+//                to issuer s % NI); each waits for its stage's expanded slot
+//                and activation, issues all of the stage's MMAs back to back
+//                into its own accumulator, and frees the slot and the
+//                activation buffer.  Warp 1 owns the TMEM.
 //   warps 4..7   epilogue (TMEM lane quadrant warp % 4), adds the NI
 //                accumulators.
 //   warps 8..15  expanders: two warps per TMEM lane quadrant, each taking two
@@ -62,7 +64,6 @@ constexpr int kExpWarp0 = 8;                  // expander warps 8..15
 constexpr int kQuadK = 4;                     // K blocks per stage
 constexpr uint32_t kRawBytes = TILE_P * 128;  // 128 rows x 128 bytes (256 codes)
 constexpr uint32_t kWStage = kRawBytes;       // packed-weight stage
-constexpr int kTSlots = 3;                    // TMEM A slots of 128 columns
 constexpr int kScWins = 4;                    // scale windows per expander warp's ring
 constexpr uint32_t kScRingBytes = kScWins * 32 * 16;
 constexpr uint32_t kASlotCol0 = 128;          // A slots at [128, 512); the accumulators below
@@ -70,12 +71,19 @@ constexpr uint32_t kASlotCol0 = 128;          // A slots at [128, 512); the accu
 template <int BN>
 struct Cfg4 {
   // MMA issuers.  One thread keeps about one narrow (N <= 64) MMA in flight,
-  // so the tensor core runs several times faster when several threads issue
-  // into accumulators of their own, which the epilogue adds.
+  // and every wait between its MMAs costs it a few hundred cycles, so the
+  // tensor core runs several times faster when several threads each issue
+  // long runs of MMAs into accumulators of their own, which the epilogue adds.
   static constexpr int NI = BN == 16 ? 3 : (BN == 32 ? 2 : 1);
+  // TMEM A slots of 128 columns and activation buffers, both multiples of
+  // NI: stage s uses slot s % TSLOTS and buffer s % XST, so each slot's and
+  // each buffer's barriers are waited on by one issuer only, in order (an
+  // issuer that skipped the stages of others could otherwise wait on a
+  // barrier two phases ahead and see the older phase's parity as complete).
+  static constexpr int TSLOTS = NI == 2 ? 2 : 3;
   static constexpr uint32_t ACT_TILE = BN * TILE_K * 2;  // one 64-deep activation box
   static constexpr uint32_t XSTAGE = kQuadK * ACT_TILE;  // a stage's activation
-  static constexpr int XST = BN == 64 ? 3 : 4;           // activation ring
+  static constexpr int XST = NI == 2 ? 4 : 3;            // activation ring
   // the tile's slice of the activation group sums, Ag[g][m0 .. m0 + BN),
   // staged in shared memory for the zero-point term (BN = 16, up to 256 groups)
   static constexpr uint32_t ZP_BYTES = BN == 16 ? 256 * BN * 4 : 0;
@@ -89,14 +97,15 @@ struct Cfg4 {
   static constexpr uint32_t SC_OFF = X_OFF + XST * XSTAGE;
   static constexpr uint32_t ZP_OFF = SC_OFF + SC_BYTES;
   static constexpr uint32_t BAR_OFF = ZP_OFF + ZP_BYTES;
-  static constexpr uint32_t NUM_BARS = 2 * WST + 2 * XST + 2 * kTSlots + 5;
+  static constexpr uint32_t NUM_BARS = 2 * WST + 2 * XST + 2 * TSLOTS + 5;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_ALLOC = MISC_OFF + 64 + 1024;  // slack for 1024-byte alignment
   static_assert(kWStage % 1024 == 0 && ACT_TILE % 1024 == 0, "swizzled buffers stay 1024-byte aligned");
   static_assert(WST >= 4 && XST >= 2, "ring depths");
-  static_assert(NI <= kMaxIssuers && NI <= kQuadK * 4, "every issuer has an MMA in every stage");
+  static_assert(NI <= kMaxIssuers, "issuer warps");
+  static_assert(TSLOTS % NI == 0 && XST % NI == 0, "one issuer per slot and per activation buffer");
   static_assert(2 * NI * BN <= static_cast<int>(kASlotCol0), "accumulators fit below the A slots");
-  static_assert(kASlotCol0 + kTSlots * 128 <= 512, "A slots fit in the TMEM allocation");
+  static_assert(kASlotCol0 + TSLOTS * 128 <= 512, "A slots fit in the TMEM allocation");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -156,29 +165,28 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
-// Issuer ISS's MMAs of one stage of NK K blocks (MMA m = 4 j + k: K block j,
-// 16-deep step k; the issuer's are those with m % NI == ISS), straight-line:
-// an MMA skipped by a runtime guard still costs its issue slot.
-template <int NI, int ISS, int NK, uint32_t ACT_TILE>
+// Every MMA of one stage of NK K blocks (MMA m = 4 j + k: K block j, 16-deep
+// step k), straight-line; `first` starts the accumulator at the first one.
+template <int NK, uint32_t ACT_TILE>
 __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint32_t a0, uint64_t bd0, uint32_t idesc, uint32_t first) {
 #pragma unroll
-  for (int m = ISS; m < 4 * NK; m += NI) {
+  for (int m = 0; m < 4 * NK; ++m) {
     const int j = m >> 2, k = m & 3;
     // A: 8 TMEM columns (16 fp16 pairs) per 16-deep step; B: +32 bytes per step
     tc_mma_f16_ts(d_tmem, a0 + static_cast<uint32_t>(j * 32 + k * 8),
                   bd0 + static_cast<uint64_t>((j * ACT_TILE) >> 4) + static_cast<uint64_t>(2 * k), idesc,
-                  (m == ISS && first) ? 0u : 1u);
+                  (m == 0 && first) ? 0u : 1u);
   }
 }
 
-template <int NI, int ISS, uint32_t ACT_TILE>
+template <uint32_t ACT_TILE>
 __device__ __forceinline__ void issue_stage_nk(int nk, uint32_t d_tmem, uint32_t a0, uint64_t bd0, uint32_t idesc,
                                                uint32_t first) {
   switch (nk) {
-    case 4: issue_stage<NI, ISS, 4, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
-    case 3: issue_stage<NI, ISS, 3, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
-    case 2: issue_stage<NI, ISS, 2, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
-    default: issue_stage<NI, ISS, 1, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
+    case 4: issue_stage<4, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
+    case 3: issue_stage<3, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
+    case 2: issue_stage<2, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
+    default: issue_stage<1, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
   }
 }
 
@@ -348,21 +356,21 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   const uint32_t bar0 = base + C::BAR_OFF;
   // full_w[s] / full_x[s]: a packed-weight / activation stage landed.
   // wfree[s]: the stage's eight expander warps read its packed weights.
-  // xfree[s]: the MMAs that read the activation stage completed (one commit
-  // per issuer).  a_full[t]: the expanders wrote a stage's weights into TMEM
-  // A slot t.  tfree[t]: the MMAs reading slot t completed (one commit per
-  // issuer).  accf / acce: accumulator buffer full (one commit per issuer) /
-  // drained by the epilogue.
+  // xfree[s]: the MMAs that read the activation stage completed (the stage's
+  // issuer commits).  a_full[t]: the expanders wrote a stage's weights into
+  // TMEM A slot t.  tfree[t]: the MMAs reading slot t completed (the stage's
+  // issuer commits).  accf / acce: accumulator buffer full (one commit per
+  // issuer at the end of each run) / drained by the epilogue.
   constexpr int kB1 = 2 * C::WST + 2 * C::XST;
   auto full_w = [&](int i) { return bar0 + 8u * i; };
   auto wfree = [&](int i) { return bar0 + 8u * (C::WST + i); };
   auto full_x = [&](int i) { return bar0 + 8u * (2 * C::WST + i); };
   auto xfree = [&](int i) { return bar0 + 8u * (2 * C::WST + C::XST + i); };
   auto a_full = [&](int t) { return bar0 + 8u * (kB1 + t); };
-  auto tfree_bar = [&](int t) { return bar0 + 8u * (kB1 + kTSlots + t); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (kB1 + 2 * kTSlots + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (kB1 + 2 * kTSlots + 2 + b); };
-  const uint32_t teardown_bar = bar0 + 8u * (kB1 + 2 * kTSlots + 4);
+  auto tfree_bar = [&](int t) { return bar0 + 8u * (kB1 + C::TSLOTS + t); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (kB1 + 2 * C::TSLOTS + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (kB1 + 2 * C::TSLOTS + 2 + b); };
+  const uint32_t teardown_bar = bar0 + 8u * (kB1 + 2 * C::TSLOTS + 4);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -373,11 +381,11 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
     }
     for (int i = 0; i < C::XST; ++i) {
       mbar_init(full_x(i), 1);
-      mbar_init(xfree(i), NI);
+      mbar_init(xfree(i), 1);
     }
-    for (int t = 0; t < kTSlots; ++t) {
+    for (int t = 0; t < C::TSLOTS; ++t) {
       mbar_init(a_full(t), 8);
-      mbar_init(tfree_bar(t), NI);
+      mbar_init(tfree_bar(t), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), NI);
@@ -468,9 +476,13 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
     }
   } else if (warp < kIssWarp0 + kMaxIssuers) {
     // ------------------------------------------------------------ MMA issuers
-    // Issuer i takes the MMAs m = 4 j + k (K block j, 16-deep step k) of
-    // every stage with m % NI == i, into its own accumulator (every issuer
-    // has one in every stage: a stage has at least 4 MMAs).
+    // Issuer i takes the CTA's stages s with s % NI == i and issues every MMA
+    // of such a stage (K block, 16-deep step) back to back into its own
+    // accumulator; the first MMA of its first stage in a run (one of the
+    // run's first NI stages) starts the accumulator.  Issuers with no stage
+    // in a run (runs of fewer than NI stages) leave theirs untouched, and the
+    // epilogue adds only the accumulators of the run's issuers.  Every
+    // issuer commits the end of every run.
     const int iss = warp - kIssWarp0;
     if (lane == 0 && iss < NI) {
       StageIter it(a);
@@ -478,7 +490,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
       bool nr;
       uint32_t d_tmem = tmem_base;
       while (it.next(a, kb0, nk, nr)) {
-        const int t = st % kTSlots, sx = st % C::XST;
+        const int t = st % C::TSLOTS, sx = st % C::XST;
         if (nr) {
           ++acc_iter;
           const int buf = acc_iter & 1;
@@ -488,20 +500,20 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
           }
           d_tmem = tmem_base + static_cast<uint32_t>((buf * NI + iss) * BN);
         }
-        if (!mbar_wait_bounded(a_full(t), (st / kTSlots) & 1, a.wait_limit_ns, abort_flag) ||
-            !mbar_wait_bounded(full_x(sx), (st / C::XST) & 1, a.wait_limit_ns, abort_flag)) {
-          if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 0);
-          break;
+        const int js = kb0 / kQuadK;  // stage index within the run
+        if (st % NI == iss) {
+          if (!mbar_wait_bounded(a_full(t), (st / C::TSLOTS) & 1, a.wait_limit_ns, abort_flag) ||
+              !mbar_wait_bounded(full_x(sx), (st / C::XST) & 1, a.wait_limit_ns, abort_flag)) {
+            if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 0);
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bd0 = sw128_desc(base + C::X_OFF + sx * C::XSTAGE, 16u, 1024u);
+          const uint32_t a0 = tmem_base + kASlotCol0 + static_cast<uint32_t>(t * 128);
+          issue_stage_nk<C::ACT_TILE>(nk, d_tmem, a0, bd0, a.idesc, js < NI ? 1u : 0u);
+          tc_commit(tfree_bar(t));
+          tc_commit(xfree(sx));
         }
-        tc_fence_after();
-        const uint64_t bd0 = sw128_desc(base + C::X_OFF + sx * C::XSTAGE, 16u, 1024u);
-        const uint32_t a0 = tmem_base + kASlotCol0 + static_cast<uint32_t>(t * 128);
-        const uint32_t first = kb0 == 0 ? 1u : 0u;
-        if (iss == 0) issue_stage_nk<NI, 0, C::ACT_TILE>(nk, d_tmem, a0, bd0, a.idesc, first);
-        if constexpr (NI > 1) if (iss == 1) issue_stage_nk<NI, 1, C::ACT_TILE>(nk, d_tmem, a0, bd0, a.idesc, first);
-        if constexpr (NI > 2) if (iss == 2) issue_stage_nk<NI, 2, C::ACT_TILE>(nk, d_tmem, a0, bd0, a.idesc, first);
-        tc_commit(tfree_bar(t));
-        tc_commit(xfree(sx));
         if (kb0 + nk == it.g.nkb) tc_commit(accf_bar(acc_iter & 1));
         ++st;
       }
@@ -576,10 +588,10 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
           c1024v[jj] = hmul2(s2, 0xE400E400u);
           c64v[jj] = hmul2(s2, 0xD400D400u);
         }
-        const int sw = st % C::WST, t = st % kTSlots;
+        const int sw = st % C::WST, t = st % C::TSLOTS;
         const bool got =
             mbar_wait_bounded(full_w(sw), (st / C::WST) & 1, a.wait_limit_ns, abort_flag) &&
-            mbar_wait_bounded(tfree_bar(t), ((st / kTSlots) & 1) ^ 1u, a.wait_limit_ns, abort_flag);
+            mbar_wait_bounded(tfree_bar(t), ((st / C::TSLOTS) & 1) ^ 1u, a.wait_limit_ns, abort_flag);
         if (!got && !*abort_flag) record_timeout(a, abort_flag, 3 * 16 + 0);
         // the warp leaves together (tcgen05.st below needs every lane)
         if (!__all_sync(0xffffffffu, got)) break;
@@ -652,15 +664,20 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         }
       }
     }
+    int st0 = 0;  // the CTA's stage index of the run's first stage
     for (int idx = 0; sched.next(a, g); ++idx) {
       fix.active = g.s0 == 0 && g.nkb > 0;
+      const int nstages = (g.nkb + kQuadK - 1) / kQuadK;
+      uint32_t mask = 0;
+      for (int j = 0; j < nstages && j < NI; ++j) mask |= 1u << ((st0 + j) % NI);
+      st0 += nstages;
       if (fix.active && idx != first_idx) {
         int32_t tp, tq, m0, m1, n0, n1;
         tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
         fix.prepare(A4, g, n0 + q4 * 32 + lane, n1, m0, zp_stage, et);
       }
       if (!epilogue_group<BN, (BN < 32 ? BN : 32), false, NI, ZpFix<BN>>(
-              a, g, tmem_base, accf_bar(0), acce_bar(0), acc_iter, abort_flag, q4, lane, et, 0, 0u, ring, fix))
+              a, g, tmem_base, accf_bar(0), acce_bar(0), acc_iter, abort_flag, q4, lane, et, 0, 0u, ring, fix, mask))
         break;
     }
   }

@@ -411,21 +411,29 @@ __device__ __noinline__ void arrive_split_tile_det(const TcArgs& a, const Group&
 // Otherwise each thread stores its own values directly.
 // The group's accumulator as NACC partial accumulators (one per MMA issuer,
 // ST columns apart, added in index order): N columns from taddr of each.
+// Only those whose bit is set in `mask` hold this group's sums (an issuer
+// with no MMA in the group leaves its accumulator untouched); all are read.
 template <int N, int NACC, int ST>
-__device__ __forceinline__ void ld_acc(uint32_t taddr, uint32_t (&v)[N]) {
+__device__ __forceinline__ void ld_acc(uint32_t taddr, uint32_t (&v)[N], uint32_t mask = (1u << NACC) - 1u) {
   static_assert(N == 16 || N == 32, "tcgen05.ld shapes used here");
   if constexpr (N == 32) tc_ld_32x32b_x32(taddr, v); else tc_ld_32x32b_x16(taddr, v);
   if constexpr (NACC > 1) {
+    const bool v0 = mask & 1u;
     uint32_t w[NACC - 1][N];
 #pragma unroll
     for (int i = 1; i < NACC; ++i) {
       if constexpr (N == 32) tc_ld_32x32b_x32(taddr + i * ST, w[i - 1]); else tc_ld_32x32b_x16(taddr + i * ST, w[i - 1]);
     }
     tc_wait_ld();
+    if (!v0) {
+#pragma unroll
+      for (int j = 0; j < N; ++j) v[j] = 0u;  // +0.0f: adding the valid ones to it is exact
+    }
 #pragma unroll
     for (int i = 1; i < NACC; ++i)
+      if ((mask >> i) & 1u)
 #pragma unroll
-      for (int j = 0; j < N; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(w[i - 1][j]));
+        for (int j = 0; j < N; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(w[i - 1][j]));
   } else {
     tc_wait_ld();
   }
@@ -441,7 +449,7 @@ template <int BN, int CH, bool PAIR = false, int NACC = 1, class Fix = NoFix>
 __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, uint32_t tmem_base, uint32_t accf_bar0,
                                                uint32_t acce_bar0, int& acc_iter, volatile int* abort_flag, int q4,
                                                int lane, int et, int half, uint32_t stage_smem, int& ring,
-                                               const Fix& fix = Fix()) {
+                                               const Fix& fix = Fix(), uint32_t nacc_mask = (1u << NACC) - 1u) {
   const int row = q4 * 32 + lane;  // accumulator row (TMEM lane)
   int32_t tp, tq, m0, m1, n0, n1;
   tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
@@ -473,7 +481,7 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += EPI_BOX) {
         uint32_t v[EPI_BOX];
-        ld_acc<EPI_BOX, NACC, BN>(t_row + c0, v);
+        ld_acc<EPI_BOX, NACC, BN>(t_row + c0, v, nacc_mask);
         fix(c0, v);
         const int32_t ybox = m0 + c0;
         if (xbox >= n1 || ybox >= m1) continue;  // block wholly outside C (warp-uniform)
@@ -514,7 +522,7 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += EPI_BOX) {
         uint32_t v[EPI_BOX];
-        ld_acc<EPI_BOX, NACC, BN>(t_row + c0, v);
+        ld_acc<EPI_BOX, NACC, BN>(t_row + c0, v, nacc_mask);
         fix(c0, v);
         const int32_t xbox = n0 + c0;
         if (ybox >= m1 || xbox >= n1) continue;  // block wholly outside C (warp-uniform)
@@ -562,7 +570,7 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
 #pragma unroll 1
     for (int c0 = 0; c0 < (staged ? 0 : BN); c0 += CH) {
       uint32_t v[CH];
-      ld_acc<CH, NACC, BN>(t_row + c0, v);
+      ld_acc<CH, NACC, BN>(t_row + c0, v, nacc_mask);
       fix(c0, v);
       if (det_slot) {
         // the run's fp32 partial into its slot (every row; the conversion clips)
