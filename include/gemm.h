@@ -90,6 +90,8 @@ typedef struct {
   int32_t kernel;      /* 0 = tensor-core any-layout, 1 = int4 dequant,
                           2 = tensor-core any-layout on CTA pairs (256 x 256 tiles) */
   int32_t streamk_tiles; /* tiles of the stream-K tail (0 = none), see gemm_create */
+  int32_t cluster_size;  /* > 1: each tile's split-K runs are the CTAs of one cluster of this size and
+                            their fp32 partials are added in shared memory (0 = split-K through the workspace) */
 } gemm_info_t;
 
 typedef struct gemm_plan gemm_plan_t;
@@ -103,6 +105,15 @@ typedef struct gemm_plan gemm_plan_t;
  * split-K partials are (so those tiles' rounding order depends on timing).
  * The workspace then holds an M x N fp32 region.  GEMM_FLAG_DETERMINISTIC
  * turns it off; gemm_info_t.streamk_tiles reports it.
+ *
+ * Split-K in a cluster.  For a skinny problem (M <= 64, run as C^T) with a
+ * split factor above 1 whose tiles are few, when c CTAs per tile (c in 8, 4,
+ * 2, dividing the factor) still cover at least 3/4 of the SMs and the
+ * device can hold the clusters at once, each tile's K range is split over
+ * the c CTAs of one cluster and their fp32 partials are added in shared
+ * memory, in a fixed order (results are then reproducible run to run); the
+ * workspace is not used.  gemm_info_t.cluster_size reports it.  Chosen only
+ * with a device (num_sms given and no device: never).
  *
  * Needs a CUDA device only when desc->num_sms == 0 (to count its SMs); the
  * plan's kernels run on the device current at gemm_create.  The plan is

@@ -262,6 +262,7 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
   args.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (plan->ldc % 8 == 0);
   args.ws_vec = (d.N % 4 == 0);
   args.pair = plan->pair;
+  args.cl_size = plan->cl_size;
   // Staged epilogue: whole-line bulk stores of C and bulk reductions of the
   // fp32 partials, where the pointers and pitches allow them (16 bytes).
   if (env_int("LGT_GEMM_TMA_EPI", 1) != 0) {
@@ -499,6 +500,34 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   p.a_pack_ld = align_up(static_cast<size_t>(p.a_row_elems), 8);
   p.b_pack_ld = align_up(static_cast<size_t>(p.b_row_elems), 8);
 
+  // Split-K through a cluster's shared memory: when the tiles are few (a
+  // skinny, swapped problem, BN <= 64) and a cluster of c CTAs per tile still
+  // covers at least 3/4 of the SMs, each tile's K range is split over the c
+  // CTAs of one cluster (c divides the split factor, so CTA b's contiguous
+  // unit range is exactly split / c units of tile b / c) and their partials
+  // are added on chip: no fp32 partial through L2, no counter, no fixup
+  // pass.  Needs a device (the cluster occupancy query).  LGT_GEMM_CLUSTER=0
+  // turns it off.
+  p.cl_size = 0;
+  if (!int4 && !p.pair && p.swap && !p.det && p.split > 1 && p.tail_tiles == 0 && p.bn <= 64 && p.device >= 0 &&
+      env_int("LGT_GEMM_CLUSTER", 1) != 0) {
+    for (int c : {8, 4, 2}) {
+      if (c > p.bn / 4 || p.split % c != 0) continue;
+      const int64_t g = tiles * c;
+      if (g > p.sms_grid || g * 4 < static_cast<int64_t>(p.sms_grid) * 3) continue;
+      int resident = 0;
+      if (lgt::tc_gemm_max_clusters(p.bn, c, &resident) != cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
+      if (resident < tiles) continue;
+      p.cl_size = c;
+      p.grid = static_cast<int>(g);
+      p.fin_tiles = 0;
+      break;
+    }
+  }
+
   if (p.det) {
     // Deterministic split-K: the tiles' runs (one per worker a tile's units
     // meet) each own a tile-shaped fp32 slot; max_runs is the most runs of
@@ -580,6 +609,7 @@ gemm_status_t gemm_query(const gemm_plan_t* plan, gemm_info_t* info) {
   info->num_units = plan->num_units;
   info->k_per_split = static_cast<int32_t>(ceil_div(plan->kb_total, plan->split_req) * kBlockK);
   info->streamk_tiles = plan->tail_tiles;
+  info->cluster_size = plan->cl_size;
   info->repack_a = plan->repack_a;
   info->repack_b = plan->repack_b;
   info->kernel = plan->kernel == 0 && plan->pair ? 2 : plan->kernel;

@@ -56,9 +56,9 @@ struct Cfg {
                                         : (2 * BN) <= 256 ? 256 : 512;
   static constexpr int CH = BN < 32 ? BN : 32;          // accumulator columns per tcgen05.ld
   static constexpr uint32_t EPI_OFF = STAGES * STAGE_BYTES;  // 1024-aligned (stages are 2 KiB multiples)
-  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], teardown
+  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], teardown, cluster ready / done
   static constexpr uint32_t BAR_OFF = EPI_OFF + EPI_STAGING_BYTES;
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 7;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_USED = MISC_OFF + 64;
   static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 + b); };
   const uint32_t teardown_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  const uint32_t cl_bar0 = bar0 + 8u * (2 * C::STAGES + 5);  // cluster split-K: ready, done
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
   volatile int* consumed_slot = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 12);
@@ -98,6 +99,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       mbar_init(acce_bar(b), kEpiThreads / 32);
     }
     mbar_init(teardown_bar, 1);
+    const uint32_t peers = a.cl_size > 1 ? static_cast<uint32_t>(a.cl_size - 1) : 1u;
+    mbar_init(cl_bar0, peers);
+    mbar_init(cl_bar0 + 8u, peers);
     *abort_flag = 0;
     *consumed_slot = 0;
     fence_barrier_init();
@@ -112,6 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the peers' barriers are initialised before anyone arrives on them remotely
+  if (a.cl_size > 1) cluster_sync_all();
   const uint32_t tmem_base = *tmem_slot;
   // operands, C and the split-K workspace may be written by the previous kernel
   pdl_wait();
@@ -231,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const uint32_t stage_smem = base + C::EPI_OFF + static_cast<uint32_t>(warp - kEpiWarp0) * 8192u;
     while (sched.next(a, g)) {
       if (!epilogue_group<BN, C::CH>(a, g, tmem_base, accf_bar(0), acce_bar(0), acc_iter, abort_flag, q4, lane, et,
-                                     0, stage_smem, ring))
+                                     0, stage_smem, ring, NoFix(), 1u, cl_bar0, base + C::EPI_OFF))
         break;
     }
     if (lane == 0) bulk_wait_group<0>();  // staged stores finished before the CTA exits
@@ -268,7 +274,29 @@ cudaError_t launch_bn(const TcArgs& args, int grid, cudaStream_t stream) {
   // CTAs that convert split tiles wait for other CTAs' partial sums; they
   // start waiting only after pdl_wait (the previous kernel has left every
   // SM), and the grid never exceeds the CTAs the device holds at once.
+  if (args.cl_size > 1)
+    return launch_pdl_cluster(tc_gemm_kernel<BN>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), C::SMEM_ALLOC,
+                              stream, static_cast<unsigned>(args.cl_size), args);
   return launch_pdl(tc_gemm_kernel<BN>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), C::SMEM_ALLOC, stream, args);
+}
+
+template <int BN>
+cudaError_t max_clusters_bn(int cluster, int* clusters) {
+  using C = Cfg<BN>;
+  cudaError_t e = set_smem_once<tc_gemm_kernel<BN>>(static_cast<int>(C::SMEM_ALLOC));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(clusters, tc_gemm_kernel<BN>, &cfg);
 }
 
 }  // namespace
@@ -282,6 +310,16 @@ size_t tc_gemm_smem_bytes(int bn) {
     case 192: return Cfg<192>::SMEM_ALLOC;
     case 256: return Cfg<256>::SMEM_ALLOC;
     default: return 0;
+  }
+}
+
+cudaError_t tc_gemm_max_clusters(int bn, int cluster, int* clusters) {
+  *clusters = 0;
+  switch (bn) {
+    case 16: return max_clusters_bn<16>(cluster, clusters);
+    case 32: return max_clusters_bn<32>(cluster, clusters);
+    case 64: return max_clusters_bn<64>(cluster, clusters);
+    default: return cudaSuccess;
   }
 }
 

@@ -50,6 +50,31 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// launch_pdl, as a grid of clusters of `cluster` CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                               unsigned cluster, Args&&... args) {
+  static const bool pdl = [] {
+    const char* v = std::getenv("LGT_GEMM_PDL");
+    return !(v && v[0] == '0');
+  }();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // MMA tile: 128 rows on the P side (the operand whose rows map to TMEM
 // lanes), BN rows on the Q side, 64 elements of K per pipeline stage.
 constexpr int TILE_P = 128;
@@ -111,6 +136,8 @@ struct TcArgs {
   int32_t pair;          // 1: CTA-pair kernel, 256-row P tiles split over the pair
   int32_t tma_c;         // full tiles leave through shared memory and bulk tile stores
   int32_t tma_ws;        // partial tiles leave through shared memory and bulk reductions
+  int32_t cl_size;       // > 1: the split-K runs of a tile are the CTAs of one cluster of this size,
+                         // reduced through distributed shared memory (single-CTA kernel, swapped, BN <= 64)
   uint32_t idesc;
 };
 
@@ -144,6 +171,9 @@ cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K,
 // Returns a cudaError_t; `bn` selects the kernel instance.
 cudaError_t launch_tc_gemm(const TcArgs& args, int bn, int grid, cudaStream_t stream);
 size_t tc_gemm_smem_bytes(int bn);
+// Clusters of `cluster` CTAs of the single-CTA kernel (tile width bn <= 64)
+// that can be resident at once on the current device (0 if none).
+cudaError_t tc_gemm_max_clusters(int bn, int cluster, int* clusters);
 
 // CTA-pair kernel (clusters of two CTAs, one cta_group::2 MMA per pair):
 // tiles of 256 P rows x `bn` Q rows; `grid` CTAs (even).  args.pair must be 1.

@@ -26,6 +26,7 @@ struct gemm_plan {
   int rr_tiles;      // tiles dealt whole before the contiguous unit ranges
   int tail_tiles;    // stream-K tail: tiles whose K blocks are spread over all workers
   int fin_tiles;     // split tiles converted by the fixup warps of all CTAs (the tail, or all tiles when split > 1)
+  int cl_size;       // > 1: each tile's split-K runs are one cluster of this many CTAs, reduced on chip
   int det;           // deterministic split-K: per-run partial slots summed in run order
   int max_runs;      // slots per strip (det)
   int tiles_p, tiles_q, num_units;

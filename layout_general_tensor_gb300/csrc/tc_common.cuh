@@ -439,6 +439,135 @@ __device__ __forceinline__ void ld_acc(uint32_t taddr, uint32_t (&v)[N], uint32_
   }
 }
 
+// Split-K within a cluster (a.cl_size > 1; single-CTA kernel, swapped
+// tiles, BN <= 64): the cluster's CTAs are the K-split runs of one tile, in
+// rank order, and CTA q finishes C rows [q W, (q + 1) W), W = BN / cl, of the
+// tile (accumulator columns; TMEM lanes are the tile's C columns n).  Each
+// CTA reads its fp32 partial from TMEM and stores the W columns that CTA q
+// finishes straight into q's epilogue staging buffer (its own included),
+// slot = the sender's rank: row r of slot p at p * 128 * 4W + r * 4W bytes.
+// Then it arrives once on every peer's `ready` mbarrier (count cl - 1,
+// release at cluster scope, after the stores), waits on its own, and sums
+// its slots in rank order (so the result does not depend on timing),
+// converts and stores its rows of C.  Nothing is read remotely, no fp32
+// partial goes through L2 and no counter is polled: the IREE page's
+// partials -> shared storage -> second reduction, with the cluster's shared
+// memory as the storage.  No peer touches a CTA's shared memory after
+// arriving on its `ready`, so a CTA may leave as soon as its own `ready`
+// completes.  A run without K blocks sends zeros.  Returns false when the
+// CTA is aborting (all 128 threads agree).
+template <int BN, int CL>
+__device__ __forceinline__ void cluster_push_partial(const uint32_t (&v)[BN], uint32_t stage0, int row) {
+  constexpr int W = BN / CL;
+  static_assert(W >= 4 && W % 4 == 0, "whole 16-byte chunks per rank");
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t mine = stage0 + rank * static_cast<uint32_t>(TILE_P * 4 * W) + static_cast<uint32_t>(row * 4 * W);
+#pragma unroll
+  for (int q = 0; q < CL; ++q) {
+    const uint32_t dst = mapa_shared(mine, static_cast<uint32_t>(q));
+#pragma unroll
+    for (int c = 0; c < W; c += 4)
+      st_shared_cluster_v4(dst + 4u * c, v[q * W + c], v[q * W + c + 1], v[q * W + c + 2], v[q * W + c + 3]);
+  }
+}
+
+template <int BN, int CL>
+__device__ __forceinline__ void cluster_sum_store(const TcArgs& a, uint32_t stage0, int row, int m0, int m1, int n,
+                                                  int n1) {
+  constexpr int W = BN / CL;
+  if (n >= n1) return;
+  const uint32_t rank = cluster_ctarank();
+  float s[W];
+#pragma unroll
+  for (int j = 0; j < W; ++j) s[j] = 0.0f;
+#pragma unroll
+  for (int p = 0; p < CL; ++p) {
+    const uint32_t src = stage0 + static_cast<uint32_t>(p * TILE_P * 4 * W + row * 4 * W);
+#pragma unroll
+    for (int c = 0; c < W; c += 4) {
+      const float4 t = ld_shared_f32x4(src + 4u * c);
+      s[c] += t.x;
+      s[c + 1] += t.y;
+      s[c + 2] += t.z;
+      s[c + 3] += t.w;
+    }
+  }
+  uint16_t* cb = reinterpret_cast<uint16_t*>(a.c);
+#pragma unroll
+  for (int j = 0; j < W; ++j) {
+    const int m = m0 + static_cast<int>(rank) * W + j;
+    if (m < m1) cb[static_cast<int64_t>(m) * a.ldc + n] = cvt1(s[j], a.c_bf16);
+  }
+}
+
+template <int BN>
+__device__ __noinline__ bool cluster_split_tile(const TcArgs& a, const Group& g, uint32_t tmem_base,
+                                                uint32_t accf_bar0, uint32_t acce_bar0, int& acc_iter,
+                                                volatile int* abort_flag, int q4, int lane, int et,
+                                                uint32_t stage0, uint32_t cl_bar0, int m0, int m1, int n0, int n1) {
+  static_assert(BN <= 64, "128 rows of BN fp32 fit the 32 KiB of epilogue staging");
+  const int row = q4 * 32 + lane;
+  const uint32_t cl = static_cast<uint32_t>(a.cl_size), rank = cluster_ctarank();
+  uint32_t v[BN];
+#pragma unroll
+  for (int j = 0; j < BN; ++j) v[j] = 0u;  // +0.0f: a run without K blocks sends zeros
+  bool ok = true;
+  if (g.nkb > 0) {
+    const int buf = acc_iter & 1;
+    const bool got = mbar_wait_bounded(accf_bar0 + 8u * buf, (acc_iter >> 1) & 1, a.wait_limit_ns, abort_flag);
+    if (!got && !*abort_flag) record_timeout(a, abort_flag, 2 * 16 + 2);
+    ok = !named_bar_or(1, kEpiThreads, !got);
+    if (ok) {
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(buf * BN);
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t t[16];
+        tc_ld_32x32b_x16(t_row + c0, t);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[c0 + j] = t[j];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar0 + 8u * buf);
+      ++acc_iter;
+    }
+  }
+  if (ok) {
+    // (the planner takes cl <= BN / 4)
+    if (cl == 2) {
+      cluster_push_partial<BN, 2>(v, stage0, row);
+    } else if (cl == 4) {
+      if constexpr (BN >= 16) cluster_push_partial<BN, 4>(v, stage0, row);
+    } else {
+      if constexpr (BN >= 32) cluster_push_partial<BN, 8>(v, stage0, row);
+    }
+    fence_acq_rel_cluster();
+  }
+  named_bar_sync(1, kEpiThreads);  // every thread's stores are issued (and fenced)
+  const uint32_t ready = cl_bar0;
+  if (et == 0 && ok)
+    for (uint32_t p = 0; p < cl; ++p)
+      if (p != rank) mbar_arrive_cluster(mapa_shared(ready, p));
+  // wait for the peers' slices even on the abort path: none may write into
+  // this CTA's shared memory after it has left
+  const bool got = mbar_wait_bounded_cluster(ready, 0, a.wait_limit_ns, abort_flag);
+  if (!got && !*abort_flag) record_timeout(a, abort_flag, 2 * 16 + 6);
+  ok = !named_bar_or(1, kEpiThreads, !got || !ok);
+  if (ok) {
+    const int n = n0 + row;
+    if (cl == 2) {
+      cluster_sum_store<BN, 2>(a, stage0, row, m0, m1, n, n1);
+    } else if (cl == 4) {
+      if constexpr (BN >= 16) cluster_sum_store<BN, 4>(a, stage0, row, m0, m1, n, n1);
+    } else {
+      if constexpr (BN >= 32) cluster_sum_store<BN, 8>(a, stage0, row, m0, m1, n, n1);
+    }
+  }
+  return ok;
+}
+
 // No change to the accumulator values.
 struct NoFix {
   template <int N>
@@ -449,12 +578,18 @@ template <int BN, int CH, bool PAIR = false, int NACC = 1, class Fix = NoFix>
 __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, uint32_t tmem_base, uint32_t accf_bar0,
                                                uint32_t acce_bar0, int& acc_iter, volatile int* abort_flag, int q4,
                                                int lane, int et, int half, uint32_t stage_smem, int& ring,
-                                               const Fix& fix = Fix(), uint32_t nacc_mask = (1u << NACC) - 1u) {
+                                               const Fix& fix = Fix(), uint32_t nacc_mask = (1u << NACC) - 1u,
+                                               uint32_t cl_bar0 = 0u, uint32_t cl_stage0 = 0u) {
   const int row = q4 * 32 + lane;  // accumulator row (TMEM lane)
   int32_t tp, tq, m0, m1, n0, n1;
   tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
   if (PAIR) narrow_to_half(a, half, m0, m1, n0, n1);
   const bool full_tile = (g.s0 == 0 && g.s1 == a.split);
+  if constexpr (!PAIR && NACC == 1 && BN <= 64) {
+    if (a.cl_size > 1 && !full_tile)
+      return cluster_split_tile<BN>(a, g, tmem_base, accf_bar0, acce_bar0, acc_iter, abort_flag, q4, lane, et,
+                                    cl_stage0, cl_bar0, m0, m1, n0, n1);
+  }
   const int cidx = PAIR ? 2 * g.tile + half : g.tile;
   // deterministic split-K: this run's slot (tile-shaped, rows = C rows)
   float* det_slot = nullptr;
