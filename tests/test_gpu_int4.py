@@ -62,10 +62,10 @@ def test_int4_group_sizes(group):
 @pytest.mark.parametrize("N,Kd,group,split", [(384, 8192, 64, 3), (300, 4096, 128, 5), (256, 16384, 512, 0),
                                                 (640, 2048, 64, 7)])
 def test_int4_scale_windows(N, Kd, group, split):
-    """Scales copied by TMA in windows of 8 groups of a tile's rows: runs
-    that start and end inside a window, several runs per CTA (split 7 over
-    5 tiles), rows beyond N (zero-filled window rows), group 64 (a window
-    every two stages) and 512 (a window every eight)."""
+    """Scales read in windows of 8 groups (16 bytes) of a row, copied ahead
+    into shared memory: runs that start and end inside a window, short runs
+    (split 7 over 5 tiles: one unit of 5 K blocks per CTA), rows beyond N,
+    group 64 (a window every two stages) and 512 (a window every eight)."""
     case = _case(16, N, Kd, group=group, split=split)
     inp = wl.make_inputs(case, seed=N + group)
     c, g, _ = run_case(case, inp, reps=2)
@@ -75,7 +75,7 @@ def test_int4_scale_windows(N, Kd, group, split):
 
 def test_int4_unaligned_scale_rows():
     """A scale array that does not start on a 16-byte boundary cannot be
-    copied by TMA: the per-K-block load path gives the same result."""
+    read 16 bytes at a time: the per-K-block load path gives the same result."""
     case = _case(16, 384, 2048, group=64, split=2)
     inp = wl.make_inputs(case, seed=21)
     ref = oracle_full(case, inp)
