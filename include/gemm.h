@@ -112,7 +112,8 @@ typedef struct gemm_plan gemm_plan_t;
  * device can hold the clusters at once, each tile's K range is split over
  * the c CTAs of one cluster and their fp32 partials are added in shared
  * memory, in a fixed order (results are then reproducible run to run); the
- * workspace is not used.  gemm_info_t.cluster_size reports it.  Chosen only
+ * workspace then holds no split-K region (gemm_workspace_size is 0 unless an
+ * operand is repacked).  gemm_info_t.cluster_size reports it.  Chosen only
  * with a device (num_sms given and no device: never).
  *
  * Needs a CUDA device only when desc->num_sms == 0 (to count its SMs); the

@@ -548,7 +548,8 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
     }
   }
   size_t off = 0;
-  if (p.split > 1) {
+  // (split-K in a cluster adds its partials in shared memory: no region)
+  if (p.split > 1 && p.cl_size <= 1) {
     p.off_partial = off;
     const size_t region = p.det ? static_cast<size_t>(tiles) * (1 + p.pair) * p.max_runs * lgt::TILE_P * p.bn *
                                       sizeof(float)
@@ -674,8 +675,9 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     ldb = plan->b_pack_ld;
   }
 
-  float* partial = plan->split > 1 ? reinterpret_cast<float*>(ws + plan->off_partial) : nullptr;
-  int32_t* counters = plan->split > 1 ? reinterpret_cast<int32_t*>(ws + plan->off_counters) : nullptr;
+  const bool split_region = plan->split > 1 && plan->cl_size <= 1;
+  float* partial = split_region ? reinterpret_cast<float*>(ws + plan->off_partial) : nullptr;
+  int32_t* counters = split_region ? reinterpret_cast<int32_t*>(ws + plan->off_counters) : nullptr;
   if (!int4) return lgt::launch_dense(plan, a_eff, lda, b_eff, ldb, C, partial, counters, stream);
 
   lgt::TcArgs args;

@@ -84,20 +84,22 @@ extern "C" gemm_status_t gemm_run_static_scratch(const gemm_plan_t* plan, const 
       align256(static_cast<size_t>(plan->num_counters) * sizeof(int32_t)) + static_cast<size_t>(d.M) * d.N * 4 >
           kStaticScratchBytes)
     plan = &no_tail;
+  // (split-K in a cluster adds its partials in shared memory: no region)
+  const bool split_region = plan->split > 1 && plan->cl_size <= 1;
   const size_t counters_bytes =
-      plan->split > 1 ? align256(static_cast<size_t>(plan->num_counters) * sizeof(int32_t)) : 0;
-  const size_t partial_bytes = plan->split > 1 ? static_cast<size_t>(d.M) * d.N * sizeof(float) : 0;
+      split_region ? align256(static_cast<size_t>(plan->num_counters) * sizeof(int32_t)) : 0;
+  const size_t partial_bytes = split_region ? static_cast<size_t>(d.M) * d.N * sizeof(float) : 0;
   if (counters_bytes + partial_bytes > kStaticScratchBytes) return GEMM_ERR_WORKSPACE;
 
   uint8_t* scratch = static_cast<uint8_t*>(scratch_address(plan->device));
   if (!scratch) return GEMM_ERR_CUDA;
-  if (plan->split > 1) {
+  if (split_region) {
     // The array keeps whatever the previous call left; the counters and the
     // partial sums must start at zero.
     if (cudaMemsetAsync(scratch, 0, counters_bytes + partial_bytes, stream) != cudaSuccess) return GEMM_ERR_CUDA;
   }
 
-  float* partial = plan->split > 1 ? reinterpret_cast<float*>(scratch + counters_bytes) : nullptr;
-  int32_t* counters = plan->split > 1 ? reinterpret_cast<int32_t*>(scratch) : nullptr;
+  float* partial = split_region ? reinterpret_cast<float*>(scratch + counters_bytes) : nullptr;
+  int32_t* counters = split_region ? reinterpret_cast<int32_t*>(scratch) : nullptr;
   return lgt::launch_dense(plan, A, plan->lda, B, plan->ldb, C, partial, counters, stream);
 }

@@ -47,6 +47,8 @@ def test_cluster_split_matches_oracle_and_is_reproducible(case, want):
     cl = g.info.cluster_size
     if want is not None:
         assert cl == want, f"cluster size {cl}, expected {want}"
+    if cl > 1 and not (g.info.repack_a or g.info.repack_b):
+        assert g.ws_bytes == 0  # partials added in shared memory: no split-K region
     assert_close(c, oracle_full(case, inp), case.name)
     if cl > 1:
         c2, g2, _ = run_case(case, inp, num_sms=148, gemm=g)
