@@ -10,14 +10,15 @@ What it computes, and the passage each function follows:
   with the operand element addressed by explicit index arithmetic for each
   storage layout (K-contiguous or M/N-contiguous).  The operand cases are
   those of the Triton inThreadTranspose page ("Feature description": a dot
-  operand is either contiguous along K or not) and the GEMM definition of
-  the benchmark spec.  A library matmul is used as the summation step.
+  operand is either contiguous along K or not) and the plain definition of
+  a matrix product.  A library matmul is used as the summation step.
 * :func:`gemm_elements` -- the same sum for selected (m, n), one dot product
   per output, for full-size problems.
 * :func:`dequant_int4` -- ``w(k,n) = (q(n,k) - z(n,g)) * s(n,g)`` with
   ``g = k // group``; the BitBLAS TileLang page ("Relevant Issues" and the
-  dequantise copy example) is the setting, the formula is the task
-  statement's (per-128-group fp16 scale, zero 8).
+  dequantise copy example) is the setting; the pages give no formula, and
+  this is the plainest reading (per-group fp16 scale and zero point, groups
+  of 128 consecutive k by default, zero point 8 when none is given).
 * :func:`splitk_factor` -- the SM-waste split-K rule of the BitBLAS page
   (the "SplitK Infer for dequantize cases" snippet).
 * :func:`perm_forward` / :func:`perm_inverse` -- the perpendicular-dimension

@@ -1,5 +1,5 @@
 """GPU parity: the tensor-core GEMM through the C ABI against the fp64 CPU
-oracle, element by element.  Tolerances (from the problem statement):
+oracle, element by element.  Tolerances (the library's acceptance bound):
 |C_gpu - C_ref| <= 2e-2 (|C_ref| + 1) elementwise and relative Frobenius
 error <= 2e-3, with C_ref the unrounded fp64 sum."""
 import numpy as np
