@@ -165,7 +165,13 @@ def test_planner_skinny_and_irregular_factors(lib):
     # the SM-waste rule's values at 148 SMs for the skinny bf16 and int4-shaped problems
     desc = lib.make_desc(64, 4096, 16384, split_k=0, num_sms=148)
     h = lib.gemm_create(desc)
-    assert lib.gemm_query(h).split_k == 128
+    info = lib.gemm_query(h)
+    assert info.split_k == 128
+    import torch
+    if not torch.cuda.is_available():
+        # split-K inside clusters needs the device's cluster occupancy: never without one
+        assert info.cluster_size == 0
+        assert lib.gemm_workspace_size(h) >= 64 * 4096 * 4
     lib.gemm_destroy(h)
     desc = lib.make_desc(4095, 3000, 2880, wl.MN_CONTIG, wl.MN_CONTIG, split_k=0, num_sms=160)
     h = lib.gemm_create(desc)
