@@ -573,7 +573,10 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
     // per-group sums follow the split-K region
     p.off_aprep = off;
     p.off_agsum = align_up(off + static_cast<size_t>(d.M) * d.K * 2, 256);
-    p.ws_bytes = align_up(p.off_agsum + static_cast<size_t>(d.M) * (d.K / p.group) * sizeof(float), 256);
+    // group sums and offset sums of the activation, fp32 [groups][M] each,
+    // then (per-group accumulator form) the per-row term, fp32 [N][16]
+    p.off_corr = align_up(p.off_agsum + 2 * static_cast<size_t>(d.M) * (d.K / p.group) * sizeof(float), 256);
+    p.ws_bytes = align_up(p.off_corr + (p.bn == 16 ? static_cast<size_t>(d.N) * 16 * sizeof(float) : 0), 256);
     p.ws_bytes_misaligned = p.ws_bytes;
   }
 
@@ -683,14 +686,33 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   lgt::TcArgs args;
   std::memset(&args, 0, sizeof(args));
   const float* args_agsum = nullptr;
+  const float* args_ogsum = nullptr;
+  // Per-group accumulators (the int4 kernel's form for one activation tile of
+  // at most 16 rows, group 128 with splits of whole groups, at most 128
+  // groups, K-contiguous activation and scale rows readable 16 bytes at a
+  // time).  Opt-in with LGT_GEMM_INT4_V2=1: its GEMM kernel is faster than
+  // the per-weight form, but with the separate kernel that forms its
+  // zero-point and offset term the whole path is still slower.
+  const bool v2 = plan->bn == 16 && plan->group == 128 && plan->kb_per_split % 2 == 0 && !plan->a_mn &&
+                  lgt::int4_prep_fused(plan->a_mn, static_cast<int>(d.K), static_cast<int>(plan->group)) &&
+                  (d.K / plan->group) % 8 == 0 && d.K / plan->group <= 128 && reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
+                  reinterpret_cast<uintptr_t>(zeros) % 16 == 0 && env_int("LGT_GEMM_INT4_V2", 0) != 0;
   {
     // prepared activation: K-block-major, in the workspace
     void* ap = ws + plan->off_aprep;
     float* agsum = reinterpret_cast<float*>(ws + plan->off_agsum);
+    float* ogsum = agsum + static_cast<size_t>(d.M) * (d.K / plan->group);
     if (lgt::launch_int4_prep(A, plan->lda, plan->a_mn, static_cast<int>(d.M), static_cast<int>(d.K),
-                              static_cast<int>(plan->group), ap, agsum, plan->sms_grid, stream) != cudaSuccess)
+                              static_cast<int>(plan->group), ap, agsum, v2 ? ogsum : nullptr, plan->sms_grid,
+                              stream) != cudaSuccess)
       return GEMM_ERR_CUDA;
     args_agsum = agsum;
+    args_ogsum = v2 ? ogsum : nullptr;
+    if (v2 && lgt::launch_int4_corr(static_cast<const uint16_t*>(scales), static_cast<const uint16_t*>(zeros), agsum,
+                                    ogsum, static_cast<int>(d.N), static_cast<int>(d.M),
+                                    static_cast<int>(d.K / plan->group),
+                                    reinterpret_cast<float*>(ws + plan->off_corr), stream) != cudaSuccess)
+      return GEMM_ERR_CUDA;
     if (!lgt::encode_int4_activation(&args.tm_q, ap, d.M, d.K, plan->bn, d.K / 64 < 4 ? static_cast<int>(d.K / 64) : 4))
       return GEMM_ERR_CUDA;
   }
@@ -735,6 +757,9 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     a4.x_box_kb = d.K / 64 < 4 ? static_cast<int32_t>(d.K / 64) : 4;
     a4.vec_sz = (a4.groups % 8 == 0) && reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
                 reinterpret_cast<uintptr_t>(zeros) % 16 == 0;
+    a4.ogsum = args_ogsum;
+    a4.corr = v2 ? reinterpret_cast<const float*>(ws + plan->off_corr) : nullptr;
+    a4.v2 = v2 ? 1 : 0;
     return lgt::launch_int4_gemm(a4, plan->bn, plan->grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
 }

@@ -39,7 +39,8 @@ struct gemm_plan {
   size_t off_partial, off_counters, off_pack_a, off_pack_b, ws_bytes;
   size_t ws_bytes_misaligned;
   size_t off_aprep;  // int4: the prepared activation
-  size_t off_agsum;  // int4: per-group sums of the activation, fp32 [groups][M]
+  size_t off_agsum;  // int4: per-group sums of the activation, fp32 [groups][M], then the offset sums
+  size_t off_corr;   // int4, tile width 16: the per-row term of the per-group accumulator form, fp32 [N][16]
   lgt::DeviceStatus* d_status;
   uint64_t wait_limit_ns;
 };
