@@ -68,7 +68,7 @@ typedef struct {
   int32_t split_k;            /* 0 = SM-waste rule; >= 1 explicit factor */
   int32_t group_size;         /* int4 quantisation group along K (0 = 128); must divide K and the split length */
   int32_t num_sms;            /* SM count the split-K rule uses: 0 = the current device's */
-  int32_t flags;              /* 0 or GEMM_FLAG_DETERMINISTIC */
+  int32_t flags;              /* 0, GEMM_FLAG_DETERMINISTIC, or GEMM_FLAG_TEST_WITHHOLD_STAGE (test aid) */
 } gemm_desc_t;
 
 /* Bitwise-reproducible results.  No stream-K tail (below); with a split-K
@@ -78,6 +78,18 @@ typedef struct {
  * instead of an M x N region.  gemm_run_static_scratch does not support
  * this mode with a split factor above 1 (GEMM_ERR_UNSUPPORTED). */
 #define GEMM_FLAG_DETERMINISTIC 1
+
+/* Test aid for the failure path (not for production use).  The plan's first
+ * gemm_run withholds the first pipeline stage of one CTA: no copy is issued
+ * for it, so the MMA issuer's bounded wait on it runs out, the kernel records
+ * GEMM_ERR_TIMEOUT (read by gemm_sync_status) and that CTA's tile of C is
+ * left unwritten; every later run of the plan is normal.  Every copy that was
+ * issued still lands before the CTA exits.  Accepted only where the plan uses
+ * the single-CTA tensor-core kernel with whole tiles (no split-K, no stream-K
+ * tail, no cluster, no CTA pair; gemm_create returns GEMM_ERR_UNSUPPORTED
+ * otherwise), so that no other CTA waits on the withheld one.  The wait limit
+ * is the plan's (LGT_GEMM_WAIT_LIMIT_MS at gemm_create, 2 s by default). */
+#define GEMM_FLAG_TEST_WITHHOLD_STAGE (1 << 30)
 
 /* What a plan decided. */
 typedef struct {
@@ -183,6 +195,17 @@ int32_t gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int32_t block_m, int32
  * invalid stride map indices to themselves).  Host computation. */
 uint32_t gemm_perm_fwd(uint32_t index, uint32_t count, uint32_t block, uint32_t stride);
 uint32_t gemm_perm_inv(uint32_t index, uint32_t count, uint32_t block, uint32_t stride);
+
+/* The same permutation computed on the device by the routine the kernels'
+ * loaders use: out[j] = gemm_perm_fwd(in[j], count, block, stride) (inverse
+ * == 0) or gemm_perm_inv(...) (inverse != 0) for j < n.  `in` and `out` are
+ * device arrays of n uint32 owned by the caller (they may be the same array);
+ * the call is asynchronous on `stream` (a cudaStream_t).  Returns
+ * GEMM_ERR_INVALID_ARG for a NULL array with n > 0, GEMM_ERR_CUDA if the
+ * launch fails.  Same rules as the host functions: `stride` must divide
+ * `block`, a trailing partial block and an invalid stride map to themselves. */
+gemm_status_t gemm_perm_device(const uint32_t* in, size_t n, uint32_t count, uint32_t block, uint32_t stride,
+                               int32_t inverse, uint32_t* out, void* stream);
 
 /* Magic-number division by a divisor fixed in advance (hipBLASLt DTL page,
  * "Add support for generalized NLC=1": static divisors use a magic multiply).

@@ -23,6 +23,7 @@ GEMM_ERR_CUDA = 5
 GEMM_ERR_TIMEOUT = 6
 
 GEMM_FLAG_DETERMINISTIC = 1
+GEMM_FLAG_TEST_WITHHOLD_STAGE = 1 << 30
 
 GEMM_K_CONTIG = 0
 GEMM_MN_CONTIG = 1
@@ -36,7 +37,7 @@ GEMM_F32 = 3
 EXPORTS = (
     "gemm_create", "gemm_workspace_size", "gemm_query", "gemm_run", "gemm_run_static_scratch",
     "gemm_sync_status", "gemm_destroy",
-    "gemm_splitk_auto", "gemm_perm_fwd", "gemm_perm_inv", "gemm_magic_divmod_host",
+    "gemm_splitk_auto", "gemm_perm_fwd", "gemm_perm_inv", "gemm_perm_device", "gemm_magic_divmod_host",
     "gemm_magic_divmod_device", "gemm_status_string",
     "reduce_rows_workspace_size", "reduce_rows_f32",
 )
@@ -81,6 +82,8 @@ def _load():
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_double]),
         "gemm_perm_fwd": (ctypes.c_uint32, [ctypes.c_uint32] * 4),
         "gemm_perm_inv": (ctypes.c_uint32, [ctypes.c_uint32] * 4),
+        "gemm_perm_device": (ctypes.c_int, [P, ctypes.c_size_t, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                                            ctypes.c_int32, P, P]),
         "gemm_magic_divmod_host": (ctypes.c_int, [P, ctypes.c_size_t, ctypes.c_uint32, P, P]),
         "gemm_magic_divmod_device": (ctypes.c_int, [P, ctypes.c_size_t, ctypes.c_uint32, P, P, P]),
         "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -173,6 +176,12 @@ def gemm_perm_fwd(index, count, block, stride) -> int:
 
 def gemm_perm_inv(index, count, block, stride) -> int:
     return _lib.gemm_perm_inv(index, count, block, stride)
+
+
+def gemm_perm_device(in_ptr, n, count, block, stride, inverse, out_ptr, stream=0) -> int:
+    """Raw entry point: device addresses of uint32 arrays; returns the status."""
+    return _lib.gemm_perm_device(in_ptr or None, n, count, block, stride, int(inverse), out_ptr or None,
+                                 stream or None)
 
 
 def gemm_magic_divmod_host(n_array, divisor):

@@ -59,7 +59,7 @@ gemm_status_t validate(const gemm_desc_t& d) {
     return GEMM_ERR_INVALID_ARG;
   }
   if (d.split_k < 0 || d.split_k > 65536 || d.num_sms < 0 || d.group_size < 0 ||
-      (d.flags & ~GEMM_FLAG_DETERMINISTIC) != 0)
+      (d.flags & ~(GEMM_FLAG_DETERMINISTIC | GEMM_FLAG_TEST_WITHHOLD_STAGE)) != 0)
     return GEMM_ERR_INVALID_ARG;
   if (d.lda < 0 || d.ldb < 0 || d.ldc < 0) return GEMM_ERR_INVALID_ARG;
   const int64_t a_min = d.a_layout == GEMM_K_CONTIG ? d.K : d.M;
@@ -162,7 +162,8 @@ bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major,
 
 // Output-side maps for the staged epilogue: a row-major rows x cols matrix
 // (row pitch `pitch_bytes`), box 32 x 32.  fp32 partials use the 128-byte
-// swizzle (32 floats = one 128-byte row); 16-bit C is unswizzled.
+// swizzle (32 floats = one 128-byte row), 16-bit C the 64-byte swizzle (32
+// halves = one 64-byte row), matching the epilogue's shared-memory writes.
 bool encode_output(CUtensorMap* map, void* ptr, bool fp32, int c_dtype, int64_t rows, int64_t cols,
                    int64_t pitch_bytes) {
   auto enc = get_encoder();
@@ -175,7 +176,7 @@ bool encode_output(CUtensorMap* map, void* ptr, bool fp32, int c_dtype, int64_t 
   cuuint32_t box[2] = {static_cast<cuuint32_t>(EPI_BOX), static_cast<cuuint32_t>(EPI_BOX)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -214,10 +215,10 @@ bool encode_int4_activation(CUtensorMap* map, const void* ptr, int64_t M, int64_
   return r == CUDA_SUCCESS;
 }
 
-gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-                           float* partial, int32_t* counters, cudaStream_t stream) {
+// The dense kernels' arguments for one run (tensor maps encoded here).
+bool build_dense_args(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                      float* partial, int32_t* counters, TcArgs& args) {
   const gemm_desc_t& d = plan->d;
-  TcArgs args;
   std::memset(&args, 0, sizeof(args));
   // P operand: the MMA's M side (128-row tiles, 256 for a CTA pair whose
   // CTAs load 128 each).  Q operand: bn-row tiles (128 per CTA for a pair).
@@ -231,8 +232,8 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
   const int64_t p_ld = a_is_p ? lda : ldb;
   const int64_t q_ld = a_is_p ? ldb : lda;
   const int q_box = plan->pair ? plan->bn / 2 : plan->bn;
-  if (!encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, TILE_P)) return GEMM_ERR_CUDA;
-  if (!encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, q_box)) return GEMM_ERR_CUDA;
+  if (!encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, TILE_P)) return false;
+  if (!encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, q_box)) return false;
   args.c = C;
   args.ldc = plan->ldc;
   args.ws = partial;
@@ -265,13 +266,44 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
   args.cl_size = plan->cl_size;
   // Staged epilogue: whole-line bulk stores of C and bulk reductions of the
   // fp32 partials, where the pointers and pitches allow them (16 bytes).
-  if (env_int("LGT_GEMM_TMA_EPI", 1) != 0) {
+  static const bool tma_epi = env_int("LGT_GEMM_TMA_EPI", 1) != 0;
+  if (tma_epi) {
     args.tma_c = args.c_vec && encode_output(&args.tm_c, C, false, d.c_dtype, d.M, d.N, plan->ldc * 2);
     args.tma_ws = partial && !plan->det && (d.N % 4 == 0) &&
                   encode_output(&args.tm_ws, partial, true, 0, d.M, d.N, d.N * 4);
   }
   args.idesc = idesc_f16(d.a_dtype == GEMM_BF16 ? 1u : 0u, static_cast<uint32_t>(p_mn), static_cast<uint32_t>(q_mn),
                          static_cast<uint32_t>(TILE_P << plan->pair), static_cast<uint32_t>(plan->bn));
+  return true;
+}
+
+gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                           float* partial, int32_t* counters, cudaStream_t stream, int withhold) {
+  ArgCache* cache = plan->cache;
+  const bool mine = cache && __atomic_exchange_n(&cache->busy, 1, __ATOMIC_ACQUIRE) == 0;
+  TcArgs args;
+  if (mine && cache->valid && cache->A == A && cache->B == B && cache->C == C && cache->partial == partial &&
+      cache->counters == counters && cache->lda == lda && cache->ldb == ldb) {
+    args = cache->args;
+  } else {
+    if (!build_dense_args(plan, A, lda, B, ldb, C, partial, counters, args)) {
+      if (mine) __atomic_store_n(&cache->busy, 0, __ATOMIC_RELEASE);
+      return GEMM_ERR_CUDA;
+    }
+    if (mine) {
+      cache->valid = 1;
+      cache->A = A;
+      cache->B = B;
+      cache->C = C;
+      cache->partial = partial;
+      cache->counters = counters;
+      cache->lda = lda;
+      cache->ldb = ldb;
+      cache->args = args;
+    }
+  }
+  if (mine) __atomic_store_n(&cache->busy, 0, __ATOMIC_RELEASE);
+  args.withhold = withhold;
   const cudaError_t e = plan->pair ? launch_tc_gemm_pair(args, plan->bn, plan->grid, stream)
                                    : launch_tc_gemm(args, plan->bn, plan->grid, stream);
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -279,6 +311,8 @@ gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, co
 
 gemm_plan plan_without_tail(const gemm_plan& p) {
   gemm_plan q = p;
+  q.cache = nullptr;  // the copy's arguments differ from the plan's
+  q.withhold_armed = 0;
   if (!q.tail_tiles) return q;
   q.split = 1;
   q.kb_per_split = q.kb_total;
@@ -319,6 +353,15 @@ uint32_t gemm_perm_fwd(uint32_t i, uint32_t count, uint32_t block, uint32_t stri
 
 uint32_t gemm_perm_inv(uint32_t i, uint32_t count, uint32_t block, uint32_t stride) {
   return lgt::perm_inv(i, count, block, stride);
+}
+
+gemm_status_t gemm_perm_device(const uint32_t* in, size_t n, uint32_t count, uint32_t block, uint32_t stride,
+                               int32_t inverse, uint32_t* out, void* stream) {
+  if (n && (!in || !out)) return GEMM_ERR_INVALID_ARG;
+  return lgt::launch_perm(in, n, count, block, stride, inverse, out, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? GEMM_OK
+             : GEMM_ERR_CUDA;
 }
 
 gemm_status_t gemm_magic_divmod_host(const uint32_t* n, size_t count, uint32_t divisor, uint32_t* q, uint32_t* r) {
@@ -580,6 +623,12 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
     p.ws_bytes_misaligned = p.ws_bytes;
   }
 
+  if (d.flags & GEMM_FLAG_TEST_WITHHOLD_STAGE) {
+    // the test aid needs a kernel in which no CTA waits on another
+    if (int4 || p.pair || p.cl_size > 1 || p.split != 1 || p.tail_tiles || p.fin_tiles) return GEMM_ERR_UNSUPPORTED;
+    p.withhold_armed = 1;
+  }
+
   if (p.device >= 0) {
     if (cudaMalloc(&p.d_status, sizeof(lgt::DeviceStatus)) != cudaSuccess) return GEMM_ERR_CUDA;
     if (cudaMemset(p.d_status, 0, sizeof(lgt::DeviceStatus)) != cudaSuccess) {
@@ -587,8 +636,10 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
       return GEMM_ERR_CUDA;
     }
   }
-  gemm_plan* h = new (std::nothrow) gemm_plan(p);
+  p.cache = new (std::nothrow) lgt::ArgCache();
+  gemm_plan* h = p.cache ? new (std::nothrow) gemm_plan(p) : nullptr;
   if (!h) {
+    delete p.cache;
     if (p.d_status) cudaFree(p.d_status);
     return GEMM_ERR_INVALID_ARG;
   }
@@ -681,7 +732,10 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   const bool split_region = plan->split > 1 && plan->cl_size <= 1;
   float* partial = split_region ? reinterpret_cast<float*>(ws + plan->off_partial) : nullptr;
   int32_t* counters = split_region ? reinterpret_cast<int32_t*>(ws + plan->off_counters) : nullptr;
-  if (!int4) return lgt::launch_dense(plan, a_eff, lda, b_eff, ldb, C, partial, counters, stream);
+  if (!int4) {
+    const int withhold = plan->withhold_armed ? __atomic_exchange_n(&plan->withhold_armed, 0, __ATOMIC_ACQ_REL) : 0;
+    return lgt::launch_dense(plan, a_eff, lda, b_eff, ldb, C, partial, counters, stream, withhold);
+  }
 
   lgt::TcArgs args;
   std::memset(&args, 0, sizeof(args));
@@ -780,6 +834,7 @@ gemm_status_t gemm_sync_status(gemm_plan_t* plan, void* stream) {
 gemm_status_t gemm_destroy(gemm_plan_t* plan) {
   if (!plan) return GEMM_OK;
   if (plan->d_status) cudaFree(plan->d_status);
+  delete plan->cache;
   delete plan;
   return GEMM_OK;
 }

@@ -1,5 +1,6 @@
-// Small HBM-bound helper kernels: the stride-realigning operand copy and the
-// device-side magic-division check.
+// Small HBM-bound helper kernels: the stride-realigning operand copy, and
+// the device-side runs of the integer helpers (magic-number division and the
+// perpendicular-dimension stride permutation) over index arrays.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -83,6 +84,18 @@ __global__ void magic_divmod_kernel(const uint32_t* __restrict__ n, size_t count
   }
 }
 
+// out[j] = the stride permutation (or its inverse) of in[j] over `count`
+// indices in blocks of `block` -- the device instance of perm_fwd / perm_inv,
+// the same code the loaders use.
+__global__ void perm_kernel(const uint32_t* __restrict__ in, size_t n, uint32_t count, uint32_t block,
+                            uint32_t stride, int inverse, uint32_t* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t j = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n; j += step)
+    out[j] = inverse ? perm_inv(in[j], count, block, stride) : perm_fwd(in[j], count, block, stride);
+}
+
 int grid_for(int64_t work, int threads) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -114,6 +127,14 @@ cudaError_t launch_magic_divmod(const uint32_t* n, size_t count, MagicDiv m, uin
   const int threads = 256;
   return launch_pdl(magic_divmod_kernel, dim3(static_cast<unsigned>(grid_for(static_cast<int64_t>(count), threads))),
                     dim3(threads), 0, stream, n, count, m, q, r);
+}
+
+cudaError_t launch_perm(const uint32_t* in, size_t n, uint32_t count, uint32_t block, uint32_t stride, int inverse,
+                        uint32_t* out, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  return launch_pdl(perm_kernel, dim3(static_cast<unsigned>(grid_for(static_cast<int64_t>(n), threads))),
+                    dim3(threads), 0, stream, in, n, count, block, stride, inverse, out);
 }
 
 }  // namespace lgt

@@ -145,6 +145,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           const uint32_t sp = base + stage * C::STAGE_BYTES;
           const uint32_t sq = sp + kP_BYTES;
           const int32_t k0 = (g.kb0 + kb) * TILE_K;
+          if (a.withhold && blockIdx.x == 0 && issued == 0) {
+            // test aid (a.withhold): this stage is never filled, so the MMA
+            // issuer's bounded wait on it runs out
+            ++issued;
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
           if (!a.p_mn) {
             tma_load_2d(sp, &a.tm_p, full_bar(stage), k0, prow);
@@ -250,8 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       // Let every TMA load still in flight land before the CTA exits.
       volatile int no_abort = 0;
       const int consumed = *consumed_slot;
-      for (int it = consumed; it < issued; ++it)
+      for (int it = consumed; it < issued; ++it) {
+        if (a.withhold && blockIdx.x == 0 && it == 0) continue;  // the withheld stage has no copy in flight
         mbar_wait_bounded(full_bar(it % C::STAGES), (it / C::STAGES) & 1, a.wait_limit_ns, &no_abort);
+      }
     }
   }
   if (warp == 1 && lane == 0) {
@@ -262,6 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   }
   tc_fence_before();
   __syncthreads();
+  // Split-K in a cluster: no CTA leaves while a peer may still push its slice
+  // into this CTA's shared memory (a peer that gave up a wait still reaches
+  // this barrier: every wait before it is bounded).
+  if (a.cl_size > 1) cluster_sync_all();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }

@@ -138,6 +138,7 @@ struct TcArgs {
   int32_t tma_ws;        // partial tiles leave through shared memory and bulk reductions
   int32_t cl_size;       // > 1: the split-K runs of a tile are the CTAs of one cluster of this size,
                          // reduced through distributed shared memory (single-CTA kernel, swapped, BN <= 64)
+  int32_t withhold;      // test aid (single-CTA kernel): CTA 0 never fills its first pipeline stage
   uint32_t idesc;
 };
 
@@ -210,5 +211,9 @@ cudaError_t launch_repack_rows(const void* src, int64_t src_pitch, void* dst, in
 
 cudaError_t launch_magic_divmod(const uint32_t* n, size_t count, MagicDiv m, uint32_t* q, uint32_t* r,
                                 cudaStream_t stream);
+
+// out[j] = perm_fwd (inverse = 0) or perm_inv (inverse != 0) of in[j].
+cudaError_t launch_perm(const uint32_t* in, size_t n, uint32_t count, uint32_t block, uint32_t stride, int inverse,
+                        uint32_t* out, cudaStream_t stream);
 
 }  // namespace lgt

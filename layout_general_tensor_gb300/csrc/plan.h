@@ -9,6 +9,10 @@
 #include "gemm.h"
 #include "kernels.h"
 
+namespace lgt {
+struct ArgCache;
+}
+
 struct gemm_plan {
   gemm_desc_t d;
   int device;        // device current at create time, -1 if none was queried
@@ -43,10 +47,29 @@ struct gemm_plan {
   size_t off_corr;   // int4, tile width 16: the per-row term of the per-group accumulator form, fp32 [N][16]
   lgt::DeviceStatus* d_status;
   uint64_t wait_limit_ns;
+  int withhold_armed;  // GEMM_FLAG_TEST_WITHHOLD_STAGE: the next run withholds a stage (one shot)
+  lgt::ArgCache* cache;  // launch arguments of the last run (owned; null in copies made by plan_without_tail)
 };
 
 
 namespace lgt {
+
+// The dense kernels' launch arguments of a plan's last run, keyed by what
+// the tensor maps and pointers depend on, so that a run with the same
+// buffers as the one before it encodes no tensor map (an encode costs about
+// a microsecond of host time).  A plan may be used from several threads: a
+// run that finds the cache busy encodes its own arguments.
+struct ArgCache {
+  int busy;  // 0 / 1, taken with an atomic exchange
+  int valid;
+  const void* A;
+  const void* B;
+  void* C;
+  float* partial;
+  int32_t* counters;
+  int64_t lda, ldb;
+  TcArgs args;
+};
 
 // Encode a 2-D TMA map over a 16-bit operand (see api.cu).
 bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major, int64_t rows_or_mn, int64_t K,
@@ -65,7 +88,8 @@ bool encode_int4_activation(CUtensorMap* map, const void* ptr, int64_t M, int64_
 // A copy of `p` that runs every tile whole (no stream-K tail).
 gemm_plan plan_without_tail(const gemm_plan& p);
 
+// withhold: the test aid of GEMM_FLAG_TEST_WITHHOLD_STAGE for this run.
 gemm_status_t launch_dense(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-                           float* partial, int32_t* counters, cudaStream_t stream);
+                           float* partial, int32_t* counters, cudaStream_t stream, int withhold = 0);
 
 }  // namespace lgt

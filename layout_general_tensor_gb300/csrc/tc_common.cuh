@@ -626,10 +626,13 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
           __syncwarp();
         }
         if (full_tile) {
-          // 16-bit C: 64-byte rows, no swizzle
+          // 16-bit C: 64-byte rows in the 64-byte swizzle (16-byte chunk c of
+          // row j stored at chunk c ^ ((j >> 1) & 3)); one row per instruction
 #pragma unroll
           for (int j = 0; j < EPI_BOX; ++j)
-            st_shared_u16(sbuf + 64u * j + 2u * lane, cvt1(__uint_as_float(v[j]), a.c_bf16));
+            st_shared_u16(sbuf + 64u * j + ((static_cast<uint32_t>(lane >> 3) ^ ((j >> 1) & 3)) << 4) +
+                              2u * (lane & 7),
+                          cvt1(__uint_as_float(v[j]), a.c_bf16));
         } else {
           // fp32: 128-byte rows in the 128-byte swizzle (16-byte chunk index XOR row & 7)
 #pragma unroll
@@ -668,11 +671,14 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
           __syncwarp();
         }
         if (full_tile) {
-          // 16-bit C: row `lane` of the block is 64 bytes, no swizzle
+          // 16-bit C: row `lane` of the block is 64 bytes in the 64-byte
+          // swizzle (chunk j stored at chunk j ^ ((lane >> 1) & 3)), so the
+          // eight lanes of each quarter-warp store to eight distinct bank groups
           const uint32_t r = sbuf + static_cast<uint32_t>(lane) * 64u;
+          const uint32_t sw = static_cast<uint32_t>(lane >> 1) & 3u;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            st_shared_v4(r + 16u * j, pack2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1]), a.c_bf16),
+            st_shared_v4(r + 16u * (static_cast<uint32_t>(j) ^ sw), pack2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1]), a.c_bf16),
                          pack2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]), a.c_bf16),
                          pack2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]), a.c_bf16),
                          pack2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]), a.c_bf16));

@@ -209,6 +209,23 @@ def test_deterministic_flag(lib):
     lib.gemm_destroy(h)
 
 
+def test_withhold_flag_only_where_no_cta_waits_on_another(lib):
+    """The failure-path test aid is accepted only for plans whose CTAs never
+    wait on each other (single-CTA kernel, whole tiles)."""
+    W = lib.GEMM_FLAG_TEST_WITHHOLD_STAGE
+    h = lib.gemm_create(lib.make_desc(256, 256, 256, a_dtype=lib.GEMM_F16, split_k=1, flags=W, num_sms=148))
+    info = lib.gemm_query(h)
+    assert info.kernel == 0 and info.split_k == 1 and info.streamk_tiles == 0
+    lib.gemm_destroy(h)
+    for d in (lib.make_desc(256, 256, 4096, split_k=4, flags=W, num_sms=148),
+              lib.make_desc(16, 256, 1024, a_dtype=lib.GEMM_F16, b_dtype=lib.GEMM_INT4, c_dtype=lib.GEMM_F16,
+                            flags=W, num_sms=148)):
+        st, h = lib.gemm_create_status(d)
+        assert st == lib.GEMM_ERR_UNSUPPORTED and h is None
+    st, h = lib.gemm_create_status(lib.make_desc(256, 256, 256, flags=W | 4, num_sms=148))
+    assert st == lib.GEMM_ERR_INVALID_ARG
+
+
 def test_no_device_paths(lib):
     import torch
     if torch.cuda.is_available():
