@@ -61,7 +61,7 @@ def kernel_name(info):
     if info.kernel == 2:
         return f"tc_gemm_pair_kernel<{info.tile_n}>"
     if info.kernel == 1:
-        return f"int4_gemm_kernel<{info.tile_m}>"
+        return "int4f8_gemm_kernel" if info.dequant_form == 2 else f"int4_gemm_kernel<{info.tile_m}>"
     return f"tc_gemm_kernel<{info.tile_m if info.swap_ab else info.tile_n}>"
 
 
@@ -185,7 +185,9 @@ class DeviceCase:
                              split_k=case.split_k, group_size=case.group_size if case.b_dtype == wl.INT4 else 0,
                              num_sms=148)
         self.g = lgt.Gemm(desc)
-        self.launches_per_run = 1 + int(self.g.info.repack_a) + int(self.g.info.repack_b)
+        # (+ the int4 path's activation pre-pass)
+        self.launches_per_run = (1 + int(self.g.info.repack_a) + int(self.g.info.repack_b)
+                                 + int(self.g.info.kernel == 1))
         self.i = 0
 
     def run(self):

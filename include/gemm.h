@@ -104,6 +104,11 @@ typedef struct {
   int32_t streamk_tiles; /* tiles of the stream-K tail (0 = none), see gemm_create */
   int32_t cluster_size;  /* > 1: each tile's split-K runs are the CTAs of one cluster of this size and
                             their fp32 partials are added in shared memory (0 = split-K through the workspace) */
+  int32_t dequant_form;  /* int4 weights: 1 = fp16 form (each weight expanded to fp16 q*s, the zero point
+                            through the activation's group sums), 2 = e4m3 form (codes as exact e4m3 values,
+                            the activation split into three e4m3 terms per 128-deep block, scales, zero
+                            points and activation scales applied in fp32 after the MMA: activations of at
+                            most 16 rows, K-contiguous, K and group_size multiples of 128); 0 otherwise */
 } gemm_info_t;
 
 typedef struct gemm_plan gemm_plan_t;

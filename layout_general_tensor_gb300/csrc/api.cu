@@ -30,20 +30,6 @@ int next_pow2_at_least16(int64_t v) {
   return p;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 bool is_half(int t) { return t == GEMM_F16 || t == GEMM_BF16; }
 
 gemm_status_t validate(const gemm_desc_t& d) {
@@ -130,6 +116,22 @@ uint64_t wait_limit_from_env() {
 
 namespace lgt {
 
+// cuTensorMapEncodeTiled, resolved once through the runtime (no link-time
+// dependency on the driver library); null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
 // 2-D tensor map over a 16-bit operand.  K-major: dims {K, rows}, box
 // {64, box_rows}.  MN-major: dims {mn, K}, box {64, 64}.  128-byte swizzle,
 // zero fill outside the tensor (ragged M / N / K tails).
@@ -177,40 +179,6 @@ bool encode_output(CUtensorMap* map, void* ptr, bool fp32, int c_dtype, int64_t 
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// Packed int4 weights: N rows of `ld_bytes` bytes (K/2 used), box 128 bytes
-// (256 codes) x 128 rows, 128-byte swizzle so that the threads' 16-byte row
-// reads fall in different bank groups.
-bool encode_int4_weights(CUtensorMap* map, const void* ptr, int64_t N, int64_t ld_bytes) {
-  auto enc = get_encoder();
-  if (!enc) return false;
-  (void)N;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(ld_bytes), static_cast<cuuint64_t>(N)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_bytes)};
-  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(TILE_P)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// Prepared int4-path activation, K-block-major fp16 (element (m, k) at
-// ((k / 64) * M + m) * 64 + k % 64): a 3-D map {64, M, K / 64}, box
-// {64, bn, kb_box}, 128-byte swizzle, so one copy brings a stage's K blocks
-// as kb_box consecutive bn x 128-byte tiles.
-bool encode_int4_activation(CUtensorMap* map, const void* ptr, int64_t M, int64_t K, int bn, int kb_box) {
-  auto enc = get_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
-  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(M) * 128};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(bn), static_cast<cuuint32_t>(kb_box)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -611,17 +579,7 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   p.ws_bytes = off_aligned;
   // When a base pointer is not 16-byte aligned the operand is repacked too.
   p.ws_bytes_misaligned = off + pack_a_bytes + pack_b_bytes;
-  if (int4) {
-    // the prepared (K-block-major, pair-ordered) activation and its
-    // per-group sums follow the split-K region
-    p.off_aprep = off;
-    p.off_agsum = align_up(off + static_cast<size_t>(d.M) * d.K * 2, 256);
-    // group sums and offset sums of the activation, fp32 [groups][M] each,
-    // then (per-group accumulator form) the per-row term, fp32 [N][16]
-    p.off_corr = align_up(p.off_agsum + 2 * static_cast<size_t>(d.M) * (d.K / p.group) * sizeof(float), 256);
-    p.ws_bytes = align_up(p.off_corr + (p.bn == 16 ? static_cast<size_t>(d.N) * 16 * sizeof(float) : 0), 256);
-    p.ws_bytes_misaligned = p.ws_bytes;
-  }
+  if (int4) lgt::int4_plan(p, off);  // form, prepared-activation region and tables
 
   if (d.flags & GEMM_FLAG_TEST_WITHHOLD_STAGE) {
     // the test aid needs a kernel in which no CTA waits on another
@@ -668,6 +626,7 @@ gemm_status_t gemm_query(const gemm_plan_t* plan, gemm_info_t* info) {
   info->repack_a = plan->repack_a;
   info->repack_b = plan->repack_b;
   info->kernel = plan->kernel == 0 && plan->pair ? 2 : plan->kernel;
+  info->dequant_form = plan->kernel == 1 ? plan->int4_form : 0;
   return GEMM_OK;
 }
 
@@ -737,85 +696,7 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     return lgt::launch_dense(plan, a_eff, lda, b_eff, ldb, C, partial, counters, stream, withhold);
   }
 
-  lgt::TcArgs args;
-  std::memset(&args, 0, sizeof(args));
-  const float* args_agsum = nullptr;
-  const float* args_ogsum = nullptr;
-  // Per-group accumulators (the int4 kernel's form for one activation tile of
-  // at most 16 rows, group 128 with splits of whole groups, at most 128
-  // groups, K-contiguous activation and scale rows readable 16 bytes at a
-  // time).  Opt-in with LGT_GEMM_INT4_V2=1: its GEMM kernel is faster than
-  // the per-weight form, but with the separate kernel that forms its
-  // zero-point and offset term the whole path is still slower.
-  const bool v2 = plan->bn == 16 && plan->group == 128 && plan->kb_per_split % 2 == 0 && !plan->a_mn &&
-                  lgt::int4_prep_fused(plan->a_mn, static_cast<int>(d.K), static_cast<int>(plan->group)) &&
-                  (d.K / plan->group) % 8 == 0 && d.K / plan->group <= 128 && reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
-                  reinterpret_cast<uintptr_t>(zeros) % 16 == 0 && env_int("LGT_GEMM_INT4_V2", 0) != 0;
-  {
-    // prepared activation: K-block-major, in the workspace
-    void* ap = ws + plan->off_aprep;
-    float* agsum = reinterpret_cast<float*>(ws + plan->off_agsum);
-    float* ogsum = agsum + static_cast<size_t>(d.M) * (d.K / plan->group);
-    if (lgt::launch_int4_prep(A, plan->lda, plan->a_mn, static_cast<int>(d.M), static_cast<int>(d.K),
-                              static_cast<int>(plan->group), ap, agsum, v2 ? ogsum : nullptr, plan->sms_grid,
-                              stream) != cudaSuccess)
-      return GEMM_ERR_CUDA;
-    args_agsum = agsum;
-    args_ogsum = v2 ? ogsum : nullptr;
-    if (v2 && lgt::launch_int4_corr(static_cast<const uint16_t*>(scales), static_cast<const uint16_t*>(zeros), agsum,
-                                    ogsum, static_cast<int>(d.N), static_cast<int>(d.M),
-                                    static_cast<int>(d.K / plan->group),
-                                    reinterpret_cast<float*>(ws + plan->off_corr), stream) != cudaSuccess)
-      return GEMM_ERR_CUDA;
-    if (!lgt::encode_int4_activation(&args.tm_q, ap, d.M, d.K, plan->bn, d.K / 64 < 4 ? static_cast<int>(d.K / 64) : 4))
-      return GEMM_ERR_CUDA;
-  }
-  args.c = C;
-  args.ldc = plan->ldc;
-  args.ws = partial;
-  args.counters = counters;
-  args.status = plan->d_status;
-  args.wait_limit_ns = plan->wait_limit_ns;
-  args.M = static_cast<int32_t>(d.M);
-  args.N = static_cast<int32_t>(d.N);
-  args.K = static_cast<int32_t>(d.K);
-  args.tiles_p = plan->tiles_p;
-  args.tiles_q = plan->tiles_q;
-  args.split = plan->split;
-  args.kb_per_split = plan->kb_per_split;
-  args.kb_total = plan->kb_total;
-  args.num_units = plan->num_units;
-  args.rr_tiles = plan->rr_tiles;
-  args.det = plan->det;
-  args.max_runs = plan->max_runs;
-  if (plan->det) args.slots = partial;
-  args.div_split = lgt::magic_encode(static_cast<uint32_t>(plan->split));
-  args.div_tiles_p = lgt::magic_encode(static_cast<uint32_t>(plan->tiles_p));
-  args.swap = plan->swap;
-  args.c_bf16 = d.c_dtype == GEMM_BF16;
-  args.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && (plan->ldc % 8 == 0);
-  args.ws_vec = (d.N % 4 == 0);
-  {
-    // MMA A operand: the dequantised weight in TMEM (K-major); B: the activation
-    args.q_mn = 0;
-    args.idesc = lgt::idesc_f16(0u, 0u, 0u, lgt::TILE_P, static_cast<uint32_t>(plan->bn));
-    lgt::Int4Args a4;
-    std::memset(&a4, 0, sizeof(a4));
-    a4.t = args;
-    if (!lgt::encode_int4_weights(&a4.tm_w, B, d.N, plan->ldb)) return GEMM_ERR_CUDA;
-    a4.agsum = args_agsum;
-    a4.scales = static_cast<const uint16_t*>(scales);
-    a4.zeros = static_cast<const uint16_t*>(zeros);
-    a4.groups = static_cast<int32_t>(d.K / plan->group);
-    a4.div_kb_per_group = lgt::magic_encode(static_cast<uint32_t>(plan->group / kBlockK));
-    a4.x_box_kb = d.K / 64 < 4 ? static_cast<int32_t>(d.K / 64) : 4;
-    a4.vec_sz = (a4.groups % 8 == 0) && reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
-                reinterpret_cast<uintptr_t>(zeros) % 16 == 0;
-    a4.ogsum = args_ogsum;
-    a4.corr = v2 ? reinterpret_cast<const float*>(ws + plan->off_corr) : nullptr;
-    a4.v2 = v2 ? 1 : 0;
-    return lgt::launch_int4_gemm(a4, plan->bn, plan->grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
-  }
+  return lgt::run_int4(plan, A, B, C, scales, zeros, ws, partial, counters, stream);
 }
 
 gemm_status_t gemm_sync_status(gemm_plan_t* plan, void* stream) {
@@ -835,6 +716,7 @@ gemm_status_t gemm_destroy(gemm_plan_t* plan) {
   if (!plan) return GEMM_OK;
   if (plan->d_status) cudaFree(plan->d_status);
   delete plan->cache;
+  lgt::int4_cache_free(plan);
   delete plan;
   return GEMM_OK;
 }

@@ -1,4 +1,6 @@
-// int4-weight GEMM with the dequantisation inside the mainloop.
+// int4-weight GEMM with the dequantisation inside the mainloop, fp16 form
+// (activations of up to 64 rows, any activation layout, groups of 64 or more;
+// the e4m3 form in gemm_int4_f8.cu takes activations of up to 16 rows).
 //
 //   C[m,n] = sum_k A[m,k] * w(k,n),  w(k,n) = (q(n,k) - z(n,g)) * s(n,g),
 //   g = k / group_size, codes two per byte (low nibble = even k).
@@ -9,14 +11,15 @@
 // weight tile is the MMA's A operand *in TMEM*; the activation its B operand
 // in shared memory.
 //
-// Expansion.  A 32-bit word of codes q0..q7 (and the word shifted right by
-// 8) gives the fp16 pairs of codes (0,4), (1,5), (2,6), (3,7) with one LOP3
-// each: a code in bits 0..3 of a half ORed into 0x6400 is the fp16 number
-// 1024 + q, a code in bits 4..7 ORed into 0x5400 is 64 + q (the mantissa's
-// unit there is 1/16).  One packed subtraction of that offset gives q
-// exactly, and one packed FMA q * s + (-z * s) gives the weight: -z * s is
-// rounded to fp16 once per (row, group), the FMA rounds once more, so the
-// weight is within one fp16 rounding of z * s of (q - z) * s.
+// Arithmetic.  C = sum_k A q s - sum_g z s Ag[g], with Ag[g][m] the sum of
+// row m of the activation over group g.  The expanded weight is q s rounded
+// to fp16 once: a code in bits 0..3 of a half ORed into 0x6400 is the fp16
+// number 1024 + q, one in bits 4..7 ORed into 0x5400 is 64 + q (the
+// mantissa's unit there is 1/16), and fma(1024 + q, s, -1024 s) is q s
+// exactly before its one rounding (1024 s and 64 s are exact), so a pair of
+// codes costs one LOP3 and one HFMA2.  The zero-point term z s Ag is formed
+// in fp32 (z s is exact there) by the epilogue of the run that starts each
+// tile and subtracted from that run's accumulator.
 // The activation is copied once, K-contiguous, with every 8-element group of
 // K reordered to that pair order (0,4,1,5,2,6,3,7) by a small pre-pass
 // (int4_prep_kmajor_kernel / int4_prep_kernel), so no code is moved in the
@@ -49,6 +52,7 @@
 //                row of the tile.
 #include <cuda_fp16.h>
 
+#include "int4.h"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc_common.cuh"
@@ -97,8 +101,7 @@ struct Cfg4 {
   static constexpr uint32_t SC_OFF = X_OFF + XST * XSTAGE;
   static constexpr uint32_t ZP_OFF = SC_OFF + SC_BYTES;
   static constexpr uint32_t BAR_OFF = ZP_OFF + ZP_BYTES;
-  // (+ the per-group accumulator form's accf2[3], acce2[3])
-  static constexpr uint32_t NUM_BARS = 2 * WST + 2 * XST + 2 * TSLOTS + 5 + 2 * kMaxIssuers;
+  static constexpr uint32_t NUM_BARS = 2 * WST + 2 * XST + 2 * TSLOTS + 5;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_ALLOC = MISC_OFF + 64 + 1024;  // slack for 1024-byte alignment
   static_assert(kWStage % 1024 == 0 && ACT_TILE % 1024 == 0, "swizzled buffers stay 1024-byte aligned");
@@ -188,20 +191,6 @@ __device__ __forceinline__ void issue_stage_nk(int nk, uint32_t d_tmem, uint32_t
     case 3: issue_stage<3, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
     case 2: issue_stage<2, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
     default: issue_stage<1, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
-  }
-}
-
-// Per-group accumulator form (group 128 = two K blocks): every MMA of one
-// stage of NK K blocks, K blocks 2i and 2i + 1 into accumulator i (BN columns
-// apart from acc0), each accumulator started by its group's first MMA.
-template <int NK, uint32_t ACT_TILE, int BN>
-__device__ __forceinline__ void issue_stage_groups(uint32_t acc0, uint32_t a0, uint64_t bd0, uint32_t idesc) {
-#pragma unroll
-  for (int m = 0; m < 4 * NK; ++m) {
-    const int j = m >> 2, k = m & 3;
-    tc_mma_f16_ts(acc0 + static_cast<uint32_t>((j >> 1) * BN), a0 + static_cast<uint32_t>(j * 32 + k * 8),
-                  bd0 + static_cast<uint64_t>((j * ACT_TILE) >> 4) + static_cast<uint64_t>(2 * k), idesc,
-                  ((j & 1) == 0 && k == 0) ? 0u : 1u);
   }
 }
 
@@ -355,129 +344,7 @@ struct ZpFix {
   }
 };
 
-// Epilogue warps of the per-group accumulator form (BN = 16, group 128: a
-// stage's K blocks 2i, 2i + 1 are its group i, in accumulator slot st % NI,
-// columns (2 slot + i) BN).  For every stage of the CTA in order: wait until
-// its groups are complete, read them, free the slot, and add s(n, g) times
-// each group's sums into the run's fp32 total for this thread's row n (the
-// scales read 8 groups at a time, the next window loaded while the current
-// one is used).  The run that starts a tile subtracts the tile's term
-// corr[n][m] = sum over g of s(n, g) (z(n, g) Ag[g][m] + Og[g][m]) (formed by
-// int4_corr_kernel).  At the end of a run: store C, or the split-K partial
-// and the tile's arrival, as the dense kernels' epilogue does.
-template <int BN, int NI>
-__device__ __noinline__ void int4_epilogue_groups(const Int4Args& A4, uint32_t tmem_base, uint32_t accf2_0,
-                                                  uint32_t acce2_0, volatile int* abort_flag, int q4, int lane,
-                                                  int et) {
-  static_assert(BN == 16, "one 16-column load per group");
-  const TcArgs& a = A4.t;
-  const int row = q4 * 32 + lane;
-  Sched sched(a);
-  Group g;
-  int st = 0;
-  while (sched.next(a, g)) {
-    int32_t tp, tq, m0, m1, n0, n1;
-    tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
-    const int n = n0 + row;
-    const uint16_t* srow = n < n1 ? A4.scales + static_cast<int64_t>(n) * A4.groups : nullptr;
-    auto load_win = [&](int w) {
-      return (srow && 8 * w < A4.groups) ? __ldg(reinterpret_cast<const uint4*>(srow + 8 * w))
-                                         : make_uint4(0u, 0u, 0u, 0u);
-    };
-    const bool starts = g.s0 == 0 && g.nkb > 0 && n < n1;
-    float4 cr[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      cr[q] = starts ? __ldg(reinterpret_cast<const float4*>(A4.corr + static_cast<int64_t>(n) * 16) + q)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-    float acc[BN];
-#pragma unroll
-    for (int j = 0; j < BN; ++j) acc[j] = 0.0f;
-    int wcur = -2;
-    uint4 win = make_uint4(0u, 0u, 0u, 0u), wnext = win;
-    for (int kb = 0; kb < g.nkb; kb += kQuadK) {
-      const int nk = min(kQuadK, g.nkb - kb);  // 2 or 4: runs hold whole groups
-      const int r = st % NI;
-      // the scales of this stage's groups, before the wait
-      const int gi0 = (g.kb0 + kb) >> 1;
-      float sc[2];
-#pragma unroll
-      for (int sg = 0; sg < 2; ++sg) {
-        const int gi = gi0 + sg;
-        const int w = gi >> 3;
-        if (w != wcur) {
-          win = (w == wcur + 1) ? wnext : load_win(w);
-          wcur = w;
-          wnext = load_win(w + 1);
-        }
-        const uint32_t word = (gi & 4) ? ((gi & 2) ? win.w : win.z) : ((gi & 2) ? win.y : win.x);
-        sc[sg] = half_bits_to_float((gi & 1) ? (word >> 16) : (word & 0xFFFFu));
-      }
-      const bool got = mbar_wait_bounded(accf2_0 + 8u * r, (st / NI) & 1, a.wait_limit_ns, abort_flag);
-      if (!got && !*abort_flag) record_timeout(a, abort_flag, 2 * 16 + 8);
-      if (named_bar_or(1, kEpiThreads, !got)) return;
-      tc_fence_after();
-      const uint32_t t0 = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(2 * r * BN);
-      uint32_t d0[16], d1[16];
-      tc_ld_32x32b_x16(t0, d0);
-      if (nk == 4) tc_ld_32x32b_x16(t0 + BN, d1);
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce2_0 + 8u * r);
-#pragma unroll
-      for (int j = 0; j < BN; ++j) acc[j] = fmaf(sc[0], __uint_as_float(d0[j]), acc[j]);
-      if (nk == 4) {
-#pragma unroll
-        for (int j = 0; j < BN; ++j) acc[j] = fmaf(sc[1], __uint_as_float(d1[j]), acc[j]);
-      }
-      ++st;
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      acc[4 * q] -= cr[q].x;
-      acc[4 * q + 1] -= cr[q].y;
-      acc[4 * q + 2] -= cr[q].z;
-      acc[4 * q + 3] -= cr[q].w;
-    }
-    // the run's total: C, or the split-K partial and the tile's arrival
-    const bool full_tile = (g.s0 == 0 && g.s1 == a.split);
-    if (a.det && !full_tile) {
-      int first, nruns;
-      tile_runs(a, g.tile, first, nruns);
-      const int rr = static_cast<int>(blockIdx.x) - first;
-      float* slot = a.slots + (static_cast<int64_t>(g.tile) * a.max_runs + rr) * (static_cast<int64_t>(TILE_P) * BN);
-#pragma unroll
-      for (int j = 0; j < BN; ++j) slot[static_cast<int64_t>(j) * TILE_P + row] = acc[j];
-    } else if (n < n1) {
-      if (full_tile) {
-        uint16_t* cc = reinterpret_cast<uint16_t*>(a.c) + n;
-#pragma unroll
-        for (int j = 0; j < BN; ++j)
-          if (m0 + j < m1) cc[static_cast<int64_t>(m0 + j) * a.ldc] = cvt1(acc[j], a.c_bf16);
-      } else {
-        float* wc = a.ws + n;
-#pragma unroll
-        for (int j = 0; j < BN; ++j)
-          if (m0 + j < m1) red_add_f32(wc + static_cast<int64_t>(m0 + j) * a.N, acc[j]);
-      }
-    }
-    if (!full_tile) {
-      if (a.det)
-        arrive_split_tile_det<BN>(a, g, g.tile, m0, m1, n0, n1, et);
-      else
-        arrive_split_tile<16>(a, g, g.tile, m0, m1, n0, n1, et);
-    }
-  }
-}
-
-// V2: the per-group accumulator form (see Int4Args::v2): the expanders write
-// 1024 + q / 64 + q without the scale, the issuers put each group of a stage
-// into an accumulator of its own (a ring of NI stages, stage s in slot
-// s % NI, which is its issuer's), and the epilogue warps scale each group's
-// sums by s(n, g) in fp32 and add them up per run, as they arrive; the term
-// term sum over g of s(n, g) (z(n, g) Ag[g][m] + Og[g][m]) comes off once per tile.
-template <int BN, bool V2>
+template <int BN>
 __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_constant__ Int4Args A4) {
   pdl_launch_dependents();
   using C = Cfg4<BN>;
@@ -508,9 +375,6 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   auto accf_bar = [&](int b) { return bar0 + 8u * (kB1 + 2 * C::TSLOTS + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (kB1 + 2 * C::TSLOTS + 2 + b); };
   const uint32_t teardown_bar = bar0 + 8u * (kB1 + 2 * C::TSLOTS + 4);
-  // V2: accf2[i] / acce2[i]: the groups of the stage in accumulator slot i are complete / drained
-  auto accf2 = [&](int i) { return bar0 + 8u * (kB1 + 2 * C::TSLOTS + 5 + i); };
-  auto acce2 = [&](int i) { return bar0 + 8u * (kB1 + 2 * C::TSLOTS + 5 + kMaxIssuers + i); };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -532,10 +396,6 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
       mbar_init(acce_bar(b), kEpiThreads / 32);
     }
     mbar_init(teardown_bar, NI);
-    for (int i = 0; i < kMaxIssuers; ++i) {
-      mbar_init(accf2(i), 1);
-      mbar_init(acce2(i), kEpiThreads / 32);
-    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -633,30 +493,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
       int kb0, nk, st = 0, acc_iter = -1;
       bool nr;
       uint32_t d_tmem = tmem_base;
-      while (V2 && it.next(a, kb0, nk, nr)) {
-        // per-group accumulators: slot st % NI (this issuer's), drained by
-        // the epilogue before it is reused
-        const int t = st % C::TSLOTS, sx = st % C::XST;
-        if (st % NI == iss) {
-          if (!mbar_wait_bounded(acce2(iss), ((st / NI) & 1) ^ 1u, a.wait_limit_ns, abort_flag) ||
-              !mbar_wait_bounded(a_full(t), (st / C::TSLOTS) & 1, a.wait_limit_ns, abort_flag) ||
-              !mbar_wait_bounded(full_x(sx), (st / C::XST) & 1, a.wait_limit_ns, abort_flag)) {
-            if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 4);
-            break;
-          }
-          tc_fence_after();
-          const uint64_t bd0 = sw128_desc(base + C::X_OFF + sx * C::XSTAGE, 16u, 1024u);
-          const uint32_t a0 = tmem_base + kASlotCol0 + static_cast<uint32_t>(t * 128);
-          const uint32_t acc0 = tmem_base + static_cast<uint32_t>(iss * 2 * BN);
-          if (nk == 4) issue_stage_groups<4, C::ACT_TILE, BN>(acc0, a0, bd0, a.idesc);
-          else issue_stage_groups<2, C::ACT_TILE, BN>(acc0, a0, bd0, a.idesc);
-          tc_commit(tfree_bar(t));
-          tc_commit(xfree(sx));
-          tc_commit(accf2(iss));
-        }
-        ++st;
-      }
-      while (!V2 && it.next(a, kb0, nk, nr)) {
+      while (it.next(a, kb0, nk, nr)) {
         const int t = st % C::TSLOTS, sx = st % C::XST;
         if (nr) {
           ++acc_iter;
@@ -715,7 +552,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         const int g0 = static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0), A4.div_kb_per_group));
         const int g1 =
             static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + it.g.nkb - 1), A4.div_kb_per_group));
-        if (!V2 && A4.vec_sz) {
+        if (A4.vec_sz) {
           cp_async_wait<0>();  // the previous run's copies have landed before slots are reused
           w_cur = g0 >> 3;
           w_last = g1 >> 3;
@@ -735,7 +572,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         for (int jj = 0; jj < 2; ++jj) {
           const int j = 2 * h + jj;
           uint32_t s2 = 0;
-          if (!V2 && j < nk) {
+          if (j < nk) {
             const int g = static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + kb0 + j), A4.div_kb_per_group));
             if (A4.vec_sz) {
               const int w = g >> 3;
@@ -752,8 +589,8 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
             }
           }
           s2v[jj] = s2;
-          c1024v[jj] = V2 ? 0u : hmul2(s2, 0xE400E400u);
-          c64v[jj] = V2 ? 0u : hmul2(s2, 0xD400D400u);
+          c1024v[jj] = hmul2(s2, 0xE400E400u);
+          c64v[jj] = hmul2(s2, 0xD400D400u);
         }
         const int sw = st % C::WST, t = st % C::TSLOTS;
         const bool got =
@@ -787,18 +624,10 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
             const uint32_t lo = words[w8], hi = lo >> 8;
             // codes (p, p + 4) of the word for p = 0..3 as 1024 + q (p even)
             // or 64 + q (p odd), then (1024 + q) s - 1024 s = q s, rounded once
-            if constexpr (V2) {
-              // the codes as 1024 + q / 64 + q; scale and offsets come later
-              vals[4 * w8 + 0] = lop3_and_or(lo, 0x000F000Fu, 0x64006400u);
-              vals[4 * w8 + 1] = lop3_and_or(lo, 0x00F000F0u, 0x54005400u);
-              vals[4 * w8 + 2] = lop3_and_or(hi, 0x000F000Fu, 0x64006400u);
-              vals[4 * w8 + 3] = lop3_and_or(hi, 0x00F000F0u, 0x54005400u);
-            } else {
-              vals[4 * w8 + 0] = hfma2(lop3_and_or(lo, 0x000F000Fu, 0x64006400u), s2, c1024);
-              vals[4 * w8 + 1] = hfma2(lop3_and_or(lo, 0x00F000F0u, 0x54005400u), s2, c64);
-              vals[4 * w8 + 2] = hfma2(lop3_and_or(hi, 0x000F000Fu, 0x64006400u), s2, c1024);
-              vals[4 * w8 + 3] = hfma2(lop3_and_or(hi, 0x00F000F0u, 0x54005400u), s2, c64);
-            }
+            vals[4 * w8 + 0] = hfma2(lop3_and_or(lo, 0x000F000Fu, 0x64006400u), s2, c1024);
+            vals[4 * w8 + 1] = hfma2(lop3_and_or(lo, 0x00F000F0u, 0x54005400u), s2, c64);
+            vals[4 * w8 + 2] = hfma2(lop3_and_or(hi, 0x000F000Fu, 0x64006400u), s2, c1024);
+            vals[4 * w8 + 3] = hfma2(lop3_and_or(hi, 0x00F000F0u, 0x54005400u), s2, c64);
           }
           // two 16-column stores (measured faster per byte than one of 32 columns)
           tc_st_32x32b_x16(slot + static_cast<uint32_t>(j * 32), vals);
@@ -818,9 +647,6 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
     // so no staging buffer)
     const int q4 = warp & 3;
     const int et = threadIdx.x - kEpiWarp04 * 32;
-    if constexpr (V2) {
-      int4_epilogue_groups<BN, NI>(A4, tmem_base, accf2(0), acce2(0), abort_flag, q4, lane, et);
-    } else {
     Sched sched(a);
     Group g;
     int acc_iter = 0, ring = 0;
@@ -858,7 +684,6 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
               a, g, tmem_base, accf_bar(0), acce_bar(0), acc_iter, abort_flag, q4, lane, et, 0, 0u, ring, fix, mask))
         break;
     }
-    }
   }
 
   // ------------------------------------------------------------ teardown
@@ -892,7 +717,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
 // its elements reordered to (0,4,1,5,2,6,3,7).
 __global__ void __launch_bounds__(256) int4_prep_kmajor_kernel(const uint16_t* __restrict__ A, int64_t lda, int vec,
                                                                int M, int K, int gc, uint16_t* __restrict__ Ap,
-                                                               float* __restrict__ agsum, float* __restrict__ ogsum) {
+                                                               float* __restrict__ agsum) {
   pdl_launch_dependents();
   pdl_wait();
   const int chunks = K / 8;
@@ -935,10 +760,7 @@ __global__ void __launch_bounds__(256) int4_prep_kmajor_kernel(const uint16_t* _
         se += __shfl_xor_sync(0xffffffffu, se, off);
         so += __shfl_xor_sync(0xffffffffu, so, off);
       }
-      if (c % gc == 0) {
-        agsum[static_cast<int64_t>(c / gc) * M + m] = se + so;
-        if (ogsum) ogsum[static_cast<int64_t>(c / gc) * M + m] = 1024.0f * se + 64.0f * so;
-      }
+      if (c % gc == 0) agsum[static_cast<int64_t>(c / gc) * M + m] = se + so;
     }
   }
 }
@@ -990,100 +812,26 @@ __global__ void __launch_bounds__(256) int4_prep_mmajor_kernel(const uint16_t* _
   }
 }
 
-// The per-group accumulator form's term corr[n][m] for M <= 16 and at most
-// 128 groups: eight threads per row n -- column quad q (4q .. 4q + 3) times
-// window half h (windows h, h + 2, ...).  A thread loads all of its scale and
-// zero windows (8 groups, 16 bytes each) at once, then sums; the two halves
-// are added by one shuffle.  The four quads of a row read 64 consecutive
-// bytes of the staged tables and the rows of a warp the same ones.  Fixed
-// summation order.
-__global__ void __launch_bounds__(256) int4_corr_kernel(const uint16_t* __restrict__ scales,
-                                                        const uint16_t* __restrict__ zeros,
-                                                        const float* __restrict__ agsum,
-                                                        const float* __restrict__ ogsum, int N, int M, int G,
-                                                        float* __restrict__ corr) {
-  __shared__ float4 tab[2 * 128 * 4];  // Ag[g][16] then Og[g][16]
-  pdl_launch_dependents();
-  pdl_wait();
-  {
-    // (every load in flight before the first store: G * 16 <= 2048 = 8 a thread)
-    float av[8], ov[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int i = threadIdx.x + 256 * k, g = i >> 4, m = i & 15;
-      const bool in = i < G * 16 && m < M;
-      av[k] = in ? __ldg(agsum + static_cast<int64_t>(g) * M + m) : 0.0f;
-      ov[k] = in ? __ldg(ogsum + static_cast<int64_t>(g) * M + m) : 0.0f;
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int i = threadIdx.x + 256 * k;
-      if (i < G * 16) {
-        reinterpret_cast<float*>(tab)[i] = av[k];
-        reinterpret_cast<float*>(tab)[G * 16 + i] = ov[k];
-      }
-    }
-  }
-  __syncthreads();
-  const int q = threadIdx.x & 3, h = (threadIdx.x >> 2) & 1;
-  const int n = blockIdx.x * 32 + (threadIdx.x >> 3);
-  const int W = G >> 3;  // at most 16: 8 windows per half
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (n < N) {
-    const uint4* srow = reinterpret_cast<const uint4*>(scales + static_cast<int64_t>(n) * G);
-    const uint4* zrow = zeros ? reinterpret_cast<const uint4*>(zeros + static_cast<int64_t>(n) * G) : nullptr;
-    const uint4 z8 = make_uint4(0x48004800u, 0x48004800u, 0x48004800u, 0x48004800u);  // fp16 8.0 pairs
-    uint4 sw[8], zw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int w = h + 2 * i;
-      sw[i] = w < W ? __ldg(srow + w) : make_uint4(0u, 0u, 0u, 0u);
-      zw[i] = (w < W && zrow) ? __ldg(zrow + w) : z8;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int w = h + 2 * i;
-      if (w >= W) break;
-      const uint32_t sv4[4] = {sw[i].x, sw[i].y, sw[i].z, sw[i].w};
-      const uint32_t zv4[4] = {zw[i].x, zw[i].y, zw[i].z, zw[i].w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int g = 8 * w + e;
-        const float sv = half_bits_to_float((e & 1) ? (sv4[e >> 1] >> 16) : (sv4[e >> 1] & 0xFFFFu));
-        const float zs = half_bits_to_float((e & 1) ? (zv4[e >> 1] >> 16) : (zv4[e >> 1] & 0xFFFFu)) * sv;
-        const float4 ag = tab[g * 4 + q], og = tab[G * 4 + g * 4 + q];
-        acc.x = fmaf(sv, og.x, fmaf(zs, ag.x, acc.x));
-        acc.y = fmaf(sv, og.y, fmaf(zs, ag.y, acc.y));
-        acc.z = fmaf(sv, og.z, fmaf(zs, ag.z, acc.z));
-        acc.w = fmaf(sv, og.w, fmaf(zs, ag.w, acc.w));
-      }
-    }
-  }
-  acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 4);
-  acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 4);
-  acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 4);
-  acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 4);
-  if (n < N && h == 0) reinterpret_cast<float4*>(corr + static_cast<int64_t>(n) * 16)[q] = acc;
-}
-
-template <int BN, bool V2>
+template <int BN>
 cudaError_t launch4(const Int4Args& args, int grid, cudaStream_t stream) {
   using C = Cfg4<BN>;
-  cudaError_t e = set_smem_once<int4_gemm_kernel<BN, V2>>(static_cast<int>(C::SMEM_ALLOC));
+  cudaError_t e = set_smem_once<int4_gemm_kernel<BN>>(static_cast<int>(C::SMEM_ALLOC));
   if (e != cudaSuccess) return e;
-  return launch_pdl(int4_gemm_kernel<BN, V2>, dim3(static_cast<unsigned>(grid)), dim3(kThreads4), C::SMEM_ALLOC,
+  return launch_pdl(int4_gemm_kernel<BN>, dim3(static_cast<unsigned>(grid)), dim3(kThreads4), C::SMEM_ALLOC,
                     stream, args);
 }
 
-}  // namespace
-
+// Whether the pre-pass forms the group sums in its one pass: a group's
+// chunks are 8, 16 or 32 consecutive lanes of a warp.
 bool int4_prep_fused(int a_mn, int K, int group) {
   const int gc = group / 8;
   return !a_mn && (gc == 8 || gc == 16 || gc == 32) && (K / 8) % 32 == 0;
 }
 
+}  // namespace
+
 cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K, int group, void* Ap, float* agsum,
-                             float* ogsum, int sms, cudaStream_t stream) {
+                             int sms, cudaStream_t stream) {
   const int64_t chunks = static_cast<int64_t>(M) * (K / 8);
   if (chunks == 0) return cudaSuccess;
   int64_t blocks = (chunks + 255) / 256;
@@ -1097,7 +845,7 @@ cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K,
     const int vec = (lda % 8 == 0) && (reinterpret_cast<uintptr_t>(A) % 16 == 0);
     cudaError_t e = launch_pdl(int4_prep_kmajor_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
                                static_cast<const uint16_t*>(A), lda, vec, M, K, fused ? gc : 0,
-                               static_cast<uint16_t*>(Ap), agsum, fused ? ogsum : nullptr);
+                               static_cast<uint16_t*>(Ap), agsum);
     if (e != cudaSuccess) return e;
   } else {
     cudaError_t e = launch_pdl(int4_prep_mmajor_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
@@ -1115,19 +863,11 @@ cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K,
   return cudaGetLastError();
 }
 
-cudaError_t launch_int4_corr(const uint16_t* scales, const uint16_t* zeros, const float* agsum, const float* ogsum,
-                             int N, int M, int G, float* corr, cudaStream_t stream) {
-  if (N == 0) return cudaSuccess;
-  if (G % 8 != 0 || G > 128 || M > 16) return cudaErrorInvalidValue;
-  return launch_pdl(int4_corr_kernel, dim3(static_cast<unsigned>((N + 31) / 32)), dim3(256), 0, stream, scales, zeros,
-                    agsum, ogsum, N, M, G, corr);
-}
-
 cudaError_t launch_int4_gemm(const Int4Args& args, int bn, int grid, cudaStream_t stream) {
   switch (bn) {
-    case 16: return args.v2 ? launch4<16, true>(args, grid, stream) : launch4<16, false>(args, grid, stream);
-    case 32: return launch4<32, false>(args, grid, stream);
-    case 64: return launch4<64, false>(args, grid, stream);
+    case 16: return launch4<16>(args, grid, stream);
+    case 32: return launch4<32>(args, grid, stream);
+    case 64: return launch4<64>(args, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -142,52 +142,6 @@ struct TcArgs {
   uint32_t idesc;
 };
 
-// int4-weight GEMM (always swapped: P = the weight rows n, Q = the activation
-// rows m).  `t` carries the scheduler, the map over the prepared activation
-// (tm_q, K-major) and the epilogue fields; tm_p is unused.
-struct Int4Args {
-  TcArgs t;
-  CUtensorMap tm_w;          // packed weight bytes: dims {ldb bytes, N}, box {128, 128}, 128-byte swizzle
-  const float* agsum;        // per-group sums of the activation, fp32 [groups][M]
-  const uint16_t* scales;    // fp16 [N][groups]
-  const uint16_t* zeros;     // fp16 [N][groups], or null for z = 8
-  int32_t groups;
-  MagicDiv div_kb_per_group; // 64-deep K block -> quantisation group
-  int32_t x_box_kb;          // K blocks per activation box (min(4, K / 64)); t.tm_q is 3-D {64, M, K / 64}
-  int32_t vec_sz;            // scale / zero rows readable 8 groups (16 bytes) at a time
-  // The kernel form with per-group accumulators (BN 16, group 128, K-contiguous
-  // activation, vec_sz): codes expanded without their scale as 1024 + q (even
-  // k) or 64 + q (odd k), scaled per group in fp32 by the epilogue warps; the
-  // offsets come back out through ogsum[g][m] = sum over group g of row m of
-  // 1024 a (even k) + 64 a (odd k).
-  const float* ogsum;
-  const float* corr;         // v2: corr[n * 16 + m] = sum over g of s(n, g) (z(n, g) agsum[g][m] + ogsum[g][m])
-  int32_t v2;
-};
-
-cudaError_t launch_int4_gemm(const Int4Args& args, int bn, int grid, cudaStream_t stream);
-
-// Activation pre-pass of the int4 GEMM: copy of A (M x K, any layout,
-// 2-byte aligned) into Ap, K-block-major: the 64 elements of row m in K block
-// kb at Ap + (kb * M + m) * 64, each 8-element group of K reordered to
-// (0,4,1,5,2,6,3,7); and agsum[g * M + m] = the fp32 sum (fixed order) of row
-// m's elements in group g (group elements of K).  K and group must be
-// multiples of 64.
-// With ogsum non-null (and the pre-pass summing groups itself), also
-// ogsum[g * M + m] = the fp32 sum over group g of row m of 1024 a(m, k) for
-// even k and 64 a(m, k) for odd k.
-cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K, int group, void* Ap, float* agsum,
-                             float* ogsum, int sms, cudaStream_t stream);
-// Whether launch_int4_prep forms the group sums (and ogsum) in its one pass.
-bool int4_prep_fused(int a_mn, int K, int group);
-// corr[n * 16 + m] (N x 16 fp32, zero for m >= M; M <= 16) = the term the
-// per-group accumulator form subtracts once per tile: the sum over the G
-// groups of s(n, g) (z(n, g) agsum[g * M + m] + ogsum[g * M + m]), z = 8 when
-// zeros is null.  G a multiple of 8, at most 128; scale and zero rows 16-byte
-// aligned.
-cudaError_t launch_int4_corr(const uint16_t* scales, const uint16_t* zeros, const float* agsum, const float* ogsum,
-                             int N, int M, int G, float* corr, cudaStream_t stream);
-
 // Returns a cudaError_t; `bn` selects the kernel instance.
 cudaError_t launch_tc_gemm(const TcArgs& args, int bn, int grid, cudaStream_t stream);
 size_t tc_gemm_smem_bytes(int bn);

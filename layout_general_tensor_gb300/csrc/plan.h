@@ -2,6 +2,7 @@
 // shared by the C-ABI translation units.
 #pragma once
 #include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include <cstddef>
 #include <cstdint>
@@ -11,6 +12,7 @@
 
 namespace lgt {
 struct ArgCache;
+struct Int4Cache;
 }
 
 struct gemm_plan {
@@ -42,13 +44,15 @@ struct gemm_plan {
   int64_t a_pack_ld, b_pack_ld;
   size_t off_partial, off_counters, off_pack_a, off_pack_b, ws_bytes;
   size_t ws_bytes_misaligned;
+  int int4_form;      // int4: 1 = fp16 form, 2 = e4m3 form (gemm_info_t.dequant_form)
   size_t off_aprep;  // int4: the prepared activation
-  size_t off_agsum;  // int4: per-group sums of the activation, fp32 [groups][M], then the offset sums
-  size_t off_corr;   // int4, tile width 16: the per-row term of the per-group accumulator form, fp32 [N][16]
+  size_t off_agsum;  // int4: activation sums (fp16 form: [groups][M]; e4m3 form: [K / 128][16]), fp32
+  size_t off_inv;    // int4, e4m3 form: 1 / S_b per 128-deep block and row, fp32 [K / 128][16]
   lgt::DeviceStatus* d_status;
   uint64_t wait_limit_ns;
   int withhold_armed;  // GEMM_FLAG_TEST_WITHHOLD_STAGE: the next run withholds a stage (one shot)
   lgt::ArgCache* cache;  // launch arguments of the last run (owned; null in copies made by plan_without_tail)
+  lgt::Int4Cache* cache4;  // the same for the int4 kernels (owned; made on first use)
 };
 
 
@@ -71,15 +75,20 @@ struct ArgCache {
   TcArgs args;
 };
 
+// cuTensorMapEncodeTiled (see api.cu); null if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder();
+
 // Encode a 2-D TMA map over a 16-bit operand (see api.cu).
 bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major, int64_t rows_or_mn, int64_t K,
                     int64_t ld, int box_rows);
 
-// Encode the TMA map over packed int4 weights (see api.cu).
-bool encode_int4_weights(CUtensorMap* map, const void* ptr, int64_t N, int64_t ld_bytes);
-
-// Encode the 3-D TMA map over the prepared int4-path activation (see api.cu).
-bool encode_int4_activation(CUtensorMap* map, const void* ptr, int64_t M, int64_t K, int bn, int kb_box);
+// int4 plans (api_int4.cu): choose the form and lay out the prepared
+// activation and its tables after the split-K region at `off`; run a plan;
+// free its argument cache.
+void int4_plan(gemm_plan& p, size_t off);
+gemm_status_t run_int4(gemm_plan* plan, const void* A, const void* B, void* C, const void* scales, const void* zeros,
+                       uint8_t* ws, float* partial, int32_t* counters, cudaStream_t stream);
+void int4_cache_free(gemm_plan* plan);
 
 // Launch the dense tensor-core kernel of `plan` on operands TMA can address
 // in place (16-byte aligned bases and pitches `lda` / `ldb` in elements),

@@ -1,8 +1,12 @@
 """GPU parity of the int4-weight GEMM (dequantisation inside the mainloop)
 against the fp64 oracle, through the C ABI.  Same tolerances as the dense
-path.  The kernel expands each weight to fp16 as q * s + (-z * s) (the
-second term rounded to fp16 once per row and group) and accumulates in fp32
-on the tensor cores."""
+path.  Every test runs in both kernel forms where the shape allows: the
+fp16 form (each weight expanded to fp16 q * s, rounded once; the zero point
+z * s times the activation's group sums, in fp32) and the e4m3 form (codes as
+exact e4m3 values, the activation as three e4m3 terms per 128-deep block,
+all scales applied in fp32 after the MMA; activations of at most 16 rows,
+K-contiguous, K and group multiples of 128).  `form` "auto" takes the
+planner's choice, "fp16" forces the fp16 form (LGT_GEMM_INT4_FORM)."""
 import numpy as np
 import pytest
 import torch
@@ -27,23 +31,38 @@ def _built():
     lib()
 
 
+@pytest.fixture(params=["auto", "fp16"])
+def form(request, monkeypatch):
+    if request.param == "fp16":
+        monkeypatch.setenv("LGT_GEMM_INT4_FORM", "fp16")
+    return request.param
+
+
+def _check_form(g, form, case):
+    want_f8 = (form == "auto" and case.M <= 16 and case.a_layout == K and case.K % 128 == 0
+               and case.group_size % 128 == 0 and (g.info.k_per_split // 64) % 2 == 0)
+    assert g.info.dequant_form == (2 if want_f8 else 1), (form, case.name)
+
+
 @pytest.mark.parametrize("M", [1, 5, 16, 33])
 @pytest.mark.parametrize("N,Kd", [(128, 128), (300, 640), (1000, 256)])
-def test_int4_small(M, N, Kd):
+def test_int4_small(M, N, Kd, form):
     for zero in (8.0, None):
         case = _case(M, N, Kd, zero=zero)
         inp = wl.make_inputs(case, seed=M + N)
         c, g, _ = run_case(case, inp)
         assert g.info.kernel == 1 and g.info.swap_ab == 1
+        _check_form(g, form, case)
         assert_close(c, oracle_full(case, inp), case.name)
         g.close()
 
 
 @pytest.mark.parametrize("split", [2, 3, 8, 0])
-def test_int4_split_k(split):
+def test_int4_split_k(split, form):
     case = _case(16, 700, 4096, split=split)
     inp = wl.make_inputs(case, seed=split + 1)
     c, g, _ = run_case(case, inp, reps=2)
+    _check_form(g, form, case)
     if split:
         assert g.info.split_k == split
     assert_close(c, oracle_full(case, inp), case.name)
@@ -51,7 +70,7 @@ def test_int4_split_k(split):
 
 
 @pytest.mark.parametrize("group", [64, 256])
-def test_int4_group_sizes(group):
+def test_int4_group_sizes(group, form):
     case = _case(9, 260, 1024, group=group, split=2)
     inp = wl.make_inputs(case, seed=group)
     c, g, _ = run_case(case, inp)
@@ -61,7 +80,7 @@ def test_int4_group_sizes(group):
 
 @pytest.mark.parametrize("N,Kd,group,split", [(384, 8192, 64, 3), (300, 4096, 128, 5), (256, 16384, 512, 0),
                                                 (640, 2048, 64, 7)])
-def test_int4_scale_windows(N, Kd, group, split):
+def test_int4_scale_windows(N, Kd, group, split, form):
     """Scales read in windows of 8 groups (16 bytes) of a row, copied ahead
     into shared memory: runs that start and end inside a window, short runs
     (split 7 over 5 tiles: one unit of 5 K blocks per CTA), rows beyond N,
@@ -73,7 +92,7 @@ def test_int4_scale_windows(N, Kd, group, split):
     g.close()
 
 
-def test_int4_unaligned_scale_rows():
+def test_int4_unaligned_scale_rows(form):
     """A scale array that does not start on a 16-byte boundary cannot be
     read 16 bytes at a time: the per-K-block load path gives the same result."""
     case = _case(16, 384, 2048, group=64, split=2)
@@ -105,10 +124,10 @@ def test_int4_activation_m_contiguous():
     g.close()
 
 
-def test_int4_general_dequant_path():
-    """Non-integer zero points and very small scales: the expanded weights
-    are fp16, so the result must match the exact oracle and also the oracle
-    on fp16-rounded weights."""
+def test_int4_general_dequant_path(form):
+    """Non-integer zero points and very small scales: the result must match
+    the exact oracle, and also the oracle on fp16-rounded weights (what the
+    fp16 form computes)."""
     case = _case(8, 384, 512, split=1, zero=7.5, scale=("uniform", 2e-4, 9e-4))
     inp = wl.make_inputs(case, seed=9)
     c, g, _ = run_case(case, inp)
@@ -122,7 +141,7 @@ def test_int4_general_dequant_path():
     g.close()
 
 
-def test_int4_closed_forms():
+def test_int4_closed_forms(form):
     m = lib()
     M, N, Kd = 4, 256, 256
     A = torch.empty(M * Kd, dtype=torch.float16).uniform_(-1, 1)
@@ -132,8 +151,9 @@ def test_int4_closed_forms():
     g = m.Gemm(desc)
     C = torch.empty(M * N, dtype=torch.float16, device="cuda")
     Ad = A.cuda()
-    # all codes 8 with zero point 8 -> zero: 8 * s is exact in fp16, so each
-    # expanded weight 8 * s - 8 * s is exactly 0.
+    # all codes 8 with zero point 8 -> zero: in the fp16 form 8 s - 8 s is
+    # exactly 0 per weight; in the e4m3 form 8 s (sum of the activation) less
+    # s z Ag cancels to fp32 rounding.
     W = torch.full((N * Kd // 2,), 0x88, dtype=torch.uint8, device="cuda")
     s = torch.full((N, Kd // 128), 0.01, dtype=torch.float16, device="cuda")
     g.run(Ad, W, C, s, None)
@@ -150,10 +170,11 @@ def test_int4_closed_forms():
     g.close()
 
 
-def test_int4_full_size_sampled():
+def test_int4_full_size_sampled(form):
     case = wl.INT4_DEQUANT
     inp = wl.make_inputs(case, seed=0)
     c, g, _ = run_case(case, inp, reps=2)
+    _check_form(g, form, case)
     assert g.info.split_k == oracle.splitk_factor(case.M, case.N, case.K, 128, 128, 64, 148)
     rows, cols = wl.sample_indices(case.M, case.N, 1500, seed=2)
     assert_close(c[rows, cols], oracle_sample(case, inp, rows, cols), case.name)
