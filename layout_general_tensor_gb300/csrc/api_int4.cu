@@ -3,10 +3,11 @@
 // launches (pre-pass, then the GEMM).  gemm_create and gemm_run in api.cu
 // call in here for b_dtype = GEMM_INT4.
 //
-// Forms.  The e4m3 form (gemm_int4_f8.cu) takes activations of up to 16 rows,
-// K-contiguous, with K and the group size multiples of 128 and split ranges of
-// whole 128-deep blocks; everything else runs the fp16 form (gemm_int4.cu).
-// LGT_GEMM_INT4_FORM=fp16 at gemm_create selects the fp16 form everywhere.
+// Forms.  Plans run the fp16 form (gemm_int4.cu), the faster of the two on
+// the shapes measured so far.  LGT_GEMM_INT4_FORM=e4m3 at gemm_create selects
+// the e4m3 form (gemm_int4_f8.cu) where it applies: activations of up to 16
+// rows, K-contiguous, with K and the group size multiples of 128 and split
+// ranges of whole 128-deep blocks.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -154,8 +155,8 @@ bool build_int4_args(const gemm_plan* plan, const void* B, void* C, const void* 
 void int4_plan(gemm_plan& p, size_t off) {
   const gemm_desc_t& d = p.d;
   const char* form = std::getenv("LGT_GEMM_INT4_FORM");
-  const bool want_fp16 = form && std::strcmp(form, "fp16") == 0;
-  p.int4_form = (!want_fp16 && int4f8_supported(p.a_mn, d.M, d.K, p.group) && p.kb_per_split % 2 == 0) ? 2 : 1;
+  const bool want_f8 = form && std::strcmp(form, "e4m3") == 0;
+  p.int4_form = (want_f8 && int4f8_supported(p.a_mn, d.M, d.K, p.group) && p.kb_per_split % 2 == 0) ? 2 : 1;
   p.off_aprep = off;
   if (p.int4_form == 2) {
     // three e4m3 terms of 16 rows per 128-deep block, then 1 / S_b and the

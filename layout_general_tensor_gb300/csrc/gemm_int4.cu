@@ -110,7 +110,6 @@ struct Cfg4 {
   static_assert(TSLOTS % NI == 0 && XST % NI == 0, "one issuer per slot and per activation buffer");
   static_assert(2 * NI * BN <= static_cast<int>(kASlotCol0), "accumulators fit below the A slots");
   static_assert(kASlotCol0 + TSLOTS * 128 <= 512, "A slots fit in the TMEM allocation");
-  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
@@ -135,28 +134,8 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 
-__device__ __forceinline__ void tc_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 
-__device__ __forceinline__ void tc_st_32x32b_x16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
 
-__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.
 __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -359,7 +338,8 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   const int lane = threadIdx.x & 31;
   const uint32_t bar0 = base + C::BAR_OFF;
   // full_w[s] / full_x[s]: a packed-weight / activation stage landed.
-  // wfree[s]: the stage's eight expander warps read its packed weights.
+  // wfree[s]: every thread of the stage's eight expander warps read its
+  // packed weights.
   // xfree[s]: the MMAs that read the activation stage completed (the stage's
   // issuer commits).  a_full[t]: the expanders wrote a stage's weights into
   // TMEM A slot t.  tfree[t]: the MMAs reading slot t completed (the stage's
@@ -381,7 +361,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::WST; ++i) {
       mbar_init(full_w(i), 1);
-      mbar_init(wfree(i), 8);
+      mbar_init(wfree(i), 8 * 32);  // every expander thread, after its loads returned
     }
     for (int i = 0; i < C::XST; ++i) {
       mbar_init(full_x(i), 1);
@@ -606,8 +586,11 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         uint4 raw[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) raw[c] = *reinterpret_cast<const uint4*>(rowp + (((4 * h + c) ^ (r & 7)) << 4));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(wfree(sw));
+        // hand the stage back once this thread's loads have returned (the
+        // arrive depends on their values)
+        const uint32_t dep = raw[0].x ^ raw[0].y ^ raw[0].z ^ raw[0].w ^ raw[1].x ^ raw[1].y ^ raw[1].z ^ raw[1].w ^
+                             raw[2].x ^ raw[2].y ^ raw[2].z ^ raw[2].w ^ raw[3].x ^ raw[3].y ^ raw[3].z ^ raw[3].w;
+        mbar_arrive_after(wfree(sw), base + C::MISC_OFF + 8u, dep);  // (misc word 2: the scratch sink)
         const uint32_t slot = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + kASlotCol0 +
                               static_cast<uint32_t>(t * 128);
         // unrolled, so that raw[] stays in registers (nk is warp-uniform)
@@ -629,11 +612,10 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
             vals[4 * w8 + 2] = hfma2(lop3_and_or(hi, 0x000F000Fu, 0x64006400u), s2, c1024);
             vals[4 * w8 + 3] = hfma2(lop3_and_or(hi, 0x00F000F0u, 0x54005400u), s2, c64);
           }
-          // two 16-column stores (measured faster per byte than one of 32 columns)
-          tc_st_32x32b_x16(slot + static_cast<uint32_t>(j * 32), vals);
-          tc_st_32x32b_x16(slot + static_cast<uint32_t>(j * 32 + 16), vals + 16);
+          // store and wait in one statement: the source registers are read
+          // before the next K block's values are formed in them
+          tc_st_32x32b_x32_wait(slot + static_cast<uint32_t>(j * 32), vals);
         }
-        tc_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(a_full(t));

@@ -51,16 +51,16 @@
 //   segment   = 128 of K (one K block of the e4m3 operand): its activation
 //               box (48 rows x 128 bytes), its TMEM A slot (32 columns), its
 //               four MMAs and its own 48-column accumulator.
-// Warp roles (576 threads):
+// Warp roles (512 threads: 128 registers a thread, none spilled):
 //   warp 0       TMA producer of the weight ring (one copy per W stage).
 //   warp 1       TMA producer of the activation ring (one copy per segment).
-//   warps 2..5   MMA issuers: segment s goes to issuer s % 4, which issues its
+//   warps 2, 3   MMA issuers: segment s goes to issuer s % 2, which issues its
 //                four MMAs back to back into accumulator slot s % 4.  Warp 2
 //                owns the TMEM.
-//   warps 6..9   epilogue (TMEM lane quadrant warp % 4): per segment, read
+//   warps 4..7   epilogue (TMEM lane quadrant warp % 4): per segment, read
 //                the accumulator, free it, scale and add into the run's fp32
 //                sums; at the end of a run store C or the split-K partial.
-//   warps 10..17 expanders, two per lane quadrant: warp h of a quadrant
+//   warps 8..15  expanders, two per lane quadrant: warp h of a quadrant
 //                expands segment h of every W stage for its 32 weight rows.
 // Every barrier that several threads wait on is waited on for each of its
 // phases in order (no waiter can skip a phase and mistake an older one for
@@ -75,18 +75,18 @@
 namespace lgt {
 namespace {
 
-constexpr int kF8Threads = 576;
+constexpr int kF8Threads = 512;
 constexpr int kF8IssWarp0 = 2;
-constexpr int kF8Issuers = 4;
-constexpr int kF8EpiWarp0 = 6;
-constexpr int kF8ExpWarp0 = 10;
+constexpr int kF8Issuers = 2;
+constexpr int kF8EpiWarp0 = 4;
+constexpr int kF8ExpWarp0 = 8;
 constexpr int kF8N = 48;                       // MMA N: three e4m3 terms x 16 activation rows
 constexpr uint32_t kF8WStage = 128 * 128;      // packed weights of one W stage
 constexpr uint32_t kF8XStage = kF8N * 128;     // activation box of one segment: 6 KiB
 constexpr int kF8WST = 8;                      // weight ring
-constexpr int kF8XST = 8;                      // activation ring (a multiple of the issuers)
+constexpr int kF8XST = 4;                      // activation ring (a multiple of the issuers)
 constexpr int kF8TSL = 8;                      // TMEM A slots (a multiple of the issuers)
-constexpr int kF8ASL = kF8Issuers;             // accumulator slots: one per issuer
+constexpr int kF8ASL = 4;                      // accumulator slots (a multiple of the issuers)
 constexpr uint32_t kF8ACol0 = 256;             // A slots at TMEM columns [256, 512); accumulators below
 constexpr int kF8TabBlocks = 256;              // activation tables staged in shared memory up to this many blocks
 constexpr uint32_t kF8TabBytes = 2 * kF8TabBlocks * 16 * 4;
@@ -97,10 +97,12 @@ constexpr uint32_t kF8BarOff = kF8TabOff + kF8TabBytes;
 constexpr uint32_t kF8NumBars = 2 * kF8WST + 2 * kF8XST + 2 * kF8TSL + 2 * kF8ASL + 1;
 constexpr uint32_t kF8MiscOff = kF8BarOff + kF8NumBars * 8;
 constexpr uint32_t kF8Smem = kF8MiscOff + 64 + 1024;
-static_assert(kF8TSL % kF8Issuers == 0 && kF8XST % kF8Issuers == 0, "one issuer per A slot and activation buffer");
+static_assert(kF8TSL % kF8Issuers == 0 && kF8XST % kF8Issuers == 0 && kF8ASL % kF8Issuers == 0,
+              "one issuer per A slot, activation buffer and accumulator slot");
 static_assert(kF8ASL * kF8N <= static_cast<int>(kF8ACol0) && kF8ACol0 + kF8TSL * 32 <= 512, "TMEM columns");
 static_assert(kF8XStage % 1024 == 0 && kF8WStage % 1024 == 0, "swizzled buffers stay 1024-byte aligned");
 static_assert(kF8Smem <= 227 * 1024, "shared memory budget");
+static_assert(kF8Issuers >= 1 && kF8IssWarp0 + kF8Issuers <= kF8EpiWarp0, "issuer warps lie between the producers and the epilogue");
 
 // D[tmem] (+)= A[tmem] * B[smem desc], kind::f8f6f4 (e4m3 x e4m3, fp32 accumulate).
 __device__ __forceinline__ void tc_mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -113,20 +115,68 @@ __device__ __forceinline__ void tc_mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
-__device__ __forceinline__ void tc_st_x16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_wait_st_f8() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
 __device__ __forceinline__ float half_bits_f32(uint32_t b) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(b)));
 }
+
+// One weight row's scales and zero points, in group order, for the
+// epilogue: read 8 groups (16 bytes) at a time with the next window already
+// in flight (rows 16-byte aligned, groups a multiple of 8), else one group at
+// a time with the next group in flight.  Each load is issued a window (or a
+// group) before it is needed, so its latency under the weight stream is
+// hidden behind the segments in between.
+struct RowParams {
+  const uint16_t* srow = nullptr;  // null: row beyond N (scale 0)
+  const uint16_t* zrow = nullptr;  // null: zero point 8
+  int G = 0;
+  bool vec = false;
+  int wcur = -2;
+  uint4 s_cur, z_cur, s_nxt, z_nxt;
+  __device__ uint4 load(const uint16_t* row, int w, uint32_t dflt) const {
+    if (!row || (vec ? w * 8 : w) >= G) return make_uint4(dflt, dflt, dflt, dflt);
+    if (vec) return __ldg(reinterpret_cast<const uint4*>(row) + w);
+    return make_uint4(static_cast<uint32_t>(__ldg(row + w)), 0u, 0u, 0u);  // scalar mode: "window" = one group
+  }
+  __device__ void reset(const uint16_t* s, const uint16_t* z, int groups, bool v, int g0) {
+    srow = s;
+    zrow = z;
+    vec = v;
+    G = groups;
+    wcur = -2;
+    fetch(g0);
+  }
+  __device__ int window_of(int g) const { return vec ? (g >> 3) : g; }
+  __device__ void fetch(int g) {
+    const int w = window_of(g);
+    if (w == wcur) return;
+    if (w == wcur + 1) {
+      s_cur = s_nxt;
+      z_cur = z_nxt;
+    } else {
+      s_cur = load(srow, w, 0u);
+      z_cur = load(zrow, w, 0x48004800u);  // fp16 8.0 pairs
+    }
+    s_nxt = load(srow, w + 1, 0u);
+    z_nxt = load(zrow, w + 1, 0x48004800u);
+    wcur = w;
+  }
+  __device__ void get(int g, float& s, float& z) {
+    fetch(g);
+    uint32_t sb, zb;
+    if (vec) {
+      const int e = g & 7;
+      const uint32_t sw = e < 4 ? (e < 2 ? s_cur.x : s_cur.y) : (e < 6 ? s_cur.z : s_cur.w);
+      const uint32_t zw = e < 4 ? (e < 2 ? z_cur.x : z_cur.y) : (e < 6 ? z_cur.z : z_cur.w);
+      sb = (e & 1) ? (sw >> 16) : (sw & 0xFFFFu);
+      zb = (e & 1) ? (zw >> 16) : (zw & 0xFFFFu);
+    } else {
+      sb = s_cur.x & 0xFFFFu;
+      zb = z_cur.x & 0xFFFFu;
+    }
+    s = half_bits_f32(sb);
+    z = half_bits_f32(zb);
+  }
+};
 
 // Segments of this CTA, in order: every run of (tile, splits) from the
 // scheduler, cut into 128-deep segments, two per W stage.
@@ -259,8 +309,8 @@ __global__ void __launch_bounds__(kF8Threads, 1) int4f8_gemm_kernel(const __grid
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t bar0 = base + kF8BarOff;
-  // full_w[i] / full_x[i]: a weight / activation copy landed.  wfree[i]: the
-  // eight expander warps read the W stage.  xfree[i]: the MMAs reading the
+  // full_w[i] / full_x[i]: a weight / activation copy landed.  wfree[i]:
+  // every thread of the eight expander warps read the W stage.  xfree[i]: the MMAs reading the
   // activation buffer completed.  a_full[t]: the four expander warps of a
   // segment wrote A slot t.  tfree[t]: the MMAs reading A slot t completed.
   // accf[i] / acce[i]: accumulator slot i complete / drained.
@@ -279,7 +329,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) int4f8_gemm_kernel(const __grid
   if (threadIdx.x == 0) {
     for (int i = 0; i < kF8WST; ++i) {
       mbar_init(full_w(i), 1);
-      mbar_init(wfree(i), 8);
+      mbar_init(wfree(i), 8 * 32);  // every expander thread, after its loads returned
     }
     for (int i = 0; i < kF8XST; ++i) {
       mbar_init(full_x(i), 1);
@@ -339,64 +389,85 @@ __global__ void __launch_bounds__(kF8Threads, 1) int4f8_gemm_kernel(const __grid
     // ------------------------------------------------------------ activation producer
     if (lane == 0) {
       SegRun it(a);
+      int ws = 0;
       bool ok = true;
       while (ok && it.next(a)) {
-        for (int j = 0; j < it.nseg; ++j) {
-          const int s = x_issued % kF8XST;
-          if (!mbar_wait_bounded(xfree(s), ((x_issued / kF8XST) & 1) ^ 1u, a.wait_limit_ns, abort_flag)) {
-            if (!*abort_flag) record_timeout(a, abort_flag, 0 * 16 + 2);
-            ok = false;
-            break;
+        for (int j = 0; ok && j < it.nseg; j += 2, ++ws) {
+          for (int h = 0; h < 2; ++h) {
+            const int sg = 2 * ws + h, s = sg % kF8XST;
+            if (!mbar_wait_bounded(xfree(s), ((sg / kF8XST) & 1) ^ 1u, a.wait_limit_ns, abort_flag)) {
+              if (!*abort_flag) record_timeout(a, abort_flag, 0 * 16 + 2);
+              ok = false;
+              break;
+            }
+            if (j + h < it.nseg) {
+              mbar_arrive_expect_tx(full_x(s), kF8XStage);
+              tma_load_3d(base + kF8XOff + s * kF8XStage, &a.tm_q, full_x(s), 0, 0, (it.g.kb0 >> 1) + j + h);
+              x_issued = sg + 1;
+            } else {
+              mbar_arrive(full_x(s));  // the empty second segment of a run's last W stage
+            }
           }
-          mbar_arrive_expect_tx(full_x(s), kF8XStage);
-          tma_load_3d(base + kF8XOff + s * kF8XStage, &a.tm_q, full_x(s), 0, 0, (it.g.kb0 >> 1) + j);
-          ++x_issued;
         }
       }
     }
-  } else if (warp < kF8IssWarp0 + kF8Issuers) {
+  } else if (warp < kF8EpiWarp0) {
     // ------------------------------------------------------------ MMA issuers
+    // Segment sg = 2 * (W stage) + h goes to issuer sg % 2 and uses A slot
+    // sg % 8, activation buffer sg % 4 and accumulator slot sg % 4 (all
+    // multiples of the issuer count, so every slot's and buffer's barriers
+    // have one waiting issuer, which sees each of their phases in order).  An empty segment (the
+    // second of a run's last W stage when the run has an odd number) issues
+    // no MMA but keeps every barrier's phase count.
     const int iss = warp - kF8IssWarp0;
-    if (lane == 0) {
+    if (lane == 0 && iss < kF8Issuers) {
       SegRun it(a);
-      int sg = 0;  // the CTA's segment counter
+      int ws = 0;
       bool ok = true;
       // B: 48 rows of 128 bytes (K-major, 128-byte swizzle, 8-row atoms 1 KiB
       // apart); +32 bytes per 32-deep step.  A: 8 TMEM columns per step.
       while (ok && it.next(a)) {
-        for (int j = 0; j < it.nseg; ++j, ++sg) {
-          if (sg % kF8Issuers != iss) continue;
-          const int acc = sg % kF8ASL, t = sg % kF8TSL, x = sg % kF8XST;
-          if (!mbar_wait_bounded(acce(acc), ((sg / kF8ASL) & 1) ^ 1u, a.wait_limit_ns, abort_flag) ||
-              !mbar_wait_bounded(a_full(t), (sg / kF8TSL) & 1, a.wait_limit_ns, abort_flag) ||
-              !mbar_wait_bounded(full_x(x), (sg / kF8XST) & 1, a.wait_limit_ns, abort_flag)) {
-            if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 4);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kF8N);
-          const uint32_t a0 = tmem_base + kF8ACol0 + static_cast<uint32_t>(t * 32);
-          const uint64_t bd0 = sw128_desc(base + kF8XOff + x * kF8XStage, 16u, 1024u);
+        for (int j = 0; ok && j < it.nseg; j += 2, ++ws) {
+          for (int h = 0; h < 2; ++h) {
+            const int sg = 2 * ws + h;
+            if (sg % kF8Issuers != iss) continue;
+            const int acc = sg % kF8ASL, t = sg % kF8TSL, x = sg % kF8XST;
+            if (!mbar_wait_bounded(acce(acc), ((sg / kF8ASL) & 1) ^ 1u, a.wait_limit_ns, abort_flag) ||
+                !mbar_wait_bounded(a_full(t), (sg / kF8TSL) & 1, a.wait_limit_ns, abort_flag) ||
+                !mbar_wait_bounded(full_x(x), (sg / kF8XST) & 1, a.wait_limit_ns, abort_flag)) {
+              if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 4);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (j + h < it.nseg) {
+              const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kF8N);
+              const uint32_t a0 = tmem_base + kF8ACol0 + static_cast<uint32_t>(t * 32);
+              const uint64_t bd0 = sw128_desc(base + kF8XOff + x * kF8XStage, 16u, 1024u);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) tc_mma_f8_ts(d, a0 + 8u * k, bd0 + 2u * k, a.idesc, k ? 1u : 0u);
-          tc_commit(tfree(t));
-          tc_commit(xfree(x));
-          tc_commit(accf(acc));
+              for (int k = 0; k < 4; ++k) tc_mma_f8_ts(d, a0 + 8u * k, bd0 + 2u * k, a.idesc, k ? 1u : 0u);
+            }
+            tc_commit(tfree(t));
+            tc_commit(xfree(x));
+            tc_commit(accf(acc));
+          }
         }
       }
     }
   } else if (warp >= kF8ExpWarp0) {
     // ------------------------------------------------------------ expanders
+    // Warp h of each lane quadrant expands segment 2 * (W stage) + h, whose A
+    // slot (sg % 8, so of this warp's parity) only its four warps write and
+    // wait on, every phase in order.
     const int q4 = warp & 3;
     const int h = (warp - kF8ExpWarp0) >> 2;  // segment h of every W stage
     const int r = q4 * 32 + lane;             // weight row within the tile (TMEM lane)
     SegRun it(a);
-    int ws = 0, sg = 0;  // W stages and segments seen
+    int ws = 0;  // W stages seen
     bool ok = true;
     while (ok && it.next(a)) {
-      for (int j = 0; j < it.nseg; j += 2, ++ws) {
-        const int cnt = min(2, it.nseg - j);
+      for (int j = 0; ok && j < it.nseg; j += 2, ++ws) {
+        const bool real = j + h < it.nseg;
         const int sw = ws % kF8WST;
         bool got = mbar_wait_bounded(full_w(sw), (ws / kF8WST) & 1, a.wait_limit_ns, abort_flag);
         if (!got && !*abort_flag) record_timeout(a, abort_flag, 3 * 16 + 0);
@@ -407,47 +478,41 @@ __global__ void __launch_bounds__(kF8Threads, 1) int4f8_gemm_kernel(const __grid
         // row r: eight 16-byte chunks, chunk c stored at c ^ (r mod 8); this
         // warp's segment is chunks 4h .. 4h + 3
         uint4 raw[4] = {};
-        if (h < cnt) {
+        if (real) {
           const uint8_t* rowp = smem + sw * kF8WStage + r * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c) raw[c] = *reinterpret_cast<const uint4*>(rowp + (((4 * h + c) ^ (r & 7)) << 4));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(wfree(sw));
-        for (int jj = 0; jj < cnt; ++jj) {
-          const int s2 = sg + jj, t = s2 % kF8TSL;
-          // every phase of every slot's tfree is waited on in order, also for the other warp's segment
-          got = mbar_wait_bounded(tfree(t), ((s2 / kF8TSL) & 1) ^ 1u, a.wait_limit_ns, abort_flag);
-          if (!got && !*abort_flag) record_timeout(a, abort_flag, 3 * 16 + 1);
-          if (!__all_sync(0xffffffffu, got)) {
-            ok = false;
-            break;
-          }
-          if (jj != h) continue;
+        // hand the stage back once this thread's loads have returned (the
+        // arrive depends on their values)
+        const uint32_t dep = raw[0].x ^ raw[0].y ^ raw[0].z ^ raw[0].w ^ raw[1].x ^ raw[1].y ^ raw[1].z ^ raw[1].w ^
+                             raw[2].x ^ raw[2].y ^ raw[2].z ^ raw[2].w ^ raw[3].x ^ raw[3].y ^ raw[3].z ^ raw[3].w;
+        mbar_arrive_after(wfree(sw), base + kF8MiscOff + 8u, dep);  // (misc word 2: the scratch sink)
+        const int sg = 2 * ws + h, t = sg % kF8TSL;
+        got = mbar_wait_bounded(tfree(t), ((sg / kF8TSL) & 1) ^ 1u, a.wait_limit_ns, abort_flag);
+        if (!got && !*abort_flag) record_timeout(a, abort_flag, 3 * 16 + 1);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        if (real) {
           tc_fence_after();
           const uint32_t slot = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + kF8ACol0 +
                                 static_cast<uint32_t>(t * 32);
+          const uint32_t words[16] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w,
+                                      raw[2].x, raw[2].y, raw[2].z, raw[2].w, raw[3].x, raw[3].y, raw[3].z, raw[3].w};
+          uint32_t v[32];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t words[8] = {raw[2 * half].x,     raw[2 * half].y,     raw[2 * half].z,
-                                       raw[2 * half].w,     raw[2 * half + 1].x, raw[2 * half + 1].y,
-                                       raw[2 * half + 1].z, raw[2 * half + 1].w};
-            uint32_t v[16];
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-              // codes k0..k7 of a word: even k in the low nibbles, odd k in the high ones
-              v[2 * w] = words[w] & 0x0F0F0F0Fu;
-              v[2 * w + 1] = (words[w] >> 4) & 0x0F0F0F0Fu;
-            }
-            tc_st_x16(slot + 16u * half, v);
+          for (int w = 0; w < 16; ++w) {
+            // codes k0..k7 of a word: even k in the low nibbles, odd k in the high ones
+            v[2 * w] = words[w] & 0x0F0F0F0Fu;
+            v[2 * w + 1] = (words[w] >> 4) & 0x0F0F0F0Fu;
           }
-          tc_wait_st_f8();
+          tc_st_32x32b_x32_wait(slot, v);  // store and wait in one statement (source registers)
           tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(a_full(t));
         }
-        if (!ok) break;
-        sg += cnt;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(a_full(t));
       }
     }
   } else {
@@ -476,7 +541,8 @@ __global__ void __launch_bounds__(kF8Threads, 1) int4f8_gemm_kernel(const __grid
     // tile's arrival counter, with a zero partial)
     Sched sched(a);
     Group g;
-    int sg = 0;
+    RowParams rp;
+    int ws = 0;  // W stages seen (segment sg = 2 ws + h)
     bool ok = true;
     while (ok && sched.next(a, g)) {
       const int nseg = g.nkb >> 1;
@@ -484,30 +550,46 @@ __global__ void __launch_bounds__(kF8Threads, 1) int4f8_gemm_kernel(const __grid
       tile_ranges(a, g.tile, 16, tp, tq, m0, m1, n0, n1);
       const int n = n0 + row;
       const bool live = n < n1;
-      const uint16_t* srow = live ? A4.scales + static_cast<int64_t>(n) * A4.groups : nullptr;
-      const uint16_t* zrow = (live && A4.zeros) ? A4.zeros + static_cast<int64_t>(n) * A4.groups : nullptr;
+      const int g_first = static_cast<int>(magic_div(static_cast<uint32_t>(g.kb0), A4.div_kb_per_group));
+      rp.reset(live ? A4.scales + static_cast<int64_t>(n) * A4.groups : nullptr,
+               (live && A4.zeros) ? A4.zeros + static_cast<int64_t>(n) * A4.groups : nullptr, A4.groups,
+               A4.vec_sz != 0, g_first);
       float out[16];
 #pragma unroll
       for (int m = 0; m < 16; ++m) out[m] = 0.0f;
       int gcur = -1;
       float sg512 = 0.0f, szg = 0.0f;
-      for (int j = 0; j < nseg; ++j, ++sg) {
+      for (int j = 0; j < nseg + (nseg & 1); ++j) {
+        const int sg = 2 * ws + (j & 1);
+        if (j & 1) ++ws;
         const int blk = (g.kb0 >> 1) + j;  // 128-deep block of K
+        if (j >= nseg) {
+          // the empty second segment of the run's last W stage: its slot
+          // holds nothing of this run; just pass it back
+          const int acc = sg % kF8ASL;
+          const bool got = mbar_wait_bounded(accf(acc), (sg / kF8ASL) & 1, a.wait_limit_ns, abort_flag);
+          if (!got && !*abort_flag) record_timeout(a, abort_flag, 2 * 16 + 9);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acce(acc));
+          continue;
+        }
         const int gi = static_cast<int>(magic_div(static_cast<uint32_t>(2 * blk), A4.div_kb_per_group));
         if (gi != gcur) {
           gcur = gi;
-          float s = 0.0f, z = 8.0f;
-          if (srow) {
-            s = half_bits_f32(__ldg(srow + gi));
-            if (zrow) z = half_bits_f32(__ldg(zrow + gi));
-          }
+          float s, z;
+          rp.get(gi, s, z);
           sg512 = 512.0f * s;
           szg = s * z;
         }
         const int acc = sg % kF8ASL;
         const bool got = mbar_wait_bounded(accf(acc), (sg / kF8ASL) & 1, a.wait_limit_ns, abort_flag);
         if (!got && !*abort_flag) record_timeout(a, abort_flag, 2 * 16 + 8);
-        if (named_bar_or(1, kEpiThreads, !got)) {
+        // (each warp decides on its own; the four agree at the end of the run)
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
@@ -520,11 +602,12 @@ __global__ void __launch_bounds__(kF8Threads, 1) int4f8_gemm_kernel(const __grid
           uint32_t d1[16], d2[16];
           tc_ld_32x32b_x16(t0, d1);
           tc_ld_32x32b_x16(t0 + 16u, d2);
-          tc_wait_ld();
+          tc_wait_ld_regs(d1);
+          tc_regs_after_wait(d2);
 #pragma unroll
           for (int m = 0; m < 16; ++m) v[m] = fmaf(__uint_as_float(d2[m]), 0.0625f, __uint_as_float(d1[m]));
           tc_ld_32x32b_x16(t0 + 32u, d1);
-          tc_wait_ld();
+          tc_wait_ld_regs(d1);
 #pragma unroll
           for (int m = 0; m < 16; ++m) v[m] = fmaf(__uint_as_float(d1[m]), 0.00390625f, v[m]);
         }
@@ -543,7 +626,11 @@ __global__ void __launch_bounds__(kF8Threads, 1) int4f8_gemm_kernel(const __grid
           }
         }
       }
-      if (!ok) break;
+      // all four epilogue warps leave together if any of them gave up a wait
+      if (named_bar_or(1, kEpiThreads, !ok)) {
+        ok = false;
+        break;
+      }
       // the run's total: C, or the split-K partial and the tile's arrival
       const bool full_tile = (g.s0 == 0 && g.s1 == a.split);
       if (a.det && !full_tile) {

@@ -82,6 +82,24 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
+// Hand a buffer back to a TMA producer after reading it with ordinary shared
+// loads.  `dep` is a value computed from everything the thread loaded; it is
+// stored to the scratch word `sink` before the arrive.  The store cannot issue
+// before the loads have returned, and the arrive (a release) is performed
+// after the store, so the producer's next copy cannot overtake the loads (an
+// operand the arrive instruction does not itself use orders nothing: the
+// assembler drops the computation and lets the arrive go first).  The proxy
+// fence orders the thread's generic accesses before the async-proxy writes of
+// that copy.
+__device__ __forceinline__ void mbar_arrive_after(uint32_t bar, uint32_t sink, uint32_t dep) {
+  asm volatile(
+      "st.volatile.shared.u32 [%1], %2;\n\t"
+      "fence.proxy.async.shared::cta;\n\t"
+      "mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar),
+      "r"(sink), "r"(dep)
+      : "memory");
+}
+
 // Non-blocking probe: has the phase with the given parity completed?
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -207,6 +225,41 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 
 __device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// The destination registers of tcgen05.ld are defined only after
+// tcgen05.wait::ld, but nothing ties them to the wait: the compiler may move
+// arithmetic on them above it (it sees no dependency), and that arithmetic
+// then reads the registers' old contents.  After the wait, an empty asm that
+// "rewrites" each register makes every later use depend on a point after the
+// wait (volatile asm statements keep their order).
+template <int N>
+__device__ __forceinline__ void tc_regs_after_wait(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns from 32 registers, and the wait
+// for its completion in the same asm statement: tcgen05.st may read its source
+// registers after it issues (until tcgen05.wait::st), and the compiler, which
+// does not know that, could otherwise reuse them for later values.
+__device__ __forceinline__ void tc_st_32x32b_x32_wait(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void tc_wait_ld_regs(uint32_t (&r)[N]) {
+  tc_wait_ld();
+  tc_regs_after_wait(r);
 }
 
 // 32 lanes x 32 bits, 16 consecutive columns: thread i gets columns

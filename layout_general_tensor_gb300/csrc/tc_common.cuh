@@ -258,6 +258,12 @@ __device__ __noinline__ void finish_tile_det(const TcArgs& a, const float* slot0
 // this arrival completes the tile, convert it (the CTA that arrives last
 // reads the full sum from L2), then reset the counter.
 // FU: loads in flight per thread in the conversion (registers permitting).
+// Ordering: every thread's partial adds are fenced before the barrier; the
+// counting thread fences again after it (so that its count, at GPU scope,
+// follows the adds of the whole CTA it has synchronised with: a relaxed
+// atomic after a CTA barrier alone does not publish other threads' writes)
+// and after its atomic (so that the reads of a finishing CTA follow every
+// count it has seen).
 template <int FU = 8>
 __device__ __forceinline__ void arrive_split_tile(const TcArgs& a, const Group& g, int counter, int m0, int m1, int n0,
                                                   int n1, int et) {
@@ -266,13 +272,18 @@ __device__ __forceinline__ void arrive_split_tile(const TcArgs& a, const Group& 
   if (a.tail_tiles) {
     // stream-K tail: count the arrival only; every CTA finishes a share of
     // the tail tiles at the end (finish_tail)
-    if (et == 0) atomicAdd(&a.counters[counter], g.s1 - g.s0);
+    if (et == 0) {
+      __threadfence();
+      atomicAdd(&a.counters[counter], g.s1 - g.s0);
+    }
     return;
   }
   bool mine_last = false;
   if (et == 0) {
+    __threadfence();
     const int old = atomicAdd(&a.counters[counter], g.s1 - g.s0);
     mine_last = (old + (g.s1 - g.s0) == a.split);
+    __threadfence();
   }
   if (named_bar_or(1, kEpiThreads, mine_last)) {
     __threadfence();
@@ -375,8 +386,10 @@ __device__ __noinline__ void arrive_split_tile_det(const TcArgs& a, const Group&
   named_bar_sync(1, kEpiThreads);
   bool mine_last = false;
   if (et == 0) {
+    __threadfence();  // (see arrive_split_tile)
     const int old = atomicAdd(&a.counters[counter], g.s1 - g.s0);
     mine_last = (old + (g.s1 - g.s0) == a.split);
+    __threadfence();
   }
   if (named_bar_or(1, kEpiThreads, mine_last)) {
     __threadfence();
@@ -424,7 +437,9 @@ __device__ __forceinline__ void ld_acc(uint32_t taddr, uint32_t (&v)[N], uint32_
     for (int i = 1; i < NACC; ++i) {
       if constexpr (N == 32) tc_ld_32x32b_x32(taddr + i * ST, w[i - 1]); else tc_ld_32x32b_x16(taddr + i * ST, w[i - 1]);
     }
-    tc_wait_ld();
+    tc_wait_ld_regs(v);
+#pragma unroll
+    for (int i = 1; i < NACC; ++i) tc_regs_after_wait(w[i - 1]);
     if (!v0) {
 #pragma unroll
       for (int j = 0; j < N; ++j) v[j] = 0u;  // +0.0f: adding the valid ones to it is exact
@@ -435,7 +450,7 @@ __device__ __forceinline__ void ld_acc(uint32_t taddr, uint32_t (&v)[N], uint32_
 #pragma unroll
         for (int j = 0; j < N; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(w[i - 1][j]));
   } else {
-    tc_wait_ld();
+    tc_wait_ld_regs(v);
   }
 }
 
@@ -524,7 +539,7 @@ __device__ __noinline__ bool cluster_split_tile(const TcArgs& a, const Group& g,
       for (int c0 = 0; c0 < BN; c0 += 16) {
         uint32_t t[16];
         tc_ld_32x32b_x16(t_row + c0, t);
-        tc_wait_ld();
+        tc_wait_ld_regs(t);
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[c0 + j] = t[j];
       }
@@ -796,7 +811,7 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
     if (a.det)
       arrive_split_tile_det<BN>(a, g, cidx, m0, m1, n0, n1, et);
     else
-      arrive_split_tile<16>(a, g, cidx, m0, m1, n0, n1, et);
+      arrive_split_tile<4>(a, g, cidx, m0, m1, n0, n1, et);  // (4 loads in flight: no spills at the int4 kernels' register caps)
   }
   return true;
 }

@@ -30,6 +30,11 @@ def _built():
     lib()
 
 
+@pytest.fixture(autouse=True)
+def _e4m3(monkeypatch):
+    monkeypatch.setenv("LGT_GEMM_INT4_FORM", "e4m3")
+
+
 @pytest.mark.parametrize("M", [1, 9, 16])
 @pytest.mark.parametrize("N,Kd,split,group", [(128, 128, 1, 128), (256, 1024, 1, 128), (300, 2048, 2, 256),
                                                 (640, 4096, 4, 128), (384, 8192, 0, 512), (1000, 3072, 3, 128)])

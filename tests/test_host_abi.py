@@ -147,7 +147,7 @@ def test_planner_int4(lib):
     info = lib.gemm_query(h)
     assert info.kernel == 1 and info.swap_ab == 1 and info.split_k == 32
     assert info.tile_m == 16 and info.tile_n == 128 and info.k_per_split == 512
-    assert info.dequant_form == 2
+    assert info.dequant_form == 1
     assert lib.gemm_workspace_size(h) >= case.M * case.N * 4
     lib.gemm_destroy(h)
     bad = [dict(group_size=96), dict(group_size=512, K=768), dict(a_dtype=lib.GEMM_BF16)]
@@ -163,10 +163,10 @@ def test_planner_int4(lib):
 
 
 def test_planner_int4_form(lib, monkeypatch):
-    """The e4m3 form needs at most 16 activation rows, a K-contiguous
+    """Plans take the fp16 form unless LGT_GEMM_INT4_FORM=e4m3 asks for the
+    e4m3 form, which needs at most 16 activation rows, a K-contiguous
     activation, K and the group multiples of 128 and splits of whole 128-deep
-    blocks; everything else takes the fp16 form, and LGT_GEMM_INT4_FORM=fp16
-    forces it."""
+    blocks (everything else stays on the fp16 form)."""
     def form(M, N, K, group=128, split=1, a_layout=wl.K_CONTIG):
         d = lib.make_desc(M, N, K, a_layout=a_layout, a_dtype=lib.GEMM_F16, b_dtype=lib.GEMM_INT4,
                           c_dtype=lib.GEMM_F16, split_k=split, group_size=group, num_sms=148)
@@ -174,6 +174,8 @@ def test_planner_int4_form(lib, monkeypatch):
         f = lib.gemm_query(h).dequant_form
         lib.gemm_destroy(h)
         return f
+    assert form(16, 512, 1024) == 1 and form(1, 256, 128) == 1
+    monkeypatch.setenv("LGT_GEMM_INT4_FORM", "e4m3")
     assert form(16, 512, 1024) == 2 and form(1, 256, 128) == 2 and form(9, 300, 2048, 256, 2) == 2
     assert form(17, 512, 1024) == 1                        # more than 16 activation rows
     assert form(16, 512, 1024, group=64) == 1              # group below 128
