@@ -68,8 +68,6 @@ constexpr int kExpWarp0 = 8;                  // expander warps 8..15
 constexpr int kQuadK = 4;                     // K blocks per stage
 constexpr uint32_t kRawBytes = TILE_P * 128;  // 128 rows x 128 bytes (256 codes)
 constexpr uint32_t kWStage = kRawBytes;       // packed-weight stage
-constexpr int kScWins = 4;                    // scale windows per expander warp's ring
-constexpr uint32_t kScRingBytes = kScWins * 32 * 16;
 constexpr uint32_t kASlotCol0 = 128;          // A slots at [128, 512); the accumulators below
 
 template <int BN>
@@ -91,15 +89,12 @@ struct Cfg4 {
   // the tile's slice of the activation group sums, Ag[g][m0 .. m0 + BN),
   // staged in shared memory for the zero-point term (BN = 16, up to 256 groups)
   static constexpr uint32_t ZP_BYTES = BN == 16 ? 256 * BN * 4 : 0;
-  // each expander warp's ring of scale windows (8 groups x 32 rows, 4 windows)
-  static constexpr uint32_t SC_BYTES = 8 * kScRingBytes;
-  static constexpr uint32_t RING_BYTES = 224 * 1024 - ZP_BYTES - SC_BYTES;
+  static constexpr uint32_t RING_BYTES = 224 * 1024 - ZP_BYTES;
   static constexpr int WST_FIT = static_cast<int>((RING_BYTES - XST * XSTAGE) / kWStage);
   static constexpr int WST = WST_FIT > 12 ? 12 : WST_FIT;  // packed-weight ring
   static constexpr uint32_t X_OFF = WST * kWStage;
   // barriers: full_w[W], wfree[W], full_x[X], xfree[X], a_full[T], tfree[T], accf[2], acce[2], teardown
-  static constexpr uint32_t SC_OFF = X_OFF + XST * XSTAGE;
-  static constexpr uint32_t ZP_OFF = SC_OFF + SC_BYTES;
+  static constexpr uint32_t ZP_OFF = X_OFF + XST * XSTAGE;
   static constexpr uint32_t BAR_OFF = ZP_OFF + ZP_BYTES;
   static constexpr uint32_t NUM_BARS = 2 * WST + 2 * XST + 2 * TSLOTS + 5;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
@@ -338,8 +333,8 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   const int lane = threadIdx.x & 31;
   const uint32_t bar0 = base + C::BAR_OFF;
   // full_w[s] / full_x[s]: a packed-weight / activation stage landed.
-  // wfree[s]: every thread of the stage's eight expander warps read its
-  // packed weights.
+  // wfree[s]: the stage's eight expander warps have expanded its packed
+  // weights into TMEM.
   // xfree[s]: the MMAs that read the activation stage completed (the stage's
   // issuer commits).  a_full[t]: the expanders wrote a stage's weights into
   // TMEM A slot t.  tfree[t]: the MMAs reading slot t completed (the stage's
@@ -361,7 +356,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::WST; ++i) {
       mbar_init(full_w(i), 1);
-      mbar_init(wfree(i), 8 * 32);  // every expander thread, after its loads returned
+      mbar_init(wfree(i), 8);  // every expander warp, after its stores
     }
     for (int i = 0; i < C::XST; ++i) {
       mbar_init(full_x(i), 1);
@@ -508,22 +503,23 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
     const int h = (warp - kExpWarp0) >> 2;  // K blocks 2h, 2h + 1 of every stage
     const int r = q4 * 32 + lane;           // weight row within the tile (TMEM lane)
     StageIter it(a);
-    // This row's scales, 8 groups (16 bytes) per window, copied with
-    // cp.async into this warp's ring of kScWins windows in shared memory,
-    // three windows ahead of the one in use: the copies queue behind the
-    // weight stream in HBM for microseconds, and nothing waits on them until
-    // their window comes up.  (Rows not 16-byte aligned: one load per K block.)
+    // This row's scales, 8 groups (16 bytes) per window, held in registers:
+    // the window in use and the next two, each read by one 16-byte load two
+    // windows before it is needed, so that the load's latency hides behind the
+    // weight stream.  (Rows not 16-byte aligned: one load per K block.)
     const uint16_t* srow = nullptr;
-    int w_cur = 0, w_next = 0, w_last = -1;
-    const uint32_t sc_mine = base + C::SC_OFF + static_cast<uint32_t>(warp - kExpWarp0) * kScRingBytes +
-                             static_cast<uint32_t>(lane) * 16u;
-    auto issue_win = [&](int w) {
-      if (srow && w <= w_last) cp_async_16(sc_mine + static_cast<uint32_t>(w & (kScWins - 1)) * 512u, srow + 8 * w);
-      cp_async_commit();  // (an empty group for windows past the run keeps the count uniform)
+    int w_cur = 0, w_last = -1;
+    uint4 win0 = make_uint4(0u, 0u, 0u, 0u), win1 = win0, win2 = win0;  // windows w_cur .. w_cur + 2
+    auto load_win = [&](int w) {
+      return (srow && w <= w_last) ? __ldg(reinterpret_cast<const uint4*>(srow) + w) : make_uint4(0u, 0u, 0u, 0u);
     };
-    int kb0, nk, st = 0;
-    bool nr;
-    while (it.next(a, kb0, nk, nr)) {
+    // The scales of this warp's two K blocks of a stage as fp16 pairs s, with
+    // -1024 s and -64 s (exact: power-of-two multiples).  Looked up one stage
+    // ahead, while the stage before is expanded; a new run's windows start here.
+    struct StageScales {
+      uint32_t s2[2], c1024[2], c64[2];
+    };
+    auto lookup = [&](int kb0, int nk, bool nr, StageScales& o) {
       if (nr) {
         int32_t tp, tq, m0, m1, n0, n1;
         tile_ranges(a, it.g.tile, BN, tp, tq, m0, m1, n0, n1);
@@ -533,96 +529,116 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         const int g1 =
             static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + it.g.nkb - 1), A4.div_kb_per_group));
         if (A4.vec_sz) {
-          cp_async_wait<0>();  // the previous run's copies have landed before slots are reused
           w_cur = g0 >> 3;
           w_last = g1 >> 3;
-          issue_win(w_cur);
-          issue_win(w_cur + 1);
-          issue_win(w_cur + 2);
-          w_next = w_cur + 3;
-          cp_async_wait<2>();  // window w_cur is in place
+          win0 = load_win(w_cur);
+          win1 = load_win(w_cur + 1);
+          win2 = load_win(w_cur + 2);
         }
       }
-      {
-        // each K block's scale as an fp16 pair, and -1024 s, -64 s (exact:
-        // power-of-two multiples); formed before the waits below, whose time
-        // hides the latency of the lookup
-        uint32_t s2v[2], c1024v[2], c64v[2];
+      // group of each K block (the second one's is usually the first's: then
+      // the lookup is not repeated)
+      int gj[2];
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * h + jj;
-          uint32_t s2 = 0;
-          if (j < nk) {
-            const int g = static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + kb0 + j), A4.div_kb_per_group));
-            if (A4.vec_sz) {
-              const int w = g >> 3;
-              while (w_cur < w) {  // groups only grow within a run
-                ++w_cur;
-                issue_win(w_next++);
-                cp_async_wait<3>();  // window w_cur is in place (the 3 newer ones may be pending)
-              }
-              if (srow)
-                s2 = ld_shared_u16(sc_mine + static_cast<uint32_t>(w & (kScWins - 1)) * 512u +
-                                   static_cast<uint32_t>(g & 7) * 2u) * 0x10001u;
-            } else {
-              s2 = (srow ? static_cast<uint32_t>(__ldg(srow + g)) : 0u) * 0x10001u;
+      for (int jj = 0; jj < 2; ++jj)
+        gj[jj] = static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + kb0 + 2 * h + jj), A4.div_kb_per_group));
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = 2 * h + jj;
+        if (jj == 1 && gj[1] == gj[0]) {
+          o.s2[1] = j < nk ? o.s2[0] : 0u;
+          o.c1024[1] = o.c1024[0];
+          o.c64[1] = o.c64[0];
+          continue;
+        }
+        const int g = gj[jj];
+        uint32_t s2 = 0;
+        if (j < nk) {
+          if (A4.vec_sz) {
+            while (w_cur < (g >> 3)) {  // groups only grow within a run
+              win0 = win1;
+              win1 = win2;
+              win2 = load_win(w_cur + 3);
+              ++w_cur;
             }
+            // group g & 7 of the window: its 16 bits in both halves
+            const int e = g & 7;
+            const uint32_t word = e < 4 ? (e < 2 ? win0.x : win0.y) : (e < 6 ? win0.z : win0.w);
+            s2 = __byte_perm(word, 0u, (e & 1) ? 0x3232u : 0x1010u);
+          } else {
+            s2 = (srow ? static_cast<uint32_t>(__ldg(srow + g)) : 0u) * 0x10001u;
           }
-          s2v[jj] = s2;
-          c1024v[jj] = hmul2(s2, 0xE400E400u);
-          c64v[jj] = hmul2(s2, 0xD400D400u);
         }
-        const int sw = st % C::WST, t = st % C::TSLOTS;
-        const bool got =
-            mbar_wait_bounded(full_w(sw), (st / C::WST) & 1, a.wait_limit_ns, abort_flag) &&
-            mbar_wait_bounded(tfree_bar(t), ((st / C::TSLOTS) & 1) ^ 1u, a.wait_limit_ns, abort_flag);
-        if (!got && !*abort_flag) record_timeout(a, abort_flag, 3 * 16 + 0);
-        // the warp leaves together (tcgen05.st below needs every lane)
-        if (!__all_sync(0xffffffffu, got)) break;
-        tc_fence_after();
-        // raw row r: eight 16-byte chunks, chunk c stored at c ^ (r mod 8)
-        // (128-byte swizzle); this warp's K blocks 2h, 2h + 1 are chunks 4h..4h+3
-        const uint8_t* rowp = smem + sw * kWStage + r * 128;
-        uint4 raw[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) raw[c] = *reinterpret_cast<const uint4*>(rowp + (((4 * h + c) ^ (r & 7)) << 4));
-        // hand the stage back once this thread's loads have returned (the
-        // arrive depends on their values)
-        const uint32_t dep = raw[0].x ^ raw[0].y ^ raw[0].z ^ raw[0].w ^ raw[1].x ^ raw[1].y ^ raw[1].z ^ raw[1].w ^
-                             raw[2].x ^ raw[2].y ^ raw[2].z ^ raw[2].w ^ raw[3].x ^ raw[3].y ^ raw[3].z ^ raw[3].w;
-        mbar_arrive_after(wfree(sw), base + C::MISC_OFF + 8u, dep);  // (misc word 2: the scratch sink)
-        const uint32_t slot = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + kASlotCol0 +
-                              static_cast<uint32_t>(t * 128);
-        // unrolled, so that raw[] stays in registers (nk is warp-uniform)
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * h + jj;
-          if (j >= nk) break;
-          const uint32_t s2 = s2v[jj], c1024 = c1024v[jj], c64 = c64v[jj];
-          const uint32_t words[8] = {raw[2 * jj].x, raw[2 * jj].y, raw[2 * jj].z, raw[2 * jj].w,
-                                     raw[2 * jj + 1].x, raw[2 * jj + 1].y, raw[2 * jj + 1].z, raw[2 * jj + 1].w};
-          uint32_t vals[32];
-#pragma unroll
-          for (int w8 = 0; w8 < 8; ++w8) {
-            const uint32_t lo = words[w8], hi = lo >> 8;
-            // codes (p, p + 4) of the word for p = 0..3 as 1024 + q (p even)
-            // or 64 + q (p odd), then (1024 + q) s - 1024 s = q s, rounded once
-            vals[4 * w8 + 0] = hfma2(lop3_and_or(lo, 0x000F000Fu, 0x64006400u), s2, c1024);
-            vals[4 * w8 + 1] = hfma2(lop3_and_or(lo, 0x00F000F0u, 0x54005400u), s2, c64);
-            vals[4 * w8 + 2] = hfma2(lop3_and_or(hi, 0x000F000Fu, 0x64006400u), s2, c1024);
-            vals[4 * w8 + 3] = hfma2(lop3_and_or(hi, 0x00F000F0u, 0x54005400u), s2, c64);
-          }
-          // store and wait in one statement: the source registers are read
-          // before the next K block's values are formed in them
-          tc_st_32x32b_x32_wait(slot + static_cast<uint32_t>(j * 32), vals);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(a_full(t));
+        o.s2[jj] = s2;
+        o.c1024[jj] = hmul2(s2, 0xE400E400u);
+        o.c64[jj] = hmul2(s2, 0xD400D400u);
       }
+    };
+    int kb0, nk, st = 0;
+    bool nr;
+    bool have = it.next(a, kb0, nk, nr);
+    StageScales cur;
+    if (have) lookup(kb0, nk, nr, cur);
+    while (have) {
+      const int sw = st % C::WST, t = st % C::TSLOTS;
+      const bool got =
+          mbar_wait_bounded(full_w(sw), (st / C::WST) & 1, a.wait_limit_ns, abort_flag) &&
+          mbar_wait_bounded(tfree_bar(t), ((st / C::TSLOTS) & 1) ^ 1u, a.wait_limit_ns, abort_flag);
+      if (!got && !*abort_flag) record_timeout(a, abort_flag, 3 * 16 + 0);
+      // the warp leaves together (tcgen05.st below needs every lane)
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      // raw row r: eight 16-byte chunks, chunk c stored at c ^ (r mod 8)
+      // (128-byte swizzle); this warp's K blocks 2h, 2h + 1 are chunks 4h..4h+3
+      const uint8_t* rowp = smem + sw * kWStage + r * 128;
+      uint4 raw[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) raw[c] = *reinterpret_cast<const uint4*>(rowp + (((4 * h + c) ^ (r & 7)) << 4));
+      // the next stage's scales while the loads are in flight
+      int kb0n, nkn;
+      bool nrn;
+      const bool haven = it.next(a, kb0n, nkn, nrn);
+      StageScales nxt = {};
+      if (haven) lookup(kb0n, nkn, nrn, nxt);
+      // both K blocks into 64 registers, stored by one instruction (columns
+      // of a K block past the run's end hold values no MMA reads)
+      uint32_t vals[64];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const uint32_t s2 = cur.s2[jj], c1024 = cur.c1024[jj], c64 = cur.c64[jj];
+        const uint32_t words[8] = {raw[2 * jj].x, raw[2 * jj].y, raw[2 * jj].z, raw[2 * jj].w,
+                                   raw[2 * jj + 1].x, raw[2 * jj + 1].y, raw[2 * jj + 1].z, raw[2 * jj + 1].w};
+#pragma unroll
+        for (int w8 = 0; w8 < 8; ++w8) {
+          const uint32_t lo = words[w8], hi = lo >> 8;
+          // codes (p, p + 4) of the word for p = 0..3 as 1024 + q (p even)
+          // or 64 + q (p odd), then (1024 + q) s - 1024 s = q s, rounded once
+          vals[32 * jj + 4 * w8 + 0] = hfma2(lop3_and_or(lo, 0x000F000Fu, 0x64006400u), s2, c1024);
+          vals[32 * jj + 4 * w8 + 1] = hfma2(lop3_and_or(lo, 0x00F000F0u, 0x54005400u), s2, c64);
+          vals[32 * jj + 4 * w8 + 2] = hfma2(lop3_and_or(hi, 0x000F000Fu, 0x64006400u), s2, c1024);
+          vals[32 * jj + 4 * w8 + 3] = hfma2(lop3_and_or(hi, 0x00F000F0u, 0x54005400u), s2, c64);
+        }
+      }
+      if (2 * h < nk) {
+        const uint32_t slot = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + kASlotCol0 +
+                              static_cast<uint32_t>(t * 128 + h * 64);
+        tc_st_32x32b_x64_wait(slot, vals);
+      }
+      tc_fence_before();
+      __syncwarp();
+      // Both handoffs after the store: the stage's packed weights were read
+      // by loads whose values the store consumed (so the next copy into the
+      // stage cannot overtake them), and the A slot is written.
+      if (lane == 0) {
+        mbar_arrive(a_full(t));
+        mbar_arrive(wfree(sw));
+      }
+      cur = nxt;
+      kb0 = kb0n;
+      nk = nkn;
+      have = haven;
       ++st;
     }
-    cp_async_wait<0>();  // no copy into shared memory outlives the CTA
   } else {
     // ------------------------------------------------------------ epilogue
     // (warps 4..7: TMEM lane quadrant warp % 4; tiles leave by plain stores,
