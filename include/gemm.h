@@ -68,7 +68,7 @@ typedef struct {
   int32_t split_k;            /* 0 = SM-waste rule; >= 1 explicit factor */
   int32_t group_size;         /* int4 quantisation group along K (0 = 128); must divide K and the split length */
   int32_t num_sms;            /* SM count the split-K rule uses: 0 = the current device's */
-  int32_t flags;              /* 0, GEMM_FLAG_DETERMINISTIC, or GEMM_FLAG_TEST_WITHHOLD_STAGE (test aid) */
+  int32_t flags;              /* GEMM_FLAG_* bits (below); 0 for none */
 } gemm_desc_t;
 
 /* Bitwise-reproducible results.  No stream-K tail (below); with a split-K

@@ -56,15 +56,18 @@ struct Cfg {
                                         : (2 * BN) <= 256 ? 256 : 512;
   static constexpr int CH = BN < 32 ? BN : 32;          // accumulator columns per tcgen05.ld
   static constexpr uint32_t EPI_OFF = STAGES * STAGE_BYTES;  // 1024-aligned (stages are 2 KiB multiples)
-  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], teardown, cluster ready / done
+  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], teardown, cluster slices received
   static constexpr uint32_t BAR_OFF = EPI_OFF + EPI_STAGING_BYTES;
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 7;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 6;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_USED = MISC_OFF + 64;
   static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be a multiple of 16 in [16, 256]");
   static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM allocation");
   static_assert(EPI_OFF % 1024 == 0 && SMEM_ALLOC <= 227 * 1024, "shared memory layout");
+  // cluster split-K (BN <= 64): the outgoing slices (up to BN x 128 fp32) and
+  // a 16-bit transpose of one slice fit in the idle pipeline stages
+  static_assert(BN > 64 || EPI_OFF >= TILE_P * 4 * BN + TILE_P * 2 * BN, "cluster split-K staging");
 };
 
 template <int BN>
@@ -84,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 + b); };
   const uint32_t teardown_bar = bar0 + 8u * (2 * C::STAGES + 4);
-  const uint32_t cl_bar0 = bar0 + 8u * (2 * C::STAGES + 5);  // cluster split-K: ready, done
+  const uint32_t cl_bar0 = bar0 + 8u * (2 * C::STAGES + 5);  // cluster split-K: slices received
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
   volatile int* consumed_slot = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 12);
@@ -99,12 +102,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       mbar_init(acce_bar(b), kEpiThreads / 32);
     }
     mbar_init(teardown_bar, 1);
-    const uint32_t peers = a.cl_size > 1 ? static_cast<uint32_t>(a.cl_size - 1) : 1u;
-    mbar_init(cl_bar0, peers);
-    mbar_init(cl_bar0 + 8u, peers);
+    mbar_init(cl_bar0, 1);
     *abort_flag = 0;
     *consumed_slot = 0;
     fence_barrier_init();
+    // cluster split-K: the (cl - 1) slices the peers send land on this
+    // barrier (they start sending only after the cluster barrier below)
+    if (a.cl_size > 1)
+      mbar_arrive_expect_tx(cl_bar0, static_cast<uint32_t>(a.cl_size - 1) * TILE_P * 4u *
+                                         static_cast<uint32_t>(BN / a.cl_size));
     fence_proxy_async_smem();
     tma_prefetch_desc(&a.tm_p);
     tma_prefetch_desc(&a.tm_q);
@@ -119,6 +125,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   // the peers' barriers are initialised before anyone arrives on them remotely
   if (a.cl_size > 1) cluster_sync_all();
   const uint32_t tmem_base = *tmem_slot;
+
+  // A stage's boxes: P (128 rows; two 64-wide boxes when MN-major) and Q.
+  auto load_p = [&](uint32_t sp, uint32_t bar, int32_t k0, int32_t prow) {
+    if (!a.p_mn) {
+      tma_load_2d(sp, &a.tm_p, bar, k0, prow);
+    } else {
+      tma_load_2d(sp, &a.tm_p, bar, prow, k0);
+      tma_load_2d(sp + kMnChunkBytes, &a.tm_p, bar, prow + 64, k0);
+    }
+  };
+  auto load_q = [&](uint32_t sq, uint32_t bar, int32_t k0, int32_t qrow) {
+    if (!a.q_mn) {
+      tma_load_2d(sq, &a.tm_q, bar, k0, qrow);
+    } else {
+#pragma unroll
+      for (int j = 0; j < BN / 64; ++j) tma_load_2d(sq + j * kMnChunkBytes, &a.tm_q, bar, qrow + 64 * j, k0);
+    }
+  };
   // operands, C and the split-K workspace may be written by the previous kernel
   pdl_wait();
 
@@ -156,19 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             continue;
           }
           mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
-          if (!a.p_mn) {
-            tma_load_2d(sp, &a.tm_p, full_bar(stage), k0, prow);
-          } else {
-            tma_load_2d(sp, &a.tm_p, full_bar(stage), prow, k0);
-            tma_load_2d(sp + kMnChunkBytes, &a.tm_p, full_bar(stage), prow + 64, k0);
-          }
-          if (!a.q_mn) {
-            tma_load_2d(sq, &a.tm_q, full_bar(stage), k0, qrow);
-          } else {
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(sq + j * kMnChunkBytes, &a.tm_q, full_bar(stage), qrow + 64 * j, k0);
-          }
+          load_p(sp, full_bar(stage), k0, prow);
+          load_q(sq, full_bar(stage), k0, qrow);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -247,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const uint32_t stage_smem = base + C::EPI_OFF + static_cast<uint32_t>(warp - kEpiWarp0) * 8192u;
     while (sched.next(a, g)) {
       if (!epilogue_group<BN, C::CH>(a, g, tmem_base, accf_bar(0), acce_bar(0), acc_iter, abort_flag, q4, lane, et,
-                                     0, stage_smem, ring, NoFix(), 1u, cl_bar0, base + C::EPI_OFF))
+                                     0, stage_smem, ring, NoFix(), 1u, cl_bar0, base + C::EPI_OFF, base))
         break;
     }
     if (lane == 0) bulk_wait_group<0>();  // staged stores finished before the CTA exits

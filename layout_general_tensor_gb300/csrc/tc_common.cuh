@@ -471,33 +471,46 @@ __device__ __forceinline__ void ld_acc(uint32_t taddr, uint32_t (&v)[N], uint32_
 // arriving on its `ready`, so a CTA may leave as soon as its own `ready`
 // completes.  A run without K blocks sends zeros.  Returns false when the
 // CTA is aborting (all 128 threads agree).
+// Split-K inside a cluster of CL CTAs (one run each, the tile's K range cut
+// CL ways): CTA `rank` ends up owning columns [rank * W, rank * W + W) of the
+// tile (W = BN / CL activation rows of C).  Every CTA writes the slices of its
+// partial that other CTAs own into its own shared memory (`out0`, its
+// pipeline stages, idle once its MMAs have completed) and sends each with one
+// bulk copy into slot `rank` of the owner's receive area (`stage0`, CL slots
+// of 128 rows x W fp32), completing on the owner's receive barrier, which
+// expects (CL - 1) slices from the start of the kernel.  Its own slice goes
+// straight into its slot.  The owner then adds its CL slots in rank order and
+// stores its W rows of C (through a 16-bit transpose in shared memory when C
+// rows allow 16-byte stores).
 template <int BN, int CL>
-__device__ __forceinline__ void cluster_push_partial(const uint32_t (&v)[BN], uint32_t stage0, int row) {
+__device__ __forceinline__ void cluster_send_slices(const uint32_t (&v)[BN], uint32_t stage0, uint32_t out0, int row) {
   constexpr int W = BN / CL;
-  static_assert(W >= 4 && W % 4 == 0, "whole 16-byte chunks per rank");
+  constexpr uint32_t SL = TILE_P * 4 * W;  // bytes of one slice
+  static_assert(W >= 4 && W % 4 == 0, "whole 16-byte chunks per slice row");
   const uint32_t rank = cluster_ctarank();
-  const uint32_t mine = stage0 + rank * static_cast<uint32_t>(TILE_P * 4 * W) + static_cast<uint32_t>(row * 4 * W);
 #pragma unroll
   for (int q = 0; q < CL; ++q) {
-    const uint32_t dst = mapa_shared(mine, static_cast<uint32_t>(q));
+    const uint32_t dst = (q == static_cast<int>(rank) ? stage0 + rank * SL : out0 + q * SL) +
+                         static_cast<uint32_t>(row * 4 * W);
 #pragma unroll
-    for (int c = 0; c < W; c += 4)
-      st_shared_cluster_v4(dst + 4u * c, v[q * W + c], v[q * W + c + 1], v[q * W + c + 2], v[q * W + c + 3]);
+    for (int c = 0; c < W; c += 4) st_shared_v4(dst + 4u * c, v[q * W + c], v[q * W + c + 1], v[q * W + c + 2], v[q * W + c + 3]);
   }
 }
 
 template <int BN, int CL>
-__device__ __forceinline__ void cluster_sum_store(const TcArgs& a, uint32_t stage0, int row, int m0, int m1, int n,
-                                                  int n1) {
+__device__ __forceinline__ void cluster_sum_store(const TcArgs& a, uint32_t stage0, uint32_t tr0, int row, int et,
+                                                  int m0, int m1, int n0, int n1) {
   constexpr int W = BN / CL;
-  if (n >= n1) return;
+  constexpr uint32_t SL = TILE_P * 4 * W;
   const uint32_t rank = cluster_ctarank();
+  const int n = n0 + row;
+  const int mr = m0 + static_cast<int>(rank) * W;  // first C row of this CTA's slice
   float s[W];
 #pragma unroll
   for (int j = 0; j < W; ++j) s[j] = 0.0f;
 #pragma unroll
   for (int p = 0; p < CL; ++p) {
-    const uint32_t src = stage0 + static_cast<uint32_t>(p * TILE_P * 4 * W + row * 4 * W);
+    const uint32_t src = stage0 + static_cast<uint32_t>(p) * SL + static_cast<uint32_t>(row * 4 * W);
 #pragma unroll
     for (int c = 0; c < W; c += 4) {
       const float4 t = ld_shared_f32x4(src + 4u * c);
@@ -508,10 +521,30 @@ __device__ __forceinline__ void cluster_sum_store(const TcArgs& a, uint32_t stag
     }
   }
   uint16_t* cb = reinterpret_cast<uint16_t*>(a.c);
+  if (!a.c_vec) {
+    if (n < n1) {
 #pragma unroll
-  for (int j = 0; j < W; ++j) {
-    const int m = m0 + static_cast<int>(rank) * W + j;
-    if (m < m1) cb[static_cast<int64_t>(m) * a.ldc + n] = cvt1(s[j], a.c_bf16);
+      for (int j = 0; j < W; ++j)
+        if (mr + j < m1) cb[static_cast<int64_t>(mr + j) * a.ldc + n] = cvt1(s[j], a.c_bf16);
+    }
+    return;
+  }
+  // [W rows][128 columns] of 16-bit C in shared memory, then 16-byte stores
+  // (8 columns of one row each; a ragged last chunk column by column)
+#pragma unroll
+  for (int j = 0; j < W; ++j) st_shared_u16(tr0 + static_cast<uint32_t>(j * TILE_P * 2 + row * 2), cvt1(s[j], a.c_bf16));
+  named_bar_sync(1, kEpiThreads);
+  for (int c = et; c < W * (TILE_P / 8); c += kEpiThreads) {
+    const int j = c / (TILE_P / 8), col = (c % (TILE_P / 8)) * 8;
+    if (mr + j >= m1 || n0 + col >= n1) continue;
+    const uint32_t src = tr0 + static_cast<uint32_t>(j * TILE_P * 2 + col * 2);
+    uint16_t* dst = cb + static_cast<int64_t>(mr + j) * a.ldc + n0 + col;
+    if (n0 + col + 8 <= n1) {
+      const uint4 w = ld_shared_v4(src);
+      *reinterpret_cast<uint4*>(dst) = w;
+    } else {
+      for (int e = 0; n0 + col + e < n1; ++e) dst[e] = ld_shared_u16(src + 2u * e);
+    }
   }
 }
 
@@ -519,7 +552,8 @@ template <int BN>
 __device__ __noinline__ bool cluster_split_tile(const TcArgs& a, const Group& g, uint32_t tmem_base,
                                                 uint32_t accf_bar0, uint32_t acce_bar0, int& acc_iter,
                                                 volatile int* abort_flag, int q4, int lane, int et,
-                                                uint32_t stage0, uint32_t cl_bar0, int m0, int m1, int n0, int n1) {
+                                                uint32_t stage0, uint32_t out0, uint32_t recv_bar, int m0, int m1,
+                                                int n0, int n1) {
   static_assert(BN <= 64, "128 rows of BN fp32 fit the 32 KiB of epilogue staging");
   const int row = q4 * 32 + lane;
   const uint32_t cl = static_cast<uint32_t>(a.cl_size), rank = cluster_ctarank();
@@ -549,35 +583,38 @@ __device__ __noinline__ bool cluster_split_tile(const TcArgs& a, const Group& g,
       ++acc_iter;
     }
   }
+  const uint32_t sl = TILE_P * 4u * (static_cast<uint32_t>(BN) / cl);  // bytes of one slice
   if (ok) {
     // (the planner takes cl <= BN / 4)
     if (cl == 2) {
-      cluster_push_partial<BN, 2>(v, stage0, row);
+      cluster_send_slices<BN, 2>(v, stage0, out0, row);
     } else if (cl == 4) {
-      if constexpr (BN >= 16) cluster_push_partial<BN, 4>(v, stage0, row);
+      if constexpr (BN >= 16) cluster_send_slices<BN, 4>(v, stage0, out0, row);
     } else {
-      if constexpr (BN >= 32) cluster_push_partial<BN, 8>(v, stage0, row);
+      if constexpr (BN >= 32) cluster_send_slices<BN, 8>(v, stage0, out0, row);
     }
-    fence_acq_rel_cluster();
+    fence_proxy_async_smem();  // the slices are written before the bulk copies read them
   }
-  named_bar_sync(1, kEpiThreads);  // every thread's stores are issued (and fenced)
-  const uint32_t ready = cl_bar0;
+  named_bar_sync(1, kEpiThreads);
   if (et == 0 && ok)
-    for (uint32_t p = 0; p < cl; ++p)
-      if (p != rank) mbar_arrive_cluster(mapa_shared(ready, p));
-  // wait for the peers' slices even on the abort path: none may write into
-  // this CTA's shared memory after it has left
-  const bool got = mbar_wait_bounded_cluster(ready, 0, a.wait_limit_ns, abort_flag);
+    for (uint32_t q = 0; q < cl; ++q)
+      if (q != rank)
+        bulk_copy_to_cluster(mapa_shared(stage0 + rank * sl, q), out0 + q * sl, sl, mapa_shared(recv_bar, q));
+  // wait for the peers' slices even on the abort path: none may land in this
+  // CTA's shared memory after it has left
+  const bool got = mbar_wait_bounded_cluster(recv_bar, 0, a.wait_limit_ns, abort_flag);
   if (!got && !*abort_flag) record_timeout(a, abort_flag, 2 * 16 + 6);
   ok = !named_bar_or(1, kEpiThreads, !got || !ok);
   if (ok) {
-    const int n = n0 + row;
+    // (the transpose buffer lies after the outgoing slices: those may still
+    // be read by the copies)
+    const uint32_t tr0 = out0 + cl * sl;
     if (cl == 2) {
-      cluster_sum_store<BN, 2>(a, stage0, row, m0, m1, n, n1);
+      cluster_sum_store<BN, 2>(a, stage0, tr0, row, et, m0, m1, n0, n1);
     } else if (cl == 4) {
-      if constexpr (BN >= 16) cluster_sum_store<BN, 4>(a, stage0, row, m0, m1, n, n1);
+      if constexpr (BN >= 16) cluster_sum_store<BN, 4>(a, stage0, tr0, row, et, m0, m1, n0, n1);
     } else {
-      if constexpr (BN >= 32) cluster_sum_store<BN, 8>(a, stage0, row, m0, m1, n, n1);
+      if constexpr (BN >= 32) cluster_sum_store<BN, 8>(a, stage0, tr0, row, et, m0, m1, n0, n1);
     }
   }
   return ok;
@@ -594,7 +631,7 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
                                                uint32_t acce_bar0, int& acc_iter, volatile int* abort_flag, int q4,
                                                int lane, int et, int half, uint32_t stage_smem, int& ring,
                                                const Fix& fix = Fix(), uint32_t nacc_mask = (1u << NACC) - 1u,
-                                               uint32_t cl_bar0 = 0u, uint32_t cl_stage0 = 0u) {
+                                               uint32_t cl_bar0 = 0u, uint32_t cl_stage0 = 0u, uint32_t cl_out0 = 0u) {
   const int row = q4 * 32 + lane;  // accumulator row (TMEM lane)
   int32_t tp, tq, m0, m1, n0, n1;
   tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);
@@ -603,7 +640,7 @@ __device__ __forceinline__ bool epilogue_group(const TcArgs& a, const Group& g, 
   if constexpr (!PAIR && NACC == 1 && BN <= 64) {
     if (a.cl_size > 1 && !full_tile)
       return cluster_split_tile<BN>(a, g, tmem_base, accf_bar0, acce_bar0, acc_iter, abort_flag, q4, lane, et,
-                                    cl_stage0, cl_bar0, m0, m1, n0, n1);
+                                    cl_stage0, cl_out0, cl_bar0, m0, m1, n0, n1);
   }
   const int cidx = PAIR ? 2 * g.tile + half : g.tile;
   // deterministic split-K: this run's slot (tile-shaped, rows = C rows)
