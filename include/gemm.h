@@ -98,7 +98,8 @@ typedef struct {
   int32_t swap_ab;     /* 1: the MMA runs C^T = B^T A^T (skinny M) */
   int32_t num_units;   /* (tile, split) work units */
   int32_t k_per_split; /* Ks in elements */
-  int32_t repack_a, repack_b; /* operand copied into the workspace first (stride TMA cannot express) */
+  int32_t repack_a, repack_b; /* operand copied into the workspace first by a pre-pass (a stride TMA cannot
+                                 express, where the kernel's realigning loader is not available) */
   int32_t kernel;      /* 0 = tensor-core any-layout, 1 = int4 dequant,
                           2 = tensor-core any-layout on CTA pairs (256 x 256 tiles) */
   int32_t streamk_tiles; /* tiles of the stream-K tail (0 = none), see gemm_create */
@@ -109,6 +110,17 @@ typedef struct {
                             the activation split into three e4m3 terms per 128-deep block, scales, zero
                             points and activation scales applied in fp32 after the MMA: activations of at
                             most 16 rows, K-contiguous, K and group_size multiples of 128); 0 otherwise */
+  int32_t realign;       /* 1: operands TMA cannot address (a leading dimension that is not a multiple of
+                            8 elements, or an A / B pointer not 16-byte aligned at gemm_run) are loaded by
+                            the kernel's realigning loader warps, which read them in place; 0: such
+                            operands are repacked by a pre-pass into the workspace (the default).
+                            LGT_GEMM_REALIGN=1 at gemm_create selects the loader where it applies: not
+                            for plans whose tensor-core CTAs convert split tiles at the end (split-K
+                            through the workspace, stream-K tails), tiny shapes (M, N or K below 8) or
+                            plans whose staging does not fit beside two pipeline stages.  The loader copies the rows of each row class (rows
+                            whose starts share their offset within a 16-byte word: the perpDim
+                            permutation of the rows with stride 16 / gcd(pitch, 16)) with TMA into a
+                            staging ring and realigns them in shared memory. */
 } gemm_info_t;
 
 typedef struct gemm_plan gemm_plan_t;

@@ -61,6 +61,7 @@ class gemm_info_t(ctypes.Structure):
         ("k_per_split", ctypes.c_int32), ("repack_a", ctypes.c_int32), ("repack_b", ctypes.c_int32),
         ("kernel", ctypes.c_int32),
         ("streamk_tiles", ctypes.c_int32), ("cluster_size", ctypes.c_int32), ("dequant_form", ctypes.c_int32),
+        ("realign", ctypes.c_int32),
     ]
 
 

@@ -12,6 +12,7 @@
 
 #include "gemm.h"
 #include "kernels.h"
+#include "realign.cuh"
 #include "plan.h"
 
 using lgt::MagicDiv;
@@ -183,6 +184,51 @@ bool encode_output(CUtensorMap* map, void* ptr, bool fp32, int c_dtype, int64_t 
   return r == CUDA_SUCCESS;
 }
 
+// Realigning loader (realign.cuh): one map per row class of an operand TMA
+// cannot address directly.  Class r: the rows r, r + P, ... (P = 16 /
+// gcd(pitch, 16)), from the 16-byte word holding row r's start, pitch P times
+// the row pitch; boxes of 72 elements by the class rows of a stage.
+bool encode_classes(TcArgs& args, int o, const void* ptr, int dtype, int mn, int64_t ext, int64_t K, int64_t ld,
+                    int tile_rows) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  const int64_t pitch = ld * 2;
+  const int P = rl_classes(pitch);
+  const int64_t nrows = mn ? K : ext;   // storage rows
+  const int64_t rowlen = mn ? ext : K;  // elements along a storage row
+  if (nrows < P) return false;
+  const CUtensorMapDataType dt = dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  for (int r = 0; r < P; ++r) {
+    const uintptr_t start = reinterpret_cast<uintptr_t>(ptr) + static_cast<uintptr_t>(r * pitch);
+    const uintptr_t word = start & ~static_cast<uintptr_t>(15);
+    const int64_t dr = static_cast<int64_t>(start - word);  // even
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(rowlen + dr / 2), static_cast<cuuint64_t>((nrows - r + P - 1) / P)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(P * pitch)};
+    const RlGeom geo = rl_geom(mn, tile_rows, P);
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(64 * geo.per_box + 8), static_cast<cuuint32_t>(geo.box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&args.tm_rl[o][r], dt, 2, reinterpret_cast<void*>(word), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+    args.rl_d[o][r] = static_cast<int32_t>(dr);
+  }
+  args.rl_on[o] = 1;
+  args.rl_cls[o] = P;
+  return true;
+}
+
+// Whether the realigning loader's staging fits the plan's kernel when A
+// (rl_a) and / or B (rl_b) go through it.
+bool rl_fits(const gemm_plan& p, bool rl_a, bool rl_b) {
+  const bool a_is_p = !p.swap;
+  const int a_cls = rl_a ? rl_classes(p.lda * 2) : 0, b_cls = rl_b ? rl_classes(p.ldb * 2) : 0;
+  const int p_cls = a_is_p ? a_cls : b_cls, q_cls = a_is_p ? b_cls : a_cls;
+  const int p_mn = a_is_p ? p.a_mn : p.b_mn, q_mn = a_is_p ? p.b_mn : p.a_mn;
+  return p.pair ? tc_gemm_pair_rl_fits(p.bn, p_mn, q_mn, p_cls, q_cls)
+                : tc_gemm_rl_fits(p.bn, p_mn, q_mn, p_cls, q_cls);
+}
+
 // The dense kernels' arguments for one run (tensor maps encoded here).
 bool build_dense_args(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                       float* partial, int32_t* counters, TcArgs& args) {
@@ -200,8 +246,23 @@ bool build_dense_args(const gemm_plan* plan, const void* A, int64_t lda, const v
   const int64_t p_ld = a_is_p ? lda : ldb;
   const int64_t q_ld = a_is_p ? ldb : lda;
   const int q_box = plan->pair ? plan->bn / 2 : plan->bn;
-  if (!encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, TILE_P)) return false;
-  if (!encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, q_box)) return false;
+  // an operand TMA cannot address (pitch or base not 16-byte aligned) goes to
+  // the kernel's realigning loader (the plan allows it, else it was repacked)
+  auto tma_ok = [](const void* ptr, int64_t ld) {
+    return reinterpret_cast<uintptr_t>(ptr) % 16 == 0 && (ld * 2) % 16 == 0;
+  };
+  const bool rl_p = plan->rl_ok && !tma_ok(p_ptr, p_ld);
+  const bool rl_q = plan->rl_ok && !tma_ok(q_ptr, q_ld);
+  if (!rl_p && !encode_operand(&args.tm_p, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, TILE_P)) return false;
+  if (!rl_q && !encode_operand(&args.tm_q, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, q_box)) return false;
+  if (rl_p || rl_q) {
+    // (gemm_run falls back to repacking when the staging does not fit)
+    const int pc = rl_p ? rl_classes(p_ld * 2) : 0, qc = rl_q ? rl_classes(q_ld * 2) : 0;
+    if (!(plan->pair ? tc_gemm_pair_rl_fits(plan->bn, p_mn, q_mn, pc, qc) : tc_gemm_rl_fits(plan->bn, p_mn, q_mn, pc, qc)))
+      return false;
+  }
+  if (rl_p && !encode_classes(args, 0, p_ptr, d.a_dtype, p_mn, p_ext, d.K, p_ld, TILE_P)) return false;
+  if (rl_q && !encode_classes(args, 1, q_ptr, d.a_dtype, q_mn, q_ext, d.K, q_ld, q_box)) return false;
   args.c = C;
   args.ldc = plan->ldc;
   args.ws = partial;
@@ -475,6 +536,11 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   // the K blocks of a last partial wave (at most 3/4 full) are spread evenly
   // over all workers, their fp32 partials reduced like split-K partials.
   // Off with GEMM_FLAG_DETERMINISTIC or LGT_GEMM_STREAMK=0.
+  // (a plan with a tail keeps its fixup warps for it: operands TMA cannot
+  // address are then repacked rather than realigned in the kernel)
+  // (opt-in: on the shapes measured so far the repacking pre-pass is faster,
+  // since it realigns each operand once while the loader pays per stage)
+  const bool realign = !int4 && env_int("LGT_GEMM_REALIGN", 0) != 0;
   if (!int4 && !p.swap && p.split == 1 && !(d.flags & GEMM_FLAG_DETERMINISTIC) && p.kb_total >= 2 && workers > 0 &&
       env_int("LGT_GEMM_STREAMK", 1) != 0) {
     const int64_t full = tiles / workers, rest = tiles % workers;
@@ -506,8 +572,10 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   p.a_row_elems = p.a_mn ? d.M : d.K;
   p.b_rows = p.b_mn ? d.K : d.N;
   p.b_row_elems = p.b_mn ? d.N : d.K;
-  p.repack_a = !int4 && (p.lda * 2) % 16 != 0;
-  p.repack_b = !int4 && (p.ldb * 2) % 16 != 0;
+  p.rl_ok = realign && p.fin_tiles == 0 && d.M >= 8 && d.N >= 8 && d.K >= 8 &&
+            lgt::rl_fits(p, (p.lda * 2) % 16 != 0, (p.ldb * 2) % 16 != 0);
+  p.repack_a = !int4 && !p.rl_ok && (p.lda * 2) % 16 != 0;
+  p.repack_b = !int4 && !p.rl_ok && (p.ldb * 2) % 16 != 0;
   p.a_pack_ld = align_up(static_cast<size_t>(p.a_row_elems), 8);
   p.b_pack_ld = align_up(static_cast<size_t>(p.b_row_elems), 8);
 
@@ -627,6 +695,7 @@ gemm_status_t gemm_query(const gemm_plan_t* plan, gemm_info_t* info) {
   info->repack_b = plan->repack_b;
   info->kernel = plan->kernel == 0 && plan->pair ? 2 : plan->kernel;
   info->dequant_form = plan->kernel == 1 ? plan->int4_form : 0;
+  info->realign = plan->rl_ok;
   return GEMM_OK;
 }
 
@@ -658,9 +727,18 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
 
   const bool a_mis = !int4 && reinterpret_cast<uintptr_t>(A) % 16 != 0;
   const bool b_mis = !int4 && reinterpret_cast<uintptr_t>(B) % 16 != 0;
-  const bool pack_a = plan->repack_a || a_mis;
-  const bool pack_b = plan->repack_b || b_mis;
-  const size_t need = (a_mis || b_mis) ? plan->ws_bytes_misaligned : plan->ws_bytes;
+  // Operands TMA cannot address: read in place by the kernel's realigning
+  // loader when the plan has it and its staging ring fits for this run's
+  // set of such operands, else repacked first.
+  const bool a_tma = !a_mis && (plan->lda * 2) % 16 == 0, b_tma = !b_mis && (plan->ldb * 2) % 16 == 0;
+  bool rl_a = !int4 && plan->rl_ok && !a_tma, rl_b = !int4 && plan->rl_ok && !b_tma;
+  if ((rl_a || rl_b) && !lgt::rl_fits(*plan, rl_a, rl_b)) rl_a = rl_b = false;
+  const bool pack_a = !int4 && !a_tma && !rl_a;
+  const bool pack_b = !int4 && !b_tma && !rl_b;
+  // (the plan's own repacks are in ws_bytes; a base pointer that must be
+  // repacked at run time needs the larger size)
+  const bool pack_mis = (pack_a && !plan->repack_a) || (pack_b && !plan->repack_b);
+  const size_t need = pack_mis ? plan->ws_bytes_misaligned : plan->ws_bytes;
   if (need > 0 && (!workspace || workspace_bytes < need)) return GEMM_ERR_WORKSPACE;
   if (need > 0 && reinterpret_cast<uintptr_t>(workspace) % 256) return GEMM_ERR_ALIGNMENT;
   uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -3,6 +3,7 @@
 // perpendicular-dimension stride permutation) over index arrays.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "realign.cuh"
 
 namespace lgt {
 namespace {
@@ -19,21 +20,7 @@ namespace {
 // loads coalesce) and realigns them with funnel shifts.  Every word read
 // holds at least one of the thread's elements, so it lies in the same page as
 // valid data.
-// Eight 2-byte elements starting at byte offset `off` (even, < 16) of the
-// aligned 16-byte word pair (a, b).
-__device__ __forceinline__ uint4 realign8(const uint4& a, const uint4& b, uint32_t off) {
-  if (!off) return a;
-  uint32_t x0, x1, x2, x3, x4;
-  switch (off >> 2) {
-    case 0: x0 = a.x; x1 = a.y; x2 = a.z; x3 = a.w; x4 = b.x; break;
-    case 1: x0 = a.y; x1 = a.z; x2 = a.w; x3 = b.x; x4 = b.y; break;
-    case 2: x0 = a.z; x1 = a.w; x2 = b.x; x3 = b.y; x4 = b.z; break;
-    default: x0 = a.w; x1 = b.x; x2 = b.y; x3 = b.z; x4 = b.w; break;
-  }
-  const uint32_t sh = (off & 3u) * 8u;  // 0 or 16 bits
-  return make_uint4(__funnelshift_r(x0, x1, sh), __funnelshift_r(x1, x2, sh), __funnelshift_r(x2, x3, sh),
-                    __funnelshift_r(x3, x4, sh));
-}
+// (realign8: realign.cuh, shared with the kernels' in-kernel loader)
 
 // One chunk per thread over a grid that covers all chunks (measured faster
 // than grid-stride loops with several chunks in flight per thread).

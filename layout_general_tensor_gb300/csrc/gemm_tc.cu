@@ -9,7 +9,12 @@
 //               store C, or add the fp32 partial into the workspace and let the
 //               last-arriving CTA of the tile convert and store.
 //   warps 6..9  stream-K fixup: convert this CTA's share of the tail tiles
-//               once their partial sums are complete (idle without a tail).
+//               once their partial sums are complete (idle without a tail);
+//               or, for an operand TMA cannot address (rows not 16-byte
+//               multiples apart, or an unaligned base), its realigning
+//               loader (realign.cuh), which fills that operand's part of each
+//               stage and arrives on the stage beside the TMA bytes of the
+//               other.
 //
 // Operand layouts.  The Triton inThreadTranspose page ("Feature description")
 // fixes the problem: a dot operand that is not contiguous along K must still
@@ -34,6 +39,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "realign.cuh"
 #include "tc_common.cuh"
 
 namespace lgt {
@@ -41,6 +47,7 @@ namespace {
 
 constexpr int kThreads = 320;  // 6 warps + 4 stream-K fixup warps
 constexpr int kFixWarp0 = 6;
+constexpr uint32_t kRlWarps = 4;  // the fixup warps, as realigning loader
 constexpr int kEpiWarp0 = 2;
 constexpr uint32_t kP_BYTES = TILE_P * TILE_K * 2;   // 16 KiB
 constexpr uint32_t kMnChunkBytes = 64 * TILE_K * 2;  // one 64-wide MN box, 64 K rows: 8 KiB
@@ -56,9 +63,10 @@ struct Cfg {
                                         : (2 * BN) <= 256 ? 256 : 512;
   static constexpr int CH = BN < 32 ? BN : 32;          // accumulator columns per tcgen05.ld
   static constexpr uint32_t EPI_OFF = STAGES * STAGE_BYTES;  // 1024-aligned (stages are 2 KiB multiples)
-  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], teardown, cluster slices received
+  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], teardown, cluster slices received,
+  // realigning loader staging slots landed[kRlMaxStg]
   static constexpr uint32_t BAR_OFF = EPI_OFF + EPI_STAGING_BYTES;
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 6;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 6 + kRlMaxStg;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_USED = MISC_OFF + 64;
   static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -88,15 +96,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 + b); };
   const uint32_t teardown_bar = bar0 + 8u * (2 * C::STAGES + 4);
   const uint32_t cl_bar0 = bar0 + 8u * (2 * C::STAGES + 5);  // cluster split-K: slices received
+  auto stg_full = [&](int i) { return bar0 + 8u * (2 * C::STAGES + 6 + i); };
+  // Realigning loader (realign.cuh): its staging ring takes the last rl_take
+  // pipeline stages' memory; nst stages remain.
+  const bool rl = a.rl_on[0] || a.rl_on[1];
+  const uint32_t rl_bytes_p = a.rl_on[0] ? rl_stage_bytes(a.p_mn, TILE_P, a.rl_cls[0]) : 0u;
+  const uint32_t rl_bytes_q = a.rl_on[1] ? rl_stage_bytes(a.q_mn, BN, a.rl_cls[1]) : 0u;
+  const uint32_t rl_slot = rl_bytes_p + rl_bytes_q;
+  int rl_take = 0, rl_nstg = 0;
+  rl_ring(C::STAGES, C::STAGE_BYTES, rl_slot, rl_take, rl_nstg);
+  const int nst = C::STAGES - rl_take;
+  const uint32_t stg0 = base + static_cast<uint32_t>(nst) * C::STAGE_BYTES;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
   volatile int* consumed_slot = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 12);
 
   if (threadIdx.x == 0) {
+    // (a realigned operand: the loader arrives on the stage too)
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), rl ? 2u : 1u);
       mbar_init(empty_bar(s), 1);
     }
+    for (int i = 0; i < kRlMaxStg; ++i) mbar_init(stg_full(i), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
       mbar_init(acce_bar(b), kEpiThreads / 32);
@@ -173,17 +194,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             // test aid (a.withhold): this stage is never filled, so the MMA
             // issuer's bounded wait on it runs out
             ++issued;
-            if (++stage == C::STAGES) {
+            if (++stage == nst) {
               stage = 0;
               phase ^= 1u;
             }
             continue;
           }
-          mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
-          load_p(sp, full_bar(stage), k0, prow);
-          load_q(sq, full_bar(stage), k0, qrow);
+          // (realigned operands come from the loader warps)
+          mbar_arrive_expect_tx(full_bar(stage), (a.rl_on[0] ? 0u : kP_BYTES) + (a.rl_on[1] ? 0u : C::Q_BYTES));
+          if (!a.rl_on[0]) load_p(sp, full_bar(stage), k0, prow);
+          if (!a.rl_on[1]) load_q(sq, full_bar(stage), k0, qrow);
           ++issued;
-          if (++stage == C::STAGES) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1u;
           }
@@ -235,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             tc_mma_f16_ss(d_tmem, pd, qd, a.idesc, (kb | k) != 0 ? 1u : 0u);
           }
           tc_commit(empty_bar(stage));
-          if (++stage == C::STAGES) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1u;
           }
@@ -247,8 +269,78 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       *consumed_slot = consumed;
     }
   } else if (warp >= kFixWarp0) {
-    // ------------------------------------------------------------ stream-K fixup
-    if (a.tail_tiles) finish_tail<BN>(a, abort_flag, threadIdx.x - kFixWarp0 * 32);
+    if (rl) {
+      // ---------------------------------------------------------- realigning loader
+      // The staging ring is the loader's own: the first loader warp copies
+      // the class boxes of K block it + rl_nstg into the slot that K block
+      // `it` has just been realigned out of (its lanes share the boxes), and
+      // all four warps realign each K block into its pipeline stage once the
+      // stage is free (the planner gives such plans no fixup work).
+      const int t = threadIdx.x - kFixWarp0 * 32;
+      const bool issuer = warp == kFixWarp0;
+      const uint32_t tx = (a.rl_on[0] ? rl_stage_tx(a.p_mn, TILE_P, a.rl_cls[0]) : 0u) +
+                          (a.rl_on[1] ? rl_stage_tx(a.q_mn, BN, a.rl_cls[1]) : 0u);
+      KbIter ahead(a);
+      int stg_issued = 0, stg_done = 0;
+      auto fill = [&](int sl) {  // the next K block's boxes into slot sl (first loader warp)
+        int tile, kb;
+        if (!ahead.next(a, tile, kb)) return;
+        int32_t tp, tq, m0, m1, n0, n1;
+        tile_ranges(a, tile, BN, tp, tq, m0, m1, n0, n1);
+        const uint32_t dst = stg0 + static_cast<uint32_t>(sl) * rl_slot;
+        if (lane == 0) mbar_arrive_expect_tx(stg_full(sl), tx);
+        __syncwarp();
+        if (a.rl_on[0]) rl_issue(a.tm_rl[0], a.rl_cls[0], a.p_mn, TILE_P, tp * TILE_P, kb * TILE_K, dst, stg_full(sl), lane, 32);
+        if (a.rl_on[1])
+          rl_issue(a.tm_rl[1], a.rl_cls[1], a.q_mn, BN, tq * BN, kb * TILE_K, dst + rl_bytes_p, stg_full(sl), lane, 32);
+        ++stg_issued;
+      };
+      if (issuer)
+        for (int sl = 0; sl < rl_nstg; ++sl) fill(sl);
+      Sched sched(a);
+      Group g;
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, sphase = 0;
+      bool ok = true;
+      while (ok && sched.next(a, g)) {
+        for (int kb = 0; kb < g.nkb; ++kb) {
+          const bool got = mbar_wait_bounded(stg_full(slot), sphase, a.wait_limit_ns, abort_flag) &&
+                           mbar_wait_bounded(empty_bar(stage), phase ^ 1u, a.wait_limit_ns, abort_flag);
+          if (!got && !*abort_flag) record_timeout(a, abort_flag, 0 * 16 + 6);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          const uint32_t src = stg0 + static_cast<uint32_t>(slot) * rl_slot;
+          const uint32_t sp = base + static_cast<uint32_t>(stage) * C::STAGE_BYTES;
+          if (a.rl_on[0]) rl_pass(a.rl_d[0], a.rl_cls[0], a.p_mn, TILE_P, src, sp, t, kRlWarps * 32);
+          if (a.rl_on[1]) rl_pass(a.rl_d[1], a.rl_cls[1], a.q_mn, BN, src + rl_bytes_p, sp + kP_BYTES, t, kRlWarps * 32);
+          // the stage is read by the MMA (async proxy); the slot is refilled by TMA
+          fence_proxy_async_smem();
+          named_bar_sync(3, kRlWarps * 32);
+          ++stg_done;
+          if (t == 0) mbar_arrive(full_bar(stage));
+          if (issuer) fill(slot);
+          if (++stage == nst) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++slot == rl_nstg) {
+            slot = 0;
+            sphase ^= 1u;
+          }
+        }
+      }
+      if (issuer && lane == 0 && *abort_flag) {
+        // copies still in flight land before the CTA exits
+        volatile int no_abort = 0;
+        for (int it = stg_done; it < stg_issued; ++it)
+          mbar_wait_bounded(stg_full(it % rl_nstg), (it / rl_nstg) & 1, a.wait_limit_ns, &no_abort);
+      }
+    } else if (a.tail_tiles) {
+      // ---------------------------------------------------------- stream-K fixup
+      finish_tail<BN>(a, abort_flag, threadIdx.x - kFixWarp0 * 32);
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;                  // TMEM lane quadrant this warp may access
@@ -275,8 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const int consumed = *consumed_slot;
       for (int it = consumed; it < issued; ++it) {
         if (a.withhold && blockIdx.x == 0 && it == 0) continue;  // the withheld stage has no copy in flight
-        mbar_wait_bounded(full_bar(it % C::STAGES), (it / C::STAGES) & 1, a.wait_limit_ns, &no_abort);
+        mbar_wait_bounded(full_bar(it % nst), (it / nst) & 1, a.wait_limit_ns, &no_abort);
       }
+
     }
   }
   if (warp == 1 && lane == 0) {
@@ -339,6 +432,23 @@ size_t tc_gemm_smem_bytes(int bn) {
     case 192: return Cfg<192>::SMEM_ALLOC;
     case 256: return Cfg<256>::SMEM_ALLOC;
     default: return 0;
+  }
+}
+
+bool tc_gemm_rl_fits(int bn, int p_mn, int q_mn, int p_cls, int q_cls) {
+  auto fits = [&](int stages, uint32_t stage_bytes) {
+    const uint32_t stg = (p_cls ? rl_stage_bytes(p_mn, TILE_P, p_cls) : 0u) + (q_cls ? rl_stage_bytes(q_mn, bn, q_cls) : 0u);
+    int take, nstg;
+    return rl_ring(stages, stage_bytes, stg, take, nstg) && (stg == 0 || nstg >= 2);
+  };
+  switch (bn) {
+    case 16: return fits(Cfg<16>::STAGES, Cfg<16>::STAGE_BYTES);
+    case 32: return fits(Cfg<32>::STAGES, Cfg<32>::STAGE_BYTES);
+    case 64: return fits(Cfg<64>::STAGES, Cfg<64>::STAGE_BYTES);
+    case 128: return fits(Cfg<128>::STAGES, Cfg<128>::STAGE_BYTES);
+    case 192: return fits(Cfg<192>::STAGES, Cfg<192>::STAGE_BYTES);
+    case 256: return fits(Cfg<256>::STAGES, Cfg<256>::STAGE_BYTES);
+    default: return false;
   }
 }
 

@@ -105,6 +105,8 @@ struct DeviceStatus {
 // operand, Q its N-side operand.  Normal mode: P = A (rows m), Q = B
 // (rows n).  Swapped mode (skinny M): P = B (rows n), Q = A (rows m), and the
 // accumulator holds C^T.
+constexpr int kRlMaxClasses = 8;  // realigning loader: row classes at most (16 / gcd(pitch, 16))
+
 struct TcArgs {
   CUtensorMap tm_p;
   CUtensorMap tm_q;
@@ -139,12 +141,25 @@ struct TcArgs {
   int32_t cl_size;       // > 1: the split-K runs of a tile are the CTAs of one cluster of this size,
                          // reduced through distributed shared memory (single-CTA kernel, swapped, BN <= 64)
   int32_t withhold;      // test aid (single-CTA kernel): CTA 0 never fills its first pipeline stage
+  // In-kernel realigning loader (realign.cuh) for operands TMA cannot address
+  // directly, [0] = P, [1] = Q: one TMA map per row class (rows whose starts
+  // share their offset within a 16-byte word), a staging ring, and a
+  // realigning pass by the fixup warps (plans without fixup work).
+  CUtensorMap tm_rl[2][kRlMaxClasses];
+  int32_t rl_on[2];                  // 1: the operand goes through the loader
+  int32_t rl_cls[2];                 // row classes P (1, 2, 4 or 8)
+  int32_t rl_d[2][kRlMaxClasses];    // byte offset of class r's rows in their 16-byte words
   uint32_t idesc;
 };
 
 // Returns a cudaError_t; `bn` selects the kernel instance.
 cudaError_t launch_tc_gemm(const TcArgs& args, int bn, int grid, cudaStream_t stream);
 size_t tc_gemm_smem_bytes(int bn);
+// Whether the realigning loader's staging ring fits beside at least two
+// pipeline stages for tile width bn (p_cls / q_cls: row classes of a
+// realigned P / Q, 0 when that operand is loaded by TMA directly).
+bool tc_gemm_rl_fits(int bn, int p_mn, int q_mn, int p_cls, int q_cls);
+bool tc_gemm_pair_rl_fits(int bn, int p_mn, int q_mn, int p_cls, int q_cls);
 // Clusters of `cluster` CTAs of the single-CTA kernel (tile width bn <= 64)
 // that can be resident at once on the current device (0 if none).
 cudaError_t tc_gemm_max_clusters(int bn, int cluster, int* clusters);

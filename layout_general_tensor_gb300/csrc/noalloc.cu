@@ -70,12 +70,15 @@ extern "C" gemm_status_t gemm_run_static_scratch(const gemm_plan_t* plan, const 
   }
   if (!A || !B) return GEMM_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(A) % 2 || reinterpret_cast<uintptr_t>(B) % 2) return GEMM_ERR_ALIGNMENT;
-  // Operands must be addressable by TMA in place: there is no room reserved
-  // for realigned copies.
+  // Operands must be addressable in place, by TMA or by the kernel's
+  // realigning loader: there is no room reserved for realigned copies.
   if (plan->det) return GEMM_ERR_UNSUPPORTED;  // per-run slots are not kept in the static array
-  if (plan->repack_a || plan->repack_b || reinterpret_cast<uintptr_t>(A) % 16 ||
-      reinterpret_cast<uintptr_t>(B) % 16)
-    return GEMM_ERR_UNSUPPORTED;
+  if (plan->repack_a || plan->repack_b) return GEMM_ERR_UNSUPPORTED;
+  {
+    const bool a_mis = reinterpret_cast<uintptr_t>(A) % 16 != 0, b_mis = reinterpret_cast<uintptr_t>(B) % 16 != 0;
+    const bool rl_a = a_mis || (plan->lda * 2) % 16 != 0, rl_b = b_mis || (plan->ldb * 2) % 16 != 0;
+    if ((a_mis || b_mis) && !(plan->rl_ok && lgt::rl_fits(*plan, rl_a, rl_b))) return GEMM_ERR_UNSUPPORTED;
+  }
 
   // Scratch layout: [tile counters][fp32 partial sums M x N].  A stream-K
   // tail that does not fit is dropped (whole tiles only).

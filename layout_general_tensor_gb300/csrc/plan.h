@@ -40,6 +40,10 @@ struct gemm_plan {
   int a_mn, b_mn;
   // operand repacking (leading dimension not a multiple of 16 bytes)
   int repack_a, repack_b;
+  // Operands TMA cannot address (unaligned row pitch, or an unaligned base at
+  // run time) are realigned by the kernel's loader warps when the plan leaves
+  // them free (no fixup work); else they are repacked by a pre-pass.
+  int rl_ok;
   int64_t a_rows, a_row_elems, b_rows, b_row_elems;  // storage rows of each operand
   int64_t a_pack_ld, b_pack_ld;
   size_t off_partial, off_counters, off_pack_a, off_pack_b, ws_bytes;
@@ -77,6 +81,9 @@ struct ArgCache {
 
 // cuTensorMapEncodeTiled (see api.cu); null if the driver does not provide it.
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder();
+// Whether the realigning loader's staging fits the plan's kernel when A
+// (rl_a) and / or B (rl_b) go through it.
+bool rl_fits(const gemm_plan& p, bool rl_a, bool rl_b);
 
 // Encode a 2-D TMA map over a 16-bit operand (see api.cu).
 bool encode_operand(CUtensorMap* map, const void* ptr, int dtype, bool mn_major, int64_t rows_or_mn, int64_t K,

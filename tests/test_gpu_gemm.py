@@ -98,11 +98,21 @@ def test_padded_leading_dims(al, bl):
     g.close()
 
 
+@pytest.fixture(params=["kernel", "prepass"])
+def realign_mode(request, monkeypatch):
+    """How operands TMA cannot address are read: by the kernel's realigning
+    loader (TMA boxes per row class, in the perpDim order, then a realigning
+    pass in shared memory), or through the repacking pre-pass."""
+    if request.param == "kernel":
+        monkeypatch.setenv("LGT_GEMM_REALIGN", "1")
+    return request.param
+
+
 @pytest.mark.parametrize("al", [K, MN])
 @pytest.mark.parametrize("bl", [K, MN])
-def test_unaligned_leading_dims_repack(al, bl):
+def test_unaligned_leading_dims(al, bl, realign_mode):
     """Leading dimensions that are not a multiple of 8 elements (rows not on
-    16-byte boundaries) go through the realigning copy."""
+    16-byte boundaries): realigned inside the kernel, or by the copy."""
     M, N, Kd = 131, 203, 517
 
     def odd_ld(base):
@@ -114,17 +124,38 @@ def test_unaligned_leading_dims_repack(al, bl):
     case = _case(M, N, Kd, al, bl, F16, lda=lda, ldb=ldb, ldc=N)
     inp = wl.make_inputs(case, seed=6)
     c, g, _ = run_case(case, inp)
-    assert g.info.repack_a and g.info.repack_b
+    prepass = realign_mode == "prepass"
+    assert g.info.realign == (0 if prepass else 1)
+    assert bool(g.info.repack_a) == prepass and bool(g.info.repack_b) == prepass
     assert_close(c, oracle_full(case, inp), case.name)
     g.close()
 
 
-def test_misaligned_base_pointers():
-    case = _case(100, 120, 200, MN, K, BF16)
-    inp = wl.make_inputs(case, seed=7)
-    c, g, _ = run_case(case, inp, seed_offsets=(1, 3))
-    assert_close(c, oracle_full(case, inp), case.name)
-    g.close()
+@pytest.mark.parametrize("shape", [(100, 120, 200), (40, 333, 130), (300, 129, 64)], ids=lambda s: "x".join(map(str, s)))
+def test_misaligned_base_pointers(shape, realign_mode):
+    M, N, Kd = shape
+    for al, bl in ((MN, K), (K, MN)):
+        case = _case(M, N, Kd, al, bl, BF16)
+        inp = wl.make_inputs(case, seed=7)
+        c, g, _ = run_case(case, inp, seed_offsets=(1, 3))
+        assert_close(c, oracle_full(case, inp), case.name)
+        g.close()
+
+
+def test_realigned_bits_match_tma_layout(monkeypatch):
+    """The same operand through TMA (aligned copy) and through the realigning
+    loader (the copy at a 2-byte offset): every element of C is the same
+    bits, for K- and M-contiguous A, swapped and not."""
+    monkeypatch.setenv("LGT_GEMM_REALIGN", "1")
+    m = lib()
+    for M, N, Kd, al in ((1000, 520, 320, MN), (1000, 520, 320, K), (40, 700, 960, K), (40, 700, 960, MN)):
+        case = _case(M, N, Kd, al, K, BF16)
+        inp = wl.make_inputs(case, seed=11)
+        c0, g0, C0 = run_case(case, inp)
+        c1, g1, C1 = run_case(case, inp, seed_offsets=(1, 0), gemm=g0)
+        assert g0.info.realign == 1
+        assert torch.equal(C0.view(torch.int16), C1.view(torch.int16)), case.name
+        g0.close()
 
 
 # ------------------------------------------------------------ split-K and swap

@@ -81,13 +81,21 @@ def test_pair_ragged(shape, al, bl):
     g.close()
 
 
-def test_pair_with_repacked_operands():
-    # odd leading dimensions: both operands are copied to 16-byte pitches first
-    case = _case(300, 260, 203, MN, K)
-    inp, c, g = _run(case, seed=5)
-    assert g.info.repack_b == 1
-    assert_close(c, oracle_full(case, inp), case.name)
-    g.close()
+@pytest.mark.parametrize("mode", ["kernel", "prepass"])
+def test_pair_with_unaligned_operands(mode, monkeypatch):
+    # odd leading dimensions: read in place by the realigning loader of both
+    # CTAs of each pair, or copied to 16-byte pitches first
+    if mode == "kernel":
+        monkeypatch.setenv("LGT_GEMM_REALIGN", "1")
+    # (pitches in bytes: 600 / 406, 406 / 1044, 1208 / 1060: none a multiple of 16)
+    for shape, al, bl in (((300, 260, 203), MN, K), ((600, 522, 203), K, MN), ((604, 530, 330), MN, MN)):
+        case = _case(*shape, al, bl)
+        inp, c, g = _run(case, seed=5)
+        assert g.info.kernel == 2
+        assert g.info.repack_b == (1 if mode == "prepass" else 0)
+        assert g.info.realign == (0 if mode == "prepass" else 1)
+        assert_close(c, oracle_full(case, inp), case.name)
+        g.close()
 
 
 @pytest.mark.parametrize("split", [2, 3, 8])

@@ -125,6 +125,9 @@ def test_planner_decisions(lib, case):
         assert info.split_k == want_split
         assert info.swap_ab == (1 if case.M <= 64 else 0)
         lda, ldb, _ = case.dense_ld()
+        # unaligned leading dimensions are repacked first (the in-kernel
+        # realigning loader is opt-in)
+        assert info.realign == 0
         assert info.repack_a == ((lda * 2) % 16 != 0)
         assert info.repack_b == ((ldb * 2) % 16 != 0)
         ws = lib.gemm_workspace_size(h)
@@ -291,3 +294,26 @@ def test_reduce_no_device(lib):
     assert lib.reduce_rows_f32(4096, 2, 8, 0, 4096) == lib.GEMM_ERR_CUDA
     st = lib._lib.reduce_rows_workspace_size(2, 8, 0, ctypes.byref(ctypes.c_size_t()))
     assert st == lib.GEMM_ERR_CUDA
+
+
+def test_planner_realign_or_repack(lib, monkeypatch):
+    """With LGT_GEMM_REALIGN=1 an unaligned leading dimension is realigned
+    inside the kernel when the plan leaves the fixup warps free (no split-K
+    through the workspace, no stream-K tail); else, and by default, it is
+    repacked first."""
+    def info(M, N, K, lda, split=1, al=wl.MN_CONTIG):
+        d = lib.make_desc(M, N, K, al, wl.K_CONTIG, lib.GEMM_BF16, lda=lda, split_k=split, num_sms=148)
+        h = lib.gemm_create(d)
+        i = lib.gemm_query(h)
+        ws = lib.gemm_workspace_size(h)
+        lib.gemm_destroy(h)
+        return i, ws
+    i, ws = info(4095, 3000, 2880, 4095)   # pitch 8190 bytes: the default repacks
+    assert i.realign == 0 and i.repack_a == 1 and ws >= 2880 * 4096 * 2
+    monkeypatch.setenv("LGT_GEMM_REALIGN", "1")
+    i, ws = info(4095, 3000, 2880, 4095)
+    assert i.realign == 1 and i.repack_a == 0 and i.streamk_tiles == 0 and ws == 0
+    i, _ = info(4095, 3000, 2880, 4096)    # aligned pitch: the same plan, nothing to realign
+    assert i.realign == 1 and i.repack_a == 0
+    i, ws = info(300, 400, 4096, 301, split=4)  # split-K through the workspace: pre-pass
+    assert i.realign == 0 and i.repack_a == 1 and ws >= 4096 * 304 * 2
