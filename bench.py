@@ -34,8 +34,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GEMM TFLOP/s & % dense-BF16 peak per shape/layout; GB/s & % HBM (skinny/int4)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# the headline kernel (the CTA-pair kernel) and what builds its arguments
 KERNEL_SOURCES = ["layout_general_tensor_gb300/csrc/" + f for f in
-                  ("api.cu", "gemm_tc.cu", "gemm_tc_pair.cu", "tc_common.cuh", "ptx.cuh", "kernels.h")]
+                  ("api.cu", "plan.h", "gemm_tc_pair.cu", "tc_common.cuh", "realign.cuh", "ptx.cuh", "kernels.h",
+                   "intmath.h")]
 
 
 def load_peaks():
@@ -247,18 +249,22 @@ def cpu_cores():
 
 
 def oracle_row_block(case, inp, rows):
-    """The oracle on the first `rows` rows of C (A is K-contiguous, so those
-    rows of A are a prefix of its storage)."""
+    """The oracle on the first `rows` rows of C (a K-contiguous A's rows are
+    a prefix of its storage; an M-contiguous A is passed whole, its leading
+    dimension unchanged)."""
     import oracle
     import workloads as wl
-    assert case.a_layout == wl.K_CONTIG
-    return oracle.gemm(rows, case.N, case.K, inp.A[: rows * inp.lda], case.a_layout, inp.lda, case.a_dtype,
+    a = inp.A[: rows * inp.lda] if case.a_layout == wl.K_CONTIG else inp.A
+    return oracle.gemm(rows, case.N, case.K, a, case.a_layout, inp.lda, case.a_dtype,
                        inp.B, case.b_layout, inp.ldb, case.b_dtype, scales=inp.scales, zeros=inp.zeros,
                        group=case.group_size)
 
 
 def cpu_baseline(case, inp, budget_s=10.0, rows=512):
-    """Time the oracle on row blocks of the workload for about `budget_s`."""
+    """Time the oracle on row blocks of the workload for about `budget_s`.
+    Reported in TFLOP/s and, for the bandwidth-bound workloads, as the
+    algorithmic bytes of the rows done per second (GB/s)."""
+    rows = min(rows, case.M)
     done = 0
     t0 = time.perf_counter()
     reps = 0
@@ -269,7 +275,9 @@ def cpu_baseline(case, inp, budget_s=10.0, rows=512):
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= 1000:
             break
+    frac = rows / case.M  # share of C (and of the work) one block is
     return {"value": done / el / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "gbs_equivalent": reps * frac * algorithmic_bytes(case) / el / 1e9,
             "sample": f"{reps} x oracle.gemm on rows 0..{rows - 1} of C ({rows}x{case.N}x{case.K}, fp64 numpy "
                       f"matmul after per-layout gather), {el:.1f} s"}
 
@@ -398,6 +406,11 @@ def gpu_arm(args, headline):
         assert st == 0, f"device status {st} on {case.name}"
         d.g.close()
         del d
+        if rank == 0 and world == 1 and not args.no_cpu_baseline and case.flops() >= 1e9:
+            # the oracle on a bounded sample of the same workload (C1's 256^3
+            # cases are too small to say anything)
+            configs[case.name]["cpu_baseline"] = cpu_baseline(case, wl.make_inputs(case, seed=0),
+                                                              budget_s=args.cpu_seconds / 3, rows=256)
 
     for rc in (wl.REDUCE_VEC, wl.REDUCE_ROWS, wl.REDUCE_LARGE):
         configs[rc.name] = reduce_config(rc, args, peaks)

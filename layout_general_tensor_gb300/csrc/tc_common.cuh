@@ -482,6 +482,15 @@ __device__ __forceinline__ void ld_acc(uint32_t taddr, uint32_t (&v)[N], uint32_
 // straight into its slot.  The owner then adds its CL slots in rank order and
 // stores its W rows of C (through a 16-bit transpose in shared memory when C
 // rows allow 16-byte stores).
+// Byte offset of 16-byte chunk c of row `row` in a slice (rows of W fp32):
+// with W = 16 (64-byte rows) the chunk index is XORed with (row / 2) mod 4,
+// so that the 16-byte accesses of eight consecutive rows hit distinct banks.
+template <int W>
+__device__ __forceinline__ uint32_t slice_off(int row, int c) {
+  const int cs = W == 16 ? (c ^ ((row >> 1) & 3)) : c;
+  return static_cast<uint32_t>(row * 4 * W + cs * 16);
+}
+
 template <int BN, int CL>
 __device__ __forceinline__ void cluster_send_slices(const uint32_t (&v)[BN], uint32_t stage0, uint32_t out0, int row) {
   constexpr int W = BN / CL;
@@ -490,10 +499,10 @@ __device__ __forceinline__ void cluster_send_slices(const uint32_t (&v)[BN], uin
   const uint32_t rank = cluster_ctarank();
 #pragma unroll
   for (int q = 0; q < CL; ++q) {
-    const uint32_t dst = (q == static_cast<int>(rank) ? stage0 + rank * SL : out0 + q * SL) +
-                         static_cast<uint32_t>(row * 4 * W);
+    const uint32_t dst = q == static_cast<int>(rank) ? stage0 + rank * SL : out0 + q * SL;
 #pragma unroll
-    for (int c = 0; c < W; c += 4) st_shared_v4(dst + 4u * c, v[q * W + c], v[q * W + c + 1], v[q * W + c + 2], v[q * W + c + 3]);
+    for (int c = 0; c < W; c += 4)
+      st_shared_v4(dst + slice_off<W>(row, c / 4), v[q * W + c], v[q * W + c + 1], v[q * W + c + 2], v[q * W + c + 3]);
   }
 }
 
@@ -510,10 +519,10 @@ __device__ __forceinline__ void cluster_sum_store(const TcArgs& a, uint32_t stag
   for (int j = 0; j < W; ++j) s[j] = 0.0f;
 #pragma unroll
   for (int p = 0; p < CL; ++p) {
-    const uint32_t src = stage0 + static_cast<uint32_t>(p) * SL + static_cast<uint32_t>(row * 4 * W);
+    const uint32_t src = stage0 + static_cast<uint32_t>(p) * SL;
 #pragma unroll
     for (int c = 0; c < W; c += 4) {
-      const float4 t = ld_shared_f32x4(src + 4u * c);
+      const float4 t = ld_shared_f32x4(src + slice_off<W>(row, c / 4));
       s[c] += t.x;
       s[c + 1] += t.y;
       s[c + 2] += t.z;
