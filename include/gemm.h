@@ -79,6 +79,17 @@ typedef struct {
  * this mode with a split factor above 1 (GEMM_ERR_UNSUPPORTED). */
 #define GEMM_FLAG_DETERMINISTIC 1
 
+/* int4 weights pre-packed by gemm_int4_prepack: gemm_run's B is the packed
+ * buffer (scales and zeros are still passed in their plain [N][groups]
+ * layout: the zero-point term reads them).  Needs b_dtype = GEMM_INT4, a
+ * group size of 64 or 128 or a multiple of 256, and split ranges of whole
+ * 256-deep stages: with split_k = 0 the planner rounds the SM-waste rule's
+ * ranges up to whole stages; a caller's split_k whose ranges
+ * (ceil(ceil(K / 64) / split_k) K blocks) are not a multiple of 4 blocks, or
+ * any other shape outside these, gets GEMM_ERR_UNSUPPORTED from gemm_create.  Plans with this flag
+ * use the fp16 form; the results are the same bits as with the plain layout. */
+#define GEMM_FLAG_INT4_PREPACKED 4
+
 /* Test aid for the failure path (not for production use).  The plan's first
  * gemm_run withholds the first pipeline stage of one CTA: no copy is issued
  * for it, so the MMA issuer's bounded wait on it runs out, the kernel records
@@ -212,6 +223,26 @@ int32_t gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int32_t block_m, int32
  * invalid stride map indices to themselves).  Host computation. */
 uint32_t gemm_perm_fwd(uint32_t index, uint32_t count, uint32_t block, uint32_t stride);
 uint32_t gemm_perm_inv(uint32_t index, uint32_t count, uint32_t block, uint32_t stride);
+
+/* Offline pre-pack of int4 weights for GEMM_FLAG_INT4_PREPACKED (the BitBLAS
+ * page's "Relevant Issues": a ladder-based basic layout, so that the
+ * dequantising producer's accesses are whole vectors without bank
+ * conflicts; here the layout is the kernel's stage).  For each 128-row tile t
+ * and 256-deep stage s (S = ceil(K / 256) stages), a block of
+ * gemm_int4_prepack_bytes(N, K, group) / (ceil(N / 128) * S) bytes at block
+ * index t * S + s: the tile's 128 rows x 128 bytes of codes of the stage, row
+ * r at r * 128, its 16-byte chunk c (codes 32c .. 32c + 31 of the stage) at
+ * chunk c ^ (r mod 8) (the 128-byte swizzle), then the stage's scales as slots
+ * of 128 fp16 (row r at 2r): one slot per group for groups of 64 or 128, one
+ * for groups of 256 or more.  Rows past N and codes past K are zero.
+ *   B: N rows of ldb bytes (ldb = 0: K / 2), codes as for gemm_run; device,
+ *      16-byte aligned, ldb a multiple of 16.  scales: fp16 [N][K / group].
+ *   out: device, 16-byte aligned, gemm_int4_prepack_bytes bytes, caller-owned.
+ * gemm_int4_prepack_bytes returns 0 for shapes it does not take (K a multiple
+ * of 64 and of the group, group 64, 128 or a multiple of 256). */
+size_t gemm_int4_prepack_bytes(int64_t N, int64_t K, int32_t group_size);
+gemm_status_t gemm_int4_prepack(const void* B, int64_t ldb, const void* scales, int64_t N, int64_t K,
+                                int32_t group_size, void* out, void* stream);
 
 /* The same permutation computed on the device by the routine the kernels'
  * loaders use: out[j] = gemm_perm_fwd(in[j], count, block, stride) (inverse

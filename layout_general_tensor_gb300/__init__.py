@@ -23,6 +23,7 @@ GEMM_ERR_CUDA = 5
 GEMM_ERR_TIMEOUT = 6
 
 GEMM_FLAG_DETERMINISTIC = 1
+GEMM_FLAG_INT4_PREPACKED = 4
 GEMM_FLAG_TEST_WITHHOLD_STAGE = 1 << 30
 
 GEMM_K_CONTIG = 0
@@ -38,7 +39,7 @@ EXPORTS = (
     "gemm_create", "gemm_workspace_size", "gemm_query", "gemm_run", "gemm_run_static_scratch",
     "gemm_sync_status", "gemm_destroy",
     "gemm_splitk_auto", "gemm_perm_fwd", "gemm_perm_inv", "gemm_perm_device", "gemm_magic_divmod_host",
-    "gemm_magic_divmod_device", "gemm_status_string",
+    "gemm_magic_divmod_device", "gemm_status_string", "gemm_int4_prepack_bytes", "gemm_int4_prepack",
     "reduce_rows_workspace_size", "reduce_rows_f32",
 )
 
@@ -88,6 +89,9 @@ def _load():
         "gemm_magic_divmod_host": (ctypes.c_int, [P, ctypes.c_size_t, ctypes.c_uint32, P, P]),
         "gemm_magic_divmod_device": (ctypes.c_int, [P, ctypes.c_size_t, ctypes.c_uint32, P, P, P]),
         "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "gemm_int4_prepack_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32]),
+        "gemm_int4_prepack": (ctypes.c_int, [P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                             P, P]),
         "reduce_rows_workspace_size": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                                       ctypes.POINTER(ctypes.c_size_t)]),
         "reduce_rows_f32": (ctypes.c_int, [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P,
@@ -169,6 +173,18 @@ def gemm_destroy(plan: int) -> None:
 
 def gemm_splitk_auto(M, N, K, block_m=128, block_n=128, block_k=64, num_sms=148, threshold=0.05) -> int:
     return _lib.gemm_splitk_auto(M, N, K, block_m, block_n, block_k, num_sms, threshold)
+
+
+def gemm_int4_prepack_bytes(N: int, K: int, group_size: int = 128) -> int:
+    """Bytes of the pre-packed int4 weight buffer (0: shape not taken)."""
+    return _lib.gemm_int4_prepack_bytes(N, K, group_size)
+
+
+def gemm_int4_prepack(B: int, ldb: int, scales: int, N: int, K: int, group_size: int, out: int,
+                      stream: int = 0) -> int:
+    """Raw entry point: device addresses of the plain int4 weights, their fp16
+    scales and the output buffer; returns the status."""
+    return _lib.gemm_int4_prepack(B or None, ldb, scales or None, N, K, group_size, out or None, stream or None)
 
 
 def gemm_perm_fwd(index, count, block, stride) -> int:
@@ -282,3 +298,18 @@ class Gemm:
             self.close()
         except Exception:
             pass
+
+
+def int4_prepack(B, scales, N, K, group_size=128, ldb=0, stream=None):
+    """Pre-pack int4 weights (device uint8 tensor, N rows of ldb bytes) and
+    their fp16 scales for GEMM_FLAG_INT4_PREPACKED; returns the packed device
+    uint8 tensor."""
+    import torch
+    nbytes = gemm_int4_prepack_bytes(N, K, group_size)
+    if nbytes == 0:
+        raise GemmError(GEMM_ERR_INVALID_ARG, "gemm_int4_prepack_bytes")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=B.device)
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    _check(gemm_int4_prepack(B.data_ptr(), ldb, scales.data_ptr(), N, K, group_size, out.data_ptr(), s),
+           "gemm_int4_prepack")
+    return out

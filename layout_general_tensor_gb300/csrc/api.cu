@@ -13,6 +13,7 @@
 #include "gemm.h"
 #include "kernels.h"
 #include "realign.cuh"
+#include "int4.h"
 #include "plan.h"
 
 using lgt::MagicDiv;
@@ -46,7 +47,7 @@ gemm_status_t validate(const gemm_desc_t& d) {
     return GEMM_ERR_INVALID_ARG;
   }
   if (d.split_k < 0 || d.split_k > 65536 || d.num_sms < 0 || d.group_size < 0 ||
-      (d.flags & ~(GEMM_FLAG_DETERMINISTIC | GEMM_FLAG_TEST_WITHHOLD_STAGE)) != 0)
+      (d.flags & ~(GEMM_FLAG_DETERMINISTIC | GEMM_FLAG_INT4_PREPACKED | GEMM_FLAG_TEST_WITHHOLD_STAGE)) != 0)
     return GEMM_ERR_INVALID_ARG;
   if (d.lda < 0 || d.ldb < 0 || d.ldc < 0) return GEMM_ERR_INVALID_ARG;
   const int64_t a_min = d.a_layout == GEMM_K_CONTIG ? d.K : d.M;
@@ -393,6 +394,29 @@ gemm_status_t gemm_perm_device(const uint32_t* in, size_t n, uint32_t count, uin
              : GEMM_ERR_CUDA;
 }
 
+size_t gemm_int4_prepack_bytes(int64_t N, int64_t K, int32_t group_size) {
+  const int group = group_size ? group_size : 128;
+  if (N <= 0 || K <= 0 || K % 64 != 0 || group % 64 != 0 || K % group != 0 ||
+      !(group == 64 || group == 128 || group % 256 == 0))
+    return 0;
+  return lgt::pre_total_bytes(N, K, group);
+}
+
+gemm_status_t gemm_int4_prepack(const void* B, int64_t ldb, const void* scales, int64_t N, int64_t K,
+                                int32_t group_size, void* out, void* stream) {
+  const int group = group_size ? group_size : 128;
+  if (gemm_int4_prepack_bytes(N, K, group) == 0) return GEMM_ERR_INVALID_ARG;
+  if (!B || !scales || !out) return GEMM_ERR_INVALID_ARG;
+  const int64_t ld = ldb ? ldb : K / 2;
+  if (ld < K / 2) return GEMM_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(B) % 16 || ld % 16 || reinterpret_cast<uintptr_t>(out) % 16 ||
+      reinterpret_cast<uintptr_t>(scales) % 2)
+    return GEMM_ERR_ALIGNMENT;
+  return lgt::launch_int4_prepack(B, ld, scales, N, K, group, out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GEMM_OK
+             : GEMM_ERR_CUDA;
+}
+
 gemm_status_t gemm_magic_divmod_host(const uint32_t* n, size_t count, uint32_t divisor, uint32_t* q, uint32_t* r) {
   if (divisor == 0 || (count && (!n || !q || !r))) return GEMM_ERR_INVALID_ARG;
   const MagicDiv m = lgt::magic_encode(divisor);
@@ -524,9 +548,15 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   } else {
     p.split = d.split_k;
   }
+  p.kb_per_split = p.kb_total > 0 ? static_cast<int>(ceil_div(p.kb_total, p.split)) : 0;
+  if ((d.flags & GEMM_FLAG_INT4_PREPACKED) && d.split_k == 0 && p.split > 1 && p.kb_per_split % 4 != 0) {
+    // pre-packed weights come in 256-deep stages: the rule's split ranges
+    // are rounded up to whole stages
+    p.kb_per_split = (p.kb_per_split + 3) / 4 * 4;
+    p.split = static_cast<int>(ceil_div(p.kb_total, p.kb_per_split));
+  }
   p.det = (d.flags & GEMM_FLAG_DETERMINISTIC) && p.split > 1;
   p.split_req = p.split;
-  p.kb_per_split = p.kb_total > 0 ? static_cast<int>(ceil_div(p.kb_total, p.split)) : 0;
   const int64_t tiles = static_cast<int64_t>(p.tiles_p) * p.tiles_q;
   if (tiles * (p.kb_total > 0 ? p.kb_total : 1) >= (1ll << 31)) return GEMM_ERR_UNSUPPORTED;
   const int workers = p.pair ? pair_clusters(p.device) : p.sms_grid;
@@ -647,6 +677,12 @@ gemm_status_t gemm_create(const gemm_desc_t* desc, gemm_plan_t** out) {
   p.ws_bytes = off_aligned;
   // When a base pointer is not 16-byte aligned the operand is repacked too.
   p.ws_bytes_misaligned = off + pack_a_bytes + pack_b_bytes;
+  if (d.flags & GEMM_FLAG_INT4_PREPACKED) {
+    // pre-packed weights: int4 only, whole 256-deep stages per split range,
+    // groups of 64 or 128 or a multiple of 256 (the fp16 form: int4_plan)
+    const bool group_ok = p.group == 64 || p.group == 128 || p.group % 256 == 0;
+    if (!int4 || !group_ok || (p.split > 1 && p.kb_per_split % 4 != 0)) return GEMM_ERR_UNSUPPORTED;
+  }
   if (int4) lgt::int4_plan(p, off);  // form, prepared-activation region and tables
 
   if (d.flags & GEMM_FLAG_TEST_WITHHOLD_STAGE) {
@@ -688,7 +724,8 @@ gemm_status_t gemm_query(const gemm_plan_t* plan, gemm_info_t* info) {
   info->tile_k = kBlockK;
   info->swap_ab = plan->swap;
   info->num_units = plan->num_units;
-  info->k_per_split = static_cast<int32_t>(ceil_div(plan->kb_total, plan->split_req) * kBlockK);
+  // (a stream-K tail's units are single K blocks; the whole tiles take all of K)
+  info->k_per_split = static_cast<int32_t>((plan->tail_tiles ? plan->kb_total : plan->kb_per_split) * kBlockK);
   info->streamk_tiles = plan->tail_tiles;
   info->cluster_size = plan->cl_size;
   info->repack_a = plan->repack_a;

@@ -107,7 +107,15 @@ bool build_int4_args(const gemm_plan* plan, const void* B, void* C, const void* 
                                      d.K / 64 < 4 ? static_cast<int>(d.K / 64) : 4)) {
     return false;
   }
-  if (!encode_int4_weights(&a4.tm_w, B, d.N, plan->ldb)) return false;
+  if (d.flags & GEMM_FLAG_INT4_PREPACKED) {
+    // B is the pre-packed buffer (gemm_int4_prepack): bulk copies, no map
+    a4.wpre = static_cast<const uint8_t*>(B);
+    a4.pre_block = static_cast<int32_t>(pre_block_bytes(static_cast<int>(plan->group)));
+    a4.pre_stages = static_cast<int32_t>((d.K + 255) / 256);
+    a4.pre_kbpg = static_cast<int32_t>(plan->group / kBlockK);
+  } else if (!encode_int4_weights(&a4.tm_w, B, d.N, plan->ldb)) {
+    return false;
+  }
   args.c = C;
   args.ldc = plan->ldc;
   args.ws = partial;
@@ -155,7 +163,8 @@ bool build_int4_args(const gemm_plan* plan, const void* B, void* C, const void* 
 void int4_plan(gemm_plan& p, size_t off) {
   const gemm_desc_t& d = p.d;
   const char* form = std::getenv("LGT_GEMM_INT4_FORM");
-  const bool want_f8 = form && std::strcmp(form, "e4m3") == 0;
+  // (pre-packed weights are the fp16 form's layout)
+  const bool want_f8 = form && std::strcmp(form, "e4m3") == 0 && !(d.flags & GEMM_FLAG_INT4_PREPACKED);
   p.int4_form = (want_f8 && int4f8_supported(p.a_mn, d.M, d.K, p.group) && p.kb_per_split % 2 == 0) ? 2 : 1;
   p.off_aprep = off;
   if (p.int4_form == 2) {

@@ -67,7 +67,7 @@ constexpr int kEpiWarp04 = 4;                 // epilogue warps 4..7
 constexpr int kExpWarp0 = 8;                  // expander warps 8..15
 constexpr int kQuadK = 4;                     // K blocks per stage
 constexpr uint32_t kRawBytes = TILE_P * 128;  // 128 rows x 128 bytes (256 codes)
-constexpr uint32_t kWStage = kRawBytes;       // packed-weight stage
+constexpr uint32_t kWStage = kRawBytes + 1024;  // packed-weight stage (+ a pre-packed block's scale slots)
 constexpr uint32_t kASlotCol0 = 128;          // A slots at [128, 512); the accumulators below
 
 template <int BN>
@@ -416,8 +416,16 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
             int32_t tp, tq, m0, m1, n0, n1;
             tile_ranges(a, itw.g.tile, BN, tp, tq, m0, m1, n0, n1);
             const int kb = itw.g.kb0 + wkb0;
-            mbar_arrive_expect_tx(full_w(s), kRawBytes);
-            tma_load_2d(base + s * kWStage, &A4.tm_w, full_w(s), kb * (TILE_K / 2), n0);
+            if (A4.wpre) {
+              // pre-packed: the stage's block (codes already swizzled, then
+              // its scales) in one bulk copy
+              const uint8_t* src = A4.wpre + (static_cast<int64_t>(tp) * A4.pre_stages + kb / kQuadK) * A4.pre_block;
+              mbar_arrive_expect_tx(full_w(s), static_cast<uint32_t>(A4.pre_block));
+              bulk_load_g2s(base + s * kWStage, src, static_cast<uint32_t>(A4.pre_block), full_w(s));
+            } else {
+              mbar_arrive_expect_tx(full_w(s), kRawBytes);
+              tma_load_2d(base + s * kWStage, &A4.tm_w, full_w(s), kb * (TILE_K / 2), n0);
+            }
             ++w_issued;
             whave = false;
             progress = true;
@@ -520,6 +528,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
       uint32_t s2[2], c1024[2], c64[2];
     };
     auto lookup = [&](int kb0, int nk, bool nr, StageScales& o) {
+      if (A4.wpre) return;  // pre-packed: the scales arrive with the stage
       if (nr) {
         int32_t tp, tq, m0, m1, n0, n1;
         tile_ranges(a, it.g.tile, BN, tp, tq, m0, m1, n0, n1);
@@ -588,6 +597,20 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
       // the warp leaves together (tcgen05.st below needs every lane)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
+      if (A4.wpre) {
+        // pre-packed: this row's scale of each of its K blocks from the
+        // stage's scale slots
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * h + jj;
+          const int slot = A4.pre_kbpg >= kQuadK ? 0 : j / A4.pre_kbpg;
+          const uint32_t s2 =
+              ld_shared_u16(base + sw * kWStage + kRawBytes + static_cast<uint32_t>(slot * 256 + r * 2)) * 0x10001u;
+          cur.s2[jj] = s2;
+          cur.c1024[jj] = hmul2(s2, 0xE400E400u);
+          cur.c64[jj] = hmul2(s2, 0xD400D400u);
+        }
+      }
       // raw row r: eight 16-byte chunks, chunk c stored at c ^ (r mod 8)
       // (128-byte swizzle); this warp's K blocks 2h, 2h + 1 are chunks 4h..4h+3
       const uint8_t* rowp = smem + sw * kWStage + r * 128;
@@ -826,7 +849,69 @@ bool int4_prep_fused(int a_mn, int K, int group) {
   return !a_mn && (gc == 8 || gc == 16 || gc == 32) && (K / 8) % 32 == 0;
 }
 
+// Offline pre-pack of the weights (layout: int4.h).  One thread per 16-byte
+// chunk of codes of a block; then one per scale of a block's slots.
+__global__ void __launch_bounds__(256) int4_prepack_kernel(const uint8_t* __restrict__ B, int64_t ldb,
+                                                           const uint16_t* __restrict__ scales, int N, int K,
+                                                           int group, int S, int block, int nslots, int64_t nblocks,
+                                                           uint8_t* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t row_bytes = K / 2;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nblocks * 1024; i += step) {
+    const int64_t blk = i >> 10;
+    const int w = static_cast<int>(i & 1023), r = w >> 3, cout = w & 7;
+    const int64_t t = blk / S, s = blk - t * S;
+    const int64_t n = t * TILE_P + r;
+    const int c = cout ^ (r & 7);  // the stage's chunk stored at cout
+    const int64_t b0 = s * 128 + c * 16;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (n < N && b0 < row_bytes) {
+      const uint8_t* src = B + n * ldb + b0;
+      if (b0 + 16 <= row_bytes) {
+        v = *reinterpret_cast<const uint4*>(src);
+      } else {
+        uint8_t tmp[16] = {};
+        for (int e = 0; b0 + e < row_bytes; ++e) tmp[e] = src[e];
+        v = *reinterpret_cast<const uint4*>(tmp);
+      }
+    }
+    *reinterpret_cast<uint4*>(out + blk * block + r * 128 + cout * 16) = v;
+  }
+  const int G = K / group;
+  const int per = nslots * TILE_P;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nblocks * per; i += step) {
+    const int64_t blk = i / per;
+    const int rem = static_cast<int>(i - blk * per), slot = rem / TILE_P, r = rem - slot * TILE_P;
+    const int64_t t = blk / S, s = blk - t * S;
+    const int64_t n = t * TILE_P + r;
+    const int64_t g = group < 256 ? s * (256 / group) + slot : (s * 256) / group;
+    const uint16_t val = (n < N && g < G) ? scales[n * G + g] : static_cast<uint16_t>(0);
+    reinterpret_cast<uint16_t*>(out + blk * block + kRawBytes)[slot * TILE_P + r] = val;
+  }
+}
+
 }  // namespace
+
+int pre_slots(int group) { return group < 256 ? 256 / group : 1; }
+size_t pre_block_bytes(int group) { return kRawBytes + static_cast<size_t>(pre_slots(group)) * TILE_P * 2; }
+size_t pre_total_bytes(int64_t N, int64_t K, int group) {
+  return static_cast<size_t>((N + TILE_P - 1) / TILE_P) * static_cast<size_t>((K + 255) / 256) * pre_block_bytes(group);
+}
+
+cudaError_t launch_int4_prepack(const void* B, int64_t ldb, const void* scales, int64_t N, int64_t K, int group,
+                                void* out, cudaStream_t stream) {
+  const int S = static_cast<int>((K + 255) / 256);
+  const int64_t nblocks = (N + TILE_P - 1) / TILE_P * S;
+  if (nblocks == 0) return cudaSuccess;
+  const int64_t want = nblocks * 1024 / 256;
+  const int grid = static_cast<int>(want < 65535 ? (want > 0 ? want : 1) : 65535);
+  return launch_pdl(int4_prepack_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream,
+                    static_cast<const uint8_t*>(B), ldb, static_cast<const uint16_t*>(scales), static_cast<int>(N),
+                    static_cast<int>(K), group, S, static_cast<int>(pre_block_bytes(group)), pre_slots(group), nblocks,
+                    static_cast<uint8_t*>(out));
+}
 
 cudaError_t launch_int4_prep(const void* A, int64_t lda, int a_mn, int M, int K, int group, void* Ap, float* agsum,
                              int sms, cudaStream_t stream) {

@@ -21,7 +21,27 @@ struct Int4Args {
   MagicDiv div_kb_per_group; // 64-deep K block -> quantisation group
   int32_t x_box_kb;          // fp16 form: K blocks per activation box (min(4, K / 64)); t.tm_q is 3-D {64, M, K / 64}
   int32_t vec_sz;            // fp16 form: scale / zero rows readable 8 groups (16 bytes) at a time
+  // fp16 form with pre-packed weights (gemm_int4_prepack): one block per
+  // 128-row tile and 256-deep stage, [tile][stage]; null: the plain layout
+  const uint8_t* wpre;
+  int32_t pre_block;         // bytes of a block (codes + scale slots)
+  int32_t pre_stages;        // blocks per tile (ceil(K / 256))
+  int32_t pre_kbpg;          // 64-deep K blocks per group (scale slot of K block j: j / kbpg, 0 when >= 4)
 };
+
+// Pre-packed int4 weights (the fp16 form's offline layout).  For each
+// 128-row tile t and 256-deep stage s, a block at (t * S + s) * block bytes:
+// the 128 rows x 128 bytes of codes, row r at r * 128, its 16-byte chunk c
+// (codes 32 c .. 32 c + 31 of the stage) at chunk c ^ (r mod 8) -- where a
+// 128-byte-swizzled TMA box of the plain layout puts them -- then the
+// stage's scale slots, 128 fp16 each (row r at 2 r): one per group for groups
+// of 64 or 128 (4 or 2 slots), one for groups of 256 or more.  Rows past N
+// and K past K are zero.
+int pre_slots(int group);
+size_t pre_block_bytes(int group);
+size_t pre_total_bytes(int64_t N, int64_t K, int group);
+cudaError_t launch_int4_prepack(const void* B, int64_t ldb, const void* scales, int64_t N, int64_t K, int group,
+                                void* out, cudaStream_t stream);
 
 // ---- fp16 form (any M <= 64, any activation layout, any group multiple of 64)
 

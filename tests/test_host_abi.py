@@ -192,6 +192,47 @@ def test_planner_int4_form(lib, monkeypatch):
     lib.gemm_destroy(h)
 
 
+def test_planner_int4_prepacked(lib, monkeypatch):
+    """GEMM_FLAG_INT4_PREPACKED: int4 plans only, the fp16 form (also when
+    the e4m3 form is asked for), groups of 64 or 128 or multiples of 256,
+    split ranges of whole 256-deep stages; the packed size is one block of
+    codes and scale slots per 128-row tile and 256-deep stage."""
+    monkeypatch.setenv("LGT_GEMM_INT4_FORM", "e4m3")
+    base = dict(a_dtype=lib.GEMM_F16, b_dtype=lib.GEMM_INT4, c_dtype=lib.GEMM_F16, num_sms=148,
+                flags=lib.GEMM_FLAG_INT4_PREPACKED, group_size=128)
+    h = lib.gemm_create(lib.make_desc(16, 16384, 16384, split_k=0, **base))
+    info = lib.gemm_query(h)
+    assert info.dequant_form == 1 and info.split_k == 32 and (info.k_per_split // 64) % 4 == 0
+    lib.gemm_destroy(h)
+    # the rule's split ranges rounded up to whole 256-deep stages
+    for M, N, K in [(16, 384, 8192), (16, 700, 4096), (1, 128, 640), (16, 4096, 2048)]:
+        d = lib.make_desc(M, N, K, split_k=0, **base)
+        h = lib.gemm_create(d)
+        info = lib.gemm_query(h)
+        lib.gemm_destroy(h)
+        kb = -(-K // 64)
+        rule = lib.gemm_splitk_auto(M, N, K, 128, 128, 64, 148, 0.05)
+        want_kbps = -(-kb // rule)
+        if rule > 1:
+            want_kbps = -(-want_kbps // 4) * 4
+        assert info.k_per_split == want_kbps * 64, (M, N, K)
+        assert info.split_k == -(-kb // want_kbps), (M, N, K)
+    for kw in [dict(M=16, N=512, K=2048, split_k=7), dict(M=16, N=512, K=768, group_size=192)]:
+        args = dict(base)
+        args.update(kw)
+        st, _ = lib.gemm_create_status(lib.make_desc(**args))
+        assert st == lib.GEMM_ERR_UNSUPPORTED, kw
+    st, _ = lib.gemm_create_status(lib.make_desc(256, 256, 256, num_sms=148, flags=lib.GEMM_FLAG_INT4_PREPACKED))
+    assert st == lib.GEMM_ERR_UNSUPPORTED
+    for N, K, g in [(16384, 16384, 128), (300, 640, 64), (130, 1280, 256), (1, 512, 512)]:
+        slots = 256 // g if g < 256 else 1
+        assert lib.gemm_int4_prepack_bytes(N, K, g) == -(-N // 128) * -(-K // 256) * (128 * 128 + slots * 256)
+    for N, K, g in [(0, 256, 128), (256, 0, 128), (256, 768, 192), (256, 100, 64), (256, 640, 256)]:
+        assert lib.gemm_int4_prepack_bytes(N, K, g) == 0, (N, K, g)
+    # null pointers are refused before any launch
+    assert lib.gemm_int4_prepack(0, 0, 0, 256, 1024, 128, 0) == lib.GEMM_ERR_INVALID_ARG
+
+
 def test_planner_skinny_and_irregular_factors(lib):
     # the SM-waste rule's values at 148 SMs for the skinny bf16 and int4-shaped problems
     desc = lib.make_desc(64, 4096, 16384, split_k=0, num_sms=148)
@@ -253,7 +294,7 @@ def test_withhold_flag_only_where_no_cta_waits_on_another(lib):
                             flags=W, num_sms=148)):
         st, h = lib.gemm_create_status(d)
         assert st == lib.GEMM_ERR_UNSUPPORTED and h is None
-    st, h = lib.gemm_create_status(lib.make_desc(256, 256, 256, flags=W | 4, num_sms=148))
+    st, h = lib.gemm_create_status(lib.make_desc(256, 256, 256, flags=W | 8, num_sms=148))
     assert st == lib.GEMM_ERR_INVALID_ARG
 
 
