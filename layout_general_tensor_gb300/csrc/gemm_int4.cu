@@ -39,17 +39,20 @@
 //
 // Warp roles (512 threads):
 //   warp 0       TMA producer for both rings.
-//   warps 1..3   MMA issuers (NI of them active, by accumulator width): the
-//                CTA's stages are dealt round-robin to the issuers (stage s
-//                to issuer s % NI); each waits for its stage's expanded slot
-//                and activation, issues all of the stage's MMAs back to back
-//                into its own accumulator, and frees the slot and the
-//                activation buffer.  Warp 1 owns the TMEM.
+//   warps 1..3   MMA issuers (NI of them active, by accumulator width).  One
+//                thread issues a narrow MMA only every 150 to 200 cycles
+//                whatever its width, so a stage's MMAs are spread over all
+//                of them: MMA m of a stage (K block m / 4, 16-deep step
+//                m % 4) goes to issuer m % NI, into that issuer's own
+//                accumulator.  Every issuer waits for every stage's expanded
+//                slot and activation and commits the slot and the activation
+//                buffer free (NI arrivals each).  Warp 1 owns the TMEM.
 //   warps 4..7   epilogue (TMEM lane quadrant warp % 4), adds the NI
 //                accumulators.
 //   warps 8..15  expanders: two warps per TMEM lane quadrant, each taking two
 //                of every stage's four K blocks; each thread owns one weight
-//                row of the tile.
+//                row of the tile.  A stage's codes are expanded before the
+//                slot they go to is waited for.
 #include <cuda_fp16.h>
 
 #include "int4.h"
@@ -72,20 +75,21 @@ constexpr uint32_t kASlotCol0 = 128;          // A slots at [128, 512); the accu
 
 template <int BN>
 struct Cfg4 {
-  // MMA issuers.  One thread keeps about one narrow (N <= 64) MMA in flight,
-  // and every wait between its MMAs costs it a few hundred cycles, so the
-  // tensor core runs several times faster when several threads each issue
-  // long runs of MMAs into accumulators of their own, which the epilogue adds.
+  // MMA issuers.  One thread issues a narrow (N <= 64) MMA about every 150
+  // to 200 cycles whatever N, and the tensor core takes them several times
+  // faster than that, so every stage's MMAs are spread over NI issuers, each
+  // with accumulators of its own (double-buffered: 2 NI BN <= 128 columns),
+  // which the epilogue adds.
   static constexpr int NI = BN == 16 ? 3 : (BN == 32 ? 2 : 1);
-  // TMEM A slots of 128 columns and activation buffers, both multiples of
-  // NI: stage s uses slot s % TSLOTS and buffer s % XST, so each slot's and
-  // each buffer's barriers are waited on by one issuer only, in order (an
-  // issuer that skipped the stages of others could otherwise wait on a
-  // barrier two phases ahead and see the older phase's parity as complete).
-  static constexpr int TSLOTS = NI == 2 ? 2 : 3;
+  // TMEM A slots of 128 columns (a stage's four K blocks as fp16 pairs);
+  // every issuer takes part in every stage, so it waits on every slot's and
+  // activation buffer's barriers in order.
+  static constexpr int TSLOTS = 3;
   static constexpr uint32_t ACT_TILE = BN * TILE_K * 2;  // one 64-deep activation box
   static constexpr uint32_t XSTAGE = kQuadK * ACT_TILE;  // a stage's activation
-  static constexpr int XST = NI == 2 ? 4 : 3;            // activation ring
+  // activation ring: one buffer per A slot (stage s uses both s % TSLOTS),
+  // so that one barrier frees both
+  static constexpr int XST = TSLOTS;
   // the tile's slice of the activation group sums, Ag[g][m0 .. m0 + BN),
   // staged in shared memory for the zero-point term (BN = 16, up to 256 groups)
   static constexpr uint32_t ZP_BYTES = BN == 16 ? 256 * BN * 4 : 0;
@@ -93,16 +97,15 @@ struct Cfg4 {
   static constexpr int WST_FIT = static_cast<int>((RING_BYTES - XST * XSTAGE) / kWStage);
   static constexpr int WST = WST_FIT > 12 ? 12 : WST_FIT;  // packed-weight ring
   static constexpr uint32_t X_OFF = WST * kWStage;
-  // barriers: full_w[W], wfree[W], full_x[X], xfree[X], a_full[T], tfree[T], accf[2], acce[2], teardown
+  // barriers: full_w[W], wfree[W], full_x[X], a_full[T], tfree[T], accf[2], acce[2], teardown
   static constexpr uint32_t ZP_OFF = X_OFF + XST * XSTAGE;
   static constexpr uint32_t BAR_OFF = ZP_OFF + ZP_BYTES;
-  static constexpr uint32_t NUM_BARS = 2 * WST + 2 * XST + 2 * TSLOTS + 5;
+  static constexpr uint32_t NUM_BARS = 2 * WST + XST + 2 * TSLOTS + 5;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_ALLOC = MISC_OFF + 64 + 1024;  // slack for 1024-byte alignment
   static_assert(kWStage % 1024 == 0 && ACT_TILE % 1024 == 0, "swizzled buffers stay 1024-byte aligned");
-  static_assert(WST >= 4 && XST >= 2, "ring depths");
+  static_assert(WST >= 4 && XST == TSLOTS, "ring depths");
   static_assert(NI <= kMaxIssuers, "issuer warps");
-  static_assert(TSLOTS % NI == 0 && XST % NI == 0, "one issuer per slot and per activation buffer");
   static_assert(2 * NI * BN <= static_cast<int>(kASlotCol0), "accumulators fit below the A slots");
   static_assert(kASlotCol0 + TSLOTS * 128 <= 512, "A slots fit in the TMEM allocation");
 };
@@ -141,31 +144,6 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
       ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
-}
-
-// Every MMA of one stage of NK K blocks (MMA m = 4 j + k: K block j, 16-deep
-// step k), straight-line; `first` starts the accumulator at the first one.
-template <int NK, uint32_t ACT_TILE>
-__device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint32_t a0, uint64_t bd0, uint32_t idesc, uint32_t first) {
-#pragma unroll
-  for (int m = 0; m < 4 * NK; ++m) {
-    const int j = m >> 2, k = m & 3;
-    // A: 8 TMEM columns (16 fp16 pairs) per 16-deep step; B: +32 bytes per step
-    tc_mma_f16_ts(d_tmem, a0 + static_cast<uint32_t>(j * 32 + k * 8),
-                  bd0 + static_cast<uint64_t>((j * ACT_TILE) >> 4) + static_cast<uint64_t>(2 * k), idesc,
-                  (m == 0 && first) ? 0u : 1u);
-  }
-}
-
-template <uint32_t ACT_TILE>
-__device__ __forceinline__ void issue_stage_nk(int nk, uint32_t d_tmem, uint32_t a0, uint64_t bd0, uint32_t idesc,
-                                               uint32_t first) {
-  switch (nk) {
-    case 4: issue_stage<4, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
-    case 3: issue_stage<3, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
-    case 2: issue_stage<2, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
-    default: issue_stage<1, ACT_TILE>(d_tmem, a0, bd0, idesc, first); break;
-  }
 }
 
 // Stages of this CTA's runs, in order: up to kQuadK K blocks of one run each
@@ -335,16 +313,15 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
   // full_w[s] / full_x[s]: a packed-weight / activation stage landed.
   // wfree[s]: the stage's eight expander warps have expanded its packed
   // weights into TMEM.
-  // xfree[s]: the MMAs that read the activation stage completed (the stage's
-  // issuer commits).  a_full[t]: the expanders wrote a stage's weights into
-  // TMEM A slot t.  tfree[t]: the MMAs reading slot t completed (the stage's
-  // issuer commits).  accf / acce: accumulator buffer full (one commit per
-  // issuer at the end of each run) / drained by the epilogue.
-  constexpr int kB1 = 2 * C::WST + 2 * C::XST;
+  // a_full[t]: the expanders wrote a stage's weights into TMEM A slot t.
+  // tfree[t]: the MMAs reading slot t and activation buffer t completed
+  // (every issuer commits), so both are free.  accf / acce: accumulator
+  // buffer full (one commit per issuer at the end of each run) / drained by
+  // the epilogue.
+  constexpr int kB1 = 2 * C::WST + C::XST;
   auto full_w = [&](int i) { return bar0 + 8u * i; };
   auto wfree = [&](int i) { return bar0 + 8u * (C::WST + i); };
   auto full_x = [&](int i) { return bar0 + 8u * (2 * C::WST + i); };
-  auto xfree = [&](int i) { return bar0 + 8u * (2 * C::WST + C::XST + i); };
   auto a_full = [&](int t) { return bar0 + 8u * (kB1 + t); };
   auto tfree_bar = [&](int t) { return bar0 + 8u * (kB1 + C::TSLOTS + t); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (kB1 + 2 * C::TSLOTS + b); };
@@ -360,11 +337,10 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
     }
     for (int i = 0; i < C::XST; ++i) {
       mbar_init(full_x(i), 1);
-      mbar_init(xfree(i), 1);
     }
     for (int t = 0; t < C::TSLOTS; ++t) {
       mbar_init(a_full(t), 8);
-      mbar_init(tfree_bar(t), 1);
+      mbar_init(tfree_bar(t), NI);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), NI);
@@ -433,7 +409,7 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         }
         if (xhave) {
           const int s = x_issued % C::XST;
-          if (mbar_test_wait(xfree(s), ((x_issued / C::XST) & 1) ^ 1u)) {
+          if (mbar_test_wait(tfree_bar(s), ((x_issued / C::XST) & 1) ^ 1u)) {
             int32_t tp, tq, m0, m1, n0, n1;
             tile_ranges(a, itx.g.tile, BN, tp, tq, m0, m1, n0, n1);
             // one box: x_box_kb K blocks of bn rows (beyond the run's K blocks
@@ -461,23 +437,26 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         __nanosleep(32);
       }
     }
-  } else if (warp < kIssWarp0 + kMaxIssuers) {
+  } else if (warp < kEpiWarp04) {
     // ------------------------------------------------------------ MMA issuers
-    // Issuer i takes the CTA's stages s with s % NI == i and issues every MMA
-    // of such a stage (K block, 16-deep step) back to back into its own
-    // accumulator; the first MMA of its first stage in a run (one of the
-    // run's first NI stages) starts the accumulator.  Issuers with no stage
-    // in a run (runs of fewer than NI stages) leave theirs untouched, and the
-    // epilogue adds only the accumulators of the run's issuers.  Every
-    // issuer commits the end of every run.
+    // Issuer i issues MMAs m = i, i + NI, ... of every stage (m = 4 j + k:
+    // K block j, 16-deep step k) into its own accumulator; its first MMA of
+    // a run's first stage starts the accumulator.  One commit per stage frees
+    // the stage's A slot and activation buffer.  An issuer with no MMA in
+    // a run (a run of fewer than NI / 4 K blocks, rounded up) leaves its accumulator
+    // untouched, and the epilogue adds only the others.  Every issuer waits
+    // for every stage, so its commits on the slot and activation barriers
+    // come after the stage was filled, in order; it commits the end of every
+    // run.
     const int iss = warp - kIssWarp0;
     if (lane == 0 && iss < NI) {
       StageIter it(a);
-      int kb0, nk, st = 0, acc_iter = -1;
+      int kb0, nk, acc_iter = -1;
       bool nr;
       uint32_t d_tmem = tmem_base;
+      int t = 0;            // A slot and activation buffer of this stage
+      uint32_t tph = 0u;    // their phase parity
       while (it.next(a, kb0, nk, nr)) {
-        const int t = st % C::TSLOTS, sx = st % C::XST;
         if (nr) {
           ++acc_iter;
           const int buf = acc_iter & 1;
@@ -487,22 +466,30 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
           }
           d_tmem = tmem_base + static_cast<uint32_t>((buf * NI + iss) * BN);
         }
-        const int js = kb0 / kQuadK;  // stage index within the run
-        if (st % NI == iss) {
-          if (!mbar_wait_bounded(a_full(t), (st / C::TSLOTS) & 1, a.wait_limit_ns, abort_flag) ||
-              !mbar_wait_bounded(full_x(sx), (st / C::XST) & 1, a.wait_limit_ns, abort_flag)) {
-            if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 0);
-            break;
-          }
-          tc_fence_after();
-          const uint64_t bd0 = sw128_desc(base + C::X_OFF + sx * C::XSTAGE, 16u, 1024u);
-          const uint32_t a0 = tmem_base + kASlotCol0 + static_cast<uint32_t>(t * 128);
-          issue_stage_nk<C::ACT_TILE>(nk, d_tmem, a0, bd0, a.idesc, js < NI ? 1u : 0u);
-          tc_commit(tfree_bar(t));
-          tc_commit(xfree(sx));
+        if (!mbar_wait_bounded(a_full(t), tph, a.wait_limit_ns, abort_flag) ||
+            !mbar_wait_bounded(full_x(t), tph, a.wait_limit_ns, abort_flag)) {
+          if (!*abort_flag) record_timeout(a, abort_flag, 1 * 16 + 0);
+          break;
         }
+        tc_fence_after();
+        const uint64_t bd0 = sw128_desc(base + C::X_OFF + t * C::XSTAGE, 16u, 1024u);
+        const uint32_t a0 = tmem_base + kASlotCol0 + static_cast<uint32_t>(t * 128);
+        const uint32_t first = kb0 == 0;  // the run's first stage
+#pragma unroll
+        for (int m = iss; m < 4 * kQuadK; m += NI) {
+          if (m >= 4 * nk) break;
+          const int j = m >> 2, k = m & 3;
+          // A: 8 TMEM columns (16 fp16 pairs) per 16-deep step; B: +32 bytes per step
+          tc_mma_f16_ts(d_tmem, a0 + static_cast<uint32_t>(j * 32 + k * 8),
+                        bd0 + static_cast<uint64_t>((j * C::ACT_TILE) >> 4) + static_cast<uint64_t>(2 * k), a.idesc,
+                        (m == iss && first) ? 0u : 1u);
+        }
+        tc_commit(tfree_bar(t));
         if (kb0 + nk == it.g.nkb) tc_commit(accf_bar(acc_iter & 1));
-        ++st;
+        if (++t == C::TSLOTS) {
+          t = 0;
+          tph ^= 1u;
+        }
       }
     }
   } else if (warp >= kExpWarp0) {
@@ -510,138 +497,97 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
     const int q4 = warp & 3;
     const int h = (warp - kExpWarp0) >> 2;  // K blocks 2h, 2h + 1 of every stage
     const int r = q4 * 32 + lane;           // weight row within the tile (TMEM lane)
-    StageIter it(a);
-    // This row's scales, 8 groups (16 bytes) per window, held in registers:
-    // the window in use and the next two, each read by one 16-byte load two
-    // windows before it is needed, so that the load's latency hides behind the
-    // weight stream.  (Rows not 16-byte aligned: one load per K block.)
-    const uint16_t* srow = nullptr;
-    int w_cur = 0, w_last = -1;
-    uint4 win0 = make_uint4(0u, 0u, 0u, 0u), win1 = win0, win2 = win0;  // windows w_cur .. w_cur + 2
-    auto load_win = [&](int w) {
-      return (srow && w <= w_last) ? __ldg(reinterpret_cast<const uint4*>(srow) + w) : make_uint4(0u, 0u, 0u, 0u);
-    };
-    // The scales of this warp's two K blocks of a stage as fp16 pairs s, with
-    // -1024 s and -64 s (exact: power-of-two multiples).  Looked up one stage
-    // ahead, while the stage before is expanded; a new run's windows start here.
-    struct StageScales {
-      uint32_t s2[2], c1024[2], c64[2];
-    };
-    auto lookup = [&](int kb0, int nk, bool nr, StageScales& o) {
-      if (A4.wpre) return;  // pre-packed: the scales arrive with the stage
-      if (nr) {
-        int32_t tp, tq, m0, m1, n0, n1;
-        tile_ranges(a, it.g.tile, BN, tp, tq, m0, m1, n0, n1);
-        const int n = n0 + r;
-        srow = n < n1 ? A4.scales + static_cast<int64_t>(n) * A4.groups : nullptr;
-        const int g0 = static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0), A4.div_kb_per_group));
-        const int g1 =
-            static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + it.g.nkb - 1), A4.div_kb_per_group));
-        if (A4.vec_sz) {
-          w_cur = g0 >> 3;
-          w_last = g1 >> 3;
-          win0 = load_win(w_cur);
-          win1 = load_win(w_cur + 1);
-          win2 = load_win(w_cur + 2);
-        }
-      }
-      // group of each K block (the second one's is usually the first's: then
-      // the lookup is not repeated)
-      int gj[2];
+    // This row's scale of each of its two K blocks of a stage (raw fp16
+    // bits).  Pre-packed weights carry them in the stage: K block j's in
+    // slot j / (K blocks per group), at an offset fixed for this thread.
+    // Otherwise they are read from the scale array two stages ahead, by a
+    // look-ahead walk over the same stages, into a three-deep register
+    // ring, so that each load's latency hides behind two stages' expansion.
+    const bool pre = A4.wpre != nullptr;
+    uint32_t pre_off[2];
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj)
-        gj[jj] = static_cast<int>(magic_div(static_cast<uint32_t>(it.g.kb0 + kb0 + 2 * h + jj), A4.div_kb_per_group));
+    for (int jj = 0; jj < 2; ++jj)
+      pre_off[jj] = kRawBytes + static_cast<uint32_t>(
+                                    (A4.pre_kbpg >= kQuadK ? 0 : (2 * h + jj) / max(A4.pre_kbpg, 1)) * 256 + r * 2);
+    StageIter ahead(a);
+    const uint16_t* arow = nullptr;  // the look-ahead stage's scale row (null: row beyond N)
+    auto fetch = [&](uint32_t (&o)[2]) {
+      o[0] = 0u;
+      o[1] = 0u;
+      int kb0a, nka;
+      bool nra;
+      if (!ahead.next(a, kb0a, nka, nra)) return;
+      if (nra) {
+        int32_t tp, tq, m0, m1, n0, n1;
+        tile_ranges(a, ahead.g.tile, BN, tp, tq, m0, m1, n0, n1);
+        const int n = n0 + r;
+        arow = n < n1 ? A4.scales + static_cast<int64_t>(n) * A4.groups : nullptr;
+      }
+      if (!arow) return;
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj) {
         const int j = 2 * h + jj;
-        if (jj == 1 && gj[1] == gj[0]) {
-          o.s2[1] = j < nk ? o.s2[0] : 0u;
-          o.c1024[1] = o.c1024[0];
-          o.c64[1] = o.c64[0];
-          continue;
+        if (j < nka) {
+          const uint32_t g = magic_div(static_cast<uint32_t>(ahead.g.kb0 + kb0a + j), A4.div_kb_per_group);
+          o[jj] = __ldg(arow + g);
         }
-        const int g = gj[jj];
-        uint32_t s2 = 0;
-        if (j < nk) {
-          if (A4.vec_sz) {
-            while (w_cur < (g >> 3)) {  // groups only grow within a run
-              win0 = win1;
-              win1 = win2;
-              win2 = load_win(w_cur + 3);
-              ++w_cur;
-            }
-            // group g & 7 of the window: its 16 bits in both halves
-            const int e = g & 7;
-            const uint32_t word = e < 4 ? (e < 2 ? win0.x : win0.y) : (e < 6 ? win0.z : win0.w);
-            s2 = __byte_perm(word, 0u, (e & 1) ? 0x3232u : 0x1010u);
-          } else {
-            s2 = (srow ? static_cast<uint32_t>(__ldg(srow + g)) : 0u) * 0x10001u;
-          }
-        }
-        o.s2[jj] = s2;
-        o.c1024[jj] = hmul2(s2, 0xE400E400u);
-        o.c64[jj] = hmul2(s2, 0xD400D400u);
       }
     };
-    int kb0, nk, st = 0;
+    uint32_t sc0[2] = {0u, 0u}, sc1[2] = {0u, 0u}, sc2[2] = {0u, 0u};
+    if (!pre) {
+      fetch(sc0);
+      fetch(sc1);
+    }
+    // One K block (eight words of eight codes) as 32 fp16 pairs: codes
+    // (p, p + 4) of a word for p = 0..3 as 1024 + q (p even) or 64 + q
+    // (p odd), then (1024 + q) s - 1024 s = q s, rounded once.
+    auto expand = [&](const uint4& r0, const uint4& r1, uint32_t s16, uint32_t* v) {
+      const uint32_t s2 = s16 * 0x10001u;
+      const uint32_t c1024 = hmul2(s2, 0xE400E400u), c64 = hmul2(s2, 0xD400D400u);
+      const uint32_t words[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+      for (int w8 = 0; w8 < 8; ++w8) {
+        const uint32_t lo = words[w8], hi = lo >> 8;
+        v[4 * w8 + 0] = hfma2(lop3_and_or(lo, 0x000F000Fu, 0x64006400u), s2, c1024);
+        v[4 * w8 + 1] = hfma2(lop3_and_or(lo, 0x00F000F0u, 0x54005400u), s2, c64);
+        v[4 * w8 + 2] = hfma2(lop3_and_or(hi, 0x000F000Fu, 0x64006400u), s2, c1024);
+        v[4 * w8 + 3] = hfma2(lop3_and_or(hi, 0x00F000F0u, 0x54005400u), s2, c64);
+      }
+    };
+    StageIter it(a);
+    int kb0, nk;
     bool nr;
-    bool have = it.next(a, kb0, nk, nr);
-    StageScales cur;
-    if (have) lookup(kb0, nk, nr, cur);
-    while (have) {
-      const int sw = st % C::WST, t = st % C::TSLOTS;
-      const bool got =
-          mbar_wait_bounded(full_w(sw), (st / C::WST) & 1, a.wait_limit_ns, abort_flag) &&
-          mbar_wait_bounded(tfree_bar(t), ((st / C::TSLOTS) & 1) ^ 1u, a.wait_limit_ns, abort_flag);
+    int sw = 0, t = 0;            // weight stage and A slot of this stage
+    uint32_t wph = 0u, tph = 0u;  // their rings' phase parities
+    while (it.next(a, kb0, nk, nr)) {
+      if (!pre) fetch(sc2);  // two stages ahead
+      const bool got = mbar_wait_bounded(full_w(sw), wph, a.wait_limit_ns, abort_flag);
       if (!got && !*abort_flag) record_timeout(a, abort_flag, 3 * 16 + 0);
       // the warp leaves together (tcgen05.st below needs every lane)
       if (!__all_sync(0xffffffffu, got)) break;
-      tc_fence_after();
-      if (A4.wpre) {
-        // pre-packed: this row's scale of each of its K blocks from the
-        // stage's scale slots
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * h + jj;
-          const int slot = A4.pre_kbpg >= kQuadK ? 0 : j / A4.pre_kbpg;
-          const uint32_t s2 =
-              ld_shared_u16(base + sw * kWStage + kRawBytes + static_cast<uint32_t>(slot * 256 + r * 2)) * 0x10001u;
-          cur.s2[jj] = s2;
-          cur.c1024[jj] = hmul2(s2, 0xE400E400u);
-          cur.c64[jj] = hmul2(s2, 0xD400D400u);
-        }
-      }
       // raw row r: eight 16-byte chunks, chunk c stored at c ^ (r mod 8)
       // (128-byte swizzle); this warp's K blocks 2h, 2h + 1 are chunks 4h..4h+3
-      const uint8_t* rowp = smem + sw * kWStage + r * 128;
+      const uint32_t stage = base + static_cast<uint32_t>(sw) * kWStage;
+      const uint8_t* rowp = smem + static_cast<uint32_t>(sw) * kWStage + r * 128;
       uint4 raw[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) raw[c] = *reinterpret_cast<const uint4*>(rowp + (((4 * h + c) ^ (r & 7)) << 4));
-      // the next stage's scales while the loads are in flight
-      int kb0n, nkn;
-      bool nrn;
-      const bool haven = it.next(a, kb0n, nkn, nrn);
-      StageScales nxt = {};
-      if (haven) lookup(kb0n, nkn, nrn, nxt);
-      // both K blocks into 64 registers, stored by one instruction (columns
-      // of a K block past the run's end hold values no MMA reads)
-      uint32_t vals[64];
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const uint32_t s2 = cur.s2[jj], c1024 = cur.c1024[jj], c64 = cur.c64[jj];
-        const uint32_t words[8] = {raw[2 * jj].x, raw[2 * jj].y, raw[2 * jj].z, raw[2 * jj].w,
-                                   raw[2 * jj + 1].x, raw[2 * jj + 1].y, raw[2 * jj + 1].z, raw[2 * jj + 1].w};
-#pragma unroll
-        for (int w8 = 0; w8 < 8; ++w8) {
-          const uint32_t lo = words[w8], hi = lo >> 8;
-          // codes (p, p + 4) of the word for p = 0..3 as 1024 + q (p even)
-          // or 64 + q (p odd), then (1024 + q) s - 1024 s = q s, rounded once
-          vals[32 * jj + 4 * w8 + 0] = hfma2(lop3_and_or(lo, 0x000F000Fu, 0x64006400u), s2, c1024);
-          vals[32 * jj + 4 * w8 + 1] = hfma2(lop3_and_or(lo, 0x00F000F0u, 0x54005400u), s2, c64);
-          vals[32 * jj + 4 * w8 + 2] = hfma2(lop3_and_or(hi, 0x000F000Fu, 0x64006400u), s2, c1024);
-          vals[32 * jj + 4 * w8 + 3] = hfma2(lop3_and_or(hi, 0x00F000F0u, 0x54005400u), s2, c64);
-        }
+      uint32_t s16[2] = {sc0[0], sc0[1]};
+      if (pre) {
+        s16[0] = ld_shared_u16(stage + pre_off[0]);
+        s16[1] = ld_shared_u16(stage + pre_off[1]);
       }
+      // both K blocks are expanded before the slot is waited for (the MMAs
+      // of the stage TSLOTS back may still be reading it), then stored by
+      // one instruction; columns of a K block past the run's end hold values
+      // no MMA reads
+      uint32_t vals[64];
+      expand(raw[0], raw[1], s16[0], vals);
+      expand(raw[2], raw[3], s16[1], vals + 32);
+      const bool freed = mbar_wait_bounded(tfree_bar(t), tph ^ 1u, a.wait_limit_ns, abort_flag);
+      if (!freed && !*abort_flag) record_timeout(a, abort_flag, 3 * 16 + 1);
+      if (!__all_sync(0xffffffffu, freed)) break;
+      tc_fence_after();
       if (2 * h < nk) {
         const uint32_t slot = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + kASlotCol0 +
                               static_cast<uint32_t>(t * 128 + h * 64);
@@ -656,11 +602,18 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         mbar_arrive(a_full(t));
         mbar_arrive(wfree(sw));
       }
-      cur = nxt;
-      kb0 = kb0n;
-      nk = nkn;
-      have = haven;
-      ++st;
+      sc0[0] = sc1[0];
+      sc0[1] = sc1[1];
+      sc1[0] = sc2[0];
+      sc1[1] = sc2[1];
+      if (++sw == C::WST) {
+        sw = 0;
+        wph ^= 1u;
+      }
+      if (++t == C::TSLOTS) {
+        t = 0;
+        tph ^= 1u;
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -689,13 +642,12 @@ __global__ void __launch_bounds__(kThreads4, 1) int4_gemm_kernel(const __grid_co
         }
       }
     }
-    int st0 = 0;  // the CTA's stage index of the run's first stage
     for (int idx = 0; sched.next(a, g); ++idx) {
       fix.active = g.s0 == 0 && g.nkb > 0;
-      const int nstages = (g.nkb + kQuadK - 1) / kQuadK;
-      uint32_t mask = 0;
-      for (int j = 0; j < nstages && j < NI; ++j) mask |= 1u << ((st0 + j) % NI);
-      st0 += nstages;
+      // issuers with an MMA in the run: those of its first stage's MMAs
+      // (a run with a second stage has a full first one, 16 >= NI MMAs)
+      const int nmma = 4 * (g.nkb < kQuadK ? g.nkb : kQuadK);
+      const uint32_t mask = nmma >= NI ? (1u << NI) - 1u : (1u << nmma) - 1u;
       if (fix.active && idx != first_idx) {
         int32_t tp, tq, m0, m1, n0, n1;
         tile_ranges(a, g.tile, BN, tp, tq, m0, m1, n0, n1);

@@ -425,30 +425,42 @@ __device__ __noinline__ void arrive_split_tile_det(const TcArgs& a, const Group&
 // The group's accumulator as NACC partial accumulators (one per MMA issuer,
 // ST columns apart, added in index order): N columns from taddr of each.
 // Only those whose bit is set in `mask` hold this group's sums (an issuer
-// with no MMA in the group leaves its accumulator untouched); all are read.
+// with no MMA in the group leaves its accumulator untouched); all are read,
+// 32 / N of them per wait after the first (32 registers in flight).
 template <int N, int NACC, int ST>
 __device__ __forceinline__ void ld_acc(uint32_t taddr, uint32_t (&v)[N], uint32_t mask = (1u << NACC) - 1u) {
   static_assert(N == 16 || N == 32, "tcgen05.ld shapes used here");
-  if constexpr (N == 32) tc_ld_32x32b_x32(taddr, v); else tc_ld_32x32b_x16(taddr, v);
+  auto ld = [&](uint32_t addr, uint32_t (&r)[N]) {
+    if constexpr (N == 32) tc_ld_32x32b_x32(addr, r); else tc_ld_32x32b_x16(addr, r);
+  };
+  ld(taddr, v);
   if constexpr (NACC > 1) {
+    constexpr int CH = 32 / N;  // further accumulators per wait
     const bool v0 = mask & 1u;
-    uint32_t w[NACC - 1][N];
 #pragma unroll
-    for (int i = 1; i < NACC; ++i) {
-      if constexpr (N == 32) tc_ld_32x32b_x32(taddr + i * ST, w[i - 1]); else tc_ld_32x32b_x16(taddr + i * ST, w[i - 1]);
+    for (int i0 = 1; i0 < NACC; i0 += CH) {
+      uint32_t w[CH][N];
+#pragma unroll
+      for (int c = 0; c < CH; ++c)
+        if (i0 + c < NACC) ld(taddr + (i0 + c) * ST, w[c]);
+      if (i0 == 1) {
+        tc_wait_ld_regs(v);
+        if (!v0) {
+#pragma unroll
+          for (int j = 0; j < N; ++j) v[j] = 0u;  // +0.0f: adding the valid ones to it is exact
+        }
+      } else {
+        tc_wait_ld();
+      }
+#pragma unroll
+      for (int c = 0; c < CH; ++c)
+        if (i0 + c < NACC) tc_regs_after_wait(w[c]);
+#pragma unroll
+      for (int c = 0; c < CH; ++c)
+        if (i0 + c < NACC && ((mask >> (i0 + c)) & 1u))
+#pragma unroll
+          for (int j = 0; j < N; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(w[c][j]));
     }
-    tc_wait_ld_regs(v);
-#pragma unroll
-    for (int i = 1; i < NACC; ++i) tc_regs_after_wait(w[i - 1]);
-    if (!v0) {
-#pragma unroll
-      for (int j = 0; j < N; ++j) v[j] = 0u;  // +0.0f: adding the valid ones to it is exact
-    }
-#pragma unroll
-    for (int i = 1; i < NACC; ++i)
-      if ((mask >> i) & 1u)
-#pragma unroll
-        for (int j = 0; j < N; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(w[i - 1][j]));
   } else {
     tc_wait_ld_regs(v);
   }
