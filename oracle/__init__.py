@@ -24,6 +24,14 @@ What it computes, and the passage each function follows:
 * :func:`perm_forward` / :func:`perm_inverse` -- the perpendicular-dimension
   stride permutation of the hipBLASLt DTL page ("Add support for permuting
   perpDim": forward and inverse mappings).
+* :func:`attention` / :func:`attention_rows` -- ``O = softmax(Q K^T * scale) V``
+  per head, in fp64: the fused attention whose second product P.V the Triton
+  inThreadTranspose page names as a non-TN dot ("Introduction": the second
+  dotOp of Flash Attention, V contiguous along the output dimension).  The
+  pages give no formula; this is the standard definition (row-wise softmax
+  of the scaled logits, then the product with V), non-causal, with
+  ``scale = 1 / sqrt(d)`` unless given, Q, K, V and O stored [head][row][d]
+  contiguous.
 * :func:`round_to` -- round-to-nearest-even of fp64 values to fp16 / bf16.
 * :func:`reduce_rows` -- ``out[r] = sum_c x[r*ldx + c]`` in fp64, the
   reduction of the IREE page ("[LLVMGPUVectorDistribute] Add support for
@@ -229,6 +237,44 @@ def gemm_elements(rows, cols, M, N, K, A, a_layout, lda, a_dtype, B, b_layout, l
     bvals = decode(B, b_dtype)
     for i, (m, n) in enumerate(zip(rows, cols)):
         out[i] = np.dot(avals[a_index(m, k, a_layout, lda)], bvals[b_index(k, n, b_layout, ldb)])
+    return out
+
+
+# ---------------------------------------------------------------------------
+# attention (the fused second product P.V with V contiguous along d)
+# ---------------------------------------------------------------------------
+
+def _softmax_rows(s: np.ndarray) -> np.ndarray:
+    """Row-wise softmax in fp64: exp(s - row max) / row sum."""
+    e = np.exp(s - s.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def attention(Q, K, V, heads, sq, sk, d, dtype, scale=None) -> np.ndarray:
+    """fp64 O[h] = softmax(Q[h] K[h]^T * scale) V[h] for every head h, from
+    flat storages laid out [head][row][d]; returns heads x sq x d."""
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
+    q = decode(Q, dtype).reshape(heads, sq, d)
+    k = decode(K, dtype).reshape(heads, sk, d)
+    v = decode(V, dtype).reshape(heads, sk, d)
+    out = np.empty((heads, sq, d), dtype=np.float64)
+    for h in range(heads):
+        p = _softmax_rows((q[h] @ k[h].T) * scale)
+        out[h] = p @ v[h]
+    return out
+
+
+def attention_rows(heads_idx, rows, Q, K, V, heads, sq, sk, d, dtype, scale=None) -> np.ndarray:
+    """fp64 O[heads_idx[i], rows[i], :] one query row at a time, for problems
+    too large to form whole; returns len(rows) x d."""
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
+    q = decode(Q, dtype).reshape(heads, sq, d)
+    k = decode(K, dtype).reshape(heads, sk, d)
+    v = decode(V, dtype).reshape(heads, sk, d)
+    out = np.empty((len(rows), d), dtype=np.float64)
+    for i, (h, r) in enumerate(zip(heads_idx, rows)):
+        p = _softmax_rows((k[h] @ q[h, r]) * scale)
+        out[i] = p @ v[h]
     return out
 
 

@@ -491,3 +491,100 @@ def test_reduce_rows_bound_holds_for_sequential_fp32():
         bound = oracle.reduce_rows_bound(oracle.reduce_rows_abs(x, 1, n), n, 0)[0]
         assert abs(seq - exact) <= bound
         assert abs(float(np.cumsum(x[:-1], dtype=np.float32)[-1]) - exact) > bound or abs(x[-1]) < bound
+
+
+# ---------------------------------------------------------------------------
+# attention: O = softmax(Q K^T * scale) V per head (the Triton page's second
+# dot of Flash Attention, with V contiguous along d)
+# ---------------------------------------------------------------------------
+
+def _attn_inputs(heads, sq, sk, d, seed, dtype=oracle.F16):
+    case = wl.attn_case(heads, sq, sk, d, dtype)
+    return wl.make_attn_inputs(case, seed)
+
+
+def test_attention_zero_queries_give_the_mean_of_v():
+    """Q = 0: every logit is 0, the softmax is uniform, and each output row is
+    the mean of V's rows (closed form, independent of the scale)."""
+    heads, sq, sk, d = 2, 3, 7, 8
+    _, k, v = _attn_inputs(heads, sq, sk, d, seed=1)
+    q = torch.zeros(heads * sq * d, dtype=torch.float16)
+    o = oracle.attention(q, k, v, heads, sq, sk, d, oracle.F16, scale=0.37)
+    vv = oracle.decode(v, oracle.F16).reshape(heads, sk, d)
+    for h in range(heads):
+        np.testing.assert_allclose(o[h], np.repeat(vv[h].mean(axis=0)[None], sq, axis=0), rtol=0, atol=1e-15)
+
+
+def test_attention_two_key_closed_form():
+    """One query e0, keys a*e0 and 0: logits (a*scale, 0), so
+    O = p V0 + (1 - p) V1 with p = 1 / (1 + exp(-a*scale)).  A dropped or
+    misplaced scale, or a missing normalisation, fails this."""
+    d, a, scale = 4, 3.0, 0.5
+    q = torch.zeros(d, dtype=torch.float16)
+    q[0] = 1.0
+    k = torch.zeros(2 * d, dtype=torch.float16)
+    k[0] = a
+    v = torch.tensor([1.0, -2.0, 0.5, 4.0, -3.0, 0.25, 2.0, 1.5], dtype=torch.float16)
+    o = oracle.attention(q, k, v, 1, 1, 2, d, oracle.F16, scale=scale)
+    p = 1.0 / (1.0 + np.exp(-a * scale))
+    want = p * np.array([1.0, -2.0, 0.5, 4.0]) + (1 - p) * np.array([-3.0, 0.25, 2.0, 1.5])
+    np.testing.assert_allclose(o[0, 0], want, rtol=1e-14, atol=0)
+    # the default scale is 1 / sqrt(d)
+    o2 = oracle.attention(q, k, v, 1, 1, 2, d, oracle.F16)
+    p2 = 1.0 / (1.0 + np.exp(-a / 2.0))
+    np.testing.assert_allclose(o2[0, 0], p2 * np.array([1.0, -2.0, 0.5, 4.0]) + (1 - p2) * np.array(
+        [-3.0, 0.25, 2.0, 1.5]), rtol=1e-14, atol=0)
+
+
+def test_attention_rows_sum_to_one_and_key_order_does_not_matter():
+    heads, sq, sk, d = 2, 5, 9, 16
+    q, k, v = _attn_inputs(heads, sq, sk, d, seed=2)
+    ones = torch.ones(heads * sk * d, dtype=torch.float16)
+    np.testing.assert_allclose(oracle.attention(q, k, ones, heads, sq, sk, d, oracle.F16), 1.0, rtol=0, atol=1e-14)
+    perm = torch.randperm(sk, generator=torch.Generator().manual_seed(3))
+    kp = k.reshape(heads, sk, d)[:, perm].reshape(-1)
+    vp = v.reshape(heads, sk, d)[:, perm].reshape(-1)
+    np.testing.assert_allclose(oracle.attention(q, kp, vp, heads, sq, sk, d, oracle.F16),
+                               oracle.attention(q, k, v, heads, sq, sk, d, oracle.F16), rtol=1e-13, atol=1e-15)
+
+
+def test_attention_composes_from_the_gemm_oracle():
+    """The same result through the pinned GEMM oracle: S = Q K^T with K as a
+    K-contiguous B operand, then a softmax written out here, then O = P V
+    with V as an N-contiguous B operand (the non-TN second dot).  A
+    transposed V (or K) fails this."""
+    heads, sq, sk, d = 2, 6, 10, 8
+    q, k, v = _attn_inputs(heads, sq, sk, d, seed=4)
+    scale = 0.3
+    o = oracle.attention(q, k, v, heads, sq, sk, d, oracle.F16, scale=scale)
+    for h in range(heads):
+        qh = q.reshape(heads, sq * d)[h]
+        kh = k.reshape(heads, sk * d)[h]
+        vh = v.reshape(heads, sk * d)[h]
+        s = oracle.gemm(sq, sk, d, qh, oracle.K_CONTIG, d, oracle.F16, kh, oracle.K_CONTIG, d, oracle.F16) * scale
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        p = e / e.sum(axis=1, keepdims=True)
+        pv = np.zeros((sq, d))
+        vv = oracle.b_logical(vh, sk, d, oracle.MN_CONTIG, d, oracle.F16)
+        for j in range(sk):
+            pv += p[:, j:j + 1] * vv[j:j + 1, :]
+        np.testing.assert_allclose(o[h], pv, rtol=1e-13, atol=1e-15)
+
+
+def test_attention_rows_match_full():
+    heads, sq, sk, d = 3, 7, 11, 16
+    q, k, v = _attn_inputs(heads, sq, sk, d, seed=5, dtype=oracle.BF16)
+    full = oracle.attention(q, k, v, heads, sq, sk, d, oracle.BF16)
+    hs, rs = [0, 2, 1, 2], [0, 6, 3, 1]
+    np.testing.assert_allclose(oracle.attention_rows(hs, rs, q, k, v, heads, sq, sk, d, oracle.BF16),
+                               full[hs, rs], rtol=1e-13, atol=1e-15)
+
+
+def test_planted_attention_mistake_is_caught(monkeypatch):
+    """A softmax normalised over the wrong axis must fail the pins above."""
+    def wrong_axis(s):
+        e = np.exp(s - s.max())
+        return e / e.sum(axis=0, keepdims=True)
+    monkeypatch.setattr(oracle, "_softmax_rows", wrong_axis)
+    with pytest.raises(AssertionError):
+        test_attention_rows_sum_to_one_and_key_order_does_not_matter()

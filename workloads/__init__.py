@@ -237,3 +237,43 @@ def make_reduce_input(case: ReduceCase, seed: int = 0) -> torch.Tensor:
     gen = torch.Generator().manual_seed(1_000_003 * seed + 29)
     return strided_matrix(case.rows, case.cols, case.pitch(), case.dist, F32, gen)
 
+
+
+# ---------------------------------------------------------------------------
+# fused attention (the second product P.V with V contiguous along d)
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class AttnCase:
+    """O = softmax(Q K^T * scale) V per head; Q (heads x sq x d), K and V
+    (heads x sk x d), O (heads x sq x d), all [head][row][d] contiguous, with
+    values drawn from ``dist``.  scale 0: 1 / sqrt(d)."""
+    name: str
+    heads: int
+    sq: int
+    sk: int
+    d: int
+    dtype: int = BF16
+    dist: tuple = ("normal", 1.0)
+    scale: float = 0.0
+
+    def flops(self):
+        return 4.0 * self.heads * self.sq * self.sk * self.d
+
+
+def attn_case(heads, sq, sk, d, dtype=BF16, dist=("normal", 1.0), scale=0.0, extra=""):
+    nm = f"attn_{DTYPE_NAME[dtype]}_h{heads}_sq{sq}_sk{sk}_d{d}" + (f"_{extra}" if extra else "")
+    return AttnCase(nm, heads, sq, sk, d, dtype, dist, scale)
+
+
+# 32 heads (e.g. batch 4 x 8 heads) of 4096 queries and keys, head dim 128.
+ATTN_BF16 = attn_case(32, 4096, 4096, 128, BF16)
+
+
+def make_attn_inputs(case: AttnCase, seed: int = 0):
+    """(Q, K, V) as flat CPU tensors."""
+    gen = torch.Generator().manual_seed(1_000_003 * seed + 43)
+    q = _draw(case.heads * case.sq * case.d, case.dist, case.dtype, gen)
+    k = _draw(case.heads * case.sk * case.d, case.dist, case.dtype, gen)
+    v = _draw(case.heads * case.sk * case.d, case.dist, case.dtype, gen)
+    return q, k, v
