@@ -41,6 +41,7 @@ EXPORTS = (
     "gemm_splitk_auto", "gemm_perm_fwd", "gemm_perm_inv", "gemm_perm_device", "gemm_magic_divmod_host",
     "gemm_magic_divmod_device", "gemm_status_string", "gemm_int4_prepack_bytes", "gemm_int4_prepack",
     "reduce_rows_workspace_size", "reduce_rows_f32",
+    "attn_create", "attn_run", "attn_sync_status", "attn_destroy",
 )
 
 
@@ -52,6 +53,13 @@ class gemm_desc_t(ctypes.Structure):
         ("a_dtype", ctypes.c_int32), ("b_dtype", ctypes.c_int32), ("c_dtype", ctypes.c_int32),
         ("split_k", ctypes.c_int32), ("group_size", ctypes.c_int32), ("num_sms", ctypes.c_int32),
         ("flags", ctypes.c_int32),
+    ]
+
+
+class attn_desc_t(ctypes.Structure):
+    _fields_ = [
+        ("heads", ctypes.c_int32), ("seq_q", ctypes.c_int32), ("seq_k", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
     ]
 
 
@@ -96,6 +104,10 @@ def _load():
                                                       ctypes.POINTER(ctypes.c_size_t)]),
         "reduce_rows_f32": (ctypes.c_int, [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P,
                                            ctypes.c_size_t, P]),
+        "attn_create": (ctypes.c_int, [ctypes.POINTER(attn_desc_t), ctypes.POINTER(P)]),
+        "attn_run": (ctypes.c_int, [P, P, P, P, P, P]),
+        "attn_sync_status": (ctypes.c_int, [P, P]),
+        "attn_destroy": (ctypes.c_int, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -313,3 +325,48 @@ def int4_prepack(B, scales, N, K, group_size=128, ldb=0, stream=None):
     _check(gemm_int4_prepack(B.data_ptr(), ldb, scales.data_ptr(), N, K, group_size, out.data_ptr(), s),
            "gemm_int4_prepack")
     return out
+
+
+def attn_create_status(desc: attn_desc_t):
+    """attn_create returning (status, handle or None) without raising."""
+    h = ctypes.c_void_p()
+    st = _lib.attn_create(ctypes.byref(desc), ctypes.byref(h))
+    return st, h.value
+
+
+def attn_run(plan: int, Q: int, K: int, V: int, O: int, stream: int = 0) -> int:
+    """Raw entry point: integer device addresses; returns the status code."""
+    return _lib.attn_run(plan, Q or None, K or None, V or None, O or None, stream or None)
+
+
+class Attention:
+    """A fused-attention plan run on torch tensors laid out [head][row][d]
+    (marshalling only: the tensors' device addresses and the current torch
+    stream go to attn_run)."""
+
+    def __init__(self, heads, seq_q, seq_k, head_dim, dtype=GEMM_BF16, scale=0.0):
+        self.desc = attn_desc_t(heads, seq_q, seq_k, head_dim, dtype, scale)
+        st, h = attn_create_status(self.desc)
+        _check(st, "attn_create")
+        self.plan = h
+
+    def run(self, Q, K, V, O, stream=None):
+        import torch
+        s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+        _check(attn_run(self.plan, Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), s), "attn_run")
+
+    def sync_status(self, stream=None) -> int:
+        import torch
+        s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+        return _lib.attn_sync_status(self.plan, s or None)
+
+    def close(self):
+        if self.plan:
+            _lib.attn_destroy(self.plan)
+            self.plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -21,7 +21,7 @@ LIB = os.path.join(OUT_DIR, "libgemm.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["api.cu", "api_int4.cu", "gemm_tc.cu", "gemm_tc_pair.cu", "gemm_int4.cu", "gemm_int4_f8.cu",
-           "aux_kernels.cu", "noalloc.cu", "reduce.cu"]
+           "aux_kernels.cu", "noalloc.cu", "reduce.cu", "attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

@@ -1,0 +1,528 @@
+// Fused attention forward: O = softmax(Q K^T * scale) V per head, the second
+// product P.V taken with V as it is stored (contiguous along head_dim), an
+// MN-major operand of the tensor core -- the non-TN second dot of Flash
+// Attention that the Triton inThreadTranspose page names ("Introduction").
+//
+// One CTA per 128 queries of a head; the head's keys in blocks of 128.
+//   S_j = Q K_j^T       tcgen05 MMA, both operands K-major (TMA, 128-byte
+//                       swizzle), fp32 accumulator in tensor memory.
+//   P_j, m, l           online softmax by four warps, one query row per
+//                       thread: running row maximum m (of the logits times
+//                       scale * log2 e), running sum l; P_j = 2^(s - m)
+//                       rounded to the input type into tensor memory;
+//                       the O accumulator rescaled by 2^(m_old - m) when m
+//                       grew (exact when it did not).
+//   O += P_j V_j        tcgen05 MMA with A = P_j from tensor memory and
+//                       B = V_j MN-major from shared memory.
+//   O / l               the softmax warps, then 16-byte stores.
+// S is double-buffered, so S_{j+1} is computed while the softmax works on
+// S_j; P is double-buffered, so P_j is written while P_{j-1} is multiplied.
+//
+// Warp roles (256 threads): warp 0 TMA producer (Q once, a ring of K / V
+// blocks), warp 1 MMA issuer (owns the tensor memory), warps 4..7 softmax
+// and epilogue (tensor-memory lane quadrant warp % 4).  Tensor memory: S at
+// columns 0 and 128, P at 256 and 320 (bf16 / fp16 pairs), O at 384.
+// Every wait is bounded; a wait that runs out records GEMM_ERR_TIMEOUT and
+// the CTA winds down.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <new>
+
+#include "attention.h"
+#include "kernels.h"
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace lgt {
+namespace {
+
+constexpr int kAttnThreads = 256;
+constexpr int kBM = 128;  // queries per CTA
+constexpr int kBN = 128;  // keys per block
+constexpr int kSoftWarp0 = 4;
+constexpr int kAttnTimeout = 6;  // GEMM_ERR_TIMEOUT
+constexpr uint32_t kTmemO = 384;
+
+struct AttnArgs {
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D {head_dim, rows, heads}, box {64, 128, 1}
+  void* o;
+  DeviceStatus* status;
+  uint64_t wait_limit_ns;
+  int32_t heads, sq, sk;
+  float cs;  // scale * log2(e)
+  uint32_t idesc_s, idesc_pv;
+  int32_t bf16;
+};
+
+template <int D>
+struct AttnCfg {
+  static constexpr uint32_t CHUNK = 128u * 128u;      // one 64-wide box of 128 rows: 16 KiB
+  static constexpr uint32_t TILE = (D / 64) * CHUNK;  // a Q, K or V tile
+  static constexpr int NS = D == 128 ? 2 : 3;         // K / V ring
+  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t KV_OFF = TILE;
+  static constexpr uint32_t STAGE = 2 * TILE;  // K, then V
+  static constexpr uint32_t BAR_OFF = KV_OFF + NS * STAGE;
+  // q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], s_free[2], p_full[2], pv_done[2], teardown
+  static constexpr int NBARS = 1 + 3 * NS + 8 + 1;
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;
+  static constexpr uint32_t SMEM = MISC_OFF + 16 + 1024;  // slack for the 1024-byte alignment
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 2^x (the hardware approximation; 2^-inf = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two floats as one word of 16-bit values (lo in the low half), rounded to nearest.
+__device__ __forceinline__ uint32_t pack_pair(float lo, float hi, int bf16) {
+  if (bf16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void attn_timeout(const AttnArgs& a, volatile int* abort_flag, int where) {
+  *abort_flag = 1;
+  if (atomicCAS(&a.status->code, 0, kAttnTimeout) == 0) a.status->where = where;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
+  using C = AttnCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_base);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int q0 = blockIdx.x * kBM;
+  const int nb = (a.sk + kBN - 1) / kBN;
+
+  const uint32_t bar0 = base + C::BAR_OFF;
+  const uint32_t q_full = bar0;
+  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + C::NS + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + 2 * C::NS + s); };
+  auto s_full = [&](int b) { return bar0 + 8u * (1 + 3 * C::NS + b); };
+  auto s_free = [&](int b) { return bar0 + 8u * (3 + 3 * C::NS + b); };
+  auto p_full = [&](int b) { return bar0 + 8u * (5 + 3 * C::NS + b); };
+  auto pv_done = [&](int b) { return bar0 + 8u * (7 + 3 * C::NS + b); };
+  const uint32_t teardown = bar0 + 8u * (9 + 3 * C::NS);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_free(b), 4);  // the four softmax warps
+      mbar_init(p_full(b), 4);
+      mbar_init(pv_done(b), 1);
+    }
+    mbar_init(teardown, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&a.tm_q);
+    tma_prefetch_desc(&a.tm_k);
+    tma_prefetch_desc(&a.tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // Q, K and V may come from the previous kernel, which may also read O
+  pdl_wait();
+
+  bool q_issued = false;
+  int kv_issued = 0;  // producer lane: K / V blocks whose loads were issued
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, C::TILE);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) tma_load_3d(base + C::Q_OFF + c * C::CHUNK, &a.tm_q, q_full, c * 64, q0, h);
+      q_issued = true;
+      for (int j = 0; j < nb; ++j) {
+        const int s = j % C::NS;
+        if (j >= C::NS && !mbar_wait_bounded(kv_empty(s), ((j / C::NS) - 1) & 1, a.wait_limit_ns, abort_flag)) {
+          if (!*abort_flag) attn_timeout(a, abort_flag, 0);
+          break;
+        }
+        const uint32_t kd = base + C::KV_OFF + s * C::STAGE, vd = kd + C::TILE;
+        mbar_arrive_expect_tx(k_full(s), C::TILE);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) tma_load_3d(kd + c * C::CHUNK, &a.tm_k, k_full(s), c * 64, j * kBN, h);
+        mbar_arrive_expect_tx(v_full(s), C::TILE);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) tma_load_3d(vd + c * C::CHUNK, &a.tm_v, v_full(s), c * 64, j * kBN, h);
+        ++kv_issued;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait_bounded(q_full, 0, a.wait_limit_ns, abort_flag);
+      // S_j = Q K_j^T into S buffer j % 2 (once the softmax has read S_{j-2}).
+      // K-major tiles: 128-byte rows of 64 elements, 8-row groups 1 KiB
+      // apart; 16-deep step k is 32 bytes into 64-wide chunk k / 4.
+      auto issue_s = [&](int j) -> bool {
+        const int b = j & 1, s = j % C::NS;
+        if (j >= 2 && !mbar_wait_bounded(s_free(b), ((j >> 1) - 1) & 1, a.wait_limit_ns, abort_flag)) return false;
+        if (!mbar_wait_bounded(k_full(s), (j / C::NS) & 1, a.wait_limit_ns, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t kb = base + C::KV_OFF + s * C::STAGE;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = static_cast<uint32_t>(k >> 2) * C::CHUNK + static_cast<uint32_t>(k & 3) * 32u;
+          tc_mma_f16_ss(tmem + static_cast<uint32_t>(b * 128), sw128_desc(base + C::Q_OFF + off, 16u, 1024u),
+                        sw128_desc(kb + off, 16u, 1024u), a.idesc_s, k > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full(b));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < nb; ++j) {
+        if (j + 1 < nb && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        const int b = j & 1, s = j % C::NS;
+        if (!mbar_wait_bounded(p_full(b), (j >> 1) & 1, a.wait_limit_ns, abort_flag) ||
+            !mbar_wait_bounded(v_full(s), (j / C::NS) & 1, a.wait_limit_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // O += P_j V_j: A = P_j (8 columns of pairs per 16 keys), B = V_j
+        // MN-major: 128-byte rows along head_dim, one per key, 8-key groups
+        // 1 KiB apart, 64-wide head_dim chunks 16 KiB apart; 16 keys = 2 KiB.
+        const uint32_t vb = base + C::KV_OFF + s * C::STAGE + C::TILE;
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          mma_ts(tmem + kTmemO, tmem + 256u + static_cast<uint32_t>(b * 64 + k * 8),
+                 sw128_desc(vb + static_cast<uint32_t>(k) * 2048u, C::CHUNK, 1024u), a.idesc_pv,
+                 (j | k) != 0 ? 1u : 0u);
+        tc_commit(pv_done(b));
+        tc_commit(kv_empty(s));
+      }
+      if (!ok && !*abort_flag) attn_timeout(a, abort_flag, 1);
+      tc_commit(teardown);  // every MMA of this thread completed before the tensor memory is freed
+    }
+  } else if (warp >= kSoftWarp0) {
+    // ------------------------------------------------------------ softmax
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);  // this warp's lane quadrant
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      const int b = j & 1;
+      bool got = mbar_wait_bounded(s_full(b), (j >> 1) & 1, a.wait_limit_ns, abort_flag);
+      // the warp leaves together (tcgen05.ld / st need every lane)
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int valid = min(kBN, a.sk - j * kBN);  // keys of this block inside the head
+      const uint32_t sb = tl + static_cast<uint32_t>(b * 128);
+      // pass 1: the block's row maximum
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tc_ld_32x32b_x32(sb + static_cast<uint32_t>(c * 32), v);
+        tc_wait_ld_regs(v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(v[i]));
+      }
+      const float m_new = fmaxf(m, mx * a.cs);
+      const float alpha = ex2(m - m_new);  // 0 on the first block
+      // P buffer b was read by PV_{j-2}
+      if (j >= 2) got = mbar_wait_bounded(pv_done(b), ((j >> 1) - 1) & 1, a.wait_limit_ns, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // pass 2: P = 2^(s cs - m_new), 64 keys (32 pair columns) at a time
+      float sum = 0.0f;
+#pragma unroll 1
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t v0[32], v1[32], pk[32];
+        tc_ld_32x32b_x32(sb + static_cast<uint32_t>(c2 * 64), v0);
+        tc_ld_32x32b_x32(sb + static_cast<uint32_t>(c2 * 64 + 32), v1);
+        tc_wait_ld_regs(v0);
+        tc_regs_after_wait(v1);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int k = c2 * 64 + 2 * i;  // keys k, k + 1 of the block
+          const float s0 = __uint_as_float(i < 16 ? v0[2 * i] : v1[2 * i - 32]);
+          const float s1 = __uint_as_float(i < 16 ? v0[2 * i + 1] : v1[2 * i - 31]);
+          const float e0 = k < valid ? ex2(fmaf(s0, a.cs, -m_new)) : 0.0f;
+          const float e1 = k + 1 < valid ? ex2(fmaf(s1, a.cs, -m_new)) : 0.0f;
+          sum += e0 + e1;
+          pk[i] = pack_pair(e0, e1, a.bf16);
+        }
+        tc_st_32x32b_x32_wait(tl + 256u + static_cast<uint32_t>(b * 64 + c2 * 32), pk);
+      }
+      // S buffer b is read: the MMA may compute S_{j+2} into it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(b));
+      l = l * alpha + sum;
+      m = m_new;
+      // O holds the sum up to block j - 1: rescale it once PV_{j-1} is done
+      if (j >= 1) {
+        got = mbar_wait_bounded(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, a.wait_limit_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha < 1.0f)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tc_ld_32x32b_x32(tl + kTmemO + static_cast<uint32_t>(c * 32), v);
+            tc_wait_ld_regs(v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tc_st_32x32b_x32_wait(tl + kTmemO + static_cast<uint32_t>(c * 32), v);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full(b));
+    }
+    if (ok) {
+      // the last PV done: O / l, rounded once, 16-byte stores of this row
+      const bool got = mbar_wait_bounded(pv_done((nb - 1) & 1), ((nb - 1) >> 1) & 1, a.wait_limit_ns, abort_flag);
+      if (__all_sync(0xffffffffu, got)) {
+        tc_fence_after();
+        const float inv = 1.0f / l;
+        const bool in = q0 + row < a.sq;
+        uint16_t* orow = static_cast<uint16_t*>(a.o) + (static_cast<int64_t>(h) * a.sq + q0 + row) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tc_ld_32x32b_x32(tl + kTmemO + static_cast<uint32_t>(c * 32), v);
+          tc_wait_ld_regs(v);
+          if (in) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_pair(__uint_as_float(v[8 * q + 2 * e]) * inv, __uint_as_float(v[8 * q + 2 * e + 1]) * inv,
+                                 a.bf16);
+              st_global_v4(orow + c * 32 + 8 * q, w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      } else if (!*abort_flag) {
+        attn_timeout(a, abort_flag, 2);
+      }
+    } else if (!*abort_flag) {
+      attn_timeout(a, abort_flag, 2);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // let the loads still in flight land before the CTA exits
+    volatile int no_abort = 0;
+    if (q_issued) mbar_wait_bounded(q_full, 0, a.wait_limit_ns, &no_abort);
+    for (int j = kv_issued > C::NS ? kv_issued - C::NS : 0; j < kv_issued; ++j) {
+      mbar_wait_bounded(k_full(j % C::NS), (j / C::NS) & 1, a.wait_limit_ns, &no_abort);
+      mbar_wait_bounded(v_full(j % C::NS), (j / C::NS) & 1, a.wait_limit_ns, &no_abort);
+    }
+  }
+  if (warp == 1 && lane == 0) {
+    volatile int no_abort = 0;
+    mbar_wait_bounded(teardown, 0, a.wait_limit_ns, &no_abort);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <int D>
+cudaError_t launch_attn(const AttnArgs& args, cudaStream_t stream) {
+  using C = AttnCfg<D>;
+  static const cudaError_t set =
+      cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
+  if (set != cudaSuccess) return set;
+  const dim3 grid(static_cast<unsigned>((args.sq + kBM - 1) / kBM), static_cast<unsigned>(args.heads));
+  return launch_pdl(attn_fwd_kernel<D>, grid, dim3(kAttnThreads), C::SMEM, stream, args);
+}
+
+// 3-D map over heads x rows x head_dim (16-bit, [head][row][d] contiguous):
+// box {64, 128, 1}, 128-byte swizzle, zero fill past the rows of a head.
+bool encode_attn(CUtensorMap* map, const void* ptr, int dtype, int64_t heads, int64_t rows, int64_t d) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  const CUtensorMapDataType dt =
+      dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows * d) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBN), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint64_t attn_wait_limit() {
+  const char* s = std::getenv("LGT_GEMM_WAIT_LIMIT_MS");
+  if (s && *s) {
+    const double ms = std::atof(s);
+    if (ms > 0) return static_cast<uint64_t>(ms * 1e6);
+  }
+  return 2000ull * 1000ull * 1000ull;  // 2 s
+}
+
+}  // namespace
+}  // namespace lgt
+
+struct attn_plan {
+  attn_desc_t d;
+  int device = -1;
+  lgt::DeviceStatus* d_status = nullptr;
+  uint64_t wait_limit_ns = 0;
+  // arguments of the last run: the maps are re-encoded only when a pointer changes
+  lgt::AttnArgs args;
+  const void* q = nullptr;
+  const void* k = nullptr;
+  const void* v = nullptr;
+  bool have = false;
+};
+
+extern "C" {
+
+gemm_status_t attn_create(const attn_desc_t* desc, attn_plan_t** plan) {
+  if (!desc || !plan) return GEMM_ERR_INVALID_ARG;
+  *plan = nullptr;
+  const attn_desc_t& d = *desc;
+  if (d.heads < 1 || d.heads > 65535 || d.seq_q < 1 || d.seq_k < 1 || (d.head_dim != 64 && d.head_dim != 128) ||
+      (d.dtype != GEMM_F16 && d.dtype != GEMM_BF16) || !(d.scale >= 0.0f) || std::isinf(d.scale))
+    return GEMM_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  attn_plan* p = new (std::nothrow) attn_plan();
+  if (!p) return GEMM_ERR_CUDA;
+  p->d = d;
+  p->device = dev;
+  p->wait_limit_ns = lgt::attn_wait_limit();
+  if (cudaMalloc(&p->d_status, 16) != cudaSuccess || cudaMemset(p->d_status, 0, 16) != cudaSuccess) {
+    cudaGetLastError();
+    if (p->d_status) cudaFree(p->d_status);
+    delete p;
+    return GEMM_ERR_CUDA;
+  }
+  *plan = p;
+  return GEMM_OK;
+}
+
+gemm_status_t attn_run(attn_plan_t* plan, const void* Q, const void* K, const void* V, void* O, void* stream) {
+  if (!plan || !Q || !K || !V || !O) return GEMM_ERR_INVALID_ARG;
+  for (const void* ptr : {Q, K, V, static_cast<const void*>(O)})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return GEMM_ERR_ALIGNMENT;
+  const attn_desc_t& d = plan->d;
+  lgt::AttnArgs& a = plan->args;
+  if (!plan->have || plan->q != Q || plan->k != K || plan->v != V) {
+    if (!lgt::encode_attn(&a.tm_q, Q, d.dtype, d.heads, d.seq_q, d.head_dim) ||
+        !lgt::encode_attn(&a.tm_k, K, d.dtype, d.heads, d.seq_k, d.head_dim) ||
+        !lgt::encode_attn(&a.tm_v, V, d.dtype, d.heads, d.seq_k, d.head_dim)) {
+      plan->have = false;
+      return GEMM_ERR_CUDA;
+    }
+    plan->q = Q;
+    plan->k = K;
+    plan->v = V;
+    plan->have = true;
+    const float scale = d.scale > 0.0f ? d.scale : 1.0f / std::sqrt(static_cast<float>(d.head_dim));
+    a.cs = scale * 1.4426950408889634f;  // log2(e)
+    a.heads = d.heads;
+    a.sq = d.seq_q;
+    a.sk = d.seq_k;
+    a.bf16 = d.dtype == GEMM_BF16;
+    a.idesc_s = lgt::idesc_f16(a.bf16, 0u, 0u, 128u, 128u);
+    a.idesc_pv = lgt::idesc_f16(a.bf16, 0u, 1u, 128u, static_cast<uint32_t>(d.head_dim));
+    a.status = plan->d_status;
+    a.wait_limit_ns = plan->wait_limit_ns;
+  }
+  a.o = O;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = d.head_dim == 128 ? lgt::launch_attn<128>(a, s) : lgt::launch_attn<64>(a, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  return GEMM_OK;
+}
+
+gemm_status_t attn_sync_status(attn_plan_t* plan, void* stream) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  if (plan->device < 0 || !plan->d_status) return GEMM_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GEMM_ERR_CUDA;
+  lgt::DeviceStatus st;
+  if (cudaMemcpy(&st, plan->d_status, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (st.code != 0) {
+    if (cudaMemset(plan->d_status, 0, sizeof(st)) != cudaSuccess) return GEMM_ERR_CUDA;
+    return static_cast<gemm_status_t>(st.code);
+  }
+  return GEMM_OK;
+}
+
+gemm_status_t attn_destroy(attn_plan_t* plan) {
+  if (!plan) return GEMM_OK;
+  if (plan->d_status) cudaFree(plan->d_status);
+  delete plan;
+  return GEMM_OK;
+}
+
+}  // extern "C"

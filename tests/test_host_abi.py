@@ -28,7 +28,7 @@ def _declared_functions():
             continue
         text = open(os.path.join(ROOT, "include", fn)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*((?:gemm|reduce)_[a-z0-9_]+)\s*\(", text, re.M):
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*((?:gemm|reduce|attn)_[a-z0-9_]+)\s*\(", text, re.M):
             names.add(m.group(1))
     return names
 
@@ -358,3 +358,15 @@ def test_planner_realign_or_repack(lib, monkeypatch):
     assert i.realign == 1 and i.repack_a == 0
     i, ws = info(300, 400, 4096, 301, split=4)  # split-K through the workspace: pre-pass
     assert i.realign == 0 and i.repack_a == 1 and ws >= 4096 * 304 * 2
+
+
+def test_attention_descriptor_checks(lib):
+    """attn_create refuses shapes and types outside the header's contract
+    before it touches a device."""
+    bad = [dict(heads=0), dict(heads=70000), dict(seq_q=0), dict(seq_k=0), dict(head_dim=96), dict(head_dim=256),
+           dict(dtype=lib.GEMM_F32), dict(scale=-1.0), dict(scale=float("inf")), dict(scale=float("nan"))]
+    for kw in bad:
+        args = dict(heads=2, seq_q=128, seq_k=128, head_dim=64, dtype=lib.GEMM_BF16, scale=0.0)
+        args.update(kw)
+        st, h = lib.attn_create_status(lib.attn_desc_t(**args))
+        assert st == lib.GEMM_ERR_INVALID_ARG and h is None, kw
