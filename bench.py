@@ -435,6 +435,7 @@ def gpu_arm(args, headline):
 
     for rc in (wl.REDUCE_VEC, wl.REDUCE_ROWS, wl.REDUCE_LARGE):
         configs[rc.name] = reduce_config(rc, args, peaks)
+    configs[wl.ATTN_BF16.name] = attn_config(wl.ATTN_BF16, args, peaks, cpu=rank == 0 and world == 1)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -505,11 +506,81 @@ def reduce_config(rc, args, peaks):
             "l2": "input larger than L2" if nbytes > DeviceCase.L2_BYTES else "input resident in L2 (latency case)"}
 
 
+class DeviceAttn:
+    """The fused-attention workload resident on the device, with enough
+    copies of Q, K, V and O that consecutive runs never find them in L2."""
+
+    def __init__(self, case, seed=0):
+        import torch
+        import workloads as wl
+        import layout_general_tensor_gb300 as lgt
+        self.case = case
+        q, k, v = wl.make_attn_inputs(case, seed)
+        self.host = (q, k, v)
+        set_bytes = (q.numel() + k.numel() + v.numel() + q.numel()) * 2
+        self.n_sets = max(1, -(-int(2.5 * DeviceCase.L2_BYTES) // set_bytes))
+        dt = wl.TORCH_DTYPE[case.dtype]
+        self.sets = [(q.cuda(), k.cuda(), v.cuda(), torch.empty(q.numel(), dtype=dt, device="cuda"))
+                     for _ in range(self.n_sets)]
+        self.a = lgt.Attention(case.heads, case.sq, case.sk, case.d, case.dtype, case.scale)
+        self.i = 0
+
+    def run(self):
+        Q, K, V, O = self.sets[self.i % self.n_sets]
+        self.i += 1
+        self.a.run(Q, K, V, O)
+
+
+def attn_cpu_baseline(case, host, budget_s):
+    """The oracle on query rows of the workload (one row at a time, all its
+    keys) for about `budget_s`, in TFLOP/s."""
+    import oracle
+    q, k, v = host
+    rows, done, reps = 16, 0, 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.attention_rows([reps % case.heads] * rows, list(range(rows)), q, k, v, case.heads, case.sq, case.sk,
+                              case.d, case.dtype)
+        done += rows * 4.0 * case.sk * case.d
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    return {"value": done / el / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{reps} x oracle.attention_rows on {rows} query rows of one head ({case.sk} keys, d "
+                      f"{case.d}), {el:.1f} s"}
+
+
+def attn_config(case, args, peaks, cpu=True):
+    d = DeviceAttn(case)
+    n = max(args.steps, 10)
+    ms = time_batched(d.run, n, max(args.warmup, 3)) / n
+    st = d.a.sync_status()
+    assert st == 0, f"device status {st} on {case.name}"
+    tf = case.flops() / (ms * 1e-3) / 1e12
+    out = {"ms_per_step": ms, "tflops": tf, "pct_bf16_peak": 100 * tf / peaks["bf16_tflops"], "flop": case.flops(),
+           "kernel": f"attn_fwd_kernel<{case.d}>", "launches_per_run": 1, "operand_sets": d.n_sets,
+           "l2": f"inputs larger than L2: {d.n_sets} sets of Q, K, V, O rotated"}
+    d.a.close()
+    if cpu and not args.no_cpu_baseline:
+        out["cpu_baseline"] = attn_cpu_baseline(case, d.host, args.cpu_seconds / 3)
+    return out
+
+
 def profile_case(args):
     import torch
     import workloads as wl
     import __graft_entry__
     __graft_entry__.build()
+    if args.profile_case == wl.ATTN_BF16.name:
+        d = DeviceAttn(wl.ATTN_BF16)
+        d.n_sets = 1
+        for _ in range(args.steps):
+            d.run()
+        torch.cuda.synchronize()
+        st = d.a.sync_status()
+        print(json.dumps({"profile_case": args.profile_case, "runs": args.steps, "status": st}))
+        return 0 if st == 0 else 1
     reduces = {c.name: c for c in (wl.REDUCE_VEC, wl.REDUCE_ROWS, wl.REDUCE_LARGE)}
     if args.profile_case in reduces:
         d = DeviceReduce(reduces[args.profile_case])

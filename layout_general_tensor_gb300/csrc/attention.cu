@@ -7,11 +7,14 @@
 //   S_j = Q K_j^T       tcgen05 MMA, both operands K-major (TMA, 128-byte
 //                       swizzle), fp32 accumulator in tensor memory.
 //   P_j, m, l           online softmax by four warps, one query row per
-//                       thread: running row maximum m (of the logits times
-//                       scale * log2 e), running sum l; P_j = 2^(s - m)
-//                       rounded to the input type into tensor memory;
-//                       the O accumulator rescaled by 2^(m_old - m) when m
-//                       grew (exact when it did not).
+//                       thread, the row's logits held in registers: a
+//                       reference maximum m (of the logits times
+//                       scale * log2 e) moved only when a block's maximum
+//                       exceeds it by more than 8, running sum l;
+//                       P_j = 2^(s - m) (at most 2^8)
+//                       rounded to the input type into tensor memory; the
+//                       O accumulator rescaled by 2^(m_old - m) in the
+//                       blocks where m moved.
 //   O += P_j V_j        tcgen05 MMA with A = P_j from tensor memory and
 //                       B = V_j MN-major from shared memory.
 //   O / l               the softmax warps, then 16-byte stores.
@@ -249,6 +252,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);  // this warp's lane quadrant
+    // m: the reference maximum of this row's scaled logits (log2 units) that
+    // P is taken against.  It moves only when a block's maximum exceeds it
+    // by more than kLazy: P then stays at most 2^kLazy (safe in 16-bit and
+    // in the fp32 sums), and O is rescaled -- after waiting for the P.V
+    // before -- only in the blocks where some row of the warp moved.  The
+    // result O / l does not depend on the reference.
+    constexpr float kLazy = 8.0f;
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
@@ -262,19 +272,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       tc_fence_after();
       const int valid = min(kBN, a.sk - j * kBN);  // keys of this block inside the head
       const uint32_t sb = tl + static_cast<uint32_t>(b * 128);
-      // pass 1: the block's row maximum
+      // the row's 128 logits in registers, then the S buffer is free for S_{j+2}
+      uint32_t sv[128];
+      tc_ld_32x32b_x32(sb, *reinterpret_cast<uint32_t(*)[32]>(sv));
+      tc_ld_32x32b_x32(sb + 32u, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tc_ld_32x32b_x32(sb + 64u, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
+      tc_ld_32x32b_x32(sb + 96u, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
+      tc_wait_ld_regs(sv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(b));
       float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tc_ld_32x32b_x32(sb + static_cast<uint32_t>(c * 32), v);
-        tc_wait_ld_regs(v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c * 32 + i < valid) mx = fmaxf(mx, __uint_as_float(v[i]));
+      for (int i = 0; i < 128; ++i)
+        if (i < valid) mx = fmaxf(mx, __uint_as_float(sv[i]));
+      mx *= a.cs;
+      float alpha = 1.0f;
+      if (mx > m + kLazy) {  // always on the first block (m = -inf)
+        alpha = ex2(m - mx);  // 0 on the first block
+        m = mx;
       }
-      const float m_new = fmaxf(m, mx * a.cs);
-      const float alpha = ex2(m - m_new);  // 0 on the first block
       // P buffer b was read by PV_{j-2}
       if (j >= 2) got = mbar_wait_bounded(pv_done(b), ((j >> 1) - 1) & 1, a.wait_limit_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
@@ -282,51 +299,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         break;
       }
       tc_fence_after();
-      // pass 2: P = 2^(s cs - m_new), 64 keys (32 pair columns) at a time
+      // P = 2^(s cs - m) as pairs, 64 keys (32 pair columns) per store
       float sum = 0.0f;
-#pragma unroll 1
+#pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t v0[32], v1[32], pk[32];
-        tc_ld_32x32b_x32(sb + static_cast<uint32_t>(c2 * 64), v0);
-        tc_ld_32x32b_x32(sb + static_cast<uint32_t>(c2 * 64 + 32), v1);
-        tc_wait_ld_regs(v0);
-        tc_regs_after_wait(v1);
+        uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int k = c2 * 64 + 2 * i;  // keys k, k + 1 of the block
-          const float s0 = __uint_as_float(i < 16 ? v0[2 * i] : v1[2 * i - 32]);
-          const float s1 = __uint_as_float(i < 16 ? v0[2 * i + 1] : v1[2 * i - 31]);
-          const float e0 = k < valid ? ex2(fmaf(s0, a.cs, -m_new)) : 0.0f;
-          const float e1 = k + 1 < valid ? ex2(fmaf(s1, a.cs, -m_new)) : 0.0f;
+          const float e0 = k < valid ? ex2(fmaf(__uint_as_float(sv[k]), a.cs, -m)) : 0.0f;
+          const float e1 = k + 1 < valid ? ex2(fmaf(__uint_as_float(sv[k + 1]), a.cs, -m)) : 0.0f;
           sum += e0 + e1;
           pk[i] = pack_pair(e0, e1, a.bf16);
         }
         tc_st_32x32b_x32_wait(tl + 256u + static_cast<uint32_t>(b * 64 + c2 * 32), pk);
       }
-      // S buffer b is read: the MMA may compute S_{j+2} into it
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(b));
       l = l * alpha + sum;
-      m = m_new;
-      // O holds the sum up to block j - 1: rescale it once PV_{j-1} is done
-      if (j >= 1) {
+      // O holds the sum up to block j - 1: rescale it (once PV_{j-1} is done)
+      // where a row's reference moved
+      if (j >= 1 && __any_sync(0xffffffffu, alpha < 1.0f)) {
         got = mbar_wait_bounded(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, a.wait_limit_ns, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha < 1.0f)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tc_ld_32x32b_x32(tl + kTmemO + static_cast<uint32_t>(c * 32), v);
-            tc_wait_ld_regs(v);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tc_ld_32x32b_x32(tl + kTmemO + static_cast<uint32_t>(c * 32), v);
+          tc_wait_ld_regs(v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tc_st_32x32b_x32_wait(tl + kTmemO + static_cast<uint32_t>(c * 32), v);
-          }
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tc_st_32x32b_x32_wait(tl + kTmemO + static_cast<uint32_t>(c * 32), v);
         }
       }
       tc_fence_before();
