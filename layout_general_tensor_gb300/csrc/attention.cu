@@ -282,10 +282,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free(b));
-      float mx = -INFINITY;
+      // (eight independent partial maxima and sums: short dependency chains)
+      float mp[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mp[u] = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 128; ++i)
-        if (i < valid) mx = fmaxf(mx, __uint_as_float(sv[i]));
+        if (i < valid) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(sv[i]));
+      float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       mx *= a.cs;
       float alpha = 1.0f;
       if (mx > m + kLazy) {  // always on the first block (m = -inf)
@@ -300,7 +304,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       }
       tc_fence_after();
       // P = 2^(s cs - m) as pairs, 64 keys (32 pair columns) per store
-      float sum = 0.0f;
+      float sp[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sp[u] = 0.0f;
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t pk[32];
@@ -309,11 +315,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
           const int k = c2 * 64 + 2 * i;  // keys k, k + 1 of the block
           const float e0 = k < valid ? ex2(fmaf(__uint_as_float(sv[k]), a.cs, -m)) : 0.0f;
           const float e1 = k + 1 < valid ? ex2(fmaf(__uint_as_float(sv[k + 1]), a.cs, -m)) : 0.0f;
-          sum += e0 + e1;
+          sp[i & 7] += e0 + e1;
           pk[i] = pack_pair(e0, e1, a.bf16);
         }
         tc_st_32x32b_x32_wait(tl + 256u + static_cast<uint32_t>(b * 64 + c2 * 32), pk);
       }
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l = l * alpha + sum;
       // O holds the sum up to block j - 1: rescale it (once PV_{j-1} is done)
       // where a row's reference moved
