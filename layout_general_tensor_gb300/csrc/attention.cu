@@ -100,13 +100,15 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Two floats as one word of 16-bit values (lo in the low half), rounded to nearest.
-__device__ __forceinline__ uint32_t pack_pair(float lo, float hi, int bf16) {
-  if (bf16) {
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack_pair(float lo, float hi) {
+  if constexpr (BF16) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
   }
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
 }
 
 __device__ __forceinline__ void attn_timeout(const AttnArgs& a, volatile int* abort_flag, int where) {
@@ -114,7 +116,7 @@ __device__ __forceinline__ void attn_timeout(const AttnArgs& a, volatile int* ab
   if (atomicCAS(&a.status->code, 0, kAttnTimeout) == 0) a.status->where = where;
 }
 
-template <int D>
+template <int D, bool BF16>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
   using C = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -259,6 +261,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     // before -- only in the blocks where some row of the warp moved.  The
     // result O / l does not depend on the reference.
     constexpr float kLazy = 8.0f;
+    const float cs = a.cs;
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
@@ -283,14 +286,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free(b));
       // (eight independent partial maxima and sums: short dependency chains)
+      // (keys past the head's end, in its last block only, count as -inf)
+      if (valid < kBN) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= valid) sv[i] = __float_as_uint(-INFINITY);
+      }
       float mp[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mp[u] = -INFINITY;
+      for (int u = 0; u < 8; ++u) mp[u] = __uint_as_float(sv[u]);
 #pragma unroll
-      for (int i = 0; i < 128; ++i)
-        if (i < valid) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(sv[i]));
+      for (int i = 8; i < 128; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(sv[i]));
       float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-      mx *= a.cs;
+      mx *= cs;
       float alpha = 1.0f;
       if (mx > m + kLazy) {  // always on the first block (m = -inf)
         alpha = ex2(m - mx);  // 0 on the first block
@@ -312,11 +320,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int k = c2 * 64 + 2 * i;  // keys k, k + 1 of the block
-          const float e0 = k < valid ? ex2(fmaf(__uint_as_float(sv[k]), a.cs, -m)) : 0.0f;
-          const float e1 = k + 1 < valid ? ex2(fmaf(__uint_as_float(sv[k + 1]), a.cs, -m)) : 0.0f;
+          const int k = c2 * 64 + 2 * i;  // keys k, k + 1 of the block (-inf past the end: 2^-inf = 0)
+          const float e0 = ex2(fmaf(__uint_as_float(sv[k]), cs, -m));
+          const float e1 = ex2(fmaf(__uint_as_float(sv[k + 1]), cs, -m));
           sp[i & 7] += e0 + e1;
-          pk[i] = pack_pair(e0, e1, a.bf16);
+          pk[i] = pack_pair<BF16>(e0, e1);
         }
         tc_st_32x32b_x32_wait(tl + 256u + static_cast<uint32_t>(b * 64 + c2 * 32), pk);
       }
@@ -364,8 +372,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
               uint32_t w[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                w[e] = pack_pair(__uint_as_float(v[8 * q + 2 * e]) * inv, __uint_as_float(v[8 * q + 2 * e + 1]) * inv,
-                                 a.bf16);
+                w[e] = pack_pair<BF16>(__uint_as_float(v[8 * q + 2 * e]) * inv,
+                                       __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
               st_global_v4(orow + c * 32 + 8 * q, w[0], w[1], w[2], w[3]);
             }
           }
@@ -399,14 +407,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int D>
+template <int D, bool BF16>
 cudaError_t launch_attn(const AttnArgs& args, cudaStream_t stream) {
   using C = AttnCfg<D>;
-  static const cudaError_t set =
-      cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
+  static const cudaError_t set = cudaFuncSetAttribute(attn_fwd_kernel<D, BF16>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                      static_cast<int>(C::SMEM));
   if (set != cudaSuccess) return set;
   const dim3 grid(static_cast<unsigned>((args.sq + kBM - 1) / kBM), static_cast<unsigned>(args.heads));
-  return launch_pdl(attn_fwd_kernel<D>, grid, dim3(kAttnThreads), C::SMEM, stream, args);
+  return launch_pdl(attn_fwd_kernel<D, BF16>, grid, dim3(kAttnThreads), C::SMEM, stream, args);
 }
 
 // 3-D map over heads x rows x head_dim (16-bit, [head][row][d] contiguous):
@@ -509,7 +518,8 @@ gemm_status_t attn_run(attn_plan_t* plan, const void* Q, const void* K, const vo
   }
   a.o = O;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = d.head_dim == 128 ? lgt::launch_attn<128>(a, s) : lgt::launch_attn<64>(a, s);
+  const cudaError_t e = d.head_dim == 128 ? (a.bf16 ? lgt::launch_attn<128, true>(a, s) : lgt::launch_attn<128, false>(a, s))
+                                          : (a.bf16 ? lgt::launch_attn<64, true>(a, s) : lgt::launch_attn<64, false>(a, s));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
