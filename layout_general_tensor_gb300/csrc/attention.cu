@@ -21,9 +21,10 @@
 // S is double-buffered, so S_{j+1} is computed while the softmax works on
 // S_j; P is double-buffered, so P_j is written while P_{j-1} is multiplied.
 //
-// Warp roles (256 threads): warp 0 TMA producer (Q once, a ring of K / V
-// blocks), warp 1 MMA issuer (owns the tensor memory), warps 4..7 softmax
-// and epilogue (tensor-memory lane quadrant warp % 4).  Tensor memory: S at
+// Warp roles (384 threads): warp 0 TMA producer (Q once, a ring of K / V
+// blocks), warp 1 MMA issuer (owns the tensor memory), warps 4..11 softmax
+// and epilogue, two per tensor-memory lane quadrant (warp % 4), each taking
+// half of a block's keys and half of O's columns.  Tensor memory: S at
 // columns 0 and 128, P at 256 and 320 (bf16 / fp16 pairs), O at 384.
 // Every wait is bounded; a wait that runs out records GEMM_ERR_TIMEOUT and
 // the CTA winds down.
@@ -46,10 +47,10 @@
 namespace lgt {
 namespace {
 
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 384;
 constexpr int kBM = 128;  // queries per CTA
 constexpr int kBN = 128;  // keys per block
-constexpr int kSoftWarp0 = 4;
+constexpr int kSoftWarp0 = 4;   // softmax warps 4..11: two per lane quadrant
 constexpr int kAttnTimeout = 6;  // GEMM_ERR_TIMEOUT
 constexpr uint32_t kTmemO = 384;
 
@@ -75,7 +76,10 @@ struct AttnCfg {
   static constexpr uint32_t BAR_OFF = KV_OFF + NS * STAGE;
   // q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], s_free[2], p_full[2], pv_done[2], teardown
   static constexpr int NBARS = 1 + 3 * NS + 8 + 1;
-  static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;
+  // the two softmax halves of a row exchange their block maxima (by block
+  // parity) and, at the end, their partial sums: fp32 [2][2][128]
+  static constexpr uint32_t XCH_OFF = BAR_OFF + ((NBARS * 8 + 15) & ~15);
+  static constexpr uint32_t MISC_OFF = XCH_OFF + 2 * 2 * 128 * 4;
   static constexpr uint32_t SMEM = MISC_OFF + 16 + 1024;  // slack for the 1024-byte alignment
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -109,6 +113,12 @@ __device__ __forceinline__ uint32_t pack_pair(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
   }
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void attn_timeout(const AttnArgs& a, volatile int* abort_flag, int where) {
@@ -150,8 +160,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
-      mbar_init(s_free(b), 4);  // the four softmax warps
-      mbar_init(p_full(b), 4);
+      mbar_init(s_free(b), 8);  // the eight softmax warps
+      mbar_init(p_full(b), 8);
       mbar_init(pv_done(b), 1);
     }
     mbar_init(teardown, 1);
@@ -252,14 +262,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   } else if (warp >= kSoftWarp0) {
     // ------------------------------------------------------------ softmax
     const int q4 = warp & 3;
+    const int hh = (warp - kSoftWarp0) >> 2;  // this warp's half of a block's keys and of O's columns
     const int row = q4 * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);  // this warp's lane quadrant
+    const uint32_t pair_bar = 1u + static_cast<uint32_t>(q4);            // named barrier of the two halves
+    const uint32_t xch = base + C::XCH_OFF;
     // m: the reference maximum of this row's scaled logits (log2 units) that
     // P is taken against.  It moves only when a block's maximum exceeds it
     // by more than kLazy: P then stays at most 2^kLazy (safe in 16-bit and
     // in the fp32 sums), and O is rescaled -- after waiting for the P.V
     // before -- only in the blocks where some row of the warp moved.  The
-    // result O / l does not depend on the reference.
+    // result O / l does not depend on the reference.  The two halves of a
+    // row see the same block maximum (exchanged) and so move m together; each
+    // keeps the partial sum of its keys.  Every wait's outcome is agreed
+    // between the two halves before they part, so both take the same path
+    // to every named barrier.
     constexpr float kLazy = 8.0f;
     const float cs = a.cs;
     float m = -INFINITY, l = 0.0f;
@@ -267,38 +284,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     for (int j = 0; j < nb; ++j) {
       const int b = j & 1;
       bool got = mbar_wait_bounded(s_full(b), (j >> 1) & 1, a.wait_limit_ns, abort_flag);
-      // the warp leaves together (tcgen05.ld / st need every lane)
-      if (!__all_sync(0xffffffffu, got)) {
+      if (named_bar_or(pair_bar, 64, !got)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int valid = min(kBN, a.sk - j * kBN);  // keys of this block inside the head
-      const uint32_t sb = tl + static_cast<uint32_t>(b * 128);
-      // the row's 128 logits in registers, then the S buffer is free for S_{j+2}
-      uint32_t sv[128];
+      const int valid = min(kBN, a.sk - j * kBN) - hh * 64;  // keys of this half inside the head
+      const uint32_t sb = tl + static_cast<uint32_t>(b * 128 + hh * 64);
+      // this half's 64 logits in registers, then the S buffer is free for S_{j+2}
+      uint32_t sv[64];
       tc_ld_32x32b_x32(sb, *reinterpret_cast<uint32_t(*)[32]>(sv));
       tc_ld_32x32b_x32(sb + 32u, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-      tc_ld_32x32b_x32(sb + 64u, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
-      tc_ld_32x32b_x32(sb + 96u, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
       tc_wait_ld_regs(sv);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free(b));
-      // (eight independent partial maxima and sums: short dependency chains)
       // (keys past the head's end, in its last block only, count as -inf)
-      if (valid < kBN) {
+      if (valid < 64) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i >= valid) sv[i] = __float_as_uint(-INFINITY);
       }
+      // (eight independent partial maxima and sums: short dependency chains)
       float mp[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mp[u] = __uint_as_float(sv[u]);
 #pragma unroll
-      for (int i = 8; i < 128; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(sv[i]));
+      for (int i = 8; i < 64; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(sv[i]));
       float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-      mx *= cs;
+      // the block maximum of the whole row: exchange with the other half
+      st_shared_f32(xch + static_cast<uint32_t>(((b * 2 + hh) * 128 + row) * 4), mx);
+      named_bar_sync(pair_bar, 64);
+      mx = fmaxf(mx, ld_shared_f32(xch + static_cast<uint32_t>(((b * 2 + (hh ^ 1)) * 128 + row) * 4))) * cs;
       float alpha = 1.0f;
       if (mx > m + kLazy) {  // always on the first block (m = -inf)
         alpha = ex2(m - mx);  // 0 on the first block
@@ -306,47 +323,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       }
       // P buffer b was read by PV_{j-2}
       if (j >= 2) got = mbar_wait_bounded(pv_done(b), ((j >> 1) - 1) & 1, a.wait_limit_ns, abort_flag);
-      if (!__all_sync(0xffffffffu, got)) {
+      if (named_bar_or(pair_bar, 64, !got)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // P = 2^(s cs - m) as pairs, 64 keys (32 pair columns) per store
+      // P = 2^(s cs - m) as pairs: 64 keys, 32 pair columns
       float sp[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) sp[u] = 0.0f;
+      uint32_t pk[32];
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int k = c2 * 64 + 2 * i;  // keys k, k + 1 of the block (-inf past the end: 2^-inf = 0)
-          const float e0 = ex2(fmaf(__uint_as_float(sv[k]), cs, -m));
-          const float e1 = ex2(fmaf(__uint_as_float(sv[k + 1]), cs, -m));
-          sp[i & 7] += e0 + e1;
-          pk[i] = pack_pair<BF16>(e0, e1);
-        }
-        tc_st_32x32b_x32_wait(tl + 256u + static_cast<uint32_t>(b * 64 + c2 * 32), pk);
+      for (int i = 0; i < 32; ++i) {
+        const float e0 = ex2(fmaf(__uint_as_float(sv[2 * i]), cs, -m));  // -inf past the end: 0
+        const float e1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), cs, -m));
+        sp[i & 7] += e0 + e1;
+        pk[i] = pack_pair<BF16>(e0, e1);
       }
+      tc_st_32x32b_x32_wait(tl + 256u + static_cast<uint32_t>(b * 64 + hh * 32), pk);
       const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l = l * alpha + sum;
-      // O holds the sum up to block j - 1: rescale it (once PV_{j-1} is done)
-      // where a row's reference moved
+      // O holds the sum up to block j - 1: rescale this half's columns (once
+      // PV_{j-1} is done) where a row's reference moved (the same rows in
+      // both halves)
       if (j >= 1 && __any_sync(0xffffffffu, alpha < 1.0f)) {
         got = mbar_wait_bounded(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, a.wait_limit_ns, abort_flag);
-        if (!__all_sync(0xffffffffu, got)) {
+        if (named_bar_or(pair_bar, 64, !got)) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
+          const uint32_t col = kTmemO + static_cast<uint32_t>(hh * (D / 2) + c * 32);
           uint32_t v[32];
-          tc_ld_32x32b_x32(tl + kTmemO + static_cast<uint32_t>(c * 32), v);
+          tc_ld_32x32b_x32(tl + col, v);
           tc_wait_ld_regs(v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tc_st_32x32b_x32_wait(tl + kTmemO + static_cast<uint32_t>(c * 32), v);
+          tc_st_32x32b_x32_wait(tl + col, v);
         }
       }
       tc_fence_before();
@@ -354,17 +369,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       if (lane == 0) mbar_arrive(p_full(b));
     }
     if (ok) {
-      // the last PV done: O / l, rounded once, 16-byte stores of this row
+      // the last PV done: O / l (the two halves' sums added), rounded once,
+      // 16-byte stores of this half of the row
       const bool got = mbar_wait_bounded(pv_done((nb - 1) & 1), ((nb - 1) >> 1) & 1, a.wait_limit_ns, abort_flag);
-      if (__all_sync(0xffffffffu, got)) {
+      if (!named_bar_or(pair_bar, 64, !got)) {
         tc_fence_after();
-        const float inv = 1.0f / l;
+        st_shared_f32(xch + static_cast<uint32_t>((hh * 128 + row) * 4), l);
+        named_bar_sync(pair_bar, 64);
+        const float inv = 1.0f / (l + ld_shared_f32(xch + static_cast<uint32_t>(((hh ^ 1) * 128 + row) * 4)));
         const bool in = q0 + row < a.sq;
-        uint16_t* orow = static_cast<uint16_t*>(a.o) + (static_cast<int64_t>(h) * a.sq + q0 + row) * D;
+        uint16_t* orow = static_cast<uint16_t*>(a.o) + (static_cast<int64_t>(h) * a.sq + q0 + row) * D + hh * (D / 2);
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t v[32];
-          tc_ld_32x32b_x32(tl + kTmemO + static_cast<uint32_t>(c * 32), v);
+          tc_ld_32x32b_x32(tl + kTmemO + static_cast<uint32_t>(hh * (D / 2) + c * 32), v);
           tc_wait_ld_regs(v);
           if (in) {
 #pragma unroll
