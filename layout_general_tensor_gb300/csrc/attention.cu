@@ -69,13 +69,17 @@ template <int D>
 struct AttnCfg {
   static constexpr uint32_t CHUNK = 128u * 128u;      // one 64-wide box of 128 rows: 16 KiB
   static constexpr uint32_t TILE = (D / 64) * CHUNK;  // a Q, K or V tile
-  static constexpr int NS = D == 128 ? 2 : 3;         // K / V ring
+  // K and V rings of their own: a K tile is free once S = Q K^T completed,
+  // a V tile only once P.V completed, so K is loaded further ahead
+  static constexpr int NSK = D == 128 ? 3 : 4;
+  static constexpr int NSV = D == 128 ? 2 : 3;
   static constexpr uint32_t Q_OFF = 0;
-  static constexpr uint32_t KV_OFF = TILE;
-  static constexpr uint32_t STAGE = 2 * TILE;  // K, then V
-  static constexpr uint32_t BAR_OFF = KV_OFF + NS * STAGE;
-  // q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], s_free[2], p_full[2], pv_done[2], teardown
-  static constexpr int NBARS = 1 + 3 * NS + 8 + 1;
+  static constexpr uint32_t K_OFF = TILE;
+  static constexpr uint32_t V_OFF = K_OFF + NSK * TILE;
+  static constexpr uint32_t BAR_OFF = V_OFF + NSV * TILE;
+  // q_full, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], s_free[2], p_full[2], pv_done[2],
+  // teardown
+  static constexpr int NBARS = 1 + 2 * NSK + 2 * NSV + 8 + 1;
   // the two softmax halves of a row exchange their block maxima (by block
   // parity) and, at the end, their partial sums: fp32 [2][2][128]
   static constexpr uint32_t XCH_OFF = BAR_OFF + ((NBARS * 8 + 15) & ~15);
@@ -140,23 +144,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
 
   const uint32_t bar0 = base + C::BAR_OFF;
   const uint32_t q_full = bar0;
+  constexpr int kB = 1 + 2 * C::NSK + 2 * C::NSV;
   auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto v_full = [&](int s) { return bar0 + 8u * (1 + C::NS + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + 2 * C::NS + s); };
-  auto s_full = [&](int b) { return bar0 + 8u * (1 + 3 * C::NS + b); };
-  auto s_free = [&](int b) { return bar0 + 8u * (3 + 3 * C::NS + b); };
-  auto p_full = [&](int b) { return bar0 + 8u * (5 + 3 * C::NS + b); };
-  auto pv_done = [&](int b) { return bar0 + 8u * (7 + 3 * C::NS + b); };
-  const uint32_t teardown = bar0 + 8u * (9 + 3 * C::NS);
+  auto k_empty = [&](int s) { return bar0 + 8u * (1 + C::NSK + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * C::NSK + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * C::NSK + C::NSV + s); };
+  auto s_full = [&](int b) { return bar0 + 8u * (kB + b); };
+  auto s_free = [&](int b) { return bar0 + 8u * (kB + 2 + b); };
+  auto p_full = [&](int b) { return bar0 + 8u * (kB + 4 + b); };
+  auto pv_done = [&](int b) { return bar0 + 8u * (kB + 6 + b); };
+  const uint32_t teardown = bar0 + 8u * (kB + 8);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < C::NS; ++s) {
+    for (int s = 0; s < C::NSK; ++s) {
       mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < C::NSV; ++s) {
       mbar_init(v_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      mbar_init(v_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
@@ -184,7 +193,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   pdl_wait();
 
   bool q_issued = false;
-  int kv_issued = 0;  // producer lane: K / V blocks whose loads were issued
+  int k_issued = 0, v_issued = 0;  // producer lane: K / V tiles whose loads were issued
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -193,20 +202,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) tma_load_3d(base + C::Q_OFF + c * C::CHUNK, &a.tm_q, q_full, c * 64, q0, h);
       q_issued = true;
-      for (int j = 0; j < nb; ++j) {
-        const int s = j % C::NS;
-        if (j >= C::NS && !mbar_wait_bounded(kv_empty(s), ((j / C::NS) - 1) & 1, a.wait_limit_ns, abort_flag)) {
-          if (!*abort_flag) attn_timeout(a, abort_flag, 0);
+      // the two rings, each fed as soon as its next buffer is free
+      uint64_t stall_t0 = 0;
+      while (k_issued < nb || v_issued < nb) {
+        bool progress = false;
+        if (k_issued < nb) {
+          const int j = k_issued, s = j % C::NSK;
+          if (j < C::NSK || mbar_test_wait(k_empty(s), ((j / C::NSK) - 1) & 1)) {
+            const uint32_t kd = base + C::K_OFF + s * C::TILE;
+            mbar_arrive_expect_tx(k_full(s), C::TILE);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tma_load_3d(kd + c * C::CHUNK, &a.tm_k, k_full(s), c * 64, j * kBN, h);
+            ++k_issued;
+            progress = true;
+          }
+        }
+        if (v_issued < nb && v_issued < k_issued) {
+          const int j = v_issued, s = j % C::NSV;
+          if (j < C::NSV || mbar_test_wait(v_empty(s), ((j / C::NSV) - 1) & 1)) {
+            const uint32_t vd = base + C::V_OFF + s * C::TILE;
+            mbar_arrive_expect_tx(v_full(s), C::TILE);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tma_load_3d(vd + c * C::CHUNK, &a.tm_v, v_full(s), c * 64, j * kBN, h);
+            ++v_issued;
+            progress = true;
+          }
+        }
+        if (progress) {
+          stall_t0 = 0;
+          continue;
+        }
+        if (*abort_flag) break;
+        const uint64_t now = global_timer_ns();
+        if (stall_t0 == 0) {
+          stall_t0 = now;
+        } else if (now - stall_t0 > a.wait_limit_ns) {
+          attn_timeout(a, abort_flag, 0);
           break;
         }
-        const uint32_t kd = base + C::KV_OFF + s * C::STAGE, vd = kd + C::TILE;
-        mbar_arrive_expect_tx(k_full(s), C::TILE);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_load_3d(kd + c * C::CHUNK, &a.tm_k, k_full(s), c * 64, j * kBN, h);
-        mbar_arrive_expect_tx(v_full(s), C::TILE);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_load_3d(vd + c * C::CHUNK, &a.tm_v, v_full(s), c * 64, j * kBN, h);
-        ++kv_issued;
+        __nanosleep(64);
       }
     }
   } else if (warp == 1) {
@@ -217,11 +251,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       // K-major tiles: 128-byte rows of 64 elements, 8-row groups 1 KiB
       // apart; 16-deep step k is 32 bytes into 64-wide chunk k / 4.
       auto issue_s = [&](int j) -> bool {
-        const int b = j & 1, s = j % C::NS;
+        const int b = j & 1, s = j % C::NSK;
         if (j >= 2 && !mbar_wait_bounded(s_free(b), ((j >> 1) - 1) & 1, a.wait_limit_ns, abort_flag)) return false;
-        if (!mbar_wait_bounded(k_full(s), (j / C::NS) & 1, a.wait_limit_ns, abort_flag)) return false;
+        if (!mbar_wait_bounded(k_full(s), (j / C::NSK) & 1, a.wait_limit_ns, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t kb = base + C::KV_OFF + s * C::STAGE;
+        const uint32_t kb = base + C::K_OFF + s * C::TILE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = static_cast<uint32_t>(k >> 2) * C::CHUNK + static_cast<uint32_t>(k & 3) * 32u;
@@ -229,6 +263,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
                         sw128_desc(kb + off, 16u, 1024u), a.idesc_s, k > 0 ? 1u : 0u);
         }
         tc_commit(s_full(b));
+        tc_commit(k_empty(s));
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -237,9 +272,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
           ok = false;
           break;
         }
-        const int b = j & 1, s = j % C::NS;
+        const int b = j & 1, s = j % C::NSV;
         if (!mbar_wait_bounded(p_full(b), (j >> 1) & 1, a.wait_limit_ns, abort_flag) ||
-            !mbar_wait_bounded(v_full(s), (j / C::NS) & 1, a.wait_limit_ns, abort_flag)) {
+            !mbar_wait_bounded(v_full(s), (j / C::NSV) & 1, a.wait_limit_ns, abort_flag)) {
           ok = false;
           break;
         }
@@ -247,14 +282,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         // O += P_j V_j: A = P_j (8 columns of pairs per 16 keys), B = V_j
         // MN-major: 128-byte rows along head_dim, one per key, 8-key groups
         // 1 KiB apart, 64-wide head_dim chunks 16 KiB apart; 16 keys = 2 KiB.
-        const uint32_t vb = base + C::KV_OFF + s * C::STAGE + C::TILE;
+        const uint32_t vb = base + C::V_OFF + s * C::TILE;
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k)
           mma_ts(tmem + kTmemO, tmem + 256u + static_cast<uint32_t>(b * 64 + k * 8),
                  sw128_desc(vb + static_cast<uint32_t>(k) * 2048u, C::CHUNK, 1024u), a.idesc_pv,
                  (j | k) != 0 ? 1u : 0u);
         tc_commit(pv_done(b));
-        tc_commit(kv_empty(s));
+        tc_commit(v_empty(s));
       }
       if (!ok && !*abort_flag) attn_timeout(a, abort_flag, 1);
       tc_commit(teardown);  // every MMA of this thread completed before the tensor memory is freed
@@ -410,10 +445,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     // let the loads still in flight land before the CTA exits
     volatile int no_abort = 0;
     if (q_issued) mbar_wait_bounded(q_full, 0, a.wait_limit_ns, &no_abort);
-    for (int j = kv_issued > C::NS ? kv_issued - C::NS : 0; j < kv_issued; ++j) {
-      mbar_wait_bounded(k_full(j % C::NS), (j / C::NS) & 1, a.wait_limit_ns, &no_abort);
-      mbar_wait_bounded(v_full(j % C::NS), (j / C::NS) & 1, a.wait_limit_ns, &no_abort);
-    }
+    for (int j = k_issued > C::NSK ? k_issued - C::NSK : 0; j < k_issued; ++j)
+      mbar_wait_bounded(k_full(j % C::NSK), (j / C::NSK) & 1, a.wait_limit_ns, &no_abort);
+    for (int j = v_issued > C::NSV ? v_issued - C::NSV : 0; j < v_issued; ++j)
+      mbar_wait_bounded(v_full(j % C::NSV), (j / C::NSV) & 1, a.wait_limit_ns, &no_abort);
   }
   if (warp == 1 && lane == 0) {
     volatile int no_abort = 0;
