@@ -21,8 +21,9 @@
 // S is double-buffered, so S_{j+1} is computed while the softmax works on
 // S_j; P is double-buffered, so P_j is written while P_{j-1} is multiplied.
 //
-// Warp roles (384 threads): warp 0 TMA producer (Q once, a ring of K / V
-// blocks), warp 1 MMA issuer (owns the tensor memory), warps 4..11 softmax
+// Warp roles (384 threads): warp 0 TMA producer (Q once, rings of K and V
+// tiles), warp 1 S issuer (owns the tensor memory), warp 2 P.V issuer,
+// warps 4..11 softmax
 // and epilogue, two per tensor-memory lane quadrant (warp % 4), each taking
 // half of a block's keys and half of O's columns.  Tensor memory: S at
 // columns 0 and 128, P at 256 and 320 (bf16 / fp16 pairs), O at 384.
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       mbar_init(p_full(b), 8);
       mbar_init(pv_done(b), 1);
     }
-    mbar_init(teardown, 1);
+    mbar_init(teardown, 2);  // both MMA issuers
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -244,16 +245,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
+    // One thread issues a tcgen05 MMA only every hundred-odd cycles, so the
+    // two products have issuers of their own: this one S = Q K^T, warp 2
+    // O += P V (disjoint accumulators; they meet only through barriers).
     if (lane == 0) {
       bool ok = mbar_wait_bounded(q_full, 0, a.wait_limit_ns, abort_flag);
       // S_j = Q K_j^T into S buffer j % 2 (once the softmax has read S_{j-2}).
       // K-major tiles: 128-byte rows of 64 elements, 8-row groups 1 KiB
       // apart; 16-deep step k is 32 bytes into 64-wide chunk k / 4.
-      auto issue_s = [&](int j) -> bool {
+      for (int j = 0; ok && j < nb; ++j) {
         const int b = j & 1, s = j % C::NSK;
-        if (j >= 2 && !mbar_wait_bounded(s_free(b), ((j >> 1) - 1) & 1, a.wait_limit_ns, abort_flag)) return false;
-        if (!mbar_wait_bounded(k_full(s), (j / C::NSK) & 1, a.wait_limit_ns, abort_flag)) return false;
+        if ((j >= 2 && !mbar_wait_bounded(s_free(b), ((j >> 1) - 1) & 1, a.wait_limit_ns, abort_flag)) ||
+            !mbar_wait_bounded(k_full(s), (j / C::NSK) & 1, a.wait_limit_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t kb = base + C::K_OFF + s * C::TILE;
 #pragma unroll
@@ -264,14 +271,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         }
         tc_commit(s_full(b));
         tc_commit(k_empty(s));
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < nb; ++j) {
-        if (j + 1 < nb && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
+      }
+      if (!ok && !*abort_flag) attn_timeout(a, abort_flag, 1);
+      tc_commit(teardown);  // every MMA of this thread completed before the tensor memory is freed
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ P.V issuer
+    if (lane == 0) {
+      bool ok = true;
+      for (int j = 0; j < nb; ++j) {
         const int b = j & 1, s = j % C::NSV;
         if (!mbar_wait_bounded(p_full(b), (j >> 1) & 1, a.wait_limit_ns, abort_flag) ||
             !mbar_wait_bounded(v_full(s), (j / C::NSV) & 1, a.wait_limit_ns, abort_flag)) {
@@ -292,7 +300,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         tc_commit(v_empty(s));
       }
       if (!ok && !*abort_flag) attn_timeout(a, abort_flag, 1);
-      tc_commit(teardown);  // every MMA of this thread completed before the tensor memory is freed
+      tc_commit(teardown);
     }
   } else if (warp >= kSoftWarp0) {
     // ------------------------------------------------------------ softmax
@@ -318,7 +326,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
       const int b = j & 1;
+      // S_j, and P buffer b free (PV_{j-2} done), agreed by both halves at once
       bool got = mbar_wait_bounded(s_full(b), (j >> 1) & 1, a.wait_limit_ns, abort_flag);
+      if (got && j >= 2) got = mbar_wait_bounded(pv_done(b), ((j >> 1) - 1) & 1, a.wait_limit_ns, abort_flag);
       if (named_bar_or(pair_bar, 64, !got)) {
         ok = false;
         break;
@@ -356,13 +366,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
         alpha = ex2(m - mx);  // 0 on the first block
         m = mx;
       }
-      // P buffer b was read by PV_{j-2}
-      if (j >= 2) got = mbar_wait_bounded(pv_done(b), ((j >> 1) - 1) & 1, a.wait_limit_ns, abort_flag);
-      if (named_bar_or(pair_bar, 64, !got)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       // P = 2^(s cs - m) as pairs: 64 keys, 32 pair columns
       float sp[8];
 #pragma unroll
