@@ -6,8 +6,9 @@
 // One CTA per 128 queries of a head; the head's keys in blocks of 128.
 //   S_j = Q K_j^T       tcgen05 MMA, both operands K-major (TMA, 128-byte
 //                       swizzle), fp32 accumulator in tensor memory.
-//   P_j, m, l           online softmax by four warps, one query row per
-//                       thread, the row's logits held in registers: a
+//   P_j, m, l           online softmax by eight warps, two per query row
+//                       quadrant (half of the keys each), one row per
+//                       thread, the logits held in registers: a
 //                       reference maximum m (of the logits times
 //                       scale * log2 e) moved only when a block's maximum
 //                       exceeds it by more than 8, running sum l;
