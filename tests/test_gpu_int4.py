@@ -83,10 +83,12 @@ def test_int4_group_sizes(group, form):
 @pytest.mark.parametrize("N,Kd,group,split", [(384, 8192, 64, 3), (300, 4096, 128, 5), (256, 16384, 512, 0),
                                                 (640, 2048, 64, 7)])
 def test_int4_scale_windows(N, Kd, group, split, form):
-    """Scales read in windows of 8 groups (16 bytes) of a row, copied ahead
-    into shared memory: runs that start and end inside a window, short runs
-    (split 7 over 5 tiles: one unit of 5 K blocks per CTA), rows beyond N,
-    group 64 (a window every two stages) and 512 (a window every eight)."""
+    """Scale reads along a run: the fp16 form loads each K block's scale two
+    stages ahead by a walk over the same stages, the e4m3 form reads windows
+    of 8 groups (16 bytes) of a row.  Runs that start and end inside a group
+    or a window, short runs (split 7 over 5 tiles: one unit of 5 K blocks per
+    CTA), rows beyond N, group 64 (two groups a stage) and 512 (a group every
+    two stages)."""
     case = _case(16, N, Kd, group=group, split=split)
     inp = wl.make_inputs(case, seed=N + group)
     c, g, _ = run_case(case, inp, reps=2)
