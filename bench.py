@@ -297,6 +297,60 @@ def cpu_baseline(case, inp, budget_s=10.0, rows=512):
                       f"matmul after per-layout gather), {el:.1f} s"}
 
 
+# ------------------------------------------------------------------ ranks
+
+class Ranks:
+    """The launch's ranks, one process per GPU, read from the torchrun
+    environment (RANK, LOCAL_RANK, WORLD_SIZE, MASTER_ADDR/PORT).
+
+    Every rank runs an independent replica of the workload: the GEMM has no
+    exchange step, so the data path holds no collective.  The only traffic
+    between ranks is the barrier around the timed region and the max over
+    ranks of its duration.  `backend` is nccl on GPUs; the same code runs
+    over gloo on CPU tensors (`device=None`)."""
+
+    def __init__(self, backend="nccl", device=None):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.device = device
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            kw = {"device_id": device} if backend == "nccl" and device is not None else {}
+            dist.init_process_group(backend, **kw)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x):
+        """The maximum of `x` over all ranks (every rank gets it)."""
+        if self.dist is None:
+            return float(x)
+        import torch
+        t = torch.tensor([float(x)], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def aggregate(self, units_per_rank, max_seconds):
+        """Whole-job throughput: the units all ranks processed over the
+        slowest rank's time (weak scaling: each rank's work is fixed)."""
+        return self.world * units_per_rank / max_seconds
+
+    def emit(self, line, out=None):
+        """Rank 0 alone prints the JSON line."""
+        if self.rank == 0:
+            print(json.dumps(line), file=out or sys.stdout, flush=True)
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.barrier()
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
 # ------------------------------------------------------------------ arms
 
 def reference_arm(args, case):
@@ -332,23 +386,16 @@ def gpu_arm(args, headline):
     import torch
     import workloads as wl
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(local)
+    torch.cuda.set_device(local)
+    ranks = Ranks("nccl", torch.device("cuda", local))
+    world, rank = ranks.world, ranks.rank
 
     import __graft_entry__
     __graft_entry__.build()
     peaks, peak_src = load_peaks()
     def barrier():
-        if dist is not None:
-            dist.barrier()
+        ranks.barrier()
         torch.cuda.synchronize()
 
     dc = DeviceCase(headline)
@@ -370,12 +417,9 @@ def gpu_arm(args, headline):
     barrier()
     clocks = sampler.stop()
     step_times = time_steps(dc.run, min(args.steps, 20), 0)  # per-step events, for the record
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = ranks.max(total_ms)
     flops = headline.flops()
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = ranks.aggregate(flops * args.steps, total_ms * 1e-3) / 1e12
     avg_launch_ms = total_ms / args.steps
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
 
@@ -394,11 +438,8 @@ def gpu_arm(args, headline):
     e2e_steps = max(3, min(args.steps, 20))
     e2e_times = time_steps(e2e_step, e2e_steps, 2)
     e2e_total = sum(e2e_times)
-    if dist is not None:
-        t = torch.tensor([e2e_total], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = world * flops * e2e_steps / (e2e_total * 1e-3) / 1e12
+    e2e_total = ranks.max(e2e_total)
+    e2e_value = ranks.aggregate(flops * e2e_steps, e2e_total * 1e-3) / 1e12
 
     # the other workloads, same timing discipline; the int4 workload also
     # on weights pre-packed offline into the kernel's stage layout
@@ -467,12 +508,9 @@ def gpu_arm(args, headline):
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    ranks.emit(line)
     dc.g.close()
-    if dist is not None:
-        dist.barrier()
-        dist.destroy_process_group()
+    ranks.close()
     return 0
 
 
