@@ -113,28 +113,41 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.close()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[4:9]))
-                except ValueError:
-                    continue
+            lines = f.readlines()
         os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        loaded = [r for r in rows if r[2] > 0] or rows
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        for r in loaded:
-            for n, v in zip(names[1:], r[3][1:]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
+        return summarize_clock_samples(lines)
+
+
+# the throttle reasons a sample line carries after clocks, max clock,
+# utilisation and power (the order of ClockSampler.FIELDS)
+CLOCK_REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def summarize_clock_samples(lines):
+    """The `clocks` record of a run from nvidia-smi's CSV lines: the median
+    SM clock over the samples taken under load (utilisation > 0; all samples
+    if none was), the largest reported maximum clock, and every throttle
+    reason seen Active under load."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[5:9]))
+        except ValueError:
+            continue
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    loaded = [r for r in rows if r[2] > 0] or rows
+    reasons = set()
+    for r in loaded:
+        for n, v in zip(CLOCK_REASONS, r[3]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+            "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
 
 
 # ------------------------------------------------------------------ helpers
