@@ -5,10 +5,11 @@ A K-contiguous, B N-contiguous, fp32 accumulation) on inputs resident in HBM;
 consecutive steps cycle through enough copies of the operands (more than
 2.5 x the 129 MB L2 in total) that no step finds its inputs in L2.  The
 same run also measures the other workloads (fp16 256^3 in four layouts, the
-skinny split-K GEMM, the irregular GEMM, the int4-weight GEMM, and the fp32
-row reductions: the IREE page's 4096 -> 1 and 4 x 4096 -> 4, and a 1 GiB
-16384 x 16384 matrix for bandwidth) and reports them under "configs".  One
-JSON line on stdout (rank 0).
+skinny split-K GEMM, the irregular GEMM, the int4-weight GEMM on plain and
+on pre-packed weights, the fp32 row reductions: the IREE page's 4096 -> 1
+and 4 x 4096 -> 4, and a 1 GiB 16384 x 16384 matrix for bandwidth, and the
+fused attention forward, 32 heads x 4096 x 4096, head_dim 128, bf16) and
+reports them under "configs".  One JSON line on stdout (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
