@@ -848,12 +848,16 @@ __global__ void __launch_bounds__(256) int4_prepack_kernel(const uint8_t* __rest
 
 int pre_slots(int group) { return group < 256 ? 256 / group : 1; }
 size_t pre_block_bytes(int group) { return kRawBytes + static_cast<size_t>(pre_slots(group)) * TILE_P * 2; }
+// 0: no pre-packed layout for these sizes (a group that is not positive, or
+// sizes past the kernel's 32-bit row and column indices).
 size_t pre_total_bytes(int64_t N, int64_t K, int group) {
+  if (N <= 0 || K <= 0 || group <= 0 || N > INT32_MAX || K > INT32_MAX) return 0;
   return static_cast<size_t>((N + TILE_P - 1) / TILE_P) * static_cast<size_t>((K + 255) / 256) * pre_block_bytes(group);
 }
 
 cudaError_t launch_int4_prepack(const void* B, int64_t ldb, const void* scales, int64_t N, int64_t K, int group,
                                 void* out, cudaStream_t stream) {
+  if (pre_total_bytes(N, K, group) == 0) return cudaErrorInvalidValue;
   const int S = static_cast<int>((K + 255) / 256);
   const int64_t nblocks = (N + TILE_P - 1) / TILE_P * S;
   if (nblocks == 0) return cudaSuccess;

@@ -227,7 +227,8 @@ def test_planner_int4_prepacked(lib, monkeypatch):
     for N, K, g in [(16384, 16384, 128), (300, 640, 64), (130, 1280, 256), (1, 512, 512)]:
         slots = 256 // g if g < 256 else 1
         assert lib.gemm_int4_prepack_bytes(N, K, g) == -(-N // 128) * -(-K // 256) * (128 * 128 + slots * 256)
-    for N, K, g in [(0, 256, 128), (256, 0, 128), (256, 768, 192), (256, 100, 64), (256, 640, 256)]:
+    for N, K, g in [(0, 256, 128), (256, 0, 128), (256, 768, 192), (256, 100, 64), (256, 640, 256), (256, 1024, -256),
+                    (256, 1024, -64), (1 << 31, 512, 128), (256, 1 << 32, 128)]:
         assert lib.gemm_int4_prepack_bytes(N, K, g) == 0, (N, K, g)
     # null pointers are refused before any launch
     assert lib.gemm_int4_prepack(0, 0, 0, 256, 1024, 128, 0) == lib.GEMM_ERR_INVALID_ARG
