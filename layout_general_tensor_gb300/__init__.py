@@ -241,6 +241,15 @@ def reduce_rows_f32(x: int, rows: int, cols: int, ldx: int, out: int, workspace:
                                 stream or None)
 
 
+def _require_device(what, **tensors):
+    """Every given tensor must live in CUDA device memory: a host address
+    handed to a kernel (or encoded into a tensor map) would fault the GPU
+    instead of returning an error."""
+    for name, t in tensors.items():
+        if t is not None and not getattr(t, "is_cuda", False):
+            raise ValueError(f"{what}: {name} must be a CUDA tensor")
+
+
 class RowReduce:
     """out[r] = sum of row r of an fp32 matrix, with its (zero-filled) device
     workspace.  Marshalling only: passes device addresses and the current
@@ -255,6 +264,7 @@ class RowReduce:
 
     def run(self, x, out, ldx: int = 0, stream=None):
         import torch
+        _require_device("RowReduce.run", x=x, out=out)
         s = torch.cuda.current_stream().cuda_stream if stream is None else stream
         st = reduce_rows_f32(x.data_ptr(), self.rows, self.cols, ldx, out.data_ptr(),
                              self.workspace.data_ptr() if self.ws_bytes else 0, self.ws_bytes, s)
@@ -286,9 +296,10 @@ class Gemm:
 
     def run(self, A, B, C, scales=None, zeros=None, stream=None, workspace=None, workspace_bytes=None):
         import torch
-        s = torch.cuda.current_stream().cuda_stream if stream is None else stream
         ws = self.workspace if workspace is None else workspace
         wsb = self.ws_bytes if workspace_bytes is None else workspace_bytes
+        _require_device("Gemm.run", A=A, B=B, C=C, scales=scales, zeros=zeros, workspace=ws if wsb else None)
+        s = torch.cuda.current_stream().cuda_stream if stream is None else stream
         st = gemm_run(self.plan, A.data_ptr(), B.data_ptr(), C.data_ptr(),
                       scales.data_ptr() if scales is not None else 0,
                       zeros.data_ptr() if zeros is not None else 0,
@@ -317,6 +328,7 @@ def int4_prepack(B, scales, N, K, group_size=128, ldb=0, stream=None):
     their fp16 scales for GEMM_FLAG_INT4_PREPACKED; returns the packed device
     uint8 tensor."""
     import torch
+    _require_device("int4_prepack", B=B, scales=scales)
     nbytes = gemm_int4_prepack_bytes(N, K, group_size)
     if nbytes == 0:
         raise GemmError(GEMM_ERR_INVALID_ARG, "gemm_int4_prepack_bytes")
@@ -352,6 +364,7 @@ class Attention:
 
     def run(self, Q, K, V, O, stream=None):
         import torch
+        _require_device("Attention.run", Q=Q, K=K, V=V, O=O)
         s = torch.cuda.current_stream().cuda_stream if stream is None else stream
         _check(attn_run(self.plan, Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), s), "attn_run")
 

@@ -371,3 +371,24 @@ def test_attention_descriptor_checks(lib):
         args.update(kw)
         st, h = lib.attn_create_status(lib.attn_desc_t(**args))
         assert st == lib.GEMM_ERR_INVALID_ARG and h is None, kw
+
+
+def test_binding_refuses_host_tensors(lib):
+    """A host tensor's address never reaches a kernel or a tensor map: every
+    run method of the binding raises before calling into the library."""
+    import torch
+    x = torch.zeros(64, dtype=torch.float16)
+    g = object.__new__(lib.Gemm)
+    g.plan, g.ws_bytes, g.workspace = None, 0, None
+    with pytest.raises(ValueError, match="Gemm.run: A must be a CUDA tensor"):
+        g.run(x, x, x)
+    a = object.__new__(lib.Attention)
+    a.plan = None
+    with pytest.raises(ValueError, match="Attention.run: Q must be a CUDA tensor"):
+        a.run(x, x, x, x)
+    r = object.__new__(lib.RowReduce)
+    r.rows, r.cols, r.ws_bytes, r.workspace = 1, 64, 0, None
+    with pytest.raises(ValueError, match="RowReduce.run: x must be a CUDA tensor"):
+        r.run(x.float(), torch.zeros(1))
+    with pytest.raises(ValueError, match="int4_prepack: B must be a CUDA tensor"):
+        lib.int4_prepack(torch.zeros(8, dtype=torch.uint8), x, 128, 256)
